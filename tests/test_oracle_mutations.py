@@ -1,0 +1,96 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in the oracle (on the CPU, through monkeypatch)
+and checks that the pin written for that part of the oracle now fails.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.adamw as OA
+import oracle.crmath as OC
+import oracle.f32 as OF
+import oracle.group as OG
+import oracle.softmax as OS
+from tests import test_oracle_adamw as TA
+from tests import test_oracle_crmath as TC
+from tests import test_oracle_f32 as TF
+from tests import test_oracle_group as TG
+from tests import test_oracle_softmax as TS
+
+
+def _sub_reversed(monkeypatch):
+    real = OG.apply_op
+
+    def wrong(name, a, b=None):
+        return real("SUB", b, a) if name == "SUB" else real(name, a, b)
+
+    monkeypatch.setattr(OG, "apply_op", wrong)
+
+
+def _max_tie_first(monkeypatch):
+    monkeypatch.setattr(OG, "_max", lambda a, b: np.where(a >= b, a, b).astype(np.float32))
+
+
+def _gelu_half_off(monkeypatch):
+    monkeypatch.setattr(OG, "INV_SQRT2", np.float32(0.7071068))
+
+
+def _bf16_truncates(monkeypatch):
+    monkeypatch.setattr(OF, "f32_to_bf16",
+                        lambda x: (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16))
+
+
+def _exp_in_binary32(monkeypatch):
+    monkeypatch.setattr(OC, "exp_f32", lambda x: np.exp(np.asarray(x, dtype=np.float32)))
+
+
+def _interleaved_combined_backwards(monkeypatch):
+    real = OS._sum_interleaved
+
+    def wrong(e, partials):
+        return real(e[:, ::-1].copy(), partials)
+
+    monkeypatch.setattr(OS, "_sum_interleaved", wrong)
+
+
+def _adamw_no_bias_correction(monkeypatch):
+    real = OA.hyper_f32
+
+    def wrong(*a, **k):
+        h = dict(real(*a, **k))
+        h["bc2"] = np.float32(1.0)
+        return h
+
+    monkeypatch.setattr(OA, "hyper_f32", wrong)
+
+
+def _adamw_eps_inside_sqrt(monkeypatch):
+    def wrong(theta, m, v, grad, grad_dtype, h):
+        th = np.asarray(theta, dtype=np.float32)
+        g = OF.widen(grad, grad_dtype)
+        m1 = (h["b1"] * m) + (h["omb1"] * g)
+        v1 = (h["b2"] * v) + (h["omb2"] * (g * g))
+        q = (m1 / h["bc1"]) / np.sqrt((v1 / h["bc2"]) + h["eps"])
+        return (th - h["lr"] * (q + h["wd"] * th)).astype(np.float32), m1, v1
+
+    monkeypatch.setattr(OA, "step_leaf", wrong)
+
+
+CASES = [
+    (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
+    (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
+    (_gelu_half_off, TG.test_small_group_against_mpmath_per_node),
+    (_bf16_truncates, TF.test_bf16_rounding_matches_torch),
+    (_exp_in_binary32, TC.test_exp_correctly_rounded_across_binades),
+    (_interleaved_combined_backwards, lambda: TS.test_tiny_rows_exact(("interleaved", 3))),
+    (_adamw_no_bias_correction, TA.test_against_torch_adamw_float64),
+    (_adamw_eps_inside_sqrt, TA.test_first_step_closed_form),
+]
+
+
+@pytest.mark.parametrize("plant,pin", CASES, ids=[c[0].__name__ for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, plant, pin):
+    plant(monkeypatch)
+    with pytest.raises(AssertionError):
+        pin()
