@@ -1,0 +1,409 @@
+"""Benchmark of the fusion-group hot path on GB300.
+
+One step = one pass of every case of the hot path over its full-size
+synthetic workload, each one launch through the C ABI:
+  * the 64-node group over bf16 x [8192, 8192] with a row vector, a column
+    vector and a scalar broadcast in (bf16 out);
+  * the softmax region over bf16 logits [32768, 4096], once with the
+    sequential order and once with interleaved(8) (exact exp);
+  * the AdamW step over the 200 leaves (1,100,046,336 parameters) of a
+    Llama-style 1.1B model (f32 params/m/v, bf16 grads).
+metric: achieved HBM GB/s = algorithmic bytes of the step (every input read
+once, every output written once) / step time.  Per-kernel figures are in
+"kernels".  Inputs (15.9 GB) exceed L2 (129 MB), so no flush is needed.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun each rank runs the whole workload on its own GPU (the cases
+shard without exchange: weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
+    p.add_argument("--softmax-exp", choices=["exact", "fast"], default="exact")
+    return p.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"psk_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", self.gpu_id], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.remove(self.path)
+        except Exception:
+            return None
+        if not rows:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev)
+
+
+# ---------------------------------------------------------------- traffic
+def _dram_traffic(kernel: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the
+    kernel's source is unchanged since it was captured; else None."""
+    path = os.path.join(HERE, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"adamw": "adamw.cu", "group": "group.cu", "softmax_sequential": "softmax.cu",
+           "softmax_interleaved8": "softmax.cu"}[kernel]
+    h = hashlib.sha256(open(os.path.join(HERE, "reduction_groups_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[1] == h:
+            return int(parts[2])
+    return None
+
+
+# --------------------------------------------------------------- CPU oracle
+def cpu_sample(scale: float = 1.0):
+    """Time the oracle, as it stands, on a bounded sample of each case.
+    Returns (algorithmic bytes processed, seconds, description)."""
+    import numpy as np
+
+    import oracle.adamw as OA
+    import oracle.group as OG
+    import oracle.softmax as OS
+    from synth import workloads as W
+
+    rows_g = max(1, int(8 * scale))
+    rows_s = max(1, int(24 * scale))
+    n_adam = max(4096, int(4_000_000 * scale))
+    wl = W.cap_group(rows_g, 8192)
+    ins = wl.host_inputs()
+    args = [(a, dt, s.strides) for (a, dt), s in zip(ins, wl.inputs)]
+    sw = W.softmax_rows(rows_s, 4096)
+    x = sw.host_x()
+    rng = np.random.default_rng(0)
+    th = (rng.standard_normal(n_adam) * 0.02).astype(np.float32)
+    m = (rng.standard_normal(n_adam) * 1e-3).astype(np.float32)
+    v = np.abs(rng.standard_normal(n_adam) * 1e-4).astype(np.float32)
+    g = (rng.standard_normal(n_adam) * 1e-3).astype(np.float32).view(np.uint32)
+    g = (g >> 16).astype(np.uint16)
+    hp = W.llama_adamw_leaves(layers=0, V=1).hp
+    h = OA.hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
+    t0 = time.perf_counter()
+    OG.evaluate(wl.tokens, wl.imm, args, wl.out_shape, wl.out_dtype)
+    OS.softmax_region(x, "bf16", "bf16", ("sequential",))
+    OS.softmax_region(x, "bf16", "bf16", ("interleaved", 8))
+    OA.step_leaf(th, m, v, g, "bf16", h)
+    dt = time.perf_counter() - t0
+    nbytes = rows_g * 8192 * 4 + 2 * rows_s * 4096 * 4 + n_adam * 26
+    desc = (f"oracle on {rows_g} rows of the 64-node group, {rows_s} rows of the softmax region in each order, "
+            f"{n_adam} AdamW parameters")
+    return nbytes, dt, desc
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(a, ws, rank, local):
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import reduction_groups_gb300 as R
+    from synth import workloads as W
+
+    # workloads (drawn on the device; seeds shared, so every rank has the same data)
+    wl = W.cap_group()
+    g_in = wl.device_inputs()
+    g_args = [(t, s.strides) for t, s in zip(g_in, wl.inputs)]
+    g_out = torch.empty(wl.out_shape, dtype=torch.bfloat16, device="cuda")
+    sw = W.softmax_rows()
+    sx = sw.device_x()
+    sy = torch.empty_like(sx)
+    tree = W.llama_adamw_leaves()
+    leaves = [tree.device_leaf(i) for i in range(len(tree.leaves))]
+    torch.cuda.synchronize()
+
+    b_group = wl.algorithmic_bytes()
+    b_soft = sw.algorithmic_bytes()
+    b_adam = tree.n_params * tree.bytes_per_param()
+    bytes_step = b_group + 2 * b_soft + b_adam
+    em = a.softmax_exp
+    kernels = ["group", "softmax_sequential", "softmax_interleaved8", "adamw"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0][0].record()
+        R.psk_group_run(wl.tokens, wl.imm, g_args, g_out)
+        if ev is not None:
+            ev[0][1].record()
+            ev[1][0].record()
+        R.psk_softmax_region(sx, sy, ("sequential",), em)
+        if ev is not None:
+            ev[1][1].record()
+            ev[2][0].record()
+        R.psk_softmax_region(sx, sy, ("interleaved", 8), em)
+        if ev is not None:
+            ev[2][1].record()
+            ev[3][0].record()
+        R.psk_adamw_tree(leaves, tree.hp)
+        if ev is not None:
+            ev[3][1].record()
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in kernels]
+           for _ in range(a.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(_gpu_uuid(torch, local))
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    start.record()
+    for i in range(a.steps):
+        step(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    per_kernel_ms = {k: sum(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(a.steps)) / a.steps
+                     for j, k in enumerate(kernels)}
+    if ws > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the public API with host buffers: per step, copy every
+    # input from pinned host memory, run the step, read every result back
+    e2e = None
+    if not a.no_e2e:
+        host_g = [t.cpu().pin_memory() for t in g_in]
+        host_gout = torch.empty(g_out.shape, dtype=g_out.dtype, pin_memory=True)
+        host_sx = sx.cpu().pin_memory()
+        host_sy = torch.empty(sy.shape, dtype=sy.dtype, pin_memory=True)
+        host_leaves = [tuple(t.cpu().pin_memory() for t in leaf) for leaf in leaves]
+        h2d = sum(t.numel() * t.element_size() for t in host_g) + host_sx.numel() * 2 + \
+            sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf)
+        d2h = host_gout.numel() * 2 + 2 * host_sy.numel() * 2 + \
+            sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf[:3])
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            for d_, h_ in zip(g_in, host_g):
+                d_.copy_(h_, non_blocking=True)
+            sx.copy_(host_sx, non_blocking=True)
+            for dl, hl in zip(leaves, host_leaves):
+                for d_, h_ in zip(dl, hl):
+                    d_.copy_(h_, non_blocking=True)
+            R.psk_group_run(wl.tokens, wl.imm, g_args, g_out)
+            host_gout.copy_(g_out, non_blocking=True)
+            R.psk_softmax_region(sx, sy, ("sequential",), em)
+            host_sy.copy_(sy, non_blocking=True)
+            R.psk_softmax_region(sx, sy, ("interleaved", 8), em)
+            host_sy.copy_(sy, non_blocking=True)
+            R.psk_adamw_tree(leaves, tree.hp)
+            for dl, hl in zip(leaves, host_leaves):
+                for d_, h_ in zip(dl[:3], hl[:3]):
+                    h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        s2.record()
+        for _ in range(a.steps):
+            e2e_step()
+        e2.record()
+        torch.cuda.synchronize()
+        ms = s2.elapsed_time(e2)
+        if ws > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        e2e = {"value": round(ws * bytes_step * a.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / a.steps, 3)}
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = _peaks()
+    kb = {"group": b_group, "softmax_sequential": b_soft, "softmax_interleaved8": b_soft, "adamw": b_adam}
+    kinfo = {}
+    for k in kernels:
+        gbs = kb[k] / (per_kernel_ms[k] / 1e3) / 1e9
+        kinfo[k] = {"ms": round(per_kernel_ms[k], 4), "algorithmic_bytes": int(kb[k]), "gbs": round(gbs, 1),
+                    "frac_of_hbm_peak": round(gbs / peak, 4)}
+    kinfo["group"]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (per_kernel_ms["group"] / 1e3), 1)
+    kinfo["group"]["node_evals_per_s"] = round(kinfo["group"]["elems_per_s"] * wl.n_ops, 1)
+    for k in ("softmax_sequential", "softmax_interleaved8"):
+        kinfo[k]["rows_per_s"] = round(sw.rows / (per_kernel_ms[k] / 1e3), 1)
+    kinfo["adamw"]["params_per_s"] = round(tree.n_params / (per_kernel_ms["adamw"] / 1e3), 1)
+    dom = max(kernels, key=lambda k: per_kernel_ms[k])
+    achieved = kb[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": _dram_traffic(dom)}
+
+    cpu = None
+    if not a.no_cpu and ws == 1:
+        nb, dt, desc = cpu_sample(15.0)
+        cpu = {"value": round(nb / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f"; {dt:.1f} s of one host core (numpy ufuncs run single-threaded)"}
+
+    value = ws * bytes_step * a.steps / (total_ms / 1e3) / 1e9
+    line = {
+        "metric": "achieved HBM GB/s (% of GB300 peak) for fused group, softmax region, AdamW params/s",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(total_ms / a.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded device draws, shapes of the workloads)",
+        "config": {"workload": "64-node group bf16 [8192,8192] + softmax region bf16 [32768,4096] "
+                               "(sequential, interleaved(8)) + AdamW tree of a Llama-style 1.1B model",
+                   "softmax_exp": em, "l2": "inputs larger than L2 (no flush needed)",
+                   "bytes_per_step": int(bytes_step), "parallelism": f"replicas x{ws}"},
+        "kernels": kinfo, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": len(kernels) * a.steps,
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ the reference arm
+def run_reference(a, ws, rank):
+    """The oracle, as it stands, on this machine's host cores: each step is a bounded
+    sample of the same workload, reported in the same unit."""
+    if rank != 0:
+        return
+    for _ in range(a.warmup):
+        cpu_sample(2.5)
+    tot_b, tot_t = 0, 0.0
+    desc = ""
+    for _ in range(a.steps):
+        nb, dt, desc = cpu_sample(2.5)
+        tot_b += nb
+        tot_t += dt
+    v = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "achieved HBM GB/s (% of GB300 peak) for fused group, softmax region, AdamW params/s",
+        "value": round(v, 6), "unit": "GB/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(tot_t / a.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "64-node group bf16 [8192,8192] + softmax region bf16 [32768,4096] "
+                               "(sequential, interleaved(8)) + AdamW tree of a Llama-style 1.1B model"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    a = _args()
+    ws, rank, local = _dist()
+    if a.impl == "reference":
+        run_reference(a, ws, rank)
+    else:
+        run_ours(a, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/* psk.h -- C ABI of the fusion-group hot path on one GB300 (sm_103a).
+ *
+ * Three entry points run the three cases of a fusion group on the caller's
+ * CUDA stream:
+ *
+ *   psk_group_run       a connected chain of up to 64 elementwise nodes sharing
+ *                       one loop nest, with broadcast inputs
+ *                       (PSK-Realize, "What a group is");
+ *   psk_softmax_region  the reduction-rooted row region Reduce(Max) -> Sub ->
+ *                       Exp -> Reduce(Sum) -> Div with a declared summation
+ *                       order (poot "Fusion and Planning", Reduction-rooted
+ *                       regions; presk "Native execution", the realization's
+ *                       order);
+ *   psk_adamw_tree      the AdamW step as one parameter-tree group over every
+ *                       leaf of a model, in one launch (PSK-Realize, Parameter
+ *                       trees; presk "The language", The optimizer).
+ *
+ * Conventions for every call:
+ * - Pointers named ptr/x/y/theta/m/v/grad are DEVICE pointers owned by the
+ *   caller; descriptor structs and arrays of them are HOST memory, read during
+ *   the call only.  The library allocates no device memory and keeps no state
+ *   across calls besides cached device attributes.
+ * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *   stream).  Return 0 means the work was enqueued.
+ * - A negative return is a refusal: nothing was launched, and
+ *   psk_last_error() (thread-local) names the argument, node or leaf at fault.
+ *   Malformed input is refused, never ignored or silently repaired.
+ * - Arithmetic is IEEE binary32 with no contraction: every node of a group is
+ *   rounded once to f32 and only the root is rounded to its storage type; exp
+ *   and erf nodes are correctly rounded.  bf16 is storage only: a shift on
+ *   the way in, one round to nearest even on the way out.
+ */
+#ifndef PSK_H
+#define PSK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ errors */
+#define PSK_OK 0
+#define PSK_E_PROGRAM (-1)        /* malformed node program */
+#define PSK_E_TOO_MANY_NODES (-2) /* more than 64 op nodes: not one group */
+#define PSK_E_SHAPE (-3)          /* shape, stride or size out of range */
+#define PSK_E_DTYPE (-4)          /* unknown storage type */
+#define PSK_E_NULL (-5)           /* a required pointer is NULL */
+#define PSK_E_ORDER (-6)          /* unknown summation order or parameter */
+#define PSK_E_CUDA (-7)           /* the CUDA runtime refused the launch */
+#define PSK_E_ALIAS (-8)          /* output overlaps an input in a way that races */
+#define PSK_E_ARG (-9)            /* any other argument out of range */
+
+/* ------------------------------------------------------- storage types */
+typedef enum { PSK_F32 = 0, PSK_BF16 = 1 } psk_dtype;
+
+/* ======================================================== psk_group_run
+ * Program format (postfix; one uint32 token per item; opcode in bits 31..24,
+ * argument in bits 23..0).  Operand tokens push a value, op tokens pop their
+ * operands and push a node (a binary op pops b then a and computes a OP b):
+ *   IN k   input k            IMM k  immediate k         REF k  op node k's value
+ *   ADD SUB MUL DIV           IEEE binary32, one rounding each
+ *   MAX MIN                   max(a,b) = a > b ? a : b, min(a,b) = a < b ? a : b
+ *                             (a tie, and NaN, give the second operand)
+ *   NEG ABS                   sign flip / sign clear
+ *   EXP ERF                   correctly rounded exp / erf
+ *   EXPC                      exp(min(max(a, -4), 4))
+ *   GELU                      a * (0.5 * (1 + erf(a * RN(1/sqrt 2))))
+ *   SQRT SQRTA                sqrt(a) / sqrt(|a|), IEEE
+ * A valid program has 1..64 op nodes (the cap at which a group stops
+ * growing, PSK-Realize "What a group is"), at most 1024 tokens, REFs only to
+ * nodes already computed, operands in range, and leaves exactly one value (the
+ * root) on the stack. */
+#define PSK_OP_IN 0x01
+#define PSK_OP_IMM 0x02
+#define PSK_OP_REF 0x03
+#define PSK_OP_ADD 0x10
+#define PSK_OP_SUB 0x11
+#define PSK_OP_MUL 0x12
+#define PSK_OP_DIV 0x13
+#define PSK_OP_MAX 0x14
+#define PSK_OP_MIN 0x15
+#define PSK_OP_NEG 0x20
+#define PSK_OP_ABS 0x21
+#define PSK_OP_EXP 0x22
+#define PSK_OP_EXPC 0x23
+#define PSK_OP_GELU 0x24
+#define PSK_OP_SQRT 0x25
+#define PSK_OP_SQRTA 0x26
+#define PSK_OP_ERF 0x27
+#define PSK_MAX_NODES 64
+#define PSK_MAX_TOKENS 1024
+#define PSK_MAX_INPUTS 16
+#define PSK_MAX_IMM 64
+#define PSK_MAX_RANK 4
+
+typedef struct {
+  const uint32_t* tokens; /* host array of n_tokens tokens */
+  int32_t n_tokens;
+  const float* imm;       /* host array of n_imm f32 immediates (may be NULL if 0) */
+  int32_t n_imm;
+} psk_program;
+
+/* An input read through element strides, one per OUTPUT axis (the output's
+ * rank): output element (i0, .., i_{r-1}) reads ptr[sum_k i_k * stride[k]].
+ * A stride of 0 broadcasts along that axis (a row vector [C] into [R, C] is
+ * stride {0, 1}; a column [R, 1] is {1, 0}; a scalar is {0, 0}).  Strides are
+ * in elements and must be >= 0. */
+typedef struct {
+  const void* ptr;
+  int32_t dtype;              /* psk_dtype */
+  int64_t stride[PSK_MAX_RANK];
+} psk_input;
+
+/* The root's storage: contiguous row-major, rank 0..4 (rank 0 = one element). */
+typedef struct {
+  void* ptr;
+  int32_t dtype;              /* psk_dtype */
+  int32_t rank;
+  int64_t shape[PSK_MAX_RANK];
+} psk_output;
+
+/* Evaluate the group over every output element, in one launch (several for
+ * more than 2^31 vectors of elements).  The output may alias an input only
+ * if that input has exactly the output's layout (same pointer, dtype and
+ * row-major strides): each element is then read before it is written.  Any
+ * other overlap is refused with PSK_E_ALIAS when the pointers show it. */
+int psk_group_run(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
+                  const psk_output* out, void* stream);
+
+/* Host-only check of a program (no launch, no device needed): returns 0 and
+ * the number of op nodes and of per-thread value slots the kernel will use,
+ * or the refusal psk_group_run would give. */
+int psk_group_check(const psk_program* prog, int32_t n_inputs, int32_t* n_nodes, int32_t* n_slots);
+
+/* ================================================== psk_softmax_region
+ * y[r, :] = softmax(x[r, :]) over rows of `cols` elements: m = max_j x[r,j]
+ * (NaN propagates), e_j = exp(x[r,j] - m), s = the sum of e_j in the declared
+ * order, y = RN(e_j / s) (IEEE division) rounded to yt.  Orders:
+ *   SEQUENTIAL       s = (((e0 + e1) + e2) + ...)
+ *   BLOCKED(w)       the same chain (register blocking keeps index order), w >= 1
+ *   INTERLEAVED(P)   partial p sums e_j, j = p mod P, in increasing j; the P
+ *                    partials are then added left to right; 1 <= P <= 64
+ *                    (INTERLEAVED(1) is SEQUENTIAL).
+ * exp_mode EXACT uses the correctly rounded exp (bit-identical to a group's EXP
+ * node); FAST uses a faithful exp (at most one f32 ulp from it), a declared
+ * realization that owes its measured gap.  x and y are row-major with leading
+ * dimensions ldx, ldy >= cols (elements); y must not overlap x unless y == x
+ * with the same dtype and leading dimension (in place).  rows or cols == 0 is
+ * an empty region (nothing launched, returns 0). */
+typedef enum { PSK_ORDER_SEQUENTIAL = 0, PSK_ORDER_BLOCKED = 1, PSK_ORDER_INTERLEAVED = 2 } psk_order_kind;
+typedef struct { int32_t kind; int32_t param; } psk_order;
+typedef enum { PSK_EXP_EXACT = 0, PSK_EXP_FAST = 1 } psk_exp_mode;
+
+int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
+                       int64_t ldx, int64_t ldy, psk_order order, int32_t exp_mode, void* stream);
+
+/* ====================================================== psk_adamw_tree
+ * One AdamW step over every leaf, in place, one launch for the whole tree
+ * (trees of more than PSK_ADAMW_MAX_LEAVES leaves take one launch per that
+ * many leaves).  Per parameter, in f32, one rounding per operation:
+ *   m' = (b1 m) + ((1-b1) g);  v' = (b2 v) + ((1-b2) (g g))
+ *   m^ = m' / (1-b1^t);  v^ = v' / (1-b2^t)
+ *   theta' = theta - lr ((m^ / (sqrt(v^) + eps)) + wd theta)
+ * The scalars b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd are computed
+ * from the binary64 hyperparameters on the host and rounded once to f32
+ * (psk_adamw_scalars returns them).  theta, m, v are f32; grad is f32 or bf16
+ * (widened exactly).  t >= 1; 0 < beta < 1; leaves must not overlap. */
+#define PSK_ADAMW_MAX_LEAVES 512
+typedef struct {
+  float* theta;
+  float* m;
+  float* v;
+  const void* grad;
+  int32_t grad_dtype;   /* psk_dtype */
+  int64_t numel;        /* >= 0; 0 skips the leaf */
+} psk_leaf;
+typedef struct { double lr, beta1, beta2, eps, weight_decay; int64_t t; } psk_adamw_hparams;
+
+int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp, void* stream);
+
+/* Host-only: the nine f32 scalars the step reads, in the order
+ * b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd. */
+int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]);
+
+/* Thread-local description of the last refusal of this thread ("" if none). */
+const char* psk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSK_H */

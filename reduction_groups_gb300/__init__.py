@@ -1,0 +1,15 @@
+"""Fusion groups on one GB300: a chain of up to 64 elementwise nodes in one
+loop nest, the reduction-rooted softmax region, and the AdamW step over a
+parameter tree, each one CUDA launch through a C ABI (include/psk.h).
+
+    from reduction_groups_gb300 import psk_group_run, psk_softmax_region, psk_adamw_tree
+"""
+
+from .ops import (  # noqa: F401
+    psk_adamw_scalars,
+    psk_adamw_tree,
+    psk_group_check,
+    psk_group_run,
+    psk_softmax_region,
+)
+from ._native import PskError  # noqa: F401

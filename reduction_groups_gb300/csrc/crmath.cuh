@@ -1,0 +1,385 @@
+// Correctly rounded binary32 exp and erf for the group and softmax kernels.
+//
+// An exp or erf node of a fusion group returns RN_f32(exp(x)) / RN_f32(erf(x))
+// (nearest, ties to even, gradual underflow, overflow to infinity).  The pages
+// ask that every executor compute the same transcendental bits ("Native
+// execution", The Cranelift backend: one libm for all executors); a correctly
+// rounded function has one value, so any correct implementation gives it.
+//
+// Each function has three tiers (Ziv's strategy: evaluate with an error bound,
+// keep the result when the bound decides the rounding, else retry more
+// accurately):
+//   1. binary32 float-float arithmetic, relative error below 2^-40; the result
+//      is kept when it lies more than the error bound away from every rounding
+//      boundary (one call in about 2^15 fails the test);
+//   2. binary64, relative error below 2^-50, kept unless within 2^-48 of a
+//      boundary (one call in about 2^25 of the calls reaching it);
+//   3. double-double Taylor series, error below 2^-95.
+// Tier 1 is all that runs in practice; tiers 2 and 3 are separate functions.
+//
+// The same source compiles as CUDA device code (the library) and as plain C++
+// for the host (a test build that checks the tiers element by element).
+
+#pragma once
+
+#include <stdint.h>
+#include <math.h>
+#include <string.h>
+
+#if defined(PSK_HOST_BUILD)
+#define PSK_HD static inline
+#define PSK_NOINLINE static
+#define PSK_TAB static const
+#else
+#define PSK_HD __device__ __forceinline__
+#define PSK_NOINLINE static __device__ __noinline__
+#define PSK_TAB static __constant__ const
+#endif
+
+#include "crmath_tables.inc"
+
+namespace psk {
+
+// ------------------------------------------------------------ bit helpers
+PSK_HD uint32_t f2u(float f) {
+#if defined(PSK_HOST_BUILD)
+  uint32_t u; memcpy(&u, &f, 4); return u;
+#else
+  return __float_as_uint(f);
+#endif
+}
+PSK_HD float u2f(uint32_t u) {
+#if defined(PSK_HOST_BUILD)
+  float f; memcpy(&f, &u, 4); return f;
+#else
+  return __uint_as_float(u);
+#endif
+}
+PSK_HD float d2f_rn(double d) {
+#if defined(PSK_HOST_BUILD)
+  return (float)d;
+#else
+  return __double2float_rn(d);
+#endif
+}
+
+// ------------------------------------------------- error-free transforms
+// (Knuth's TwoSum, Dekker's Fast2Sum, and the product error by fma.)
+PSK_HD void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+PSK_HD void fast_two_sum(float a, float b, float& s, float& e) {  // |a| >= |b| or a == 0
+  s = a + b;
+  e = b - (s - a);
+}
+PSK_HD void two_prod(float a, float b, float& p, float& e) {
+  p = a * b;
+  e = fmaf(a, b, -p);
+}
+PSK_HD void two_sum_d(double a, double b, double& s, double& e) {
+  s = a + b;
+  double bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+PSK_HD void fast_two_sum_d(double a, double b, double& s, double& e) {
+  s = a + b;
+  e = b - (s - a);
+}
+
+// double-double value hi + lo, |lo| <= ulp(hi)/2
+struct dd { double hi, lo; };
+
+PSK_HD dd dd_add(dd a, dd b) {
+  double s, e, t, f;
+  two_sum_d(a.hi, b.hi, s, e);
+  two_sum_d(a.lo, b.lo, t, f);
+  e += t;
+  fast_two_sum_d(s, e, s, e);
+  e += f;
+  fast_two_sum_d(s, e, s, e);
+  return dd{s, e};
+}
+PSK_HD dd dd_mul(dd a, dd b) {
+  double p = a.hi * b.hi;
+  double e = fma(a.hi, b.hi, -p);
+  e = fma(a.hi, b.lo, e);
+  e = fma(a.lo, b.hi, e);
+  double s;
+  fast_two_sum_d(p, e, s, e);
+  return dd{s, e};
+}
+PSK_HD dd dd_div_d(dd a, double b) {  // a / b, b a small exact value
+  double q1 = a.hi / b;
+  double p = q1 * b;
+  double pe = fma(q1, b, -p);
+  double r = ((a.hi - p) - pe) + a.lo;
+  double q2 = r / b;
+  double s, e;
+  fast_two_sum_d(q1, q2, s, e);
+  return dd{s, e};
+}
+
+// ------------------------------------------------------------ rounding
+// RN_f32 of a binary64 value y known to within rel*|y|; ok = false when the
+// interval of possible exact values reaches a binary32 rounding boundary.
+PSK_HD float round_checked(double y, double rel, bool& ok) {
+  float r = d2f_rn(y);
+  double ay = fabs(y);
+  float ar = fabsf(r);
+  double a = (double)ar, up, dn;
+  if (isinf(ar)) {
+    a = 0x1p128;
+    dn = 0x1.fffffep127;
+    up = 0x1p129;
+  } else {
+    up = (ar == 0x1.fffffep127f) ? 0x1p128 : (double)nextafterf(ar, INFINITY);
+    dn = (ar == 0.0f) ? -0x1p-149 : (double)nextafterf(ar, 0.0f);
+  }
+  double tol = rel * ay;
+  ok = (fabs(ay - 0.5 * (a + up)) > tol) && (fabs(ay - 0.5 * (a + dn)) > tol);
+  return r;
+}
+
+// RN_f32 of the double-double value hi + lo (|lo| <= ulp(hi)/2).  Rounding hi
+// alone is right unless hi is exactly halfway between two binary32 values;
+// then the sign of lo says on which side the exact value lies.
+PSK_HD float dd_to_f32(dd v) {
+  double A = fabs(v.hi);
+  double L = (v.hi < 0) ? -v.lo : v.lo;     // exact magnitude is A + L
+  float r = d2f_rn(A);
+  if ((double)r == A) return copysignf(r, (float)v.hi);
+  double below, above;                       // binary32 neighbours around A
+  if (isinf(r)) {
+    below = 0x1.fffffep127; above = 0x1p128;
+  } else if ((double)r > A) {
+    above = (double)r; below = (r == 0.0f) ? 0.0 : (double)nextafterf(r, 0.0f);
+  } else {
+    below = (double)r;
+    above = (r == 0x1.fffffep127f) ? 0x1p128 : (double)nextafterf(r, INFINITY);
+  }
+  double mid = 0.5 * (below + above);
+  float out = r;
+  if (A == mid && L != 0.0) out = (L > 0) ? (above >= 0x1p128 ? INFINITY : (float)above) : (float)below;
+  return copysignf(out, (float)v.hi);
+}
+
+// ====================================================================== exp
+
+// Tier 3: double-double.  exp(x) = 2^k exp(r), r = x - k ln2, Taylor to 2^-106.
+PSK_NOINLINE float exp_tier3(float xf) {
+  const dd LN2 = {PSK_DD_LN2_HI, PSK_DD_LN2_LO};
+  double x = (double)xf;
+  double k = rint(x * PSK_DD_INV_LN2);
+  dd kl = dd_mul(LN2, dd{k, 0.0});
+  dd r = dd_add(dd{x, 0.0}, dd{-kl.hi, -kl.lo});
+  dd term = {1.0, 0.0}, sum = {1.0, 0.0};
+  for (int n = 1; n < 40; ++n) {
+    term = dd_div_d(dd_mul(term, r), (double)n);
+    sum = dd_add(sum, term);
+    if (fabs(term.hi) < 0x1p-110 * fabs(sum.hi)) break;
+  }
+  int ki = (int)k;
+  return dd_to_f32(dd{ldexp(sum.hi, ki), ldexp(sum.lo, ki)});
+}
+
+// Tier 2: binary64, table 2^(j/32) and a degree-6 polynomial on |r| <= ln2/64.
+PSK_NOINLINE float exp_tier2(float xf) {
+  if (isnan(xf)) return xf + xf;
+  if (xf > 89.0f) return INFINITY;
+  if (xf < -104.0f) return 0.0f;
+  double x = (double)xf;
+  double kd = rint(x * PSK_EXP_INV_LD);
+  int k = (int)kd;
+  double r = fma(-kd, PSK_EXP_L1D, x);  // exact
+  r = fma(-kd, PSK_EXP_L2D, r);
+  double p = 1.0 / 720.0;
+  p = fma(p, r, 1.0 / 120.0);
+  p = fma(p, r, 1.0 / 24.0);
+  p = fma(p, r, 1.0 / 6.0);
+  p = fma(p, r, 0.5);
+  p = fma(p, r * r, r);                 // e^r - 1
+  int j = k & 31, n = k >> 5;
+  double T = psk_exp_tab_d[j];
+  double y = ldexp(fma(T, p, T), n);
+  bool ok;
+  float res = round_checked(y, 0x1p-48, ok);
+  return ok ? res : exp_tier3(xf);
+}
+
+// Tier 1 core, |x| <= 87 (normal results).  thi/tlo: 2^(j/32) as float
+// pairs.  Returns R (the nearest float to the approximation) and d, with
+// exp(x) = (R + d) 2^n (1 + delta), |delta| < 2^-42.
+PSK_HD void exp_tier1_core(float x, const float* thi, const float* tlo, float& R, float& d, int& n) {
+  float kf = rintf(x * PSK_EXP_INV_L);
+  int k = (int)kf;
+  int j = k & 31;
+  n = k >> 5;
+  // r = x - k ln2/32 as rh + rl (Cody-Waite, three pieces; the first two
+  // products are exact and x - k L1 is exact by Sterbenz's lemma)
+  float r1 = fmaf(-kf, PSK_EXP_L1, x);
+  float p2 = kf * PSK_EXP_L2;
+  float p3 = kf * PSK_EXP_L3;
+  float ph, pl;
+  fast_two_sum(-p2, -p3, ph, pl);
+  float rh, rl;
+  two_sum(r1, ph, rh, rl);
+  rl = rl + pl;
+  float Th = thi[j], Tl = tlo[j];
+  // e^r - 1 = rh + rh^2/2 + C,  C = rl (1 + rh + rh^2/2) + (rh^2 - s)/2 + rh^3 (1/6 + rh/24 + rh^2/120)
+  float s, se;
+  two_prod(rh, rh, s, se);
+  float B = 0.5f * s;
+  float q3 = fmaf(fmaf(rh, 1.0f / 120.0f, 1.0f / 24.0f), rh, 1.0f / 6.0f);
+  float C = fmaf(rl, rh + B, rl);
+  C = fmaf(0.5f, se, C);
+  C = fmaf(s * rh, q3, C);
+  // y = Th + Th rh + Th B + [Th C + Tl (1 + rh + B)]
+  float m1, e1, m2, e2;
+  two_prod(Th, rh, m1, e1);
+  two_prod(Th, B, m2, e2);
+  float low = fmaf(Th, C, Tl);
+  low = fmaf(Tl, rh + B, low);
+  low = low + (e1 + e2);
+  float h1, l1, h2, l2;
+  fast_two_sum(Th, m1, h1, l1);
+  fast_two_sum(h1, m2, h2, l2);
+  float lo = (l1 + l2) + low;
+  R = h2 + lo;
+  d = lo - (R - h2);
+}
+
+// Keep R when |d| plus the error bound stays below half an ulp of R (R not a
+// power of two, whose lower neighbour is nearer).  With a relative error
+// below 2^-40 this decides the rounding of the exact value.
+PSK_HD bool tier1_decided(float R, float d) {
+  uint32_t rb = f2u(R);
+  float hu = u2f((rb & 0x7f800000u) - (24u << 23));
+  return ((rb & 0x007fffffu) != 0u) && (fabsf(d) <= hu * 0.99996948f);
+}
+
+PSK_HD bool exp_tier1(float x, const float* thi, const float* tlo, float& out) {
+  float R, d;
+  int n;
+  exp_tier1_core(x, thi, tlo, R, d, n);
+  out = u2f((uint32_t)((int32_t)f2u(R) + n * (1 << 23)));
+  return tier1_decided(R, d);
+}
+
+// Correctly rounded exp; thi/tlo point at the 2^(j/32) float-pair table
+// (shared memory in kernels).
+PSK_HD float exp_cr(float x, const float* thi, const float* tlo) {
+  float r;
+  if (fabsf(x) <= 87.0f && exp_tier1(x, thi, tlo, r)) return r;
+  return exp_tier2(x);
+}
+
+// ====================================================================== erf
+
+// Tier 3: Maclaurin series in double-double (|a| < 4), error below 2^-95.
+PSK_NOINLINE float erf_tier3(float af) {
+  double a = (double)af;
+  dd a2 = dd_mul(dd{a, 0.0}, dd{a, 0.0});
+  dd term = {a, 0.0};      // a^(2n+1) / n!
+  dd sum = {a, 0.0};
+  for (int n = 1; n < 200; ++n) {
+    term = dd_div_d(dd_mul(term, a2), (double)n);
+    dd t = dd_div_d(term, (double)(2 * n + 1));
+    if (n & 1) t = dd{-t.hi, -t.lo};
+    sum = dd_add(sum, t);
+    if (fabs(t.hi) < 0x1p-112 * fabs(sum.hi)) break;
+  }
+  return dd_to_f32(dd_mul(sum, dd{PSK_DD_TWO_OVER_SQRTPI_HI, PSK_DD_TWO_OVER_SQRTPI_LO}));
+}
+
+// Tier 2: binary64 Taylor polynomials of degree 12 about i/8.  a = |x|.
+PSK_NOINLINE float erf_tier2(float af) {
+  double a = (double)af, y;
+  if (af < 0x1p-60f) {
+    y = PSK_TWO_OVER_SQRTPI_D * a;
+  } else {
+    int i = (int)rint(a * 8.0);
+    double t = a - 0.125 * i;
+    y = psk_erf_c64[PSK_ERF_D64][i];
+    for (int k = PSK_ERF_D64 - 1; k >= 0; --k) y = fma(y, t, psk_erf_c64[k][i]);
+  }
+  bool ok;
+  float res = round_checked(y, 0x1p-48, ok);
+  return ok ? res : erf_tier3(af);
+}
+
+// Tier 1 core, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375).  chi: [10][32]
+// coefficient table (hi parts), clo: [5][32] low parts of coefficients 0..4
+// (shared memory in kernels).  erf(a) = (R + d)(1 + delta), |delta| < 2^-42.
+PSK_HD void erf_tier1_core(float a, const float* chi, const float* clo, float& R, float& d) {
+  int i = (int)rintf(a * 8.0f);
+  float t = a - (float)i * 0.125f;   // exact
+  float H = chi[9 * 32 + i];
+  H = fmaf(H, t, chi[8 * 32 + i]);
+  H = fmaf(H, t, chi[7 * 32 + i]);
+  H = fmaf(H, t, chi[6 * 32 + i]);
+  H = fmaf(H, t, chi[5 * 32 + i]);
+  // V4 = c4 + t H as a normalised pair; then V_k = c_k + t V_{k+1}, k = 3..0,
+  // each product exact (two_prod) and each sum renormalised (Fast2Sum)
+  float p, pe, vh, vl;
+  two_prod(t, H, p, pe);
+  fast_two_sum(chi[4 * 32 + i], p, vh, vl);
+  vl = vl + (pe + clo[4 * 32 + i]);
+#pragma unroll
+  for (int k = 3; k >= 0; --k) {
+    two_prod(t, vh, p, pe);
+    pe = fmaf(t, vl, pe);
+    float ch = chi[k * 32 + i], cl = clo[k * 32 + i];
+    fast_two_sum(ch, p, vh, vl);
+    vl = vl + (pe + cl);
+  }
+  R = vh + vl;
+  d = vl - (R - vh);
+}
+
+PSK_HD bool erf_tier1(float a, const float* chi, const float* clo, float& out) {
+  float d;
+  erf_tier1_core(a, chi, clo, out, d);
+  return tier1_decided(out, d);
+}
+
+// Correctly rounded erf (odd; erf(+-0) = +-0, erf(+-inf) = +-1, NaN stays NaN).
+PSK_HD float erf_cr(float x, const float* chi, const float* clo) {
+  float a = fabsf(x);
+  if (!(a == a)) return x + x;
+  float r;
+  if (a < PSK_ERF_ONE_FROM && a >= 0x1p-60f) {
+    if (!erf_tier1(a, chi, clo, r)) r = erf_tier2(a);
+  } else if (a >= PSK_ERF_ONE_FROM) {
+    r = 1.0f;                          // erfc(a) < 2^-25 from here on: rounds to 1
+  } else {
+    r = (a == 0.0f) ? 0.0f : erf_tier2(a);
+  }
+  return copysignf(r, x);
+}
+
+// ============================================ exp, fast faithful variant
+// Used only where a realization declares the fast exp (the softmax region's
+// fast mode): Cody-Waite reduction to |r| <= ln2/2 and a degree-7 Taylor
+// polynomial; error at most one ulp, not correctly rounded.
+PSK_HD float exp_faithful(float x) {
+  float kf = rintf(x * PSK_FEXP_INV_LN2);
+  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);         // exact: ln2 hi carries 16 bits
+  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int k = (int)kf;
+  if (k > 127) return (x == x) ? INFINITY : x;
+  if (k < -149 - 24) return 0.0f;
+  if (k >= -125) return p * u2f((uint32_t)(k + 127) << 23);
+  return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
+}
+
+}  // namespace psk

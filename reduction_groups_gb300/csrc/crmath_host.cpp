@@ -1,0 +1,58 @@
+// Host build of the device exp / erf (crmath.cuh compiled as plain C++), for
+// tests that check every tier element by element on the CPU.  Not part of the
+// library's compute path: the kernels run the CUDA build of the same source.
+
+#define PSK_HOST_BUILD 1
+#include "crmath.cuh"
+
+using namespace psk;
+
+extern "C" {
+
+// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful
+void psk_host_unary(int which, const float* x, float* y, long n) {
+  for (long i = 0; i < n; ++i) {
+    switch (which) {
+      case 0: y[i] = exp_cr(x[i], psk_exp_tab_hi, psk_exp_tab_lo); break;
+      case 1: y[i] = erf_cr(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0]); break;
+      default: y[i] = exp_faithful(x[i]); break;
+    }
+  }
+}
+
+// Tier-by-tier: tier 1 with its decision flag (inputs must be in its range),
+// tiers 2 and 3 on their own.  which: 0 exp, 1 erf.
+void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char* ok, long n) {
+  for (long i = 0; i < n; ++i) {
+    float r = 0.0f;
+    bool k = true;
+    if (tier == 1) {
+      k = which == 0 ? exp_tier1(x[i], psk_exp_tab_hi, psk_exp_tab_lo, r)
+                     : erf_tier1(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0], r);
+    } else if (tier == 2) {
+      r = which == 0 ? exp_tier2(x[i]) : erf_tier2(x[i]);
+    } else {
+      r = which == 0 ? exp_tier3(x[i]) : erf_tier3(x[i]);
+    }
+    y[i] = r;
+    if (ok) ok[i] = k ? 1 : 0;
+  }
+}
+
+// Tier-1 approximations before rounding, as binary64 (R + d) 2^n, to
+// measure their error against a reference.  which: 0 exp, 1 erf.
+void psk_host_tier1_value(int which, const float* x, double* y, long n) {
+  for (long i = 0; i < n; ++i) {
+    float R, d;
+    if (which == 0) {
+      int e;
+      exp_tier1_core(x[i], psk_exp_tab_hi, psk_exp_tab_lo, R, d, e);
+      y[i] = ldexp((double)R + (double)d, e);
+    } else {
+      erf_tier1_core(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0], R, d);
+      y[i] = (double)R + (double)d;
+    }
+  }
+}
+
+}  // extern "C"

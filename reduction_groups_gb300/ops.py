@@ -1,0 +1,120 @@
+"""Python binding of the C ABI with the same names: psk_group_run,
+psk_softmax_region, psk_adamw_tree (plus the host-only psk_group_check and
+psk_adamw_scalars).  Each function marshals torch tensors (device memory and
+the current stream) or plain host arrays into the C structs and calls the
+library; every step of the hot path runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _native as N
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return N.PSK_F32
+    if t.dtype == torch.bfloat16:
+        return N.PSK_BF16
+    raise TypeError(f"storage type {t.dtype} is not f32 or bf16")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _program(tokens, imm):
+    toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.uint32).reshape(-1))
+    ims = np.ascontiguousarray(np.asarray(imm if imm is not None else [], dtype=np.float32).reshape(-1))
+    p = N.psk_program()
+    p.tokens = toks.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
+    p.n_tokens = int(toks.size)
+    p.imm = ims.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) if ims.size else None
+    p.n_imm = int(ims.size)
+    return p, (toks, ims)
+
+
+def psk_group_check(tokens, n_inputs: int, imm=None):
+    """Validate a program on the host; returns (n_nodes, n_slots)."""
+    p, keep = _program(tokens, imm)
+    nn, ns = ctypes.c_int32(0), ctypes.c_int32(0)
+    N.check(N.lib().psk_group_check(ctypes.byref(p), int(n_inputs), ctypes.byref(nn), ctypes.byref(ns)))
+    return nn.value, ns.value
+
+
+def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
+    """inputs: list of (tensor, strides) with one element stride per output axis
+    (0 = broadcast); out: a contiguous row-major tensor (f32 or bf16)."""
+    p, keep = _program(tokens, imm)
+    n = len(inputs)
+    arr = (N.psk_input * max(n, 1))()
+    for i, (t, strides) in enumerate(inputs):
+        arr[i].ptr = t.data_ptr()
+        arr[i].dtype = _dtype_code(t)
+        st = list(strides) + [0] * (N.PSK_MAX_RANK - len(strides))
+        for k in range(N.PSK_MAX_RANK):
+            arr[i].stride[k] = int(st[k])
+    if not out.is_contiguous():
+        raise ValueError("the output must be contiguous (row-major)")
+    o = N.psk_output()
+    o.ptr = out.data_ptr()
+    o.dtype = _dtype_code(out)
+    o.rank = out.dim()
+    for k, s in enumerate(out.shape):
+        o.shape[k] = int(s)
+    N.check(N.lib().psk_group_run(ctypes.byref(p), arr, n, ctypes.byref(o), _stream_handle(stream)))
+
+
+_ORDER = {"sequential": N.PSK_ORDER_SEQUENTIAL, "blocked": N.PSK_ORDER_BLOCKED,
+          "interleaved": N.PSK_ORDER_INTERLEAVED}
+
+
+def psk_softmax_region(x, y, order=("sequential",), exp_mode: str = "exact", stream=None) -> None:
+    """Row softmax of the 2-D tensor x into y (same shape; row strides may
+    exceed the row length).  order: ("sequential",), ("blocked", w) or
+    ("interleaved", P); exp_mode: "exact" (correctly rounded) or "fast"."""
+    if x.dim() != 2 or y.dim() != 2 or tuple(x.shape) != tuple(y.shape):
+        raise ValueError("x and y must be 2-D tensors of one shape")
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    o = N.psk_order(_ORDER[order[0]], int(order[1]) if len(order) > 1 else 0)
+    em = {"exact": N.PSK_EXP_EXACT, "fast": N.PSK_EXP_FAST}[exp_mode]
+    rows, cols = x.shape
+    N.check(N.lib().psk_softmax_region(x.data_ptr(), _dtype_code(x), y.data_ptr(), _dtype_code(y), rows, cols,
+                                       max(x.stride(0), cols), max(y.stride(0), cols), o, em, _stream_handle(stream)))
+
+
+def _hparams(hp) -> N.psk_adamw_hparams:
+    h = N.psk_adamw_hparams()
+    h.lr, h.beta1, h.beta2 = float(hp.lr), float(hp.beta1), float(hp.beta2)
+    h.eps, h.weight_decay, h.t = float(hp.eps), float(hp.weight_decay), int(hp.t)
+    return h
+
+
+def psk_adamw_scalars(hp):
+    """The nine f32 scalars the step reads (b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd)."""
+    h = _hparams(hp)
+    out = (ctypes.c_float * 9)()
+    N.check(N.lib().psk_adamw_scalars(ctypes.byref(h), out))
+    return np.array(list(out), dtype=np.float32)
+
+
+def psk_adamw_tree(leaves, hp, stream=None) -> None:
+    """leaves: list of (theta, m, v, grad) tensors, updated in place."""
+    n = len(leaves)
+    arr = (N.psk_leaf * max(n, 1))()
+    for i, (th, m, v, g) in enumerate(leaves):
+        arr[i].theta, arr[i].m, arr[i].v, arr[i].grad = th.data_ptr(), m.data_ptr(), v.data_ptr(), g.data_ptr()
+        arr[i].grad_dtype = _dtype_code(g)
+        arr[i].numel = int(th.numel())
+    h = _hparams(hp)
+    N.check(N.lib().psk_adamw_tree(arr, n, ctypes.byref(h), _stream_handle(stream)))

@@ -1,0 +1,145 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every entry point include/psk.h declares, validates programs exactly as the
+oracle's definition does, and injects the AdamW scalars the oracle computes."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.adamw as OA
+import oracle.group as OG
+from synth import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    from reduction_groups_gb300 import build as B
+
+    B.build()
+    from reduction_groups_gb300 import _native as N
+
+    return N
+
+
+def test_library_exports_every_declared_symbol(native):
+    header = open(os.path.join(ROOT, "include", "psk.h")).read()
+    declared = set(re.findall(r"^\s*(?:int|const char\*)\s+(psk_\w+)\s*\(", header, re.M))
+    assert declared == set(native.EXPORTS)
+    L = native.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_opcodes_agree_across_header_oracle_and_inputs():
+    header = open(os.path.join(ROOT, "include", "psk.h")).read()
+    hdr = {k: int(v, 16) for k, v in re.findall(r"#define PSK_OP_(\w+) (0x[0-9a-fA-F]+)", header)}
+    assert hdr == OG.OP
+    assert hdr == W.OPCODES
+
+
+def _rand_program(rng, n_in, n_imm, valid=True):
+    ops_b = ["ADD", "SUB", "MUL", "DIV", "MAX", "MIN"]
+    ops_u = ["NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF"]
+    seq, depth, nodes = [], 0, 0
+    n_ops = int(rng.integers(1, 70))
+    while nodes < n_ops:
+        r = rng.random()
+        if depth < 2 or r < 0.35:
+            kind = rng.choice(["IN", "IMM", "REF"] if nodes else ["IN", "IMM"])
+            if kind == "IN":
+                seq.append(("IN", int(rng.integers(0, n_in))))
+            elif kind == "IMM" and n_imm:
+                seq.append(("IMM", int(rng.integers(0, n_imm))))
+            elif kind == "REF":
+                seq.append(("REF", int(rng.integers(0, nodes))))
+            else:
+                continue
+            depth += 1
+        elif r < 0.6:
+            seq.append((str(rng.choice(ops_u)),))
+            nodes += 1
+        else:
+            seq.append((str(rng.choice(ops_b)),))
+            depth -= 1
+            nodes += 1
+    while depth > 1:
+        seq.append(("ADD",))
+        depth -= 1
+        nodes += 1
+    if not valid:
+        k = int(rng.integers(0, 5))
+        if k == 0:
+            seq.append(("ADD",))                      # underflow
+        elif k == 1:
+            seq.insert(0, ("IN", n_in))               # input out of range
+        elif k == 2:
+            seq.append(("IN", 0))                     # two values left
+        elif k == 3:
+            seq.insert(1, ("REF", 99))                # REF ahead
+        else:
+            seq += [("NEG",)] * 70                    # past the cap
+    return W.encode(seq)
+
+
+def test_program_check_matches_oracle_definition(native):
+    from reduction_groups_gb300 import ops
+
+    rng = np.random.default_rng(12)
+    for trial in range(600):
+        valid = trial % 3 != 0
+        toks = _rand_program(rng, 3, 2, valid)
+        imm = np.array([1.5, -2.0], dtype=np.float32)
+        try:
+            prog = OG.decode(toks, 3, 2)
+            want = ("ok", sum(1 for n, _ in prog if n not in ("IN", "IMM", "REF")))
+        except OG.ProgramError:
+            want = ("refused", None)
+        try:
+            nn, ns = ops.psk_group_check(toks, 3, imm)
+            got = ("ok", nn)
+            assert ns >= 3
+        except native.PskError as e:
+            assert e.name in ("PSK_E_PROGRAM", "PSK_E_TOO_MANY_NODES")
+            got = ("refused", None)
+        assert got == want, (toks, got, want)
+
+
+def test_refusals_name_the_fault(native):
+    from reduction_groups_gb300 import ops
+
+    with pytest.raises(native.PskError) as e:
+        ops.psk_group_check(W.encode([("IN", 0)] + [("NEG",)] * 65), 1)
+    assert e.value.name == "PSK_E_TOO_MANY_NODES" and "cap" in str(e.value)
+    with pytest.raises(native.PskError) as e:
+        ops.psk_group_check(np.array([0x7F000000], dtype=np.uint32), 1)
+    assert e.value.name == "PSK_E_PROGRAM" and "opcode" in str(e.value)
+    with pytest.raises(native.PskError):
+        ops.psk_group_check(W.encode([("IN", 0), ("NEG",)]), 17)
+
+
+def test_adamw_scalars_equal_oracle_injection(native):
+    from reduction_groups_gb300 import ops
+
+    rng = np.random.default_rng(3)
+    ts = list(range(1, 3001)) + [int(t) for t in rng.integers(3001, 1_000_001, 400)] + [1_000_000]
+    for beta1, beta2 in ((0.9, 0.999), (0.8, 0.95), (0.99, 0.9999), (0.3, 0.7)):
+        for t in ts if beta1 == 0.9 else ts[::10]:
+            hp = W.AdamWHyper(lr=3e-4, beta1=beta1, beta2=beta2, eps=1e-8, weight_decay=0.01, t=t)
+            got = ops.psk_adamw_scalars(hp)
+            h = OA.hyper_f32(hp.lr, beta1, beta2, hp.eps, hp.weight_decay, t)
+            want = np.array([h[k] for k in ("b1", "b2", "omb1", "omb2", "bc1", "bc2", "lr", "eps", "wd")],
+                            dtype=np.float32)
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (beta1, beta2, t, got, want)
+
+
+def test_adamw_scalars_refuse_bad_hyperparameters(native):
+    from reduction_groups_gb300 import ops
+
+    for bad in (dict(t=0), dict(beta1=1.0), dict(beta2=0.0), dict(lr=float("nan"))):
+        hp = W.AdamWHyper(**bad)
+        with pytest.raises(native.PskError):
+            ops.psk_adamw_scalars(hp)

@@ -1,0 +1,111 @@
+"""The device exp/erf source, compiled for the host, against the oracle.
+
+The library's kernels run the CUDA build of csrc/crmath.cuh; the same source
+compiled as plain C++ (libpsk_hostmath.so) lets the CPU check every tier
+element by element: tier 1's decision never keeps a wrong rounding, tiers 2
+and 3 are correctly rounded on their own, and the composed functions equal the
+oracle's correctly rounded exp and erf bit for bit.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+import pytest
+
+from oracle.crmath import erf_f32, exp_f32
+from tests.exact import same_bits
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hm():
+    from reduction_groups_gb300 import build as B
+
+    B.build()
+    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
+    P = ctypes.c_void_p
+
+    def unary(which, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty_like(x)
+        L.psk_host_unary(ctypes.c_int(which), P(x.ctypes.data), P(y.ctypes.data), ctypes.c_long(x.size))
+        return y
+
+    def tier(which, t, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty_like(x)
+        ok = np.empty(x.shape, dtype=np.uint8)
+        L.psk_host_tier(ctypes.c_int(which), ctypes.c_int(t), P(x.ctypes.data), P(y.ctypes.data),
+                        P(ok.ctypes.data), ctypes.c_long(x.size))
+        return y, ok.astype(bool)
+
+    return unary, tier
+
+
+def _all_binades(lo, hi, per, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for e in range(lo, hi + 1):
+        m = rng.integers(0, 2 ** 23, per, dtype=np.uint64).astype(np.uint32)
+        v = ((np.uint32(e + 127) << np.uint32(23)) | m).view(np.float32)
+        out += [v, -v]
+    return np.concatenate(out)
+
+
+def _specials():
+    return np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 88.72283935546875, 88.7228317,
+                     -87.33654, -103.97208, -103.97207, -104.0, 87.0, -87.0, 3.9192059, 3.9192057, 3.9375,
+                     2 ** -60, 2 ** -61, 1.0, -1.0], dtype=np.float32)
+
+
+def test_exp_composed_equals_oracle(hm):
+    unary, _ = hm
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(-110, 95, 1_500_000).astype(np.float32), _all_binades(-149 + 23, 7, 2000, 2),
+                        _specials()])
+    assert same_bits(unary(0, x), exp_f32(x))
+
+
+def test_erf_composed_equals_oracle(hm):
+    unary, _ = hm
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-4.5, 4.5, 1_500_000).astype(np.float32), _all_binades(-126, 2, 2000, 4),
+                        _specials()])
+    assert same_bits(unary(1, x), erf_f32(x))
+
+
+def test_tier1_keeps_only_correct_roundings(hm):
+    _, tier = hm
+    rng = np.random.default_rng(5)
+    x = rng.uniform(-87, 87, 2_000_000).astype(np.float32)
+    y, ok = tier(0, 1, x)
+    assert same_bits(y[ok], exp_f32(x[ok]))
+    assert 1 - ok.mean() < 2.0 ** -12          # about one call in 2^15 falls through
+    a = rng.uniform(2.0 ** -60, 3.919, 2_000_000).astype(np.float32)
+    y, ok = tier(1, 1, a)
+    assert same_bits(y[ok], erf_f32(a[ok]))
+    assert 1 - ok.mean() < 2.0 ** -12
+
+
+@pytest.mark.parametrize("t", [2, 3])
+def test_tiers_2_and_3_correctly_rounded_alone(hm, t):
+    _, tier = hm
+    rng = np.random.default_rng(7 + t)
+    xe = np.concatenate([rng.uniform(-104, 89, 30000).astype(np.float32), _specials()[5:18]])
+    y, _ = tier(0, t, xe)
+    assert same_bits(y, exp_f32(xe))
+    xr = np.concatenate([rng.uniform(0, 3.9375, 30000).astype(np.float32),
+                         np.array([1e-30, 3e-20, 2 ** -61], dtype=np.float32)])
+    y, _ = tier(1, t, xr)
+    assert same_bits(y, erf_f32(xr))
+
+
+def test_fast_exp_within_one_ulp(hm):
+    unary, _ = hm
+    rng = np.random.default_rng(11)
+    x = rng.uniform(-87, 0, 1_000_000).astype(np.float32)
+    y, ref = unary(2, x), exp_f32(x)
+    d = np.abs(y.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert d.max() <= 1

@@ -1,0 +1,375 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+The bar: bit for bit for every exact-op group, every exp/erf/gelu group (the
+transcendental nodes are correctly rounded on both sides), the AdamW tree and
+the softmax region with exact exp; the softmax region with the declared fast
+exp within one bf16 ulp (two f32 ulp) of the oracle, its measured gap printed.
+bf16 results compare as bit patterns, any NaN equal to any NaN.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.adamw as OA
+import oracle.group as OG
+import oracle.softmax as OS
+from oracle.f32 import bf16_to_f32, f32_to_bf16
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import reduction_groups_gb300 as R
+
+    return R
+
+
+def _to_dev(a, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _to_host(t):
+    if t.dtype == torch.bfloat16:
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _as_f32(a, dtype):
+    return bf16_to_f32(a) if dtype == "bf16" else np.asarray(a, dtype=np.float32)
+
+
+def _same(a, b, dtype):
+    x, y = _as_f32(a, dtype), _as_f32(b, dtype)
+    both_nan = np.isnan(x) & np.isnan(y)
+    return (x.view(np.uint32) == y.view(np.uint32)) | both_nan
+
+
+def _run_group(R, wl, inputs_host, out_shape=None):
+    out_shape = out_shape or wl.out_shape
+    dts = [dt for _, dt in inputs_host]
+    dins = [(_to_dev(a, dt), spec.strides) for (a, dt), spec in zip(inputs_host, wl.inputs)]
+    out = torch.empty(out_shape, dtype=torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32, device="cuda")
+    out.fill_(float("nan"))     # poisoned: every element must be written
+    R.psk_group_run(wl.tokens, wl.imm, dins, out)
+    torch.cuda.synchronize()
+    return _to_host(out)
+
+
+def _oracle_group(wl, inputs_host):
+    ins = [(a, dt, spec.strides) for (a, dt), spec in zip(inputs_host, wl.inputs)]
+    return OG.evaluate(wl.tokens, wl.imm, ins, wl.out_shape, wl.out_dtype)
+
+
+# ------------------------------------------------------------------ groups
+
+def test_small_group_bitwise(dev):
+    wl = W.small_group()
+    ins = wl.host_inputs()
+    got, want = _run_group(dev, wl, ins), _oracle_group(wl, ins)
+    assert _same(got, want, "f32").all()
+
+
+@pytest.mark.parametrize("shape", [(96, 200), (37, 53), (1, 4), (3, 1), (130, 1024)])
+def test_cap_group_bitwise(dev, shape):
+    wl = W.cap_group(*shape)
+    ins = wl.host_inputs()
+    got, want = _run_group(dev, wl, ins), _oracle_group(wl, ins)
+    ok = _same(got, want, "bf16")
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} differ"
+
+
+def _special_values(n, rng):
+    base = rng.standard_normal(n).astype(np.float32) * np.float32(3)
+    sp = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-40, 3e38, -3e38, 88.8, -104.0, 4.0, -4.0,
+                   3.9192, 1.0, -1.0], dtype=np.float32)
+    base[: len(sp)] = sp
+    return base
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_programs_all_ops_bitwise(dev, seed):
+    rng = np.random.default_rng(100 + seed)
+    ops_b = ["ADD", "SUB", "MUL", "DIV", "MAX", "MIN"]
+    ops_u = ["NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF"]
+    R_, C_ = 33, 64
+    seq = [("IN", 0)]
+    n_ops = int(rng.integers(8, 64))
+    nodes = 0
+    for i in range(n_ops):
+        if nodes >= 62:
+            break
+        r = rng.random()
+        if r < 0.45:
+            c = int(rng.integers(0, 3 + 1 + i))
+            if c < 3:
+                seq.append(("IN", c))
+            elif c == 3 or c - 4 >= nodes:
+                seq.append(("IMM", int(rng.integers(0, 2))))
+            else:
+                seq.append(("REF", c - 4))
+            seq.append((str(rng.choice(ops_b)),))
+            nodes += 1
+        elif r < 0.55 and i > 2:
+            # a subtree on the other side: push two operands, combine, then combine with acc
+            seq += [("IN", int(rng.integers(0, 3))), ("IN", int(rng.integers(0, 3))), (str(rng.choice(ops_b)),),
+                    (str(rng.choice(ops_b)),)]
+            nodes += 2
+        else:
+            seq.append((str(rng.choice(ops_u)),))
+            nodes += 1
+    toks = W.encode(seq)
+    n_nodes = len(OG.decode(toks, 3, 2)) - sum(1 for s in seq if s[0] in ("IN", "IMM", "REF"))
+    assert n_nodes <= 64
+    imm = np.array([0.5, -1.25], dtype=np.float32)
+    x = _special_values(R_ * C_, rng).reshape(R_, C_)
+    rowv = (rng.standard_normal(C_) * 2).astype(np.float32)
+    col = (rng.standard_normal(R_) * 2).astype(np.float32)
+    inputs = [(x, "f32", (C_, 1)), (rowv, "f32", (0, 1)), (col, "f32", (1, 0))]
+    want = OG.evaluate(toks, imm, inputs, (R_, C_), "f32")
+    out = torch.empty((R_, C_), dtype=torch.float32, device="cuda")
+    dev.psk_group_run(toks, imm, [(_to_dev(a, dt), st) for a, dt, st in inputs], out)
+    torch.cuda.synchronize()
+    ok = _same(_to_host(out), want, "f32")
+    assert ok.all(), f"{(~ok).sum()} differ"
+
+
+@pytest.mark.parametrize("op", ["EXP", "ERF", "GELU", "EXPC", "SQRT"])
+def test_unary_node_over_many_inputs(dev, op):
+    rng = np.random.default_rng(7)
+    n = 1 << 22
+    if op in ("EXP", "EXPC"):
+        x = rng.uniform(-105, 90, n).astype(np.float32)
+    elif op in ("ERF", "GELU"):
+        x = rng.uniform(-6, 6, n).astype(np.float32)
+    else:
+        x = rng.standard_normal(n).astype(np.float32)
+    bits = rng.integers(0, 2 ** 32, n // 4, dtype=np.uint64).astype(np.uint32)
+    x[: n // 4] = bits.view(np.float32)       # every binade, NaN and inf included
+    x[: 16] = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 88.72283935546875, 88.7228317,
+                        -103.97208, 3.9192059, 2 ** -60, 2 ** -61, 87.0, -87.0, 1.0], dtype=np.float32)
+    toks = W.encode([("IN", 0), (op,)])
+    inputs = [(x, "f32", (1,))]
+    want = OG.evaluate(toks, [], inputs, (n,), "f32")
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    dev.psk_group_run(toks, [], [(_to_dev(x, "f32"), (1,))], out)
+    torch.cuda.synchronize()
+    ok = _same(_to_host(out), want, "f32")
+    assert ok.all(), f"{(~ok).sum()} differ, e.g. x={x[~ok][:5]}"
+
+
+def test_rank4_broadcast_and_gather_layouts(dev):
+    rng = np.random.default_rng(9)
+    shape = (3, 5, 7, 12)
+    a = rng.standard_normal(shape).astype(np.float32)
+    b = rng.standard_normal((5, 1, 12)).astype(np.float32)           # broadcast over axes 0 and 2
+    big = rng.standard_normal((3, 5, 7, 24)).astype(np.float32)      # read every other element
+    toks = W.encode([("IN", 0), ("IN", 1), ("MUL",), ("IN", 2), ("SUB",), ("GELU",), ("IN", 1), ("MAX",)])
+    sa = (5 * 7 * 12, 7 * 12, 12, 1)
+    sb = (0, 12, 0, 1)
+    sg = (5 * 7 * 24, 7 * 24, 24, 2)
+    inputs = [(a, "f32", sa), (b, "f32", sb), (big, "f32", sg)]
+    want = OG.evaluate(toks, [], inputs, shape, "bf16")
+    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    dev.psk_group_run(toks, [], [(_to_dev(x, dt), st) for x, dt, st in inputs], out)
+    torch.cuda.synchronize()
+    assert _same(_to_host(out), want, "bf16").all()
+
+
+def test_unaligned_inputs_take_the_scalar_path(dev):
+    wl = W.small_group(16, 64)
+    ins = wl.host_inputs()
+    want = _oracle_group(wl, ins)
+    dins = []
+    for (a, dt), spec in zip(ins, wl.inputs):
+        flat = np.concatenate([np.zeros(1, np.float32), np.asarray(a, np.float32).reshape(-1)])
+        t = _to_dev(flat, dt)[1:]            # 4-byte offset: not 16-byte aligned
+        dins.append((t, spec.strides))
+    out = torch.empty(wl.out_shape, dtype=torch.float32, device="cuda")
+    dev.psk_group_run(wl.tokens, wl.imm, dins, out)
+    torch.cuda.synchronize()
+    assert _same(_to_host(out), want, "f32").all()
+
+
+def test_in_place_and_refused_overlap(dev):
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((64, 64)).astype(np.float32)
+    toks = W.encode([("IN", 0), ("EXP",), ("IN", 0), ("ADD",)])
+    want = OG.evaluate(toks, [], [(x, "f32", (64, 1))], (64, 64), "f32")
+    t = _to_dev(x, "f32")
+    dev.psk_group_run(toks, [], [(t, (64, 1))], t)           # y = x in place
+    torch.cuda.synchronize()
+    assert _same(_to_host(t), want, "f32").all()
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_group_run(toks, [], [(t, (1, 64))], t)       # transposed read of the output
+    assert e.value.name == "PSK_E_ALIAS"
+
+
+def test_empty_output_launches_nothing(dev):
+    toks = W.encode([("IN", 0), ("NEG",)])
+    out = torch.empty((0, 16), dtype=torch.float32, device="cuda")
+    dev.psk_group_run(toks, [], [(torch.empty(16, device="cuda"), (0, 1))], out)
+
+
+def test_cap_group_full_size_sampled_rows(dev):
+    """The 64-node workload at its full size [8192, 8192], launched as the
+    benchmark launches it; sampled rows against the oracle."""
+    wl = W.cap_group()
+    dins = wl.device_inputs()
+    out = torch.empty(wl.out_shape, dtype=torch.bfloat16, device="cuda")
+    dev.psk_group_run(wl.tokens, wl.imm, [(t, s.strides) for t, s in zip(dins, wl.inputs)], out)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 4095, 4096, 8190, 8191] + list(np.random.default_rng(1).integers(0, 8192, 10)))
+    x = _to_host(dins[0][torch.from_numpy(rows).cuda()])
+    rowv = _to_host(dins[1])
+    col = _to_host(dins[2]).reshape(-1)[rows]
+    sc = _to_host(dins[3]).reshape(1)
+    ins = [(x, "bf16", (8192, 1)), (rowv, "bf16", (0, 1)), (col, "bf16", (1, 0)), (sc, "bf16", (0, 0))]
+    want = OG.evaluate(wl.tokens, wl.imm, ins, (len(rows), 8192), "bf16")
+    got = _to_host(out[torch.from_numpy(rows).cuda()])
+    ok = _same(got, want, "bf16")
+    assert ok.all(), f"{(~ok).sum()} differ"
+
+
+# ----------------------------------------------------------------- softmax
+
+ORDERS = [("sequential",), ("blocked", 16), ("interleaved", 8), ("interleaved", 3), ("interleaved", 1)]
+
+
+@pytest.mark.parametrize("order", ORDERS)
+@pytest.mark.parametrize("shape", [(64, 4096), (37, 999), (5, 10000), (8, 64), (3, 1)])
+def test_softmax_exact_bitwise(dev, order, shape):
+    wl = W.softmax_rows(*shape)
+    x = wl.host_x()
+    want = OS.softmax_region(x, "bf16", "bf16", order)
+    xd = _to_dev(x, "bf16")
+    y = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    dev.psk_softmax_region(xd, y, order, "exact")
+    torch.cuda.synchronize()
+    ok = _same(_to_host(y), want, "bf16")
+    assert ok.all(), f"{(~ok).sum()} differ"
+
+
+def test_softmax_f32_io_in_place_and_nan(dev):
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((20, 520)) * 4).astype(np.float32)
+    x[3, 7] = np.nan
+    x[5, :] = -np.inf
+    for order in (("sequential",), ("interleaved", 8)):
+        want = OS.softmax_region(x, "f32", "f32", order)
+        t = _to_dev(x, "f32")
+        dev.psk_softmax_region(t, t, order, "exact")
+        torch.cuda.synchronize()
+        assert _same(_to_host(t), want, "f32").all()
+
+
+@pytest.mark.parametrize("order", [("sequential",), ("interleaved", 8)])
+def test_softmax_fast_exp_within_tolerance(dev, order):
+    wl = W.softmax_rows(256, 4096)
+    x = wl.host_x()
+    want = OS.softmax_region(x, "bf16", "f32", order)
+    y = torch.empty((256, 4096), dtype=torch.float32, device="cuda")
+    dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, "fast")
+    torch.cuda.synchronize()
+    got = _to_host(y)
+    ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
+    print(f"fast exp gap, order {order}: max {ulps.max()} f32 ulp, {np.mean(ulps > 0):.4f} of outputs differ")
+    assert ulps.max() <= 2
+    gb = f32_to_bf16(got)
+    wb = f32_to_bf16(want)
+    assert np.max(np.abs(gb.astype(np.int32) - wb.astype(np.int32))) <= 1
+
+
+def test_softmax_refusals(dev):
+    x = torch.zeros((4, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_softmax_region(x, x.clone(), ("interleaved", 0))
+    assert e.value.name == "PSK_E_ORDER"
+    with pytest.raises(dev.PskError):
+        dev.psk_softmax_region(x, x.clone(), ("interleaved", 65))
+
+
+@pytest.mark.parametrize("order", [("sequential",), ("interleaved", 8)])
+def test_softmax_full_size_sampled_rows(dev, order):
+    wl = W.softmax_rows()
+    x = wl.device_x()
+    y = torch.empty_like(x)
+    dev.psk_softmax_region(x, y, order, "exact")
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 16383, 32767] + list(np.random.default_rng(2).integers(0, 32768, 12)))
+    idx = torch.from_numpy(rows).cuda()
+    want = OS.softmax_region(_to_host(x[idx]), "bf16", "bf16", order)
+    assert _same(_to_host(y[idx]), want, "bf16").all()
+
+
+# ------------------------------------------------------------------- AdamW
+
+def _tree_on_device(tree):
+    return [tuple(_to_dev(a, tree.grad_dtype if k == 3 else "f32") for k, a in enumerate(tree.host_leaf(i)))
+            for i in range(len(tree.leaves))]
+
+
+def test_adamw_small_gpt_tree_bitwise(dev):
+    tree = W.gpt_adamw_leaves()
+    host = [tree.host_leaf(i) for i in range(len(tree.leaves))]
+    want = OA.step_tree(host, tree.grad_dtype, tree.hp)
+    leaves = _tree_on_device(tree)
+    dev.psk_adamw_tree(leaves, tree.hp)
+    torch.cuda.synchronize()
+    for (th, m, v, g), (wt, wm, wv) in zip(leaves, want):
+        assert np.array_equal(_to_host(th).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v).view(np.uint32), wv.view(np.uint32))
+
+
+def test_adamw_unaligned_ragged_bf16_leaves(dev):
+    rng = np.random.default_rng(5)
+    hp = W.AdamWHyper(lr=1e-3, t=3)
+    sizes = [1, 3, 4095, 4097, 10007, 64]
+    host, leaves = [], []
+    for n in sizes:
+        th = (rng.standard_normal(n + 1) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n + 1) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n + 1) * 1e-4).astype(np.float32)
+        g = f32_to_bf16((rng.standard_normal(n + 1) * 1e-3).astype(np.float32))
+        host.append((th[1:], m[1:], v[1:], g[1:]))
+        leaves.append(tuple(_to_dev(a, "bf16" if k == 3 else "f32")[1:] for k, a in enumerate((th, m, v, g))))
+    want = OA.step_tree(host, "bf16", hp)
+    dev.psk_adamw_tree(leaves, hp)
+    torch.cuda.synchronize()
+    for (th, m, v, g), (wt, wm, wv) in zip(leaves, want):
+        assert np.array_equal(_to_host(th).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v).view(np.uint32), wv.view(np.uint32))
+
+
+def test_adamw_llama_tree_full_size_sampled(dev):
+    """The 1.1B-parameter tree in one launch, as the benchmark runs it; every
+    parameter of the small leaves and 65,536 sampled ones (plus both ends) of
+    each large leaf against the oracle."""
+    tree = W.llama_adamw_leaves()
+    leaves = [tree.device_leaf(i) for i in range(len(tree.leaves))]
+    rng = np.random.default_rng(8)
+    picks, before = [], []
+    for (th, m, v, g) in leaves:
+        n = th.numel()
+        idx = np.arange(n) if n <= 65536 else np.unique(np.concatenate(
+            [np.arange(4), np.arange(n - 4, n), rng.integers(0, n, 65536)]))
+        it = torch.from_numpy(idx).cuda()
+        picks.append(it)
+        before.append(tuple(_to_host(a[it]) for a in (th, m, v, g)))
+    h = OA.hyper_f32(tree.hp.lr, tree.hp.beta1, tree.hp.beta2, tree.hp.eps, tree.hp.weight_decay, tree.hp.t)
+    dev.psk_adamw_tree(leaves, tree.hp)
+    torch.cuda.synchronize()
+    for (th, m, v, g), it, (bt, bm, bv, bg) in zip(leaves, picks, before):
+        wt, wm, wv = OA.step_leaf(bt, bm, bv, bg, "bf16", h)
+        assert np.array_equal(_to_host(th[it]).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m[it]).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v[it]).view(np.uint32), wv.view(np.uint32))
