@@ -272,16 +272,22 @@ def test_softmax_f32_io_in_place_and_nan(dev):
 
 @pytest.mark.parametrize("order", [("sequential",), ("interleaved", 8)])
 def test_softmax_fast_exp_within_tolerance(dev, order):
+    """The fast exp is within one f32 ulp of the correctly rounded one; through
+    the row sum and the division the f32 outputs stay within 1e-6 relative of
+    the oracle (the tolerance stated for reassociated softmax sums) and the
+    bf16 outputs within one bf16 ulp.  The measured gap is printed."""
     wl = W.softmax_rows(256, 4096)
     x = wl.host_x()
-    want = OS.softmax_region(x, "bf16", "f32", order)
+    want, _, ws = OS.softmax_region(x, "bf16", "f32", order, return_stats=True)
     y = torch.empty((256, 4096), dtype=torch.float32, device="cuda")
     dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, "fast")
     torch.cuda.synchronize()
     got = _to_host(y)
     ulps = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
-    print(f"fast exp gap, order {order}: max {ulps.max()} f32 ulp, {np.mean(ulps > 0):.4f} of outputs differ")
-    assert ulps.max() <= 2
+    rel = np.abs(got.astype(np.float64) - want) / np.maximum(np.abs(want.astype(np.float64)), 1e-38)
+    print(f"fast exp gap, order {order}: max {ulps.max()} f32 ulp, max rel {rel.max():.3g}, "
+          f"{np.mean(ulps > 0):.4f} of outputs differ")
+    assert rel.max() <= 1e-6
     gb = f32_to_bf16(got)
     wb = f32_to_bf16(want)
     assert np.max(np.abs(gb.astype(np.int32) - wb.astype(np.int32))) <= 1
