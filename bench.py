@@ -43,6 +43,10 @@ def _args():
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
     p.add_argument("--softmax-exp", choices=["exact", "fast"], default="exact")
+    p.add_argument("--only", choices=["all", "group", "softmax", "adamw"], default="all",
+                   help="time one case only (profiling captures)")
+    p.add_argument("--scale", type=float, default=1.0,
+                   help="shrink the group rows, softmax rows and model layers (profiling captures only)")
     return p.parse_args()
 
 
@@ -193,42 +197,39 @@ def run_ours(a, ws, rank, local):
     from synth import workloads as W
 
     # workloads (drawn on the device; seeds shared, so every rank has the same data)
-    wl = W.cap_group()
+    sc = a.scale
+    wl = W.cap_group(rows=max(1, int(8192 * sc)))
     g_in = wl.device_inputs()
     g_args = [(t, s.strides) for t, s in zip(g_in, wl.inputs)]
     g_out = torch.empty(wl.out_shape, dtype=torch.bfloat16, device="cuda")
-    sw = W.softmax_rows()
+    sw = W.softmax_rows(rows=max(1, int(32768 * sc)))
     sx = sw.device_x()
     sy = torch.empty_like(sx)
-    tree = W.llama_adamw_leaves()
+    tree = W.llama_adamw_leaves(layers=max(1, int(round(22 * sc))))
     leaves = [tree.device_leaf(i) for i in range(len(tree.leaves))]
     torch.cuda.synchronize()
 
     b_group = wl.algorithmic_bytes()
     b_soft = sw.algorithmic_bytes()
     b_adam = tree.n_params * tree.bytes_per_param()
-    bytes_step = b_group + 2 * b_soft + b_adam
     em = a.softmax_exp
-    kernels = ["group", "softmax_sequential", "softmax_interleaved8", "adamw"]
+    launches = {
+        "group": lambda: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out),
+        "softmax_sequential": lambda: R.psk_softmax_region(sx, sy, ("sequential",), em),
+        "softmax_interleaved8": lambda: R.psk_softmax_region(sx, sy, ("interleaved", 8), em),
+        "adamw": lambda: R.psk_adamw_tree(leaves, tree.hp),
+    }
+    kernels = [k for k in launches if a.only == "all" or k.startswith(a.only)]
+    b_all = {"group": b_group, "softmax_sequential": b_soft, "softmax_interleaved8": b_soft, "adamw": b_adam}
+    bytes_step = sum(b_all[k] for k in kernels)
 
     def step(ev=None):
-        if ev is not None:
-            ev[0][0].record()
-        R.psk_group_run(wl.tokens, wl.imm, g_args, g_out)
-        if ev is not None:
-            ev[0][1].record()
-            ev[1][0].record()
-        R.psk_softmax_region(sx, sy, ("sequential",), em)
-        if ev is not None:
-            ev[1][1].record()
-            ev[2][0].record()
-        R.psk_softmax_region(sx, sy, ("interleaved", 8), em)
-        if ev is not None:
-            ev[2][1].record()
-            ev[3][0].record()
-        R.psk_adamw_tree(leaves, tree.hp)
-        if ev is not None:
-            ev[3][1].record()
+        for j, k in enumerate(kernels):
+            if ev is not None:
+                ev[j][0].record()
+            launches[k]()
+            if ev is not None:
+                ev[j][1].record()
 
     for _ in range(a.warmup):
         step()
@@ -267,7 +268,7 @@ def run_ours(a, ws, rank, local):
     # end to end through the public API with host buffers: per step, copy every
     # input from pinned host memory, run the step, read every result back
     e2e = None
-    if not a.no_e2e:
+    if not a.no_e2e and a.only == "all":
         host_g = [t.cpu().pin_memory() for t in g_in]
         host_gout = torch.empty(g_out.shape, dtype=g_out.dtype, pin_memory=True)
         host_sx = sx.cpu().pin_memory()
@@ -329,11 +330,14 @@ def run_ours(a, ws, rank, local):
         gbs = kb[k] / (per_kernel_ms[k] / 1e3) / 1e9
         kinfo[k] = {"ms": round(per_kernel_ms[k], 4), "algorithmic_bytes": int(kb[k]), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4)}
-    kinfo["group"]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (per_kernel_ms["group"] / 1e3), 1)
-    kinfo["group"]["node_evals_per_s"] = round(kinfo["group"]["elems_per_s"] * wl.n_ops, 1)
+    if "group" in kinfo:
+        kinfo["group"]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (per_kernel_ms["group"] / 1e3), 1)
+        kinfo["group"]["node_evals_per_s"] = round(kinfo["group"]["elems_per_s"] * wl.n_ops, 1)
     for k in ("softmax_sequential", "softmax_interleaved8"):
-        kinfo[k]["rows_per_s"] = round(sw.rows / (per_kernel_ms[k] / 1e3), 1)
-    kinfo["adamw"]["params_per_s"] = round(tree.n_params / (per_kernel_ms["adamw"] / 1e3), 1)
+        if k in kinfo:
+            kinfo[k]["rows_per_s"] = round(sw.rows / (per_kernel_ms[k] / 1e3), 1)
+    if "adamw" in kinfo:
+        kinfo["adamw"]["params_per_s"] = round(tree.n_params / (per_kernel_ms["adamw"] / 1e3), 1)
     dom = max(kernels, key=lambda k: per_kernel_ms[k])
     achieved = kb[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
@@ -341,7 +345,7 @@ def run_ours(a, ws, rank, local):
                 "traffic": _dram_traffic(dom)}
 
     cpu = None
-    if not a.no_cpu and ws == 1:
+    if not a.no_cpu and ws == 1 and a.only == "all":
         nb, dt, desc = cpu_sample(15.0)
         cpu = {"value": round(nb / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": desc + f"; {dt:.1f} s of one host core (numpy ufuncs run single-threaded)"}
@@ -359,6 +363,8 @@ def run_ours(a, ws, rank, local):
         "kernels": kinfo, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": len(kernels) * a.steps,
     }
+    if a.only != "all" or a.scale != 1.0:
+        line["config"]["partial"] = f"only={a.only} scale={a.scale}: a profiling run, not the benchmark"
     print(json.dumps(line))
     if ws > 1:
         import torch.distributed as dist

@@ -359,6 +359,18 @@ PSK_HD float erf_cr(float x, const float* chi, const float* clo) {
   return copysignf(r, x);
 }
 
+// ================================================ division by a fixed b
+// a / b correctly rounded from rb = RN(1/b), for |a| >= 2^-100, 1 <= b < 2^20
+// (Markstein's correction: q = RN(a rb) is within an ulp of a/b, the residual
+// r = a - b q is exact by fma, and RN(q + r rb) is the correctly rounded
+// quotient).  Other operands go to IEEE division.
+PSK_HD float div_by_recip(float a, float b, float rb) {
+  if (!(fabsf(a) >= 0x1p-100f) || !(b >= 1.0f && b < 0x1p20f) || isinf(a)) return a / b;
+  float q = a * rb;
+  float r = fmaf(-q, b, a);
+  return fmaf(r, rb, q);
+}
+
 // ============================================ exp, fast faithful variant
 // Used only where a realization declares the fast exp (the softmax region's
 // fast mode): Cody-Waite reduction to |r| <= ln2/2 and a degree-7 Taylor

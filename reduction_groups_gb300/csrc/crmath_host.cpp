@@ -55,4 +55,25 @@ void psk_host_tier1_value(int which, const float* x, double* y, long n) {
   }
 }
 
+// Division through the reciprocal against IEEE division, n random pairs
+// drawn with a 64-bit LCG; returns the number of differing results.
+long psk_host_div_check(unsigned long seed, long n, float a_lo_exp, float a_hi_exp, float b_hi) {
+  unsigned long s = seed * 6364136223846793005ul + 1442695040888963407ul;
+  long bad = 0;
+  for (long i = 0; i < n; ++i) {
+    s = s * 6364136223846793005ul + 1442695040888963407ul;
+    uint32_t u1 = (uint32_t)(s >> 32);
+    s = s * 6364136223846793005ul + 1442695040888963407ul;
+    uint32_t u2 = (uint32_t)(s >> 32);
+    // a: random sign-free mantissa and exponent in [a_lo_exp, a_hi_exp); b in [1, b_hi)
+    float fa = ldexpf(1.0f + (float)(u1 & 0x7fffff) * 0x1p-23f,
+                      (int)(a_lo_exp + (a_hi_exp - a_lo_exp) * ((u1 >> 23) / 512.0f)));
+    float fb = 1.0f + (b_hi - 1.0f) * ((float)(u2 >> 8) * 0x1p-24f);
+    volatile float ieee = fa / fb;
+    float rb = 1.0f / fb;
+    if (div_by_recip(fa, fb, rb) != ieee) ++bad;
+  }
+  return bad;
+}
+
 }  // extern "C"

@@ -109,3 +109,17 @@ def test_fast_exp_within_one_ulp(hm):
     y, ref = unary(2, x), exp_f32(x)
     d = np.abs(y.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
     assert d.max() <= 1
+
+
+def test_division_through_reciprocal_equals_ieee():
+    """The softmax divides by the row sum through its reciprocal with
+    Markstein's correction; on the operand ranges it accepts the result equals
+    IEEE division (others fall back to it)."""
+    from reduction_groups_gb300 import build as B
+
+    B.build()
+    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
+    L.psk_host_div_check.restype = ctypes.c_long
+    L.psk_host_div_check.argtypes = [ctypes.c_ulong, ctypes.c_long, ctypes.c_float, ctypes.c_float, ctypes.c_float]
+    for seed, lo, hi, bmax in ((1, -100, 1, 4097.0), (2, -126, 1, 1e6), (3, -100, 100, 2.0 ** 20), (4, -30, 1, 3.0)):
+        assert L.psk_host_div_check(seed, 5_000_000, lo, hi, bmax) == 0
