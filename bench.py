@@ -42,7 +42,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
-    p.add_argument("--softmax-exp", choices=["exact", "fast"], default="exact")
+    p.add_argument("--softmax-exp", choices=["exact", "fast"], default="fast",
+                   help="exp of the softmax region inside the step (the other mode is timed beside it)")
     p.add_argument("--only", choices=["all", "group", "softmax", "adamw"], default="all",
                    help="time one case only (profiling captures)")
     p.add_argument("--scale", type=float, default=1.0,
@@ -265,6 +266,21 @@ def run_ours(a, ws, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
 
+    # the softmax region in the other exp mode, timed beside the step (not in value)
+    other = "exact" if em == "fast" else "fast"
+    extra_ms = {}
+    if "softmax_sequential" in kernels:
+        for name, order in (("softmax_sequential", ("sequential",)), ("softmax_interleaved8", ("interleaved", 8))):
+            for _ in range(2):
+                R.psk_softmax_region(sx, sy, order, other)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(a.steps):
+                R.psk_softmax_region(sx, sy, order, other)
+            e1.record()
+            torch.cuda.synchronize()
+            extra_ms[f"{name}_{other}_exp"] = e0.elapsed_time(e1) / a.steps
+
     # end to end through the public API with host buffers: per step, copy every
     # input from pinned host memory, run the step, read every result back
     e2e = None
@@ -330,6 +346,11 @@ def run_ours(a, ws, rank, local):
         gbs = kb[k] / (per_kernel_ms[k] / 1e3) / 1e9
         kinfo[k] = {"ms": round(per_kernel_ms[k], 4), "algorithmic_bytes": int(kb[k]), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4)}
+    for k, ms in extra_ms.items():
+        gbs = b_soft / (ms / 1e3) / 1e9
+        kinfo[k] = {"ms": round(ms, 4), "algorithmic_bytes": int(b_soft), "gbs": round(gbs, 1),
+                    "frac_of_hbm_peak": round(gbs / peak, 4), "in_value": False,
+                    "rows_per_s": round(sw.rows / (ms / 1e3), 1)}
     if "group" in kinfo:
         kinfo["group"]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (per_kernel_ms["group"] / 1e3), 1)
         kinfo["group"]["node_evals_per_s"] = round(kinfo["group"]["elems_per_s"] * wl.n_ops, 1)

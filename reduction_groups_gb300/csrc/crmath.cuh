@@ -344,18 +344,21 @@ PSK_HD bool erf_tier1(float a, const float* chi, const float* clo, float& out) {
   return tier1_decided(out, d);
 }
 
+// erf of |x| outside tier 1's reach or undecided by it: NaN, 0, tiny
+// arguments and undecided ones by tier 2, saturation at 1.
+PSK_NOINLINE float erf_abs_rest(float a) {
+  if (!(a == a)) return a + a;
+  if (a >= PSK_ERF_ONE_FROM) return 1.0f;   // erfc(a) < 2^-25 from here on: rounds to 1
+  if (a == 0.0f) return 0.0f;
+  return erf_tier2(a);
+}
+
 // Correctly rounded erf (odd; erf(+-0) = +-0, erf(+-inf) = +-1, NaN stays NaN).
 PSK_HD float erf_cr(float x, const float* chi, const float* clo) {
-  float a = fabsf(x);
-  if (!(a == a)) return x + x;
+  const float a = fabsf(x);
+  const bool inr = a < PSK_ERF_ONE_FROM && a >= 0x1p-60f;
   float r;
-  if (a < PSK_ERF_ONE_FROM && a >= 0x1p-60f) {
-    if (!erf_tier1(a, chi, clo, r)) r = erf_tier2(a);
-  } else if (a >= PSK_ERF_ONE_FROM) {
-    r = 1.0f;                          // erfc(a) < 2^-25 from here on: rounds to 1
-  } else {
-    r = (a == 0.0f) ? 0.0f : erf_tier2(a);
-  }
+  if (!(inr && erf_tier1(a, chi, clo, r))) r = erf_abs_rest(a);
   return copysignf(r, x);
 }
 
@@ -391,6 +394,27 @@ PSK_HD float exp_faithful(float x) {
   if (k > 127) return (x == x) ? INFINITY : x;
   if (k < -149 - 24) return 0.0f;
   if (k >= -125) return p * u2f((uint32_t)(k + 127) << 23);
+  return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
+}
+
+// The same faithful exp for x <= 0 or NaN (the softmax region's x - max):
+// no overflow to handle, and the scale stays a plain exponent add until the
+// result leaves the normal range.
+PSK_HD float exp_faithful_nonpos(float x) {
+  float kf = rintf(x * PSK_FEXP_INV_LN2);
+  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);
+  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  int k = (int)kf;
+  if (k >= -125) return p * u2f((uint32_t)(k + 127) << 23);
+  if (k < -149 - 24) return 0.0f * p;
   return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
 }
 

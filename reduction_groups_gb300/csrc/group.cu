@@ -29,13 +29,16 @@
 namespace psk {
 
 // ------------------------------------------------------ device code format
+// Instructions with an operand come first (LOAD .. MIN_R); the _R forms take
+// the operand as their first argument (acc = operand OP acc).
 enum : uint32_t {
-  D_LOAD = 1, D_STORE = 2,
-  D_ADD = 3, D_SUB, D_MUL, D_DIV, D_MAX, D_MIN,
+  D_LOAD = 1,
+  D_ADD, D_SUB, D_MUL, D_DIV, D_MAX, D_MIN,
+  D_SUB_R, D_DIV_R, D_MAX_R, D_MIN_R,
+  D_STORE,
   D_NEG, D_ABS, D_EXP, D_EXPC, D_GELU, D_SQRT, D_SQRTA, D_ERF,
 };
 constexpr uint32_t F_IMM = 1u << 8;   // operand is an immediate (else a slot)
-constexpr uint32_t F_REV = 1u << 9;   // acc = operand OP acc
 constexpr int MAX_CODE = 3 * PSK_MAX_NODES + 8;
 
 enum : int32_t { IN_CONTIG = 0, IN_BCAST = 1, IN_GATHER = 2 };
@@ -128,6 +131,8 @@ static int compile_program(const psk_program* p, int n_in, Compiled& c) {
     for (auto& e : st) if (e.kind == 0) { int s = alloc(); emit(D_STORE, 0, s); e = Ent{1, s, true}; }
   };
   static const uint32_t bin_map[6] = {D_ADD, D_SUB, D_MUL, D_DIV, D_MAX, D_MIN};
+  // reversed operand order; ADD and MUL are commutative bit for bit
+  static const uint32_t rev_map[6] = {D_ADD, D_SUB_R, D_MUL, D_DIV_R, D_MAX_R, D_MIN_R};
   static const uint32_t un_map[8] = {D_NEG, D_ABS, D_EXP, D_EXPC, D_GELU, D_SQRT, D_SQRTA, D_ERF};
   // REF entries of one node share its slot; it is freed after the last REF is consumed.
   std::vector<int> ref_pending(c.n_nodes, 0);
@@ -154,7 +159,7 @@ static int compile_program(const psk_program* p, int n_in, Compiled& c) {
       if (a.kind == 0) {
         emit(dop, operand_flags(b), b.idx);
       } else if (b.kind == 0) {
-        emit(dop, operand_flags(a) | F_REV, a.idx);
+        emit(rev_map[op - PSK_OP_ADD], operand_flags(a), a.idx);
       } else {
         spill_acc();
         emit(D_LOAD, operand_flags(a), a.idx);
@@ -234,19 +239,76 @@ __device__ __forceinline__ Vec<V> load_input(const GroupInput& in, int64_t off, 
   return r;
 }
 
-__device__ __forceinline__ float op_binary(uint32_t dop, float a, float b) {
+// Unary nodes on the V accumulator lanes.  For exp and erf the tier-1 cores
+// of all V elements run first (independent chains the scheduler interleaves),
+// and only undecided elements go to the slower tiers.
+template <int V>
+__device__ __forceinline__ void op_unary(uint32_t dop, Vec<V>& acc, const MathTables& tab) {
   switch (dop) {
-    case D_ADD: return __fadd_rn(a, b);
-    case D_SUB: return __fsub_rn(a, b);
-    case D_MUL: return __fmul_rn(a, b);
-    case D_DIV: return __fdiv_rn(a, b);
-    case D_MAX: return a > b ? a : b;
-    default:    return a < b ? a : b;   // D_MIN
+    case D_NEG:
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc.v[j] = -acc.v[j];
+      break;
+    case D_ABS:
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc.v[j] = fabsf(acc.v[j]);
+      break;
+    case D_EXP:
+    case D_EXPC: {
+      float a[V], R[V], d[V];
+      int n[V];
+      bool inr[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        a[j] = acc.v[j];
+        if (dop == D_EXPC) {
+          a[j] = a[j] > -4.0f ? a[j] : -4.0f;
+          a[j] = a[j] < 4.0f ? a[j] : 4.0f;
+        }
+        inr[j] = fabsf(a[j]) <= 87.0f;
+        exp_tier1_core(inr[j] ? a[j] : 0.0f, tab.exp_hi, tab.exp_lo, R[j], d[j], n[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        float o = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
+        if (!(inr[j] && tier1_decided(R[j], d[j]))) o = exp_tier2(a[j]);
+        acc.v[j] = o;
+      }
+      break;
+    }
+    case D_GELU:
+    case D_ERF: {
+      float tt[V], R[V], d[V];
+      bool inr[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        tt[j] = dop == D_GELU ? __fmul_rn(acc.v[j], PSK_INV_SQRT2) : acc.v[j];
+        const float aa = fabsf(tt[j]);
+        inr[j] = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
+        erf_tier1_core(inr[j] ? aa : 0.5f, tab.erf_hi, tab.erf_lo, R[j], d[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        float r = R[j];
+        if (!(inr[j] && tier1_decided(R[j], d[j]))) r = erf_abs_rest(fabsf(tt[j]));
+        r = copysignf(r, tt[j]);
+        acc.v[j] = dop == D_GELU ? __fmul_rn(acc.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, r))) : r;
+      }
+      break;
+    }
+    case D_SQRT:
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc.v[j] = __fsqrt_rn(acc.v[j]);
+      break;
+    default:  // D_SQRTA
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc.v[j] = __fsqrt_rn(fabsf(acc.v[j]));
+      break;
   }
 }
 
 template <int V, int OUT>
-__global__ void __launch_bounds__(GROUP_THREADS) group_kernel(const __grid_constant__ GroupParams P) {
+__global__ void __launch_bounds__(GROUP_THREADS, 4) group_kernel(const __grid_constant__ GroupParams P) {
   __shared__ MathTables tab;
   extern __shared__ float4 slot_mem[];
   load_tables(tab);
@@ -286,68 +348,38 @@ __global__ void __launch_bounds__(GROUP_THREADS) group_kernel(const __grid_const
       const uint32_t ins = P.code[pc];
       const uint32_t dop = ins & 0xFFu;
       const uint32_t idx = ins >> 16;
-      if (dop == D_STORE) { slots[idx * bd + tid] = acc; continue; }
-      if (dop <= D_MIN) {
-        Vec<V> b;
+      Vec<V> b;
+      if (dop <= D_MIN_R) {                      // the operand: a slot or an immediate
         if (ins & F_IMM) {
-          float q = P.imm[idx];
+          const float q = P.imm[idx];
 #pragma unroll
           for (int j = 0; j < V; ++j) b.v[j] = q;
         } else {
           b = slots[idx * bd + tid];
         }
-        if (dop == D_LOAD) { acc = b; continue; }
-        if (ins & F_REV) {
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = op_binary(dop, b.v[j], acc.v[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = op_binary(dop, acc.v[j], b.v[j]);
-        }
-        continue;
       }
       switch (dop) {
-        case D_NEG:
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = -acc.v[j];
+        case D_LOAD: acc = b; break;
+#define PSK_BIN(CASE, EXPR)                                  \
+        case CASE:                                           \
+          _Pragma("unroll") for (int j = 0; j < V; ++j) {    \
+            const float x = acc.v[j], y = b.v[j];            \
+            acc.v[j] = (EXPR);                               \
+          }                                                  \
           break;
-        case D_ABS:
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = fabsf(acc.v[j]);
-          break;
-        case D_EXP:
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = exp_cr(acc.v[j], tab.exp_hi, tab.exp_lo);
-          break;
-        case D_EXPC:
-#pragma unroll
-          for (int j = 0; j < V; ++j) {
-            float a = acc.v[j];
-            a = a > -4.0f ? a : -4.0f;
-            a = a < 4.0f ? a : 4.0f;
-            acc.v[j] = exp_cr(a, tab.exp_hi, tab.exp_lo);
-          }
-          break;
-        case D_GELU:
-#pragma unroll
-          for (int j = 0; j < V; ++j) {
-            float a = acc.v[j];
-            float e = erf_cr(__fmul_rn(a, PSK_INV_SQRT2), tab.erf_hi, tab.erf_lo);
-            acc.v[j] = __fmul_rn(a, __fmul_rn(0.5f, __fadd_rn(1.0f, e)));
-          }
-          break;
-        case D_SQRT:
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = __fsqrt_rn(acc.v[j]);
-          break;
-        case D_SQRTA:
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = __fsqrt_rn(fabsf(acc.v[j]));
-          break;
-        default:  // D_ERF
-#pragma unroll
-          for (int j = 0; j < V; ++j) acc.v[j] = erf_cr(acc.v[j], tab.erf_hi, tab.erf_lo);
-          break;
+        PSK_BIN(D_ADD, __fadd_rn(x, y))
+        PSK_BIN(D_SUB, __fsub_rn(x, y))
+        PSK_BIN(D_MUL, __fmul_rn(x, y))
+        PSK_BIN(D_DIV, __fdiv_rn(x, y))
+        PSK_BIN(D_MAX, x > y ? x : y)
+        PSK_BIN(D_MIN, x < y ? x : y)
+        PSK_BIN(D_SUB_R, __fsub_rn(y, x))
+        PSK_BIN(D_DIV_R, __fdiv_rn(y, x))
+        PSK_BIN(D_MAX_R, y > x ? y : x)
+        PSK_BIN(D_MIN_R, y < x ? y : x)
+#undef PSK_BIN
+        case D_STORE: slots[idx * bd + tid] = acc; break;
+        default: op_unary<V>(dop, acc, tab); break;
       }
     }
     // root -> storage, row-major output

@@ -52,7 +52,7 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 
 template <int EXPM>
 __device__ __forceinline__ float region_exp(float d, const float* thi, const float* tlo) {
-  if (EXPM == PSK_EXP_FAST) return exp_faithful(d);
+  if (EXPM == PSK_EXP_FAST) return exp_faithful_nonpos(d);
   return exp_cr(d, thi, tlo);
 }
 
@@ -62,7 +62,7 @@ template <int EXPM>
 __device__ __forceinline__ void region_exp8(float* v, const float* thi, const float* tlo) {
   if (EXPM == PSK_EXP_FAST) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = exp_faithful(v[q]);
+    for (int q = 0; q < 8; ++q) v[q] = exp_faithful_nonpos(v[q]);
     return;
   }
   float R[8], d[8];
@@ -144,6 +144,17 @@ __device__ __forceinline__ void store_y8(void* base, int64_t off, const float* v
   }
 }
 
+// e / s for one row: Markstein's correction through rs = RN(1/s) when the row
+// sum allows it (1 <= s < 2^20, true of every finite row), IEEE division for
+// the rare tiny e and for rows with a NaN or infinite sum.
+__device__ __forceinline__ float row_div(float e, float s, float rs, bool fast_ok) {
+  float q = e * rs;
+  float r = fmaf(-q, s, e);
+  float y = fmaf(r, rs, q);
+  if (!(fast_ok && e >= 0x1p-100f)) y = __fdiv_rn(e, s);
+  return y;
+}
+
 // One chain: acc over E[p], E[p+P], ... (n elements in the row), in index order.
 __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) {
   float acc = E[p];
@@ -173,7 +184,7 @@ __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) 
 
 // --------------------------------------------------- resident rows (<= 4096)
 template <int XT, int YT, int EXPM, bool VEC>
-__global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_constant__ SoftmaxParams P) {
+__global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __grid_constant__ SoftmaxParams P) {
   constexpr int NBMAX = (XT == PSK_BF16) ? 4 : 2;
   extern __shared__ __align__(16) float smem[];
   __shared__ float exp_hi[32], exp_lo[32];
@@ -187,23 +198,43 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
   const int64_t nbatch = (P.rows + nb - 1) / nb;
   const size_t xsz = XT == PSK_F32 ? 4 : 2, ysz = YT == PSK_F32 ? 4 : 2;
 
-  for (int64_t bt = blockIdx.x; bt < nbatch; bt += gridDim.x) {
-    const int64_t row0 = bt * nb;
-    const int nr = (int)((P.rows - row0) < nb ? (P.rows - row0) : nb);
-    // 1. load every row of the batch, packed in registers; local maxima
-    Raw8<XT> raw[NBMAX][2];
-    float xs[NBMAX][SM_EPT];                       // scalar path only
-    float mloc[NBMAX];
+  Raw8<XT> raw[NBMAX][2];
+  float xs[NBMAX][SM_EPT];                         // scalar path only
+  // loads of one batch into registers (issued a batch ahead, so their latency
+  // overlaps the previous batch's chain and output phases)
+  auto load_batch = [&](int64_t bt) {
+    const int64_t r0 = bt * nb;
+    const int nrr = bt < nbatch ? (int)((P.rows - r0) < nb ? (P.rows - r0) : nb) : 0;
 #pragma unroll
     for (int b = 0; b < NBMAX; ++b) {
-      mloc[b] = -INFINITY;
-      if (b >= nb) continue;
-      const void* xr = (const char*)P.x + (row0 + b) * P.ldx * xsz;
+      const void* xr = (const char*)P.x + (r0 + b) * P.ldx * xsz;
       if (VEC) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int j = (k * SM_THREADS + t) * 8;
-          if (b < nr && j < cols) raw_load<XT>(raw[b][k], xr, j); else raw_fill(raw[b][k]);
+          if (b < nrr && j < cols) raw_load<XT>(raw[b][k], xr, j); else raw_fill(raw[b][k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < SM_EPT; ++k) {
+          const int j = k * SM_THREADS + t;
+          xs[b][k] = (b < nrr && j < cols) ? load_x1<XT>(xr, j) : -INFINITY;
+        }
+      }
+    }
+  };
+  load_batch(blockIdx.x);
+  for (int64_t bt = blockIdx.x; bt < nbatch; bt += gridDim.x) {
+    const int64_t row0 = bt * nb;
+    const int nr = (int)((P.rows - row0) < nb ? (P.rows - row0) : nb);
+    // 1. local maxima of the batch held in registers
+    float mloc[NBMAX];
+#pragma unroll
+    for (int b = 0; b < NBMAX; ++b) {
+      mloc[b] = -INFINITY;
+      if (VEC) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
           float v[8];
           raw_unpack(raw[b][k], v);
 #pragma unroll
@@ -211,11 +242,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < SM_EPT; ++k) {
-          const int j = k * SM_THREADS + t;
-          xs[b][k] = (b < nr && j < cols) ? load_x1<XT>(xr, j) : -INFINITY;
-          mloc[b] = max_nan(mloc[b], xs[b][k]);
-        }
+        for (int k = 0; k < SM_EPT; ++k) mloc[b] = max_nan(mloc[b], xs[b][k]);
       }
     }
     // 2. the NB row maxima, one barrier
@@ -261,6 +288,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
       }
     }
     __syncthreads();
+    load_batch(bt + gridDim.x);
     // 4. every chain of the batch in warp 0: lane (b, p) sums chain p of row b
     if (w == 0) {
       const int nlanes = nr * parts;
@@ -305,6 +333,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
       if (b >= nr) continue;
       const float* E = smem + b * P.estride;
       const float s = rowsum[b], rs = rowrcp[b];
+      const bool fast_ok = s >= 1.0f && s < 0x1p20f;
       void* yr = (char*)P.y + (row0 + b) * P.ldy * ysz;
       if (VEC) {
 #pragma unroll
@@ -314,7 +343,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
             float4 a = *(const float4*)&E[j], c = *(const float4*)&E[j + 4];
             float o[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = div_by_recip(o[q], s, rs);
+            for (int q = 0; q < 8; ++q) o[q] = row_div(o[q], s, rs, fast_ok);
             store_y8<YT>(yr, j, o);
           }
         }
@@ -322,7 +351,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_batch_kernel(const __grid_
 #pragma unroll
         for (int k = 0; k < SM_EPT; ++k) {
           const int j = k * SM_THREADS + t;
-          if (j < cols) store_y1<YT>(yr, j, div_by_recip(E[j], s, rs));
+          if (j < cols) store_y1<YT>(yr, j, row_div(E[j], s, rs, fast_ok));
         }
       }
     }
