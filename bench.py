@@ -58,6 +58,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest value of x across ranks (the job's time is its slowest
+    rank's); identity without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return world * bytes_per_rank_step * steps / (max_ms / 1e3) / 1e9
+
+
 def _peaks():
     try:
         with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
@@ -128,11 +147,12 @@ def _gpu_uuid(torch, dev):
         return str(dev)
 
 
-# ---------------------------------------------------------------- traffic
-def _dram_traffic(kernel: str):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the
-    kernel's source is unchanged since it was captured; else None."""
-    path = os.path.join(HERE, "profiles", "dram_traffic.txt")
+# ------------------------------------------------------------ ncu counters
+def _counter(kernel: str, name: str):
+    """A per-launch counter of a kernel at full size from the committed ncu
+    summaries (profiles/kernel_counters.txt), if the kernel's source is
+    unchanged since the capture; else None."""
+    path = os.path.join(HERE, "profiles", "kernel_counters.txt")
     if not os.path.exists(path):
         return None
     src = {"adamw": "adamw.cu", "group": "group.cu", "softmax_sequential": "softmax.cu",
@@ -140,9 +160,20 @@ def _dram_traffic(kernel: str):
     h = hashlib.sha256(open(os.path.join(HERE, "reduction_groups_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 3 and parts[0] == kernel and parts[1] == h:
-            return int(parts[2])
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == h and parts[2] == name:
+            return int(parts[3])
     return None
+
+
+def _issue_peak():
+    """Warp-instruction issue peak: 152 SMs x 4 schedulers x 1 warp-instruction
+    per cycle at the maximum SM clock."""
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return 152 * 4 * mhz * 1e6 / 1e9, mhz
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -259,12 +290,7 @@ def run_ours(a, ws, rank, local):
     total_ms = start.elapsed_time(end)
     per_kernel_ms = {k: sum(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(a.steps)) / a.steps
                      for j, k in enumerate(kernels)}
-    if ws > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms)
 
     # the softmax region in the other exp mode, timed beside the step (not in value)
     other = "exact" if em == "fast" else "fast"
@@ -322,14 +348,8 @@ def run_ours(a, ws, rank, local):
             e2e_step()
         e2.record()
         torch.cuda.synchronize()
-        ms = s2.elapsed_time(e2)
-        if ws > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        e2e = {"value": round(ws * bytes_step * a.steps / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        ms = max_over_ranks(s2.elapsed_time(e2))
+        e2e = {"value": round(job_value(bytes_step, a.steps, ws, ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / a.steps, 3)}
 
     if rank != 0:
@@ -360,10 +380,26 @@ def run_ours(a, ws, rank, local):
     if "adamw" in kinfo:
         kinfo["adamw"]["params_per_s"] = round(tree.n_params / (per_kernel_ms["adamw"] / 1e3), 1)
     dom = max(kernels, key=lambda k: per_kernel_ms[k])
-    achieved = kb[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": _dram_traffic(dom)}
+    ipeak, mhz = _issue_peak()
+    winst = _counter("group", "warp_instructions") if "group" in kernels and a.scale == 1.0 else None
+    if winst is not None:
+        ach = winst / (per_kernel_ms["group"] / 1e3) / 1e9
+        kinfo["group"]["issue_rate_gwarp_instr_s"] = round(ach, 1)
+        kinfo["group"]["frac_of_issue_peak"] = round(ach / ipeak, 4)
+    if dom == "group" and winst is not None:
+        # bound by instruction issue: executed warp-instructions per launch
+        # (ncu, unchanged source) over the launch time, against the issue peak
+        roofline = {"kernel": dom, "bound": "alu", "achieved": kinfo["group"]["issue_rate_gwarp_instr_s"],
+                    "peak": round(ipeak, 1), "peak_source": f"152 SM x 4 issue/clk x {mhz:.0f} MHz",
+                    "unit": "G warp-instr/s", "frac": kinfo["group"]["frac_of_issue_peak"], "traffic": None,
+                    "hbm_gbs": kinfo["group"]["gbs"]}
+    else:
+        achieved = kb[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                    "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": _counter(dom, "dram_bytes") if a.scale == 1.0 else None}
+    if "adamw" in kinfo:
+        kinfo["adamw"]["dram_traffic"] = _counter("adamw", "dram_bytes") if a.scale == 1.0 else None
 
     cpu = None
     if not a.no_cpu and ws == 1 and a.only == "all":
@@ -371,7 +407,7 @@ def run_ours(a, ws, rank, local):
         cpu = {"value": round(nb / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": desc + f"; {dt:.1f} s of one host core (numpy ufuncs run single-threaded)"}
 
-    value = ws * bytes_step * a.steps / (total_ms / 1e3) / 1e9
+    value = job_value(bytes_step, a.steps, ws, total_ms)
     line = {
         "metric": "achieved HBM GB/s (% of GB300 peak) for fused group, softmax region, AdamW params/s",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
