@@ -19,7 +19,8 @@
  * - Pointers named ptr/x/y/theta/m/v/grad are DEVICE pointers owned by the
  *   caller; descriptor structs and arrays of them are HOST memory, read during
  *   the call only.  The library allocates no device memory and keeps no state
- *   across calls besides cached device attributes.
+ *   across calls besides cached device attributes and one device status word
+ *   (psk_device_status).
  * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  *   stream).  Return 0 means the work was enqueued.
  * - A negative return is a refusal: nothing was launched, and
@@ -182,6 +183,13 @@ int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hpa
 /* Host-only: the nine f32 scalars the step reads, in the order
  * b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd. */
 int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]);
+
+/* Host-only, synchronous: the device status word of the pipelined kernels of
+ * the current device (0 = no bounded wait ever timed out; bit 0 = a wait gave
+ * up and the kernel wound down, its output then unspecified).  reset != 0
+ * clears the word after reading it.  A timeout is never expected: it would
+ * mean a pipeline bug, and this lets a caller detect it without a hang. */
+int psk_device_status(uint32_t* status, int32_t reset);
 
 /* Thread-local description of the last refusal of this thread ("" if none). */
 const char* psk_last_error(void);

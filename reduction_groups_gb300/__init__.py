@@ -8,6 +8,7 @@ parameter tree, each one CUDA launch through a C ABI (include/psk.h).
 from .ops import (  # noqa: F401
     psk_adamw_scalars,
     psk_adamw_tree,
+    psk_device_status,
     psk_group_check,
     psk_group_run,
     psk_softmax_region,

@@ -24,7 +24,7 @@ ERRORS = {
 }
 
 EXPORTS = ("psk_group_run", "psk_group_check", "psk_softmax_region", "psk_adamw_tree",
-           "psk_adamw_scalars", "psk_last_error")
+           "psk_adamw_scalars", "psk_device_status", "psk_last_error")
 
 
 class psk_program(ctypes.Structure):
@@ -79,8 +79,10 @@ def lib() -> ctypes.CDLL:
                                          psk_order, ctypes.c_int32, ctypes.c_void_p]
         L.psk_adamw_tree.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_hparams), ctypes.c_void_p]
         L.psk_adamw_scalars.argtypes = [P(psk_adamw_hparams), P(ctypes.c_float)]
+        L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_last_error.restype = ctypes.c_char_p
-        for f in ("psk_group_run", "psk_group_check", "psk_softmax_region", "psk_adamw_tree", "psk_adamw_scalars"):
+        for f in ("psk_group_run", "psk_group_check", "psk_softmax_region", "psk_adamw_tree", "psk_adamw_scalars",
+                  "psk_device_status"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib

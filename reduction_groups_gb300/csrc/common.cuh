@@ -9,13 +9,9 @@
 
 #include "../../include/psk.h"
 
-namespace psk {
+#include "host.h"
 
-// Record a refusal for psk_last_error() and return its code.
-int fail(int code, const char* fmt, ...);
-void clear_error();
-// Map a CUDA runtime error after a launch to PSK_E_CUDA with its name.
-int check_launch(const char* what);
+namespace psk {
 
 inline int dtype_size(int32_t dt) { return dt == PSK_BF16 ? 2 : 4; }
 inline bool dtype_ok(int32_t dt) { return dt == PSK_F32 || dt == PSK_BF16; }

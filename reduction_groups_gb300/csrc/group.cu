@@ -403,23 +403,10 @@ __global__ void __launch_bounds__(GROUP_THREADS, 4) group_kernel(const __grid_co
 }
 
 // ----------------------------------------------------------- host launch
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  }
-  return n;
-}
-
 template <int V, int OUT>
 static int launch_group(GroupParams& P, uint64_t n_vec_total, size_t smem, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(group_kernel<V, OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set = true;
-  }
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)group_kernel<V, OUT>, 200 * 1024, attr);
   int blocks_per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, group_kernel<V, OUT>, GROUP_THREADS, smem);
   if (blocks_per_sm < 1) return fail(PSK_E_SHAPE, "group needs %zu bytes of shared memory per CTA", smem);
@@ -429,7 +416,7 @@ static int launch_group(GroupParams& P, uint64_t n_vec_total, size_t smem, cudaS
     P.v_begin = b;
     P.n_vec = (uint32_t)n;
     uint64_t want = (n + GROUP_THREADS - 1) / GROUP_THREADS;
-    uint64_t cap = (uint64_t)sm_count() * blocks_per_sm;
+    uint64_t cap = (uint64_t)device_sm_count() * blocks_per_sm;
     unsigned grid = (unsigned)(want < cap ? want : cap);
     group_kernel<V, OUT><<<grid, GROUP_THREADS, smem, stream>>>(P);
     int rc = check_launch("group kernel");

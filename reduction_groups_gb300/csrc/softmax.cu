@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "crmath.cuh"
+#include "pipe.cuh"
 
 namespace psk {
 
@@ -38,8 +39,9 @@ struct SoftmaxParams {
   void* y;
   int64_t rows, cols, ldx, ldy;
   int32_t partials;     // 1 for sequential / blocked
-  int32_t nb;           // rows per batch (resident kernel)
+  int32_t nb;           // rows per batch (resident kernel) / per chain group (pipelined)
   int32_t estride;      // floats between row buffers in shared memory
+  int32_t sx, se;       // pipelined kernel: x and exp ring slots
 };
 
 // NaN-propagating max (exact; the order of a max reduction changes no bit
@@ -60,24 +62,24 @@ __device__ __forceinline__ float region_exp(float d, const float* thi, const flo
 // (independent chains for the scheduler), the rare undecided lanes after.
 template <int EXPM>
 __device__ __forceinline__ void region_exp8(float* v, const float* thi, const float* tlo) {
-  if (EXPM == PSK_EXP_FAST) {
+  if constexpr (EXPM == PSK_EXP_FAST) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = exp_faithful_nonpos(v[q]);
-    return;
-  }
-  float R[8], d[8];
-  int n[8];
-  bool inr[8];
+  } else {
+    float R[8], d[8];
+    int n[8];
+    bool inr[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    inr[q] = fabsf(v[q]) <= 87.0f;
-    exp_tier1_core(inr[q] ? v[q] : 0.0f, thi, tlo, R[q], d[q], n[q]);
-  }
+    for (int q = 0; q < 8; ++q) {
+      inr[q] = fabsf(v[q]) <= 87.0f;
+      exp_tier1_core(inr[q] ? v[q] : 0.0f, thi, tlo, R[q], d[q], n[q]);
+    }
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float out = u2f((uint32_t)((int32_t)f2u(R[q]) + n[q] * (1 << 23)));
-    if (!(inr[q] && tier1_decided(R[q], d[q]))) out = exp_tier2(v[q]);
-    v[q] = out;
+    for (int q = 0; q < 8; ++q) {
+      float out = u2f((uint32_t)((int32_t)f2u(R[q]) + n[q] * (1 << 23)));
+      if (!(inr[q] && tier1_decided(R[q], d[q]))) out = exp_tier2(v[q]);
+      v[q] = out;
+    }
   }
 }
 
@@ -359,6 +361,205 @@ __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __gr
   }
 }
 
+
+// ------------------------------------- pipelined rows (bf16, <= 4096 columns)
+// One persistent CTA per SM with three roles:
+//   a producer warp streams this CTA's rows (bf16) into a shared ring of SX
+//   slots with 1-D bulk copies (TMA) that complete on the slot's mbarrier;
+//   4 teams of 4 compute warps each take every 4th row of the CTA (so four
+//   rows are in the compute stage at once, each team synchronising only
+//   within itself): the row's max (warp shuffles + a team barrier), e =
+//   exp(x - m) into a shared ring of SE f32 rows, then -- LAG = SE/4 - 1 team
+//   rows later, once the chain warps have published the row sum -- e / s,
+//   stored with streaming stores;
+//   3 chain warps each take groups of G consecutive rows: lane (row, p) adds
+//   chain p of its row in index order, the partials are combined left to
+//   right, and the row's sum and RN(1/s) are published on the row's mbarrier.
+// A row's chain is a serial run of cols/P dependent adds, so about 4 LAG
+// rows chain at once; long chains (sequential order) get a deeper exp ring
+// and a shallower x ring.  Every wait is bounded (pipe.cuh).
+constexpr int PIPE_TEAMS = 4;
+constexpr int PIPE_TW = 4;                                   // warps per team
+constexpr int PIPE_CW = PIPE_TEAMS * PIPE_TW;                // compute warps (16)
+constexpr int PIPE_TT = PIPE_TW * 32;                        // threads per team (128)
+constexpr int PIPE_EPT = SM_CAP / PIPE_TT;                   // row elements per team thread (32)
+constexpr int PIPE_KW = 3;                                   // chain warps
+constexpr int PIPE_THREADS = (PIPE_CW + PIPE_KW + 1) * 32;   // + producer warp
+constexpr int PIPE_SX_MAX = 8;                               // x ring slots
+constexpr int PIPE_SE_MAX = 16;                              // exp ring slots (a multiple of the teams)
+constexpr size_t PIPE_SMEM_BUDGET = 225 * 1024;              // dynamic shared memory of one CTA
+
+template <int YT, int EXPM>
+__global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __grid_constant__ SoftmaxParams P) {
+  extern __shared__ __align__(128) unsigned char pipe_smem[];
+  __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
+  __shared__ float rowsum[PIPE_SE_MAX], rowrcp[PIPE_SE_MAX];
+  __shared__ float red[PIPE_TEAMS][2][PIPE_TW];
+  __shared__ float exp_hi[32], exp_lo[32];
+  __shared__ volatile int abort_flag;
+
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int cols = (int)P.cols;
+  const uint32_t xbytes = (uint32_t)cols * 2u;
+  const int xstr = (int)(((xbytes + 127u) / 128u) * 64u);    // ring slot stride in bf16 elements
+  const int SX = P.sx, SE = P.se, LAG = P.se / PIPE_TEAMS - 1;
+  uint16_t* X = reinterpret_cast<uint16_t*>(pipe_smem);
+  float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xstr * 2);
+  const int estride = P.estride;
+  const int parts = P.partials;
+  const int G = P.nb;                                        // rows per chain group
+  const int n_local = blockIdx.x < P.rows ? (int)((P.rows - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < SX; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], 1); }
+    for (int i = 0; i < SE; ++i) { mbar_init(&efull[i], PIPE_TT); mbar_init(&sready[i], 1); }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (EXPM == PSK_EXP_EXACT && tid < 32) { exp_hi[tid] = psk_exp_tab_hi[tid]; exp_lo[tid] = psk_exp_tab_lo[tid]; }
+  __syncthreads();
+
+  if (w == PIPE_CW + PIPE_KW) {
+    // ---------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      const uint16_t* src = (const uint16_t*)P.x + (int64_t)blockIdx.x * P.ldx;
+      const int64_t step = (int64_t)gridDim.x * P.ldx;
+      for (int i = 0; i < n_local; ++i) {
+        const int s = i % SX;
+        if (i >= SX && !mbar_wait(&xempty[s], (uint32_t)((i / SX) - 1) & 1u)) { abort_flag = 1; break; }
+        if (abort_flag) break;
+        mbar_arrive_expect_tx(&xfull[s], xbytes);
+        bulk_copy_g2s(X + (size_t)s * xstr, src, xbytes, &xfull[s]);
+        src += step;
+        issued = i + 1;
+      }
+      if (abort_flag)   // copies still in flight land before the CTA retires
+        for (int i = issued > SX ? issued - SX : 0; i < issued; ++i) mbar_wait(&xfull[i % SX], (uint32_t)(i / SX) & 1u);
+    }
+    return;
+  }
+
+  if (w >= PIPE_CW) {
+    // ---------------- chain warps
+    // A parity wait must never run two phases ahead of its barrier (it would
+    // pass at once), so every slot group of the exp ring (G consecutive
+    // slots) belongs to one chain warp, which visits its phases in order.
+    const int c = w - PIPE_CW;
+    const int b = lane / parts, p = lane - (lane / parts) * parts;
+    const int n_groups = SE / G;
+    for (int g = 0; g * G < n_local; ++g) {
+      if ((g % n_groups) % PIPE_KW != c) continue;
+      if (abort_flag) break;
+      const int j = g * G + b;
+      const bool act = b < G && j < n_local;
+      const int se = j % SE;
+      bool ok = true;
+      if (act) ok = mbar_wait(&efull[se], (uint32_t)(j / SE) & 1u);
+      if (__any_sync(0xffffffffu, !ok)) { abort_flag = 1; break; }
+      const float acc = act ? run_chain(E + (size_t)se * estride, cols, p, parts) : 0.0f;
+      float sum = acc;
+      for (int q = 1; q < parts; ++q) {
+        const float o = __shfl_sync(0xffffffffu, acc, (lane - p + q) & 31);
+        if (act) sum = __fadd_rn(sum, o);
+      }
+      if (act && p == 0) {
+        rowsum[se] = sum;
+        rowrcp[se] = __frcp_rn(sum);
+        mbar_arrive(&sready[se]);
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute teams: team t takes rows t, t + 4, ...; team
+  // thread tt owns elements 4 tt + 512 k (+0..3), k = 0..7.  After a timeout
+  // (`dead`) a team skips every wait and all work but keeps meeting its
+  // barrier, so every thread leaves in bounded time.
+  const int team = w / PIPE_TW, tw = w % PIPE_TW, tt = tid % PIPE_TT;
+  bool dead = false;
+  const size_t ysz = YT == PSK_F32 ? 4 : 2;
+  for (int k = 0;; ++k) {
+    const int i = team + PIPE_TEAMS * k;                     // row produced in this team iteration
+    const int o = i - PIPE_TEAMS * LAG;                      // row output in this team iteration
+    if (o >= n_local) break;
+    dead = dead || abort_flag;
+    if (i < n_local) {
+      const int s = i % SX;
+      if (!dead && !mbar_wait(&xfull[s], (uint32_t)(i / SX) & 1u)) { abort_flag = 1; dead = true; }
+      const uint16_t* xs = X + (size_t)s * xstr;
+      float v[PIPE_EPT];
+      float m = -INFINITY;
+#pragma unroll
+      for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+        const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+        if (j < cols && !dead) {
+          const uint2 q = *reinterpret_cast<const uint2*>(xs + j);
+          v[4 * c4 + 0] = __uint_as_float(q.x << 16);
+          v[4 * c4 + 1] = __uint_as_float(q.x & 0xFFFF0000u);
+          v[4 * c4 + 2] = __uint_as_float(q.y << 16);
+          v[4 * c4 + 3] = __uint_as_float(q.y & 0xFFFF0000u);
+        } else {
+          v[4 * c4 + 0] = v[4 * c4 + 1] = v[4 * c4 + 2] = v[4 * c4 + 3] = -INFINITY;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = max_nan(m, v[4 * c4 + q]);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[team][k & 1][tw] = m;
+      named_barrier(1 + team, PIPE_TT);
+      m = red[team][k & 1][0];
+#pragma unroll
+      for (int q = 1; q < PIPE_TW; ++q) m = max_nan(m, red[team][k & 1][q]);
+      if (tt == 0) mbar_arrive(&xempty[s]);              // every team thread has read x
+      const int se = i % SE;
+      float* Er = E + (size_t)se * estride;
+      if (!dead) {
+#pragma unroll
+        for (int h = 0; h < PIPE_EPT / 8; ++h) {
+          float u[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
+          region_exp8<EXPM>(u, exp_hi, exp_lo);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int j = (2 * h + kk) * (PIPE_TT * 4) + 4 * tt;
+            if (j < cols)
+              *reinterpret_cast<float4*>(Er + j) = make_float4(u[4 * kk], u[4 * kk + 1], u[4 * kk + 2], u[4 * kk + 3]);
+          }
+        }
+      }
+      mbar_arrive(&efull[se]);
+    }
+    if (o >= 0 && !dead) {
+      const int se = o % SE;
+      if (!mbar_wait(&sready[se], (uint32_t)(o / SE) & 1u)) { abort_flag = 1; dead = true; continue; }
+      const float sm = rowsum[se], rs = rowrcp[se];
+      const bool fast_ok = sm >= 1.0f && sm < 0x1p20f;
+      const float* Er = E + (size_t)se * estride;
+      char* yr = (char*)P.y + ((int64_t)blockIdx.x + (int64_t)o * gridDim.x) * P.ldy * ysz;
+#pragma unroll
+      for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+        const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+        if (j < cols) {
+          const float4 e = *reinterpret_cast<const float4*>(Er + j);
+          const float o0 = row_div(e.x, sm, rs, fast_ok), o1 = row_div(e.y, sm, rs, fast_ok);
+          const float o2 = row_div(e.z, sm, rs, fast_ok), o3 = row_div(e.w, sm, rs, fast_ok);
+          if (YT == PSK_F32) {
+            __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o0, o1, o2, o3));
+          } else {
+            uint2 q;
+            q.x = f32x2_to_bf16x2(o0, o1);
+            q.y = f32x2_to_bf16x2(o2, o3);
+            __stcs(reinterpret_cast<uint2*>(yr) + (j >> 2), q);
+          }
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------- streaming rows (> 4096)
 struct StreamShared {
   float E[SM_CAP];
@@ -426,16 +627,6 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid
 }
 
 // ------------------------------------------------------------------ host
-static int sm_count_softmax() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  }
-  return n;
-}
-
 template <int XT, int YT, int EXPM, bool VEC>
 static int launch_batch(SoftmaxParams P, cudaStream_t stream) {
   constexpr int NBMAX = (XT == PSK_BF16) ? 4 : 2;
@@ -446,17 +637,13 @@ static int launch_batch(SoftmaxParams P, cudaStream_t stream) {
   P.nb = NBMAX;
   P.estride = (int)(((P.cols + 31) / 32) * 32 + (pad % 32));
   const size_t smem = (size_t)(P.nb * P.estride + P.nb * P.partials + 64) * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(softmax_batch_kernel<XT, YT, EXPM, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         100 * 1024);
-    attr = true;
-  }
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)softmax_batch_kernel<XT, YT, EXPM, VEC>, 100 * 1024, attr);
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, softmax_batch_kernel<XT, YT, EXPM, VEC>, SM_THREADS, smem);
   if (per_sm < 1) per_sm = 1;
   const int64_t nbatch = (P.rows + P.nb - 1) / P.nb;
-  const int64_t cap = (int64_t)sm_count_softmax() * per_sm;
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
   const unsigned grid = (unsigned)(nbatch < cap ? nbatch : cap);
   softmax_batch_kernel<XT, YT, EXPM, VEC><<<grid, SM_THREADS, smem, stream>>>(P);
   return check_launch("softmax region kernel");
@@ -467,15 +654,53 @@ static int launch_stream(const SoftmaxParams& P, cudaStream_t stream) {
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, softmax_stream_kernel<XT, YT, EXPM>, SM_THREADS, 0);
   if (per_sm < 1) per_sm = 1;
-  const int64_t cap = (int64_t)sm_count_softmax() * per_sm;
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
   const unsigned grid = (unsigned)(P.rows < cap ? P.rows : cap);
   softmax_stream_kernel<XT, YT, EXPM><<<grid, SM_THREADS, 0, stream>>>(P);
   return check_launch("softmax region kernel (streaming rows)");
 }
 
+// Ring depths from the shared-memory budget.  Eight bf16 rows in flight per
+// SM cover HBM latency; the exp ring holds SE = 4 (LAG + 1) rows, about 4 LAG
+// of them in their chains.  A long chain (cols / P >= 1024 adds, e.g. the
+// sequential order over 4096 columns) is the bottleneck, so it gets the exp
+// ring first (x ring down to 4 slots); otherwise the x ring comes first.
+// Chain groups take G <= 4 consecutive rows (one per team).
+template <int YT, int EXPM>
+static int launch_pipe(SoftmaxParams P, cudaStream_t stream) {
+  const int pad = P.partials < 4 ? 4 : ((P.partials + 3) / 4) * 4;
+  P.estride = (int)(((P.cols + 31) / 32) * 32 + pad);
+  const size_t xrow = (size_t)((P.cols * 2 + 127) / 128) * 128;
+  const size_t erow = (size_t)P.estride * sizeof(float);
+  const size_t budget = PIPE_SMEM_BUDGET;
+  const bool long_chain = (P.cols + P.partials - 1) / P.partials >= 1024;
+  int sx = long_chain ? 4 : PIPE_SX_MAX;
+  int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
+  if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
+  // x slots stay a multiple of the team count, so that each slot serves one
+  // team and its parity waits run in order
+  if (sx < PIPE_SX_MAX && PIPE_SX_MAX * xrow + se * erow <= budget) sx = PIPE_SX_MAX;
+  if (se < 2 * PIPE_TEAMS) {  // cannot happen for cols <= 4096; kept as a guard
+    return fail(PSK_E_ARG, "softmax ring does not fit shared memory (cols %lld)", (long long)P.cols);
+  }
+  P.sx = sx;
+  P.se = se;
+  // chain group: G in {4, 2, 1} rows (a divisor of SE) of 32 / P lanes at most
+  const int glanes = 32 / P.partials;
+  P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
+  const size_t smem = sx * xrow + se * erow;
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)softmax_pipe_kernel<YT, EXPM>, (int)budget, attr);
+  const int64_t sms = device_sm_count();
+  const unsigned grid = (unsigned)(P.rows < sms ? P.rows : sms);
+  softmax_pipe_kernel<YT, EXPM><<<grid, PIPE_THREADS, smem, stream>>>(P);
+  return check_launch("softmax region kernel (pipelined)");
+}
+
 template <int XT, int YT, int EXPM>
 static int dispatch_exp(const SoftmaxParams& P, bool vec, cudaStream_t s) {
   if (P.cols > SM_CAP) return launch_stream<XT, YT, EXPM>(P, s);
+  if (XT == PSK_BF16 && vec && P.partials <= 32 && P.cols >= 8) return launch_pipe<YT, EXPM>(P, s);
   return vec ? launch_batch<XT, YT, EXPM, true>(P, s) : launch_batch<XT, YT, EXPM, false>(P, s);
 }
 
@@ -488,6 +713,19 @@ static int dispatch_softmax(const SoftmaxParams& P, int exp_mode, bool vec, cuda
 }  // namespace psk
 
 using namespace psk;
+
+extern "C" int psk_device_status(uint32_t* status, int32_t reset) {
+  clear_error();
+  if (!status) return fail(PSK_E_NULL, "status is NULL");
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pipe_status, sizeof(v)) != cudaSuccess) return check_launch("device status read");
+  if (reset) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_pipe_status, &z, sizeof(z)) != cudaSuccess) return check_launch("device status reset");
+  }
+  *status = v;
+  return PSK_OK;
+}
 
 extern "C" int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
                                   int64_t ldx, int64_t ldy, psk_order order, int32_t exp_mode, void* stream) {
@@ -521,7 +759,7 @@ extern "C" int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt
   const char* yhi = ylo + ((rows - 1) * ldy + cols) * dtype_size(yt);
   if (xlo < yhi && ylo < xhi && !(x == y && xt == yt && ldx == ldy))
     return fail(PSK_E_ALIAS, "y overlaps x and is not the same buffer");
-  SoftmaxParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0};
+  SoftmaxParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0, 0, 0};
   const bool vec = (cols % 8 == 0) && (ldx % 8 == 0) && (ldy % 8 == 0) && ((uintptr_t)x % 16 == 0) &&
                    ((uintptr_t)y % 16 == 0);
   cudaStream_t s = (cudaStream_t)stream;

@@ -93,6 +93,13 @@ def psk_softmax_region(x, y, order=("sequential",), exp_mode: str = "exact", str
                                        max(x.stride(0), cols), max(y.stride(0), cols), o, em, _stream_handle(stream)))
 
 
+def psk_device_status(reset: bool = False) -> int:
+    """The pipelined kernels' status word (0: no bounded wait ever timed out)."""
+    v = ctypes.c_uint32(0)
+    N.check(N.lib().psk_device_status(ctypes.byref(v), 1 if reset else 0))
+    return v.value
+
+
 def _hparams(hp) -> N.psk_adamw_hparams:
     h = N.psk_adamw_hparams()
     h.lr, h.beta1, h.beta2 = float(hp.lr), float(hp.beta1), float(hp.beta2)

@@ -257,6 +257,34 @@ def test_softmax_exact_bitwise(dev, order, shape):
     assert ok.all(), f"{(~ok).sum()} differ"
 
 
+_MANY_ROWS = ([(4000, 512, o, yt) for o in (("sequential",), ("interleaved", 2), ("interleaved", 3),
+                                           ("interleaved", 8), ("interleaved", 10), ("interleaved", 16),
+                                           ("interleaved", 32), ("interleaved", 40)) for yt in ("bf16", "f32")]
+              + [(2000, 4096, o, "bf16") for o in (("sequential",), ("interleaved", 2), ("interleaved", 8),
+                                                   ("interleaved", 12))]
+              + [(2000, 4096, ("sequential",), "f32"), (3000, 2048, ("sequential",), "bf16")])
+
+
+@pytest.mark.parametrize("rows,cols,order,yt", _MANY_ROWS)
+def test_softmax_many_rows_per_cta_bitwise(dev, rows, cols, order, yt):
+    """Enough rows that every CTA's ring buffers wrap several times, for short
+    chains (512 columns) and long ones (2048 and 4096 columns, whose rings are
+    sized differently)."""
+    wl = W.softmax_rows(rows, cols)
+    x = wl.host_x()
+    want = OS.softmax_region(x, "bf16", yt, order)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16 if yt == "bf16" else torch.float32, device="cuda")
+    dev.psk_device_status(reset=True)
+    for mode in ("exact", "fast"):
+        dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, mode)
+        torch.cuda.synchronize()
+        got = _to_host(y)
+        if mode == "exact":
+            ok = _same(got, want, yt)
+            assert ok.all(), f"{(~ok).sum()} differ"
+    assert dev.psk_device_status() == 0
+
+
 def test_softmax_f32_io_in_place_and_nan(dev):
     rng = np.random.default_rng(4)
     x = (rng.standard_normal((20, 520)) * 4).astype(np.float32)
