@@ -148,6 +148,23 @@ def _gpu_uuid(torch, dev):
 
 
 # ------------------------------------------------------------ ncu counters
+# the sources each kernel's device code is built from (the group kernel is
+# generated from group.cu and compiled at run time from the device headers)
+_KERNEL_SOURCES = {
+    "adamw": ["adamw.cu"],
+    "group": ["group.cu", "group_dev.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+    "softmax_sequential": ["softmax.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+    "softmax_interleaved8": ["softmax.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+}
+
+
+def _source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in _KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(HERE, "reduction_groups_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def _counter(kernel: str, name: str):
     """A per-launch counter of a kernel at full size from the committed ncu
     summaries (profiles/kernel_counters.txt), if the kernel's source is
@@ -155,9 +172,7 @@ def _counter(kernel: str, name: str):
     path = os.path.join(HERE, "profiles", "kernel_counters.txt")
     if not os.path.exists(path):
         return None
-    src = {"adamw": "adamw.cu", "group": "group.cu", "softmax_sequential": "softmax.cu",
-           "softmax_interleaved8": "softmax.cu"}[kernel]
-    h = hashlib.sha256(open(os.path.join(HERE, "reduction_groups_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
+    h = _source_hash(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == h and parts[2] == name:

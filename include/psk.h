@@ -34,7 +34,9 @@
 #ifndef PSK_H
 #define PSK_H
 
+#if !defined(__CUDACC_RTC__)
 #include <stdint.h>
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -122,17 +124,29 @@ typedef struct {
 } psk_output;
 
 /* Evaluate the group over every output element, in one launch (several for
- * more than 2^31 vectors of elements).  The output may alias an input only
+ * more than 2^30 vectors of elements) of a kernel generated for this program
+ * and compiled at run time on its first use (see psk_group_prepare).  The output may alias an input only
  * if that input has exactly the output's layout (same pointer, dtype and
  * row-major strides): each element is then read before it is written.  Any
  * other overlap is refused with PSK_E_ALIAS when the pointers show it. */
 int psk_group_run(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
                   const psk_output* out, void* stream);
 
-/* Host-only check of a program (no launch, no device needed): returns 0 and
- * the number of op nodes and of per-thread value slots the kernel will use,
- * or the refusal psk_group_run would give. */
-int psk_group_check(const psk_program* prog, int32_t n_inputs, int32_t* n_nodes, int32_t* n_slots);
+/* Host-only check of a program (no launch, no device needed): returns 0, the
+ * number of op nodes and the most f32 values (inputs and node results) one
+ * element keeps live at once, or the refusal psk_group_run would give. */
+int psk_group_check(const psk_program* prog, int32_t n_inputs, int32_t* n_nodes, int32_t* n_values);
+
+/* Host-only, synchronous, needs no device: everything psk_group_run does
+ * before the launch -- validate the program and the descriptors, and compile
+ * (once per process; cached) the kernel specialised for this program, its
+ * inputs' storage types and access modes, the vector width and the root's
+ * storage type.  Pointers are inspected for alignment and overlap only, never
+ * dereferenced.  Lets a caller take the compile (about a second) out of a
+ * timed or latency-sensitive region; psk_group_run compiles on first use
+ * otherwise.  Returns the refusal psk_group_run would give, or PSK_E_CUDA
+ * with the compiler's message. */
+int psk_group_prepare(const psk_program* prog, const psk_input* inputs, int32_t n_inputs, const psk_output* out);
 
 /* ================================================== psk_softmax_region
  * y[r, :] = softmax(x[r, :]) over rows of `cols` elements: m = max_j x[r,j]

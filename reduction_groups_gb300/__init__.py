@@ -10,6 +10,7 @@ from .ops import (  # noqa: F401
     psk_adamw_tree,
     psk_device_status,
     psk_group_check,
+    psk_group_prepare,
     psk_group_run,
     psk_softmax_region,
 )

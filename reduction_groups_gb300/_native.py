@@ -23,7 +23,7 @@ ERRORS = {
     -5: "PSK_E_NULL", -6: "PSK_E_ORDER", -7: "PSK_E_CUDA", -8: "PSK_E_ALIAS", -9: "PSK_E_ARG",
 }
 
-EXPORTS = ("psk_group_run", "psk_group_check", "psk_softmax_region", "psk_adamw_tree",
+EXPORTS = ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_adamw_tree",
            "psk_adamw_scalars", "psk_device_status", "psk_last_error")
 
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         P = ctypes.POINTER
         L.psk_group_run.argtypes = [P(psk_program), P(psk_input), ctypes.c_int32, P(psk_output), ctypes.c_void_p]
         L.psk_group_check.argtypes = [P(psk_program), ctypes.c_int32, P(ctypes.c_int32), P(ctypes.c_int32)]
+        L.psk_group_prepare.argtypes = [P(psk_program), P(psk_input), ctypes.c_int32, P(psk_output)]
         L.psk_softmax_region.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          psk_order, ctypes.c_int32, ctypes.c_void_p]
@@ -81,7 +82,8 @@ def lib() -> ctypes.CDLL:
         L.psk_adamw_scalars.argtypes = [P(psk_adamw_hparams), P(ctypes.c_float)]
         L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_last_error.restype = ctypes.c_char_p
-        for f in ("psk_group_run", "psk_group_check", "psk_softmax_region", "psk_adamw_tree", "psk_adamw_scalars",
+        for f in ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_adamw_tree",
+                  "psk_adamw_scalars",
                   "psk_device_status"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L

@@ -22,9 +22,11 @@
 
 #pragma once
 
+#if !defined(__CUDACC_RTC__)   // the run-time compiler has its own built-ins
 #include <stdint.h>
 #include <math.h>
 #include <string.h>
+#endif
 
 #if defined(PSK_HOST_BUILD)
 #define PSK_HD static inline

@@ -1,0 +1,239 @@
+// Device side of a fusion group (PSK-Realize, "What a group is"): the kernel
+// parameter block and the pieces every specialised group kernel is built
+// from -- coordinates of a vector of V output elements, input loads, the node
+// operations, the root's store.  The host generates, per program, a kernel
+// that calls these pieces in the program's node order and compiles it at run
+// time; this header is part of that kernel's source (no host headers).
+#pragma once
+
+#include "../../include/psk.h"
+#include "devcommon.cuh"
+#include "crmath.cuh"
+
+namespace psk {
+
+constexpr int GROUP_THREADS = 128;
+
+// How an input walks the last (collapsed) output axis.
+enum : int32_t { IN_CONTIG = 0, IN_BCAST = 1, IN_GATHER = 2 };
+
+struct GroupInput {
+  const void* ptr;
+  int64_t stride[4];   // elements per step of each collapsed output axis
+  int32_t dtype;
+  int32_t mode;
+};
+
+// The launch parameter (a __grid_constant__ block in the constant bank).
+struct GroupParams {
+  GroupInput in[PSK_MAX_INPUTS];
+  float imm[PSK_MAX_IMM];
+  void* out;
+  uint32_t rank;            // collapsed rank, 1..4 (axes padded at the front)
+  uint32_t dim[4];          // collapsed dims (dim[3] = last axis)
+  FastDiv div_cv;           // vectors per row: dim[3] / V
+  FastDiv div2, div1;       // dim[2], dim[1]
+  uint64_t v_begin;         // first vector of this launch
+  uint32_t n_vec;           // vectors in this launch
+};
+
+// exp and erf tables staged once per CTA in shared memory.
+struct MathTables {
+  float exp_hi[32], exp_lo[32];
+  float erf_hi[(PSK_ERF_D32 + 1) * 32];
+  float erf_lo[PSK_ERF_NPAIR * 32];
+};
+
+__device__ __forceinline__ void load_tables(MathTables& t) {
+  for (int i = threadIdx.x; i < 32; i += blockDim.x) { t.exp_hi[i] = psk_exp_tab_hi[i]; t.exp_lo[i] = psk_exp_tab_lo[i]; }
+  for (int i = threadIdx.x; i < (PSK_ERF_D32 + 1) * 32; i += blockDim.x) t.erf_hi[i] = (&psk_erf_c32hi[0][0])[i];
+  for (int i = threadIdx.x; i < PSK_ERF_NPAIR * 32; i += blockDim.x) t.erf_lo[i] = (&psk_erf_c32lo[0][0])[i];
+}
+
+template <int V> struct Vec { float v[V]; };
+
+template <int V>
+__device__ __forceinline__ Vec<V> splat(float q) {
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) r.v[j] = q;
+  return r;
+}
+
+// Output vector v -> coordinates (i0, i1, i2, i3) of its first element in the
+// collapsed output (i3 along the last axis).
+template <int V>
+__device__ __forceinline__ void vec_coords(const GroupParams& P, uint64_t v, uint32_t& i0, uint32_t& i1, uint32_t& i2,
+                                           uint32_t& i3) {
+  const uint32_t vlo = (uint32_t)v;   // a call never indexes past 2^32 vectors
+  const uint32_t row = P.div_cv.div(vlo);
+  i3 = (vlo - row * (P.dim[3] / V)) * V;
+  i2 = row;
+  i1 = 0;
+  i0 = 0;
+  if (P.rank > 2) {
+    const uint32_t q2 = P.div2.div(row);
+    i2 = row - q2 * P.dim[2];
+    if (P.rank > 3) {
+      const uint32_t q1 = P.div1.div(q2);
+      i1 = q2 - q1 * P.dim[1];
+      i0 = q1;
+    } else {
+      i1 = q2;
+    }
+  }
+}
+
+// Input k at the vector's coordinates: contiguous inputs load 16 B (f32) or
+// 8 B (bf16) at once, broadcast ones one element, the rest gather.
+template <int V, int DT, int MODE>
+__device__ __forceinline__ Vec<V> load_in(const GroupInput& in, uint32_t i0, uint32_t i1, uint32_t i2, uint32_t i3) {
+  const int64_t off = (int64_t)i0 * in.stride[0] + (int64_t)i1 * in.stride[1] + (int64_t)i2 * in.stride[2] +
+                      (int64_t)i3 * in.stride[3];
+  Vec<V> r;
+  if (DT == PSK_F32) {
+    const float* p = (const float*)in.ptr + off;
+    if (V == 4 && MODE == IN_CONTIG) {
+      const float4 q = __ldg((const float4*)p);
+      r.v[0] = q.x; r.v[1 % V] = q.y; r.v[2 % V] = q.z; r.v[3 % V] = q.w;
+    } else if (MODE == IN_BCAST) {
+      r = splat<V>(__ldg(p));
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) r.v[j] = __ldg(p + j * in.stride[3]);
+    }
+  } else {
+    const uint16_t* p = (const uint16_t*)in.ptr + off;
+    if (V == 4 && MODE == IN_CONTIG) {
+      const uint2 q = __ldg((const uint2*)p);
+      r.v[0] = __uint_as_float(q.x << 16);
+      r.v[1 % V] = __uint_as_float(q.x & 0xFFFF0000u);
+      r.v[2 % V] = __uint_as_float(q.y << 16);
+      r.v[3 % V] = __uint_as_float(q.y & 0xFFFF0000u);
+    } else if (MODE == IN_BCAST) {
+      r = splat<V>(bf16_bits_to_f32(__ldg(p)));
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) r.v[j] = bf16_bits_to_f32(__ldg(p + j * in.stride[3]));
+    }
+  }
+  return r;
+}
+
+// ------------------------------------------------------------- node ops
+// Binary nodes: IEEE binary32, one rounding; max(a, b) = a > b ? a : b and
+// min(a, b) = a < b ? a : b (a tie, and NaN, give the second operand).
+#define PSK_NODE2(NAME, EXPR)                                                        \
+  template <int V>                                                                   \
+  __device__ __forceinline__ Vec<V> NAME(const Vec<V>& A, const Vec<V>& B) {         \
+    Vec<V> r;                                                                        \
+    _Pragma("unroll") for (int j = 0; j < V; ++j) {                                  \
+      const float a = A.v[j], b = B.v[j];                                            \
+      r.v[j] = (EXPR);                                                               \
+    }                                                                                \
+    return r;                                                                        \
+  }
+PSK_NODE2(node_add, __fadd_rn(a, b))
+PSK_NODE2(node_sub, __fsub_rn(a, b))
+PSK_NODE2(node_mul, __fmul_rn(a, b))
+PSK_NODE2(node_div, __fdiv_rn(a, b))
+PSK_NODE2(node_max, a > b ? a : b)
+PSK_NODE2(node_min, a < b ? a : b)
+#undef PSK_NODE2
+
+#define PSK_NODE1(NAME, EXPR)                                                        \
+  template <int V>                                                                   \
+  __device__ __forceinline__ Vec<V> NAME(const Vec<V>& A) {                          \
+    Vec<V> r;                                                                        \
+    _Pragma("unroll") for (int j = 0; j < V; ++j) {                                  \
+      const float a = A.v[j];                                                        \
+      r.v[j] = (EXPR);                                                               \
+    }                                                                                \
+    return r;                                                                        \
+  }
+PSK_NODE1(node_neg, -a)
+PSK_NODE1(node_abs, fabsf(a))
+PSK_NODE1(node_sqrt, __fsqrt_rn(a))
+PSK_NODE1(node_sqrta, __fsqrt_rn(fabsf(a)))
+#undef PSK_NODE1
+
+// exp, exp(clamp(a, -4, 4)), erf and gelu: one out-of-line copy each, called
+// by every such node (the kernel's code stays small enough for the
+// instruction cache).  The tier-1 cores of the V elements run side by side
+// (independent chains for the scheduler); undecided elements go on to the
+// slower tiers.
+template <int V, bool CLAMP>
+__device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
+  float a[V], R[V], d[V];
+  int n[V];
+  bool inr[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    a[j] = A.v[j];
+    if (CLAMP) {
+      a[j] = a[j] > -4.0f ? a[j] : -4.0f;
+      a[j] = a[j] < 4.0f ? a[j] : 4.0f;
+    }
+    inr[j] = fabsf(a[j]) <= 87.0f;
+    exp_tier1_core(inr[j] ? a[j] : 0.0f, tab.exp_hi, tab.exp_lo, R[j], d[j], n[j]);
+  }
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    float o = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
+    if (!(inr[j] && tier1_decided(R[j], d[j]))) o = exp_tier2(a[j]);
+    r.v[j] = o;
+  }
+  return r;
+}
+
+// gelu(a) = a * (0.5 * (1 + erf(a * RN(1/sqrt 2)))), every step rounded.
+template <int V, bool GELU>
+__device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
+  float tt[V], R[V], d[V];
+  bool inr[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    tt[j] = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
+    const float aa = fabsf(tt[j]);
+    inr[j] = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
+    erf_tier1_core(inr[j] ? aa : 0.5f, tab.erf_hi, tab.erf_lo, R[j], d[j]);
+  }
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    float e = R[j];
+    if (!(inr[j] && tier1_decided(R[j], d[j]))) e = erf_abs_rest(fabsf(tt[j]));
+    e = copysignf(e, tt[j]);
+    r.v[j] = GELU ? __fmul_rn(A.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, e))) : e;
+  }
+  return r;
+}
+
+template <int V> __device__ __forceinline__ Vec<V> node_exp(const Vec<V>& a, const MathTables& t) { return node_exp_any<V, false>(a, t); }
+template <int V> __device__ __forceinline__ Vec<V> node_expc(const Vec<V>& a, const MathTables& t) { return node_exp_any<V, true>(a, t); }
+template <int V> __device__ __forceinline__ Vec<V> node_erf(const Vec<V>& a, const MathTables& t) { return node_erf_any<V, false>(a, t); }
+template <int V> __device__ __forceinline__ Vec<V> node_gelu(const Vec<V>& a, const MathTables& t) { return node_erf_any<V, true>(a, t); }
+
+// The root, rounded once to its storage type, row-major.
+template <int V, int OUT>
+__device__ __forceinline__ void store_root(const GroupParams& P, uint64_t v, const Vec<V>& r) {
+  const uint64_t e0 = v * V;
+  if (OUT == PSK_F32) {
+    float* o = (float*)P.out + e0;
+    if (V == 4) *(float4*)o = make_float4(r.v[0], r.v[1 % V], r.v[2 % V], r.v[3 % V]);
+    else o[0] = r.v[0];
+  } else {
+    uint16_t* o = (uint16_t*)P.out + e0;
+    if (V == 4) {
+      uint2 q;
+      q.x = f32x2_to_bf16x2(r.v[0], r.v[1 % V]);
+      q.y = f32x2_to_bf16x2(r.v[2 % V], r.v[3 % V]);
+      *(uint2*)o = q;
+    } else {
+      o[0] = f32_to_bf16_bits(r.v[0]);
+    }
+  }
+}
+
+}  // namespace psk

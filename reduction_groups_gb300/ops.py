@@ -44,17 +44,14 @@ def _program(tokens, imm):
 
 
 def psk_group_check(tokens, n_inputs: int, imm=None):
-    """Validate a program on the host; returns (n_nodes, n_slots)."""
+    """Validate a program on the host; returns (n_nodes, n_values)."""
     p, keep = _program(tokens, imm)
     nn, ns = ctypes.c_int32(0), ctypes.c_int32(0)
     N.check(N.lib().psk_group_check(ctypes.byref(p), int(n_inputs), ctypes.byref(nn), ctypes.byref(ns)))
     return nn.value, ns.value
 
 
-def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
-    """inputs: list of (tensor, strides) with one element stride per output axis
-    (0 = broadcast); out: a contiguous row-major tensor (f32 or bf16)."""
-    p, keep = _program(tokens, imm)
+def _group_args(inputs, out):
     n = len(inputs)
     arr = (N.psk_input * max(n, 1))()
     for i, (t, strides) in enumerate(inputs):
@@ -71,6 +68,22 @@ def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
     o.rank = out.dim()
     for k, s in enumerate(out.shape):
         o.shape[k] = int(s)
+    return arr, n, o
+
+
+def psk_group_prepare(tokens, imm, inputs, out) -> None:
+    """Validate and compile (cached) the kernel psk_group_run would launch for
+    these arguments; needs no device (tensors are inspected, not read)."""
+    p, keep = _program(tokens, imm)
+    arr, n, o = _group_args(inputs, out)
+    N.check(N.lib().psk_group_prepare(ctypes.byref(p), arr, n, ctypes.byref(o)))
+
+
+def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
+    """inputs: list of (tensor, strides) with one element stride per output axis
+    (0 = broadcast); out: a contiguous row-major tensor (f32 or bf16)."""
+    p, keep = _program(tokens, imm)
+    arr, n, o = _group_args(inputs, out)
     N.check(N.lib().psk_group_run(ctypes.byref(p), arr, n, ctypes.byref(o), _stream_handle(stream)))
 
 

@@ -101,7 +101,7 @@ def test_program_check_matches_oracle_definition(native):
         try:
             nn, ns = ops.psk_group_check(toks, 3, imm)
             got = ("ok", nn)
-            assert ns >= 3
+            assert 1 <= ns <= nn + 3
         except native.PskError as e:
             assert e.name in ("PSK_E_PROGRAM", "PSK_E_TOO_MANY_NODES")
             got = ("refused", None)
@@ -143,3 +143,40 @@ def test_adamw_scalars_refuse_bad_hyperparameters(native):
         hp = W.AdamWHyper(**bad)
         with pytest.raises(native.PskError):
             ops.psk_adamw_scalars(hp)
+
+
+def test_group_prepare_compiles_every_op_and_layout(native):
+    """The kernel generator and the run-time compiler on the host (no device):
+    one program with every op, in each storage type, access mode and vector
+    width; tensors are inspected, never read."""
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    seq = [("IN", 0), ("IN", 1), ("ADD",), ("IN", 2), ("SUB",), ("IMM", 0), ("MUL",), ("IN", 0), ("DIV",),
+           ("REF", 0), ("MAX",), ("IN", 1), ("MIN",), ("NEG",), ("ABS",), ("EXP",), ("EXPC",), ("GELU",),
+           ("SQRT",), ("SQRTA",), ("ERF",), ("IMM", 1), ("REF", 2), ("SUB",), ("ADD",)]
+    toks = W.encode(seq)
+    imm = np.array([0.5, -3.0], dtype=np.float32)
+    for din in (torch.float32, torch.bfloat16):
+        for dout in (torch.float32, torch.bfloat16):
+            for cols, step in ((16, 1), (15, 1), (16, 2)):     # contiguous, V = 1, gathered
+                x = torch.zeros(8, cols * step, dtype=din)
+                row = torch.zeros(cols, dtype=din)
+                col = torch.zeros(8, 1, dtype=din)
+                out = torch.zeros(8, cols, dtype=dout)
+                ops.psk_group_prepare(toks, imm, [(x, (cols * step, step)), (row, (0, 1)), (col, (1, 0))], out)
+
+
+def test_group_prepare_refuses_as_check(native):
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    x = torch.zeros(4, 4)
+    bad = W.encode([("IN", 0)] + [("NEG",)] * 65)
+    with pytest.raises(native.PskError) as e:
+        ops.psk_group_prepare(bad, None, [(x, (4, 1))], torch.zeros(4, 4))
+    assert e.value.name == "PSK_E_TOO_MANY_NODES"
+    ops.psk_group_prepare(W.encode([("IN", 0), ("NEG",)]), None, [(x, (4, 1))], x)      # in place: allowed
+    with pytest.raises(native.PskError) as e:                                             # transposed: races
+        ops.psk_group_prepare(W.encode([("IN", 0), ("NEG",)]), None, [(x, (1, 4))], x)
+    assert e.value.name == "PSK_E_ALIAS"
