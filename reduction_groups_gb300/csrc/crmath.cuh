@@ -28,14 +28,19 @@
 #include <string.h>
 #endif
 
+// PSK_TAB: tables read with a uniform index (constant memory on the device);
+// PSK_GTAB: tables read with a per-lane index (global memory, cached in L1,
+// or staged by a kernel into shared memory).
 #if defined(PSK_HOST_BUILD)
 #define PSK_HD static inline
 #define PSK_NOINLINE static
 #define PSK_TAB static const
+#define PSK_GTAB static const
 #else
 #define PSK_HD __device__ __forceinline__
 #define PSK_NOINLINE static __device__ __noinline__
 #define PSK_TAB static __constant__ const
+#define PSK_GTAB static __device__ const
 #endif
 
 #include "crmath_tables.inc"
@@ -210,46 +215,55 @@ PSK_NOINLINE float exp_tier2(float xf) {
   return ok ? res : exp_tier3(xf);
 }
 
-// Tier 1 core, |x| <= 87 (normal results).  thi/tlo: 2^(j/32) as float
-// pairs.  Returns R (the nearest float to the approximation) and d, with
-// exp(x) = (R + d) 2^n (1 + delta), |delta| < 2^-42.
-PSK_HD void exp_tier1_core(float x, const float* thi, const float* tlo, float& R, float& d, int& n) {
-  float kf = rintf(x * PSK_EXP_INV_L);
-  int k = (int)kf;
-  int j = k & 31;
-  n = k >> 5;
-  // r = x - k ln2/32 as rh + rl (Cody-Waite, three pieces; the first two
-  // products are exact and x - k L1 is exact by Sterbenz's lemma)
-  float r1 = fmaf(-kf, PSK_EXP_L1, x);
-  float p2 = kf * PSK_EXP_L2;
-  float p3 = kf * PSK_EXP_L3;
-  float ph, pl;
-  fast_two_sum(-p2, -p3, ph, pl);
-  float rh, rl;
-  two_sum(r1, ph, rh, rl);
-  rl = rl + pl;
-  float Th = thi[j], Tl = tlo[j];
-  // e^r - 1 = rh + rh^2/2 + C,  C = rl (1 + rh + rh^2/2) + (rh^2 - s)/2 + rh^3 (1/6 + rh/24 + rh^2/120)
-  float s, se;
-  two_prod(rh, rh, s, se);
-  float B = 0.5f * s;
-  float q3 = fmaf(fmaf(rh, 1.0f / 120.0f, 1.0f / 24.0f), rh, 1.0f / 6.0f);
-  float C = fmaf(rl, rh + B, rl);
-  C = fmaf(0.5f, se, C);
-  C = fmaf(s * rh, q3, C);
-  // y = Th + Th rh + Th B + [Th C + Tl (1 + rh + B)]
-  float m1, e1, m2, e2;
-  two_prod(Th, rh, m1, e1);
-  two_prod(Th, B, m2, e2);
-  float low = fmaf(Th, C, Tl);
-  low = fmaf(Tl, rh + B, low);
-  low = low + (e1 + e2);
-  float h1, l1, h2, l2;
-  fast_two_sum(Th, m1, h1, l1);
-  fast_two_sum(h1, m2, h2, l2);
-  float lo = (l1 + l2) + low;
-  R = h2 + lo;
-  d = lo - (R - h2);
+// Entry j of a table of float pairs (hi, lo) stored interleaved; one 8-byte
+// load on the device (the table is 8-byte aligned).
+PSK_HD void load_pair(const float* tab2, int j, float& hi, float& lo) {
+#if defined(PSK_HOST_BUILD)
+  hi = tab2[2 * j];
+  lo = tab2[2 * j + 1];
+#else
+  const float2 t = *reinterpret_cast<const float2*>(tab2 + 2 * j);
+  hi = t.x;
+  lo = t.y;
+#endif
+}
+
+// Tier 1 core, |x| <= 87 (normal results).  tab2: 2^(j/1024), j = 0..1023,
+// as float pairs (hi, lo) interleaved.  Returns R (the nearest float to the
+// approximation) and d, with exp(x) = (R + d) 2^n (1 + delta), |delta| < 2^-42.
+//
+// x = k ln2/1024 + r, |r| <= ln2/2048 (< 2^-11.4), k = 1024 n + j; and
+// r = r1 + c with r1 = x - k L1 exact (L1 = RN(ln2/1024): r1 is a multiple
+// of 2^-35 below 2^-11, so 24 bits hold it) and c = -k (L2 + L3),
+// |c| < 2^-21.99.  Then e^r - 1 = r1 + ql with
+//   ql = c (1 + r1) + r1^2 (1/2 + r1/6)
+// (dropped: r^4/24, c^2/2 and c r1^2/2, each below 2^-45), and
+//   exp(x) 2^-n = Th + Th r1 + [Th ql + Tl (1 + r1)]
+// (dropped: Tl ql < 2^-45), where Th r1 is split exactly (two_prod) and added
+// to Th exactly (Fast2Sum, |Th r1| < Th), and the bracket (< 2^-20.5) takes one
+// rounding of its own.
+PSK_HD void exp_tier1_core(float x, const float* tab2, float& R, float& d, int& n) {
+  const float kf = rintf(x * PSK_EXP_INV_L);
+  const int k = (int)kf;
+  n = k >> 10;
+  const int j = k & 1023;
+  const float r1 = fmaf(-kf, PSK_EXP_L1, x);
+  const float c = fmaf(-kf, PSK_EXP_L2, -kf * PSK_EXP_L3);
+  float Th, Tl;
+  load_pair(tab2, j, Th, Tl);
+  const float s = r1 * r1;
+  const float p = fmaf(r1, 1.0f / 6.0f, 0.5f);
+  const float u = fmaf(c, r1, c);
+  const float ql = fmaf(s, p, u);
+  float m1, e1;
+  two_prod(Th, r1, m1, e1);
+  const float t = fmaf(Tl, r1, Tl + e1);
+  const float low = fmaf(Th, ql, t);
+  float h, l;
+  fast_two_sum(Th, m1, h, l);
+  const float lo = l + low;
+  R = h + lo;
+  d = lo - (R - h);
 }
 
 // Keep R when |d| plus the error bound stays below half an ulp of R (R not a
@@ -261,19 +275,19 @@ PSK_HD bool tier1_decided(float R, float d) {
   return ((rb & 0x007fffffu) != 0u) && (fabsf(d) <= hu * 0.99996948f);
 }
 
-PSK_HD bool exp_tier1(float x, const float* thi, const float* tlo, float& out) {
+PSK_HD bool exp_tier1(float x, const float* tab2, float& out) {
   float R, d;
   int n;
-  exp_tier1_core(x, thi, tlo, R, d, n);
+  exp_tier1_core(x, tab2, R, d, n);
   out = u2f((uint32_t)((int32_t)f2u(R) + n * (1 << 23)));
   return tier1_decided(R, d);
 }
 
-// Correctly rounded exp; thi/tlo point at the 2^(j/32) float-pair table
-// (shared memory in kernels).
-PSK_HD float exp_cr(float x, const float* thi, const float* tlo) {
+// Correctly rounded exp; tab2 points at the 2^(j/1024) float-pair table
+// (psk_exp_tab2, or a copy of it in shared memory).
+PSK_HD float exp_cr(float x, const float* tab2) {
   float r;
-  if (fabsf(x) <= 87.0f && exp_tier1(x, thi, tlo, r)) return r;
+  if (fabsf(x) <= 87.0f && exp_tier1(x, tab2, r)) return r;
   return exp_tier2(x);
 }
 

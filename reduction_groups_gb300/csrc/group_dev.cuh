@@ -39,13 +39,14 @@ struct GroupParams {
 
 // exp and erf tables staged once per CTA in shared memory.
 struct MathTables {
-  float exp_hi[32], exp_lo[32];
+  float2 exp_tab[PSK_EXP_TAB_N];   // 2^(j/1024) as (hi, lo)
   float erf_hi[(PSK_ERF_D32 + 1) * 32];
   float erf_lo[PSK_ERF_NPAIR * 32];
 };
 
 __device__ __forceinline__ void load_tables(MathTables& t) {
-  for (int i = threadIdx.x; i < 32; i += blockDim.x) { t.exp_hi[i] = psk_exp_tab_hi[i]; t.exp_lo[i] = psk_exp_tab_lo[i]; }
+  const float2* src = reinterpret_cast<const float2*>(psk_exp_tab2);
+  for (int i = threadIdx.x; i < PSK_EXP_TAB_N; i += blockDim.x) t.exp_tab[i] = src[i];
   for (int i = threadIdx.x; i < (PSK_ERF_D32 + 1) * 32; i += blockDim.x) t.erf_hi[i] = (&psk_erf_c32hi[0][0])[i];
   for (int i = threadIdx.x; i < PSK_ERF_NPAIR * 32; i += blockDim.x) t.erf_lo[i] = (&psk_erf_c32lo[0][0])[i];
 }
@@ -175,7 +176,7 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
       a[j] = a[j] < 4.0f ? a[j] : 4.0f;
     }
     inr[j] = fabsf(a[j]) <= 87.0f;
-    exp_tier1_core(inr[j] ? a[j] : 0.0f, tab.exp_hi, tab.exp_lo, R[j], d[j], n[j]);
+    exp_tier1_core(inr[j] ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
   }
   Vec<V> r;
 #pragma unroll

@@ -53,15 +53,15 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 template <int EXPM>
-__device__ __forceinline__ float region_exp(float d, const float* thi, const float* tlo) {
+__device__ __forceinline__ float region_exp(float d) {
   if (EXPM == PSK_EXP_FAST) return exp_faithful_nonpos(d);
-  return exp_cr(d, thi, tlo);
+  return exp_cr(d, psk_exp_tab2);
 }
 
 // exp of eight values: the correctly rounded tier-1 cores run side by side
 // (independent chains for the scheduler), the rare undecided lanes after.
 template <int EXPM>
-__device__ __forceinline__ void region_exp8(float* v, const float* thi, const float* tlo) {
+__device__ __forceinline__ void region_exp8(float* v) {
   if constexpr (EXPM == PSK_EXP_FAST) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = exp_faithful_nonpos(v[q]);
@@ -72,7 +72,7 @@ __device__ __forceinline__ void region_exp8(float* v, const float* thi, const fl
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       inr[q] = fabsf(v[q]) <= 87.0f;
-      exp_tier1_core(inr[q] ? v[q] : 0.0f, thi, tlo, R[q], d[q], n[q]);
+      exp_tier1_core(inr[q] ? v[q] : 0.0f, psk_exp_tab2, R[q], d[q], n[q]);
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -189,11 +189,9 @@ template <int XT, int YT, int EXPM, bool VEC>
 __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __grid_constant__ SoftmaxParams P) {
   constexpr int NBMAX = (XT == PSK_BF16) ? 4 : 2;
   extern __shared__ __align__(16) float smem[];
-  __shared__ float exp_hi[32], exp_lo[32];
   __shared__ float red[SM_THREADS / 32][NBMAX];
   __shared__ float rowsum[NBMAX], rowrcp[NBMAX];
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
-  if (EXPM == PSK_EXP_EXACT && t < 32) { exp_hi[t] = psk_exp_tab_hi[t]; exp_lo[t] = psk_exp_tab_lo[t]; }
   const int cols = (int)P.cols;
   const int nb = P.nb;
   const int parts = P.partials < cols ? P.partials : cols;
@@ -276,7 +274,7 @@ __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __gr
             raw_unpack(raw[b][k], v);
 #pragma unroll
             for (int q = 0; q < 8; ++q) v[q] = __fsub_rn(v[q], m[b]);
-            region_exp8<EXPM>(v, exp_hi, exp_lo);
+            region_exp8<EXPM>(v);
             *(float4*)&E[j] = make_float4(v[0], v[1], v[2], v[3]);
             *(float4*)&E[j + 4] = make_float4(v[4], v[5], v[6], v[7]);
           }
@@ -285,7 +283,7 @@ __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __gr
 #pragma unroll
         for (int k = 0; k < SM_EPT; ++k) {
           const int j = k * SM_THREADS + t;
-          if (j < cols) E[j] = region_exp<EXPM>(__fsub_rn(xs[b][k], m[b]), exp_hi, exp_lo);
+          if (j < cols) E[j] = region_exp<EXPM>(__fsub_rn(xs[b][k], m[b]));
         }
       }
     }
@@ -395,7 +393,6 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
   __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
   __shared__ float rowsum[PIPE_SE_MAX], rowrcp[PIPE_SE_MAX];
   __shared__ float red[PIPE_TEAMS][2][PIPE_TW];
-  __shared__ float exp_hi[32], exp_lo[32];
   __shared__ volatile int abort_flag;
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -416,7 +413,6 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
     abort_flag = 0;
     fence_barrier_init();
   }
-  if (EXPM == PSK_EXP_EXACT && tid < 32) { exp_hi[tid] = psk_exp_tab_hi[tid]; exp_lo[tid] = psk_exp_tab_lo[tid]; }
   __syncthreads();
 
   if (w == PIPE_CW + PIPE_KW) {
@@ -521,7 +517,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
           float u[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
-          region_exp8<EXPM>(u, exp_hi, exp_lo);
+          region_exp8<EXPM>(u);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const int j = (2 * h + kk) * (PIPE_TT * 4) + 4 * tt;
@@ -563,7 +559,6 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
 // ------------------------------------------------- streaming rows (> 4096)
 struct StreamShared {
   float E[SM_CAP];
-  float exp_hi[32], exp_lo[32];
   float red[SM_THREADS / 32];
   float part[SM_MAX_PARTIALS];
   float bcast;
@@ -584,7 +579,6 @@ template <int XT, int YT, int EXPM>
 __global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid_constant__ SoftmaxParams P) {
   __shared__ __align__(16) StreamShared sh;
   const int t = threadIdx.x;
-  if (EXPM == PSK_EXP_EXACT && t < 32) { sh.exp_hi[t] = psk_exp_tab_hi[t]; sh.exp_lo[t] = psk_exp_tab_lo[t]; }
   __syncthreads();
   const int64_t cols = P.cols;
   const int nP = (int)(cols < P.partials ? cols : P.partials);
@@ -598,7 +592,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid
     for (int64_t base = 0; base < cols; base += SM_CAP) {
       const int n = (int)((cols - base) < SM_CAP ? (cols - base) : SM_CAP);
       for (int i = t; i < n; i += SM_THREADS)
-        sh.E[i] = region_exp<EXPM>(__fsub_rn(load_x1<XT>(xr, base + i), m), sh.exp_hi, sh.exp_lo);
+        sh.E[i] = region_exp<EXPM>(__fsub_rn(load_x1<XT>(xr, base + i), m));
       __syncthreads();
       if (t < nP) {
         // chain t continues over the indices j = t (mod nP) of this chunk
@@ -619,7 +613,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid
     __syncthreads();
     const float s = sh.bcast, rs = __frcp_rn(s);
     for (int64_t j = t; j < cols; j += SM_THREADS) {
-      float e = region_exp<EXPM>(__fsub_rn(load_x1<XT>(xr, j), m), sh.exp_hi, sh.exp_lo);
+      float e = region_exp<EXPM>(__fsub_rn(load_x1<XT>(xr, j), m));
       store_y1<YT>(yr, j, div_by_recip(e, s, rs));
     }
     __syncthreads();

@@ -123,3 +123,35 @@ def test_division_through_reciprocal_equals_ieee():
     L.psk_host_div_check.argtypes = [ctypes.c_ulong, ctypes.c_long, ctypes.c_float, ctypes.c_float, ctypes.c_float]
     for seed, lo, hi, bmax in ((1, -100, 1, 4097.0), (2, -126, 1, 1e6), (3, -100, 100, 2.0 ** 20), (4, -30, 1, 3.0)):
         assert L.psk_host_div_check(seed, 5_000_000, lo, hi, bmax) == 0
+
+
+def test_tier1_relative_error_below_the_decision_bound(hm):
+    """Tier 1's decision assumes a relative error below 2^-40.  The value it
+    returns, (R + d) 2^n, against binary64 exp and erf (errors below 2^-52) on
+    every binade, uniform reals and the reduction's worst points (|r| at its
+    ln2/2048 limit); measured over every float in [-87, 87] the exp bound is
+    2^-43.2."""
+    from scipy.special import erf as erf64
+
+    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
+
+    def value(which, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.float64)
+        L.psk_host_tier1_value(ctypes.c_int(which), ctypes.c_void_p(x.ctypes.data), ctypes.c_void_p(y.ctypes.data),
+                               ctypes.c_long(x.size))
+        return y
+
+    rng = np.random.default_rng(11)
+    k = rng.integers(-128000, 128000, 400_000)
+    edge = ((k + 0.5) * np.log(2) / 1024).astype(np.float32)           # |r| near ln2/2048
+    xe = np.concatenate([_all_binades(-30, 6, 40_000, 12), rng.uniform(-87, 87, 1_000_000).astype(np.float32),
+                         edge])
+    xe = xe[np.abs(xe) <= 87]
+    rel = np.abs(value(0, xe) / np.exp(xe.astype(np.float64)) - 1)
+    assert rel.max() < 2.0 ** -42, np.log2(rel.max())
+    xa = np.concatenate([_all_binades(-60, 1, 20_000, 13), rng.uniform(0, 3.919, 1_000_000).astype(np.float32)])
+    xa = xa[(xa >= 2.0 ** -60) & (xa < 3.9192)]
+    ref = erf64(xa.astype(np.float64))
+    rel = np.abs(value(1, xa) / ref - 1)
+    assert rel.max() < 2.0 ** -42, np.log2(rel.max())
