@@ -35,12 +35,12 @@
 #define PSK_HD static inline
 #define PSK_NOINLINE static
 #define PSK_TAB static const
-#define PSK_GTAB static const
+#define PSK_GTAB alignas(16) static const
 #else
 #define PSK_HD __device__ __forceinline__
 #define PSK_NOINLINE static __device__ __noinline__
 #define PSK_TAB static __constant__ const
-#define PSK_GTAB static __device__ const
+#define PSK_GTAB static __device__ const __attribute__((aligned(16)))
 #endif
 
 #include "crmath_tables.inc"
@@ -325,28 +325,33 @@ PSK_NOINLINE float erf_tier2(float af) {
   return ok ? res : erf_tier3(af);
 }
 
-// Tier 1 core, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375).  chi: [10][32]
-// coefficient table (hi parts), clo: [5][32] low parts of coefficients 0..4
-// (shared memory in kernels).  erf(a) = (R + d)(1 + delta), |delta| < 2^-42.
-PSK_HD void erf_tier1_core(float a, const float* chi, const float* clo, float& R, float& d) {
-  int i = (int)rintf(a * 8.0f);
-  float t = a - (float)i * 0.125f;   // exact
-  float H = chi[9 * 32 + i];
-  H = fmaf(H, t, chi[8 * 32 + i]);
-  H = fmaf(H, t, chi[7 * 32 + i]);
-  H = fmaf(H, t, chi[6 * 32 + i]);
-  H = fmaf(H, t, chi[5 * 32 + i]);
-  // V4 = c4 + t H as a normalised pair; then V_k = c_k + t V_{k+1}, k = 3..0,
-  // each product exact (two_prod) and each sum renormalised (Fast2Sum)
-  float p, pe, vh, vl;
-  two_prod(t, H, p, pe);
-  fast_two_sum(chi[4 * 32 + i], p, vh, vl);
-  vl = vl + (pe + clo[4 * 32 + i]);
+// Tier 1 core, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375).  p2: coefficients
+// 0..3 of the 128 Taylor polynomials (width 1/32, centres i/32) as float pairs
+// [k][interval][hi, lo]; h: coefficients 4..D as floats [k - 4][interval]
+// (psk_erf_p2 / psk_erf_h, or copies in shared memory).
+// erf(a) = (R + d)(1 + delta), |delta| < 2^-42.
+//
+// t = a - i/32 (exact, |t| <= 1/64).  Coefficients 4..D by Horner in binary32
+// (their terms stay below 2^-18 of erf(a)); then V_k = c_k + t V_{k+1} for
+// k = 3..0 in float-float, each product split exactly (two_prod) and each
+// sum renormalised (Fast2Sum: |c_k| >= |t V_{k+1}| or c_k = 0 on every
+// interval, checked when the tables are generated).
+PSK_HD void erf_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
+  const int i = (int)rintf(a * 32.0f);
+  const float t = fmaf((float)i, -0.03125f, a);   // exact
+  float H = h[(PSK_ERF_D32 - PSK_ERF_NPAIR) * PSK_ERF_N32 + i];
 #pragma unroll
-  for (int k = 3; k >= 0; --k) {
+  for (int k = PSK_ERF_D32 - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
+  float p, pe, vh, vl, ch, cl;
+  two_prod(t, H, p, pe);
+  load_pair(p2 + (PSK_ERF_NPAIR - 1) * 2 * PSK_ERF_N32, i, ch, cl);
+  fast_two_sum(ch, p, vh, vl);
+  vl = vl + (pe + cl);
+#pragma unroll
+  for (int k = PSK_ERF_NPAIR - 2; k >= 0; --k) {
     two_prod(t, vh, p, pe);
     pe = fmaf(t, vl, pe);
-    float ch = chi[k * 32 + i], cl = clo[k * 32 + i];
+    load_pair(p2 + k * 2 * PSK_ERF_N32, i, ch, cl);
     fast_two_sum(ch, p, vh, vl);
     vl = vl + (pe + cl);
   }
@@ -354,9 +359,9 @@ PSK_HD void erf_tier1_core(float a, const float* chi, const float* clo, float& R
   d = vl - (R - vh);
 }
 
-PSK_HD bool erf_tier1(float a, const float* chi, const float* clo, float& out) {
+PSK_HD bool erf_tier1(float a, const float* p2, const float* h, float& out) {
   float d;
-  erf_tier1_core(a, chi, clo, out, d);
+  erf_tier1_core(a, p2, h, out, d);
   return tier1_decided(out, d);
 }
 
@@ -370,11 +375,11 @@ PSK_NOINLINE float erf_abs_rest(float a) {
 }
 
 // Correctly rounded erf (odd; erf(+-0) = +-0, erf(+-inf) = +-1, NaN stays NaN).
-PSK_HD float erf_cr(float x, const float* chi, const float* clo) {
+PSK_HD float erf_cr(float x, const float* p2, const float* h) {
   const float a = fabsf(x);
   const bool inr = a < PSK_ERF_ONE_FROM && a >= 0x1p-60f;
   float r;
-  if (!(inr && erf_tier1(a, chi, clo, r))) r = erf_abs_rest(a);
+  if (!(inr && erf_tier1(a, p2, h, r))) r = erf_abs_rest(a);
   return copysignf(r, x);
 }
 

@@ -14,7 +14,7 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
   for (long i = 0; i < n; ++i) {
     switch (which) {
       case 0: y[i] = exp_cr(x[i], psk_exp_tab2); break;
-      case 1: y[i] = erf_cr(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0]); break;
+      case 1: y[i] = erf_cr(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0]); break;
       default: y[i] = exp_faithful(x[i]); break;
     }
   }
@@ -28,7 +28,7 @@ void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char*
     bool k = true;
     if (tier == 1) {
       k = which == 0 ? exp_tier1(x[i], psk_exp_tab2, r)
-                     : erf_tier1(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0], r);
+                     : erf_tier1(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0], r);
     } else if (tier == 2) {
       r = which == 0 ? exp_tier2(x[i]) : erf_tier2(x[i]);
     } else {
@@ -49,7 +49,7 @@ void psk_host_tier1_value(int which, const float* x, double* y, long n) {
       exp_tier1_core(x[i], psk_exp_tab2, R, d, e);
       y[i] = ldexp((double)R + (double)d, e);
     } else {
-      erf_tier1_core(x[i], &psk_erf_c32hi[0][0], &psk_erf_c32lo[0][0], R, d);
+      erf_tier1_core(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0], R, d);
       y[i] = (double)R + (double)d;
     }
   }

@@ -40,15 +40,17 @@ struct GroupParams {
 // exp and erf tables staged once per CTA in shared memory.
 struct MathTables {
   float2 exp_tab[PSK_EXP_TAB_N];   // 2^(j/1024) as (hi, lo)
-  float erf_hi[(PSK_ERF_D32 + 1) * 32];
-  float erf_lo[PSK_ERF_NPAIR * 32];
+  float2 erf_p2[PSK_ERF_NPAIR * PSK_ERF_N32];                  // coefficients 0..3 as (hi, lo)
+  float erf_h[(PSK_ERF_D32 + 1 - PSK_ERF_NPAIR) * PSK_ERF_N32];  // coefficients 4..D
 };
 
 __device__ __forceinline__ void load_tables(MathTables& t) {
   const float2* src = reinterpret_cast<const float2*>(psk_exp_tab2);
   for (int i = threadIdx.x; i < PSK_EXP_TAB_N; i += blockDim.x) t.exp_tab[i] = src[i];
-  for (int i = threadIdx.x; i < (PSK_ERF_D32 + 1) * 32; i += blockDim.x) t.erf_hi[i] = (&psk_erf_c32hi[0][0])[i];
-  for (int i = threadIdx.x; i < PSK_ERF_NPAIR * 32; i += blockDim.x) t.erf_lo[i] = (&psk_erf_c32lo[0][0])[i];
+  const float2* p2 = reinterpret_cast<const float2*>(&psk_erf_p2[0][0]);
+  for (int i = threadIdx.x; i < PSK_ERF_NPAIR * PSK_ERF_N32; i += blockDim.x) t.erf_p2[i] = p2[i];
+  for (int i = threadIdx.x; i < (PSK_ERF_D32 + 1 - PSK_ERF_NPAIR) * PSK_ERF_N32; i += blockDim.x)
+    t.erf_h[i] = (&psk_erf_h[0][0])[i];
 }
 
 template <int V> struct Vec { float v[V]; };
@@ -198,7 +200,7 @@ __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
     tt[j] = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
     const float aa = fabsf(tt[j]);
     inr[j] = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
-    erf_tier1_core(inr[j] ? aa : 0.5f, tab.erf_hi, tab.erf_lo, R[j], d[j]);
+    erf_tier1_core(inr[j] ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h, R[j], d[j]);
   }
   Vec<V> r;
 #pragma unroll
