@@ -177,7 +177,7 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
       a[j] = a[j] > -4.0f ? a[j] : -4.0f;
       a[j] = a[j] < 4.0f ? a[j] : 4.0f;
     }
-    inr[j] = fabsf(a[j]) <= 87.0f;
+    inr[j] = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range (NaN clamps to -4)
     exp_tier1_core(inr[j] ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
   }
   Vec<V> r;
