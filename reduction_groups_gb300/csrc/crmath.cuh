@@ -418,11 +418,13 @@ PSK_HD float exp_faithful(float x) {
   return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
 }
 
-// The same faithful exp for x <= 0 or NaN (the softmax region's x - max):
-// no overflow to handle, and the scale stays a plain exponent add until the
-// result leaves the normal range.
+// The same faithful exp for x <= 0, NaN or -inf (the softmax region's
+// x - max), without branches: 2^k is applied as 2^(k+64) and then 2^-64 (one
+// rounding, in the second product, where the result is subnormal; exact
+// scalings otherwise), k held at -189, and x < -104 (below half the least
+// subnormal; -inf, whose reduction is NaN, included) gives 0.
 PSK_HD float exp_faithful_nonpos(float x) {
-  float kf = rintf(x * PSK_FEXP_INV_LN2);
+  const float kf = rintf(x * PSK_FEXP_INV_LN2);
   float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);
   r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
   float p = 1.0f / 5040.0f;
@@ -433,10 +435,9 @@ PSK_HD float exp_faithful_nonpos(float x) {
   p = fmaf(p, r, 0.5f);
   p = fmaf(p, r, 1.0f);
   p = fmaf(p, r, 1.0f);
-  int k = (int)kf;
-  if (k >= -125) return p * u2f((uint32_t)(k + 127) << 23);
-  if (k < -149 - 24) return 0.0f * p;
-  return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
+  const int k = kf > -189.0f ? (int)kf : -189;
+  const float y = (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
+  return x < -104.0f ? 0.0f : y;
 }
 
 }  // namespace psk

@@ -157,6 +157,29 @@ __device__ __forceinline__ float row_div(float e, float s, float rs, bool fast_o
   return y;
 }
 
+// N quotients e_q / s at once: Markstein's correction for all, one test for
+// the whole group, and the per-element path (IEEE division where the
+// correction's operand range is left) only for a group that needs it.
+template <int N>
+__device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast_ok) {
+  float y[N];
+  bool bad = !fast_ok;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const float e = o[q];
+    const float qq = e * rs;
+    const float r = fmaf(-qq, s, e);
+    y[q] = fmaf(r, rs, qq);
+    bad = bad || !(e >= 0x1p-100f);
+  }
+  if (bad) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) y[q] = row_div(o[q], s, rs, fast_ok);
+  }
+#pragma unroll
+  for (int q = 0; q < N; ++q) o[q] = y[q];
+}
+
 // One chain: acc over E[p], E[p+P], ... (n elements in the row), in index order.
 __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) {
   float acc = E[p];
@@ -342,8 +365,7 @@ __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __gr
           if (j < cols) {
             float4 a = *(const float4*)&E[j], c = *(const float4*)&E[j + 4];
             float o[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = row_div(o[q], s, rs, fast_ok);
+            row_div_n<8>(o, s, rs, fast_ok);
             store_y8<YT>(yr, j, o);
           }
         }
@@ -540,8 +562,9 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
         if (j < cols) {
           const float4 e = *reinterpret_cast<const float4*>(Er + j);
-          const float o0 = row_div(e.x, sm, rs, fast_ok), o1 = row_div(e.y, sm, rs, fast_ok);
-          const float o2 = row_div(e.z, sm, rs, fast_ok), o3 = row_div(e.w, sm, rs, fast_ok);
+          float o[4] = {e.x, e.y, e.z, e.w};
+          row_div_n<4>(o, sm, rs, fast_ok);
+          const float o0 = o[0], o1 = o[1], o2 = o[2], o3 = o[3];
           if (YT == PSK_F32) {
             __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o0, o1, o2, o3));
           } else {

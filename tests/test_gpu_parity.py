@@ -321,6 +321,43 @@ def test_softmax_fast_exp_within_tolerance(dev, order):
     assert np.max(np.abs(gb.astype(np.int32) - wb.astype(np.int32))) <= 1
 
 
+@pytest.mark.parametrize("xt", ["bf16", "f32"])
+def test_softmax_infinities_nan_and_underflow(dev, xt):
+    """-inf entries (exp gives 0), entries 90..130 below the row max (exp
+    subnormal or 0), an all -inf row and a row with a NaN (NaN rows), in both
+    exp modes: exact bit for bit; fast with the same zeros and NaNs, within
+    1e-6 relative on normal outputs and two units of 2^-149 on subnormal ones."""
+    rng = np.random.default_rng(21)
+    rows, cols = 12, 512
+    x = (rng.standard_normal((rows, cols)) * 3).astype(np.float32)
+    x[0, ::7] = -np.inf
+    x[1, 5:40] = np.linspace(-120.0, -80.0, 35)
+    x[1, 0] = 10.0
+    x[2, :] = -np.inf
+    x[3, 100] = np.nan
+    x[4, 3] = np.inf
+    x[5, 17:30] = -104.5
+    x[5, 0] = 0.0
+    xs = f32_to_bf16(x) if xt == "bf16" else x
+    for order in (("sequential",), ("interleaved", 8)):
+        want = OS.softmax_region(xs, xt, "f32", order)
+        y = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+        dev.psk_softmax_region(_to_dev(xs, xt), y, order, "exact")
+        torch.cuda.synchronize()
+        assert _same(_to_host(y), want, "f32").all()
+        dev.psk_softmax_region(_to_dev(xs, xt), y, order, "fast")
+        torch.cuda.synchronize()
+        got = _to_host(y)
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        fin = ~np.isnan(want)
+        xin = bf16_to_f32(xs) if xt == "bf16" else xs
+        assert np.all(got[fin & np.isneginf(xin)] == 0)          # exp(-inf) is 0 in both modes
+        w, g = want[fin].astype(np.float64), got[fin].astype(np.float64)
+        normal = np.abs(w) >= 2.0 ** -126
+        assert np.all(np.abs(g - w)[normal] <= 1e-6 * np.abs(w[normal]))
+        assert np.all(np.abs(g - w)[~normal] <= 2 * 2.0 ** -149)
+
+
 def test_softmax_refusals(dev):
     x = torch.zeros((4, 8), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dev.PskError) as e:
