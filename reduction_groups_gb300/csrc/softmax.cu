@@ -180,28 +180,49 @@ __device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast
   for (int q = 0; q < N; ++q) o[q] = y[q];
 }
 
-// One chain: acc over E[p], E[p+P], ... (n elements in the row), in index order.
+// One chain: acc over E[p], E[p+P], ... (n elements in the row), in index
+// order.  The loads of the next block are issued before the dependent adds of
+// the current one (registers double-buffered), so the chain runs at the add
+// latency instead of add + shared-memory latency per block.
 __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) {
   float acc = E[p];
   int j = p + P;
   if (P == 1) {
     for (; (j & 3) != 0 && j < n; ++j) acc = __fadd_rn(acc, E[j]);
-    for (; j + 15 < n; j += 16) {
+    if (j + 15 < n) {
       float4 a = *(const float4*)&E[j], b = *(const float4*)&E[j + 4];
       float4 c = *(const float4*)&E[j + 8], d = *(const float4*)&E[j + 12];
+      for (; j + 31 < n; j += 16) {
+        const float4 na = *(const float4*)&E[j + 16], nb = *(const float4*)&E[j + 20];
+        const float4 nc = *(const float4*)&E[j + 24], nd = *(const float4*)&E[j + 28];
+        acc = __fadd_rn(acc, a.x); acc = __fadd_rn(acc, a.y); acc = __fadd_rn(acc, a.z); acc = __fadd_rn(acc, a.w);
+        acc = __fadd_rn(acc, b.x); acc = __fadd_rn(acc, b.y); acc = __fadd_rn(acc, b.z); acc = __fadd_rn(acc, b.w);
+        acc = __fadd_rn(acc, c.x); acc = __fadd_rn(acc, c.y); acc = __fadd_rn(acc, c.z); acc = __fadd_rn(acc, c.w);
+        acc = __fadd_rn(acc, d.x); acc = __fadd_rn(acc, d.y); acc = __fadd_rn(acc, d.z); acc = __fadd_rn(acc, d.w);
+        a = na; b = nb; c = nc; d = nd;
+      }
       acc = __fadd_rn(acc, a.x); acc = __fadd_rn(acc, a.y); acc = __fadd_rn(acc, a.z); acc = __fadd_rn(acc, a.w);
       acc = __fadd_rn(acc, b.x); acc = __fadd_rn(acc, b.y); acc = __fadd_rn(acc, b.z); acc = __fadd_rn(acc, b.w);
       acc = __fadd_rn(acc, c.x); acc = __fadd_rn(acc, c.y); acc = __fadd_rn(acc, c.z); acc = __fadd_rn(acc, c.w);
       acc = __fadd_rn(acc, d.x); acc = __fadd_rn(acc, d.y); acc = __fadd_rn(acc, d.z); acc = __fadd_rn(acc, d.w);
+      j += 16;
     }
-  } else {
-    for (; j + 7 * P < n; j += 8 * P) {
-      float v[8];
+  } else if (j + 7 * P < n) {
+    float v[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = E[j + i * P];
+    for (int i = 0; i < 8; ++i) v[i] = E[j + i * P];
+    for (; j + 15 * P < n; j += 8 * P) {
+      float nv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nv[i] = E[j + (8 + i) * P];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, v[i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = nv[i];
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, v[i]);
+    j += 8 * P;
   }
   for (; j < n; j += P) acc = __fadd_rn(acc, E[j]);
   return acc;
@@ -425,7 +446,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
   uint16_t* X = reinterpret_cast<uint16_t*>(pipe_smem);
   float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xstr * 2);
   const int estride = P.estride;
-  const int parts = P.partials;
+  const int parts = P.partials < cols ? P.partials : cols;  // a partial beyond the row is empty
   const int G = P.nb;                                        // rows per chain group
   const int n_local = blockIdx.x < P.rows ? (int)((P.rows - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 
@@ -702,8 +723,9 @@ static int launch_pipe(SoftmaxParams P, cudaStream_t stream) {
   }
   P.sx = sx;
   P.se = se;
-  // chain group: G in {4, 2, 1} rows (a divisor of SE) of 32 / P lanes at most
-  const int glanes = 32 / P.partials;
+  // chain group: G in {4, 2, 1} rows (a divisor of SE) of 32 / P lanes at
+  // most (P partials, at most one per column)
+  const int glanes = 32 / (P.partials < P.cols ? P.partials : (int)P.cols);
   P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
   const size_t smem = sx * xrow + se * erow;
   static bool attr[PSK_MAX_DEVICES] = {};

@@ -262,7 +262,9 @@ _MANY_ROWS = ([(4000, 512, o, yt) for o in (("sequential",), ("interleaved", 2),
                                            ("interleaved", 32), ("interleaved", 40)) for yt in ("bf16", "f32")]
               + [(2000, 4096, o, "bf16") for o in (("sequential",), ("interleaved", 2), ("interleaved", 8),
                                                    ("interleaved", 12))]
-              + [(2000, 4096, ("sequential",), "f32"), (3000, 2048, ("sequential",), "bf16")])
+              + [(2000, 4096, ("sequential",), "f32"), (3000, 2048, ("sequential",), "bf16"),
+                 (600, 16, ("interleaved", 32), "bf16"), (600, 24, ("interleaved", 30), "f32"),
+                 (900, 1032, ("interleaved", 5), "bf16")])
 
 
 @pytest.mark.parametrize("rows,cols,order,yt", _MANY_ROWS)
