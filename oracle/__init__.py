@@ -15,6 +15,11 @@ What it computes, and where the pages define it:
   Reduce(Sum) -> Div over the last axis, with the sum's bracketing tree fixed
   by the declared order (poot "Fusion and Planning", Reduction-rooted regions;
   presk "Native execution", The realization: ``order``) -- ``oracle.softmax``;
+* the reduction-rooted normalization regions RMSNorm (sum of squares -> mean
+  -> +eps -> sqrt -> divide) and LayerNorm (mean -> x - mu -> sum of squares
+  -> mean -> +eps -> sqrt -> divide), with an optional scale and bias (poot
+  "Fusion and Planning", Reduction-rooted regions; PSK-Realize, "What it
+  removes") -- ``oracle.norm``;
 * the AdamW step as PyTorch defines it, one f32 chain per parameter over every
   leaf of the tree (presk "The language", The optimizer) -- ``oracle.adamw``;
 * exp and erf nodes return the correctly rounded f32 value of the function

@@ -187,6 +187,72 @@ def softmax_rows(rows: int = 32768, cols: int = 4096) -> SoftmaxWorkload:
     return SoftmaxWorkload("softmax_rows", SEED_BASE + 2, rows, cols, "bf16", "bf16", 3.0)
 
 
+@dataclass
+class NormWorkload:
+    """Rows of activations x ~N(mean, std^2) for a normalization region, a scale
+    gamma ~1 + N(0, 0.1^2) and (LayerNorm) a bias beta ~N(0, 0.1^2), stored in
+    x_dtype / param_dtype."""
+    name: str
+    seed: int
+    rows: int
+    cols: int
+    kind: str            # "rms" or "layer"
+    eps: float
+    x_dtype: str = "bf16"
+    y_dtype: str = "bf16"
+    param_dtype: str = "bf16"
+    std: float = 1.0
+    mean: float = 0.25
+
+    def _store(self, v, dtype):
+        return G.host_bf16_bits(v) if dtype == "bf16" else v
+
+    def host_x(self) -> np.ndarray:
+        v = (G.host_normal((self.rows, self.cols), self.std, self.seed, 0) + np.float32(self.mean)).astype(np.float32)
+        return self._store(v, self.x_dtype)
+
+    def host_gamma(self) -> np.ndarray:
+        v = (G.host_normal((self.cols,), 0.1, self.seed, 1) + np.float32(1.0)).astype(np.float32)
+        return self._store(v, self.param_dtype)
+
+    def host_beta(self):
+        if self.kind != "layer":
+            return None
+        return self._store(G.host_normal((self.cols,), 0.1, self.seed, 2), self.param_dtype)
+
+    def device_x(self, device="cuda"):
+        import torch
+
+        dt = torch.bfloat16 if self.x_dtype == "bf16" else torch.float32
+        v = G.device_normal((self.rows, self.cols), self.std, self.seed, 0, device, torch.float32) + self.mean
+        return v.to(dt)
+
+    def device_params(self, device="cuda"):
+        """(gamma, beta or None) on the device, drawn on the host (they are small)."""
+        import torch
+
+        def dev(a):
+            if a is None:
+                return None
+            if self.param_dtype == "bf16":
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+            return torch.from_numpy(a).to(device)
+
+        return dev(self.host_gamma()), dev(self.host_beta())
+
+    def algorithmic_bytes(self) -> int:
+        n = self.rows * self.cols
+        return n * (2 if self.x_dtype == "bf16" else 4) + n * (2 if self.y_dtype == "bf16" else 4)
+
+
+def norm_rows(kind: str, rows: int = 32768, cols: int = 4096) -> NormWorkload:
+    """RMSNorm (eps 1e-6) or LayerNorm (eps 1e-5) over bf16 rows, bf16 scale and
+    bias, f32 arithmetic, bf16 output: the softmax region's shape."""
+    if kind == "rms":
+        return NormWorkload("rms_rows", SEED_BASE + 5, rows, cols, "rms", 1e-6)
+    return NormWorkload("layer_rows", SEED_BASE + 6, rows, cols, "layer", 1e-5)
+
+
 # ----------------------------------------------------------- parameter trees
 
 @dataclass

@@ -11,11 +11,13 @@ import oracle.adamw as OA
 import oracle.crmath as OC
 import oracle.f32 as OF
 import oracle.group as OG
+import oracle.norm as ON
 import oracle.softmax as OS
 from tests import test_oracle_adamw as TA
 from tests import test_oracle_crmath as TC
 from tests import test_oracle_f32 as TF
 from tests import test_oracle_group as TG
+from tests import test_oracle_norm as TN
 from tests import test_oracle_softmax as TS
 
 
@@ -77,6 +79,36 @@ def _adamw_eps_inside_sqrt(monkeypatch):
     monkeypatch.setattr(OA, "step_leaf", wrong)
 
 
+def _norm_variance_over_n_minus_1(monkeypatch):
+    calls = {"k": 0}
+
+    def wrong(s, n):
+        calls["k"] += 1
+        return (s / (n - np.float32(1))).astype(np.float32) if calls["k"] % 2 == 0 else (s / n).astype(np.float32)
+
+    monkeypatch.setattr(ON, "_mean", wrong)
+
+
+def _norm_eps_after_sqrt(monkeypatch):
+    monkeypatch.setattr(ON, "_divisor", lambda var, e: (np.sqrt(var).astype(np.float32) + e).astype(np.float32))
+
+
+def _norm_no_mean_in_rms(monkeypatch):
+    real = ON._mean
+    monkeypatch.setattr(ON, "_mean", lambda s, n: real(s, np.float32(1)))
+
+
+def _norm_bias_before_scale(monkeypatch):
+    def wrong(y, g, b):
+        if b is not None:
+            y = (y + b[None, :]).astype(np.float32)
+        if g is not None:
+            y = (y * g[None, :]).astype(np.float32)
+        return y
+
+    monkeypatch.setattr(ON, "_affine", wrong)
+
+
 CASES = [
     (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
     (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
@@ -86,6 +118,10 @@ CASES = [
     (_interleaved_combined_backwards, lambda: TS.test_tiny_rows_exact(("interleaved", 3))),
     (_adamw_no_bias_correction, TA.test_against_torch_adamw_float64),
     (_adamw_eps_inside_sqrt, TA.test_first_step_closed_form),
+    (_norm_variance_over_n_minus_1, TN.test_layer_norm_of_two_values_is_plus_minus_one),
+    (_norm_eps_after_sqrt, TN.test_rms_closed_form_with_eps),
+    (_norm_no_mean_in_rms, TN.test_rms_of_a_constant_row_is_one),
+    (_norm_bias_before_scale, TN.test_gamma_and_beta),
 ]
 
 
