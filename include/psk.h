@@ -1,7 +1,7 @@
 /* psk.h -- C ABI of the fusion-group hot path on one GB300 (sm_103a).
  *
- * Three entry points run the three cases of a fusion group on the caller's
- * CUDA stream:
+ * Four entry points run the cases of a fusion group on the caller's CUDA
+ * stream:
  *
  *   psk_group_run       a connected chain of up to 64 elementwise nodes sharing
  *                       one loop nest, with broadcast inputs
@@ -11,6 +11,8 @@
  *                       order (poot "Fusion and Planning", Reduction-rooted
  *                       regions; presk "Native execution", the realization's
  *                       order);
+ *   psk_norm_region     the RMSNorm and LayerNorm row regions, the same
+ *                       skeleton with their own reductions and epilogues;
  *   psk_adamw_tree      the AdamW step as one parameter-tree group over every
  *                       leaf of a model, in one launch (PSK-Realize, Parameter
  *                       trees; presk "The language", The optimizer).
@@ -169,6 +171,30 @@ typedef enum { PSK_EXP_EXACT = 0, PSK_EXP_FAST = 1 } psk_exp_mode;
 
 int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
                        int64_t ldx, int64_t ldy, psk_order order, int32_t exp_mode, void* stream);
+
+/* ==================================================== psk_norm_region
+ * The normalization regions over rows of `cols` elements, each a last-axis
+ * reduction and its pointwise epilogue in one launch (poot "Fusion and
+ * Planning", Reduction-rooted regions: RMSNorm is sum-of-squares -> sqrt ->
+ * div; presk PSK-Realize, "What it removes": the layer normalization chain
+ * (x - mu)^2 -> mean -> +eps -> sqrt -> divide).  In f32, one rounding per
+ * operation, n = cols, eps rounded once to f32, every sum in the declared
+ * order (as psk_softmax_region's):
+ *   RMSNorm   ss = sum RN(x_j^2); d = sqrt(RN(RN(ss / n) + eps));
+ *             y_j = RN(x_j / d) [then RN(. * gamma_j)]
+ *   LayerNorm mu = RN(sum x_j / n); c_j = RN(x_j - mu); ss = sum RN(c_j^2);
+ *             d = sqrt(RN(RN(ss / n) + eps));
+ *             y_j = RN(c_j / d) [then RN(. * gamma_j)] [then RN(. + beta_j)]
+ * Divisions and sqrt are IEEE.  gamma and beta are DEVICE vectors of cols
+ * elements of param_dtype (f32 or bf16, widened exactly), or NULL for none;
+ * RMSNorm takes no beta.  x, y, ldx, ldy, rows, cols and in-place use as in
+ * psk_softmax_region; y must not overlap gamma or beta.  cols up to 49152;
+ * eps must be finite. */
+typedef enum { PSK_NORM_RMS = 0, PSK_NORM_LAYER = 1 } psk_norm_kind;
+
+int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
+                    int64_t ldx, int64_t ldy, int32_t kind, double eps, const void* gamma, const void* beta,
+                    int32_t param_dtype, psk_order order, void* stream);
 
 /* ====================================================== psk_adamw_tree
  * One AdamW step over every leaf, in place, one launch for the whole tree

@@ -12,6 +12,7 @@ from .ops import (  # noqa: F401
     psk_group_check,
     psk_group_prepare,
     psk_group_run,
+    psk_norm_region,
     psk_softmax_region,
 )
 from ._native import PskError  # noqa: F401

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libpsk.so")
 PSK_F32, PSK_BF16 = 0, 1
 PSK_ORDER_SEQUENTIAL, PSK_ORDER_BLOCKED, PSK_ORDER_INTERLEAVED = 0, 1, 2
 PSK_EXP_EXACT, PSK_EXP_FAST = 0, 1
+PSK_NORM_RMS, PSK_NORM_LAYER = 0, 1
 PSK_MAX_RANK = 4
 PSK_ADAMW_MAX_LEAVES = 512
 
@@ -23,7 +24,8 @@ ERRORS = {
     -5: "PSK_E_NULL", -6: "PSK_E_ORDER", -7: "PSK_E_CUDA", -8: "PSK_E_ALIAS", -9: "PSK_E_ARG",
 }
 
-EXPORTS = ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_adamw_tree",
+EXPORTS = ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_norm_region",
+           "psk_adamw_tree",
            "psk_adamw_scalars", "psk_device_status", "psk_last_error")
 
 
@@ -78,11 +80,16 @@ def lib() -> ctypes.CDLL:
         L.psk_softmax_region.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          psk_order, ctypes.c_int32, ctypes.c_void_p]
+        L.psk_norm_region.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
+                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int32, ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int32, psk_order, ctypes.c_void_p]
         L.psk_adamw_tree.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_hparams), ctypes.c_void_p]
         L.psk_adamw_scalars.argtypes = [P(psk_adamw_hparams), P(ctypes.c_float)]
         L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_last_error.restype = ctypes.c_char_p
-        for f in ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_adamw_tree",
+        for f in ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_norm_region",
+                  "psk_adamw_tree",
                   "psk_adamw_scalars",
                   "psk_device_status"):
             getattr(L, f).restype = ctypes.c_int

@@ -1,27 +1,32 @@
-// psk_softmax_region: the reduction-rooted row region Reduce(Max) -> Sub ->
-// Exp -> Reduce(Sum) -> Div over the last axis, in one kernel: the row is
-// reduced on chip, then the pointwise epilogue runs in the same kernel (poot
-// "Fusion and Planning", Reduction-rooted regions).  Arithmetic is f32 for
-// bf16 storage, and the sum follows the declared order's bracketing tree
+// Reduction-rooted row regions: a last-axis, keepdim reduction followed by
+// its pointwise epilogue, in one kernel -- the row is reduced on chip and the
+// epilogue runs in the same kernel (poot "Fusion and Planning",
+// Reduction-rooted regions).  Arithmetic is f32 for bf16 storage, one rounding
+// per operation, and every sum follows the declared order's bracketing tree
 // (presk "Native execution", the realization's order; metrale "The LKB in
 // Mathematics", section 2: bit parity is the same bracketing tree):
-//   sequential / blocked(w): one chain ((e0 + e1) + e2) + ... in index order;
+//   sequential / blocked(w): one chain ((v0 + v1) + v2) + ... in index order;
 //   interleaved(P): P chains, chain p over j = p mod P in increasing j, then
 //   the P partials added left to right.
 //
-// Rows of up to 4096 columns (the resident kernel): a CTA of 256 threads takes
-// NB rows at a time (4 for bf16 input, 2 for f32).  Each thread loads 16
-// elements of every row with 16-byte loads and keeps them packed in
-// registers; the NB row maxima are reduced together (warp shuffles, one
-// barrier); e = exp(x - m) goes to a shared-memory buffer per row; then one
-// warp runs every chain of the batch at once -- lane (b, p) adds chain p of
-// row b, eight loads issued ahead of each eight dependent adds -- and combines
-// each row's partials left to right; finally every thread divides its
-// elements by the row sum (Markstein's reciprocal correction, bit-identical to
-// IEEE division) and stores.  While one CTA's chain warp works, the other
-// CTAs on the SM compute, so the chain latency (512 dependent adds per chain
-// under interleaved(8), 4096 under sequential) overlaps the streaming work.
-// Longer rows stream through a second kernel in chunks of 4096.
+// Regions:
+//   psk_softmax_region  Reduce(Max) -> Sub -> Exp -> Reduce(Sum) -> Div;
+//   psk_norm_region     RMSNorm: Reduce(Sum of x^2) -> mean -> +eps -> sqrt ->
+//                       Div (-> * gamma); LayerNorm: Reduce(Sum) -> mean ->
+//                       x - mu -> Reduce(Sum of squares) -> mean -> +eps ->
+//                       sqrt -> Div (-> * gamma -> + beta) (PSK-Realize,
+//                       "What it removes").
+//
+// Kernels:
+//   region_pipe_kernel   rows of <= 4096 columns, 16-byte aligned, <= 32
+//                        partials (both regions): a warp-specialised pipeline,
+//                        described where it is defined;
+//   softmax_batch_kernel other softmax rows of <= 4096 columns: NB rows per
+//                        CTA, warp 0 runs the chains;
+//   softmax_stream_kernel softmax rows longer than 4096, in chunks (exp
+//                        recomputed in the output pass, bit-identical);
+//   norm_row_kernel      other norm rows: one row at a time per CTA, held in
+//                        shared memory as f32.
 
 #include "common.cuh"
 #include "crmath.cuh"
@@ -34,14 +39,22 @@ constexpr int SM_EPT = 16;                      // row elements per thread when 
 constexpr int SM_CAP = SM_THREADS * SM_EPT;     // 4096
 constexpr int SM_MAX_PARTIALS = 64;
 
-struct SoftmaxParams {
+// Region kinds of the pipelined kernel.
+enum : int { REGION_SOFTMAX = 0, REGION_RMS = 1, REGION_LAYER = 2 };
+
+struct RegionParams {
   const void* x;
   void* y;
   int64_t rows, cols, ldx, ldy;
   int32_t partials;     // 1 for sequential / blocked
   int32_t nb;           // rows per batch (resident kernel) / per chain group (pipelined)
   int32_t estride;      // floats between row buffers in shared memory
-  int32_t sx, se;       // pipelined kernel: x and exp ring slots
+  int32_t sx, se;       // pipelined kernel: x and value ring slots
+  // normalization regions
+  const void* gamma;    // scale per column, NULL if none
+  const void* beta;     // bias per column (LayerNorm), NULL if none
+  int32_t param_dtype;  // storage type of gamma and beta
+  float eps;            // RN_f32 of the eps argument
 };
 
 // NaN-propagating max (exact; the order of a max reduction changes no bit
@@ -180,31 +193,43 @@ __device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast
   for (int q = 0; q < N; ++q) o[q] = y[q];
 }
 
-// One chain: acc over E[p], E[p+P], ... (n elements in the row), in index
-// order.  The loads of the next block are issued before the dependent adds of
-// the current one (registers double-buffered), so the chain runs at the add
-// latency instead of add + shared-memory latency per block.
-__device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) {
-  float acc = E[p];
+// Value transforms a chain applies to each stored element before adding it.
+struct ChainIdentity {
+  __device__ __forceinline__ float operator()(float v) const { return v; }
+};
+struct ChainSquare {            // RN(v * v)
+  __device__ __forceinline__ float operator()(float v) const { return __fmul_rn(v, v); }
+};
+struct ChainCenteredSquare {    // RN(RN(v - mu)^2)
+  float mu;
+  __device__ __forceinline__ float operator()(float v) const {
+    const float c = __fsub_rn(v, mu);
+    return __fmul_rn(c, c);
+  }
+};
+
+// One chain: acc over f(E[p]), f(E[p+P]), ... (n elements in the row), in
+// index order.  The loads of the next block are issued before the dependent
+// adds of the current one (registers double-buffered), so the chain runs at
+// the add latency instead of add + shared-memory latency per block.
+template <class F>
+__device__ __forceinline__ float run_chain(const float* E, int n, int p, int P, F f) {
+  float acc = f(E[p]);
   int j = p + P;
+#define PSK_ADD4(q) acc = __fadd_rn(acc, f(q.x)); acc = __fadd_rn(acc, f(q.y)); \
+                    acc = __fadd_rn(acc, f(q.z)); acc = __fadd_rn(acc, f(q.w));
   if (P == 1) {
-    for (; (j & 3) != 0 && j < n; ++j) acc = __fadd_rn(acc, E[j]);
+    for (; (j & 3) != 0 && j < n; ++j) acc = __fadd_rn(acc, f(E[j]));
     if (j + 15 < n) {
       float4 a = *(const float4*)&E[j], b = *(const float4*)&E[j + 4];
       float4 c = *(const float4*)&E[j + 8], d = *(const float4*)&E[j + 12];
       for (; j + 31 < n; j += 16) {
         const float4 na = *(const float4*)&E[j + 16], nb = *(const float4*)&E[j + 20];
         const float4 nc = *(const float4*)&E[j + 24], nd = *(const float4*)&E[j + 28];
-        acc = __fadd_rn(acc, a.x); acc = __fadd_rn(acc, a.y); acc = __fadd_rn(acc, a.z); acc = __fadd_rn(acc, a.w);
-        acc = __fadd_rn(acc, b.x); acc = __fadd_rn(acc, b.y); acc = __fadd_rn(acc, b.z); acc = __fadd_rn(acc, b.w);
-        acc = __fadd_rn(acc, c.x); acc = __fadd_rn(acc, c.y); acc = __fadd_rn(acc, c.z); acc = __fadd_rn(acc, c.w);
-        acc = __fadd_rn(acc, d.x); acc = __fadd_rn(acc, d.y); acc = __fadd_rn(acc, d.z); acc = __fadd_rn(acc, d.w);
+        PSK_ADD4(a) PSK_ADD4(b) PSK_ADD4(c) PSK_ADD4(d)
         a = na; b = nb; c = nc; d = nd;
       }
-      acc = __fadd_rn(acc, a.x); acc = __fadd_rn(acc, a.y); acc = __fadd_rn(acc, a.z); acc = __fadd_rn(acc, a.w);
-      acc = __fadd_rn(acc, b.x); acc = __fadd_rn(acc, b.y); acc = __fadd_rn(acc, b.z); acc = __fadd_rn(acc, b.w);
-      acc = __fadd_rn(acc, c.x); acc = __fadd_rn(acc, c.y); acc = __fadd_rn(acc, c.z); acc = __fadd_rn(acc, c.w);
-      acc = __fadd_rn(acc, d.x); acc = __fadd_rn(acc, d.y); acc = __fadd_rn(acc, d.z); acc = __fadd_rn(acc, d.w);
+      PSK_ADD4(a) PSK_ADD4(b) PSK_ADD4(c) PSK_ADD4(d)
       j += 16;
     }
   } else if (j + 7 * P < n) {
@@ -216,21 +241,69 @@ __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) 
 #pragma unroll
       for (int i = 0; i < 8; ++i) nv[i] = E[j + (8 + i) * P];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, v[i]);
+      for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, f(v[i]));
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = nv[i];
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, v[i]);
+    for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, f(v[i]));
     j += 8 * P;
   }
-  for (; j < n; j += P) acc = __fadd_rn(acc, E[j]);
+#undef PSK_ADD4
+  for (; j < n; j += P) acc = __fadd_rn(acc, f(E[j]));
   return acc;
+}
+
+__device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) {
+  return run_chain(E, n, p, P, ChainIdentity());
+}
+
+// Division by a row's divisor d > 0 of any magnitude (the norms' sqrt):
+// d = dd 2^-k with dd in [1, 2); a / d = (a 2^k) / dd exactly, and for
+// 2^-100 <= |a 2^k| <= 2^100 Markstein's correction through RN(1/dd) gives the
+// IEEE quotient; other operands, and rows whose d is not a normal number
+// below 2^127, take IEEE division.
+struct RowDivisor {
+  float d, dd, rdd, scale;
+  bool ok;
+};
+
+__device__ __forceinline__ RowDivisor make_divisor(float d) {
+  RowDivisor r;
+  r.d = d;
+  const uint32_t b = __float_as_uint(d);
+  const int e = (int)((b >> 23) & 0xFFu) - 127;
+  r.ok = d > 0.0f && e >= -126 && e <= 126;
+  r.dd = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+  r.scale = __uint_as_float((uint32_t)(r.ok ? 127 - e : 127) << 23);
+  r.rdd = __frcp_rn(r.dd);
+  return r;
+}
+
+template <int N>
+__device__ __forceinline__ void divide_n(float* o, const RowDivisor& D) {
+  float y[N];
+  bool bad = !D.ok;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const float a = __fmul_rn(o[q], D.scale);
+    const float qq = a * D.rdd;
+    const float r = fmaf(-qq, D.dd, a);
+    y[q] = fmaf(r, D.rdd, qq);
+    const float aa = fabsf(a);
+    bad = bad || !(aa >= 0x1p-100f && aa <= 0x1p100f);
+  }
+  if (bad) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) y[q] = __fdiv_rn(o[q], D.d);
+  }
+#pragma unroll
+  for (int q = 0; q < N; ++q) o[q] = y[q];
 }
 
 // --------------------------------------------------- resident rows (<= 4096)
 template <int XT, int YT, int EXPM, bool VEC>
-__global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __grid_constant__ SoftmaxParams P) {
+__global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __grid_constant__ RegionParams P) {
   constexpr int NBMAX = (XT == PSK_BF16) ? 4 : 2;
   extern __shared__ __align__(16) float smem[];
   __shared__ float red[SM_THREADS / 32][NBMAX];
@@ -403,21 +476,26 @@ __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __gr
 }
 
 
-// ------------------------------------- pipelined rows (bf16, <= 4096 columns)
+// ------------------------------------- pipelined rows (<= 4096 columns)
 // One persistent CTA per SM with three roles:
-//   a producer warp streams this CTA's rows (bf16) into a shared ring of SX
-//   slots with 1-D bulk copies (TMA) that complete on the slot's mbarrier;
+//   a producer warp streams this CTA's rows (bf16 or f32) into a shared ring
+//   of SX slots with 1-D bulk copies (TMA) that complete on the slot's
+//   mbarrier;
 //   4 teams of 4 compute warps each take every 4th row of the CTA (so four
 //   rows are in the compute stage at once, each team synchronising only
-//   within itself): the row's max (warp shuffles + a team barrier), e =
-//   exp(x - m) into a shared ring of SE f32 rows, then -- LAG = SE/4 - 1 team
-//   rows later, once the chain warps have published the row sum -- e / s,
-//   stored with streaming stores;
-//   3 chain warps each take groups of G consecutive rows: lane (row, p) adds
-//   chain p of its row in index order, the partials are combined left to
-//   right, and the row's sum and RN(1/s) are published on the row's mbarrier.
+//   within itself) and write the row's values into a shared ring of SE f32
+//   rows -- softmax: e = exp(x - max) (the max by warp shuffles and a team
+//   barrier); norms: x widened -- then, LAG = SE/4 - 1 team rows later, once
+//   the chain warps have published the row's reductions, the epilogue
+//   (softmax: e / s; RMSNorm: x / d, * gamma; LayerNorm: (x - mu) / d,
+//   * gamma, + beta), stored with streaming stores;
+//   3 chain warps own the value ring's slot groups (G <= 4 consecutive rows):
+//   lane (row, p) adds chain p of its row in index order, the partials are
+//   combined left to right by shuffles and the row's scalars published on
+//   the row's mbarrier (LayerNorm runs two chains per row, the sum and then
+//   the sum of squares about the mean).
 // A row's chain is a serial run of cols/P dependent adds, so about 4 LAG
-// rows chain at once; long chains (sequential order) get a deeper exp ring
+// rows chain at once; long chains (sequential order) get a deeper value ring
 // and a shallower x ring.  Every wait is bounded (pipe.cuh).
 constexpr int PIPE_TEAMS = 4;
 constexpr int PIPE_TW = 4;                                   // warps per team
@@ -427,24 +505,54 @@ constexpr int PIPE_EPT = SM_CAP / PIPE_TT;                   // row elements per
 constexpr int PIPE_KW = 3;                                   // chain warps
 constexpr int PIPE_THREADS = (PIPE_CW + PIPE_KW + 1) * 32;   // + producer warp
 constexpr int PIPE_SX_MAX = 8;                               // x ring slots
-constexpr int PIPE_SE_MAX = 16;                              // exp ring slots (a multiple of the teams)
+constexpr int PIPE_SE_MAX = 16;                              // value ring slots (a multiple of the teams)
 constexpr size_t PIPE_SMEM_BUDGET = 225 * 1024;              // dynamic shared memory of one CTA
 
-template <int YT, int EXPM>
-__global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __grid_constant__ SoftmaxParams P) {
+// Four consecutive stored elements at j, widened.
+template <int T>
+__device__ __forceinline__ void load4(const void* base, int j, float* v) {
+  if (T == PSK_F32) {
+    const float4 q = *reinterpret_cast<const float4*>((const float*)base + j);
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  } else {
+    const uint2 q = *reinterpret_cast<const uint2*>((const uint16_t*)base + j);
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+  }
+}
+
+// The same from global memory through the read-only path (norm parameters).
+__device__ __forceinline__ void load4_param(const void* base, int dtype, int j, float* v) {
+  if (dtype == PSK_F32) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>((const float*)base + j));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  } else {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>((const uint16_t*)base + j));
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+  }
+}
+
+template <int KIND, int XT, int YT, int EXPM>
+__global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(128) unsigned char pipe_smem[];
   __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
-  __shared__ float rowsum[PIPE_SE_MAX], rowrcp[PIPE_SE_MAX];
+  __shared__ float rowsum[PIPE_SE_MAX], rowrcp[PIPE_SE_MAX];   // softmax: s, RN(1/s); norms: d, mu
   __shared__ float red[PIPE_TEAMS][2][PIPE_TW];
   __shared__ volatile int abort_flag;
 
+  constexpr uint32_t XSZ = XT == PSK_F32 ? 4u : 2u;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cols = (int)P.cols;
-  const uint32_t xbytes = (uint32_t)cols * 2u;
-  const int xstr = (int)(((xbytes + 127u) / 128u) * 64u);    // ring slot stride in bf16 elements
+  const uint32_t xbytes = (uint32_t)cols * XSZ;
+  const uint32_t xslot = ((xbytes + 127u) / 128u) * 128u;     // ring slot stride in bytes
   const int SX = P.sx, SE = P.se, LAG = P.se / PIPE_TEAMS - 1;
-  uint16_t* X = reinterpret_cast<uint16_t*>(pipe_smem);
-  float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xstr * 2);
+  unsigned char* X = pipe_smem;
+  float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xslot);
   const int estride = P.estride;
   const int parts = P.partials < cols ? P.partials : cols;  // a partial beyond the row is empty
   const int G = P.nb;                                        // rows per chain group
@@ -462,14 +570,14 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
     // ---------------- producer
     if (lane == 0) {
       int issued = 0;
-      const uint16_t* src = (const uint16_t*)P.x + (int64_t)blockIdx.x * P.ldx;
-      const int64_t step = (int64_t)gridDim.x * P.ldx;
+      const unsigned char* src = (const unsigned char*)P.x + (int64_t)blockIdx.x * P.ldx * XSZ;
+      const int64_t step = (int64_t)gridDim.x * P.ldx * XSZ;
       for (int i = 0; i < n_local; ++i) {
         const int s = i % SX;
         if (i >= SX && !mbar_wait(&xempty[s], (uint32_t)((i / SX) - 1) & 1u)) { abort_flag = 1; break; }
         if (abort_flag) break;
         mbar_arrive_expect_tx(&xfull[s], xbytes);
-        bulk_copy_g2s(X + (size_t)s * xstr, src, xbytes, &xfull[s]);
+        bulk_copy_g2s(X + (size_t)s * xslot, src, xbytes, &xfull[s]);
         src += step;
         issued = i + 1;
       }
@@ -482,11 +590,12 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
   if (w >= PIPE_CW) {
     // ---------------- chain warps
     // A parity wait must never run two phases ahead of its barrier (it would
-    // pass at once), so every slot group of the exp ring (G consecutive
+    // pass at once), so every slot group of the value ring (G consecutive
     // slots) belongs to one chain warp, which visits its phases in order.
     const int c = w - PIPE_CW;
     const int b = lane / parts, p = lane - (lane / parts) * parts;
     const int n_groups = SE / G;
+    const float n_f = (float)cols;                           // exact: cols <= 4096
     for (int g = 0; g * G < n_local; ++g) {
       if ((g % n_groups) % PIPE_KW != c) continue;
       if (abort_flag) break;
@@ -496,17 +605,40 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
       bool ok = true;
       if (act) ok = mbar_wait(&efull[se], (uint32_t)(j / SE) & 1u);
       if (__any_sync(0xffffffffu, !ok)) { abort_flag = 1; break; }
-      const float acc = act ? run_chain(E + (size_t)se * estride, cols, p, parts) : 0.0f;
-      float sum = acc;
-      for (int q = 1; q < parts; ++q) {
-        const float o = __shfl_sync(0xffffffffu, acc, (lane - p + q) & 31);
-        if (act) sum = __fadd_rn(sum, o);
+      const float* Er = E + (size_t)se * estride;
+      // partials of the row are combined left to right in lane p = 0
+      auto combine = [&](float acc) {
+        float sum = acc;
+        for (int q = 1; q < parts; ++q) {
+          const float o = __shfl_sync(0xffffffffu, acc, (lane - p + q) & 31);
+          if (act) sum = __fadd_rn(sum, o);
+        }
+        return sum;
+      };
+      if (KIND == REGION_SOFTMAX) {
+        const float sum = combine(act ? run_chain(Er, cols, p, parts) : 0.0f);
+        if (act && p == 0) {
+          rowsum[se] = sum;
+          rowrcp[se] = __frcp_rn(sum);
+        }
+      } else {
+        float mu = 0.0f;
+        float ss;
+        if (KIND == REGION_LAYER) {
+          const float s1 = combine(act ? run_chain(Er, cols, p, parts) : 0.0f);
+          mu = __fdiv_rn(s1, n_f);
+          mu = __shfl_sync(0xffffffffu, mu, (lane - p) & 31);   // the row's mean, to every lane of the row
+          ss = combine(act ? run_chain(Er, cols, p, parts, ChainCenteredSquare{mu}) : 0.0f);
+        } else {
+          ss = combine(act ? run_chain(Er, cols, p, parts, ChainSquare()) : 0.0f);
+        }
+        if (act && p == 0) {
+          const float var = __fdiv_rn(ss, n_f);
+          rowsum[se] = __fsqrt_rn(__fadd_rn(var, P.eps));
+          rowrcp[se] = mu;
+        }
       }
-      if (act && p == 0) {
-        rowsum[se] = sum;
-        rowrcp[se] = __frcp_rn(sum);
-        mbar_arrive(&sready[se]);
-      }
+      if (act && p == 0) mbar_arrive(&sready[se]);
     }
     return;
   }
@@ -526,41 +658,48 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
     if (i < n_local) {
       const int s = i % SX;
       if (!dead && !mbar_wait(&xfull[s], (uint32_t)(i / SX) & 1u)) { abort_flag = 1; dead = true; }
-      const uint16_t* xs = X + (size_t)s * xstr;
+      const unsigned char* xs = X + (size_t)s * xslot;
       float v[PIPE_EPT];
       float m = -INFINITY;
 #pragma unroll
       for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
         if (j < cols && !dead) {
-          const uint2 q = *reinterpret_cast<const uint2*>(xs + j);
-          v[4 * c4 + 0] = __uint_as_float(q.x << 16);
-          v[4 * c4 + 1] = __uint_as_float(q.x & 0xFFFF0000u);
-          v[4 * c4 + 2] = __uint_as_float(q.y << 16);
-          v[4 * c4 + 3] = __uint_as_float(q.y & 0xFFFF0000u);
+          load4<XT>(xs, j, &v[4 * c4]);
         } else {
           v[4 * c4 + 0] = v[4 * c4 + 1] = v[4 * c4 + 2] = v[4 * c4 + 3] = -INFINITY;
         }
+        if (KIND == REGION_SOFTMAX) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) m = max_nan(m, v[4 * c4 + q]);
+          for (int q = 0; q < 4; ++q) m = max_nan(m, v[4 * c4 + q]);
+        }
       }
+      if (KIND == REGION_SOFTMAX) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[team][k & 1][tw] = m;
-      named_barrier(1 + team, PIPE_TT);
-      m = red[team][k & 1][0];
+        for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) red[team][k & 1][tw] = m;
+      }
+      named_barrier(1 + team, PIPE_TT);                      // every team thread has read x
+      if (KIND == REGION_SOFTMAX) {
+        m = red[team][k & 1][0];
 #pragma unroll
-      for (int q = 1; q < PIPE_TW; ++q) m = max_nan(m, red[team][k & 1][q]);
-      if (tt == 0) mbar_arrive(&xempty[s]);              // every team thread has read x
+        for (int q = 1; q < PIPE_TW; ++q) m = max_nan(m, red[team][k & 1][q]);
+      }
+      if (tt == 0) mbar_arrive(&xempty[s]);
       const int se = i % SE;
       float* Er = E + (size_t)se * estride;
       if (!dead) {
 #pragma unroll
         for (int h = 0; h < PIPE_EPT / 8; ++h) {
           float u[8];
+          if (KIND == REGION_SOFTMAX) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
-          region_exp8<EXPM>(u);
+            for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
+            region_exp8<EXPM>(u);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) u[q] = v[8 * h + q];
+          }
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const int j = (2 * h + kk) * (PIPE_TT * 4) + 4 * tt;
@@ -576,6 +715,8 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
       if (!mbar_wait(&sready[se], (uint32_t)(o / SE) & 1u)) { abort_flag = 1; dead = true; continue; }
       const float sm = rowsum[se], rs = rowrcp[se];
       const bool fast_ok = sm >= 1.0f && sm < 0x1p20f;
+      RowDivisor D;
+      if (KIND != REGION_SOFTMAX) D = make_divisor(sm);
       const float* Er = E + (size_t)se * estride;
       char* yr = (char*)P.y + ((int64_t)blockIdx.x + (int64_t)o * gridDim.x) * P.ldy * ysz;
 #pragma unroll
@@ -583,15 +724,34 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) softmax_pipe_kernel(const __g
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
         if (j < cols) {
           const float4 e = *reinterpret_cast<const float4*>(Er + j);
-          float o[4] = {e.x, e.y, e.z, e.w};
-          row_div_n<4>(o, sm, rs, fast_ok);
-          const float o0 = o[0], o1 = o[1], o2 = o[2], o3 = o[3];
+          float o4[4] = {e.x, e.y, e.z, e.w};
+          if (KIND == REGION_SOFTMAX) {
+            row_div_n<4>(o4, sm, rs, fast_ok);
+          } else {
+            if (KIND == REGION_LAYER) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) o4[q] = __fsub_rn(o4[q], rs);
+            }
+            divide_n<4>(o4, D);
+            if (P.gamma) {
+              float g4[4];
+              load4_param(P.gamma, P.param_dtype, j, g4);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) o4[q] = __fmul_rn(o4[q], g4[q]);
+            }
+            if (KIND == REGION_LAYER && P.beta) {
+              float b4[4];
+              load4_param(P.beta, P.param_dtype, j, b4);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) o4[q] = __fadd_rn(o4[q], b4[q]);
+            }
+          }
           if (YT == PSK_F32) {
-            __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o0, o1, o2, o3));
+            __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o4[0], o4[1], o4[2], o4[3]));
           } else {
             uint2 q;
-            q.x = f32x2_to_bf16x2(o0, o1);
-            q.y = f32x2_to_bf16x2(o2, o3);
+            q.x = f32x2_to_bf16x2(o4[0], o4[1]);
+            q.y = f32x2_to_bf16x2(o4[2], o4[3]);
             __stcs(reinterpret_cast<uint2*>(yr) + (j >> 2), q);
           }
         }
@@ -620,7 +780,7 @@ __device__ __forceinline__ float block_max(float v, StreamShared& sh) {
 }
 
 template <int XT, int YT, int EXPM>
-__global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid_constant__ SoftmaxParams P) {
+__global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid_constant__ RegionParams P) {
   __shared__ __align__(16) StreamShared sh;
   const int t = threadIdx.x;
   __syncthreads();
@@ -666,7 +826,7 @@ __global__ void __launch_bounds__(SM_THREADS) softmax_stream_kernel(const __grid
 
 // ------------------------------------------------------------------ host
 template <int XT, int YT, int EXPM, bool VEC>
-static int launch_batch(SoftmaxParams P, cudaStream_t stream) {
+static int launch_batch(RegionParams P, cudaStream_t stream) {
   constexpr int NBMAX = (XT == PSK_BF16) ? 4 : 2;
   // row buffers padded so that lanes of different rows start in different
   // banks: buffer b begins at b * estride, estride = cols rounded to 32 plus
@@ -688,7 +848,7 @@ static int launch_batch(SoftmaxParams P, cudaStream_t stream) {
 }
 
 template <int XT, int YT, int EXPM>
-static int launch_stream(const SoftmaxParams& P, cudaStream_t stream) {
+static int launch_stream(const RegionParams& P, cudaStream_t stream) {
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, softmax_stream_kernel<XT, YT, EXPM>, SM_THREADS, 0);
   if (per_sm < 1) per_sm = 1;
@@ -699,19 +859,22 @@ static int launch_stream(const SoftmaxParams& P, cudaStream_t stream) {
 }
 
 // Ring depths from the shared-memory budget.  Eight bf16 rows in flight per
-// SM cover HBM latency; the exp ring holds SE = 4 (LAG + 1) rows, about 4 LAG
-// of them in their chains.  A long chain (cols / P >= 1024 adds, e.g. the
-// sequential order over 4096 columns) is the bottleneck, so it gets the exp
-// ring first (x ring down to 4 slots); otherwise the x ring comes first.
-// Chain groups take G <= 4 consecutive rows (one per team).
-template <int YT, int EXPM>
-static int launch_pipe(SoftmaxParams P, cudaStream_t stream) {
+// SM cover HBM latency; the value ring holds SE = 4 (LAG + 1) rows, about
+// 4 LAG of them in their chains.  A long chain (>= 1024 dependent adds per
+// row: cols / P, twice that for LayerNorm's two chains; e.g. the sequential
+// order over 4096 columns) is the bottleneck, so it gets the value ring first
+// (x ring down to 4 slots); otherwise the x ring comes first.  Chain groups
+// take G <= 4 consecutive rows (one per team).
+template <int KIND, int XT, int YT, int EXPM>
+static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const int pad = P.partials < 4 ? 4 : ((P.partials + 3) / 4) * 4;
   P.estride = (int)(((P.cols + 31) / 32) * 32 + pad);
-  const size_t xrow = (size_t)((P.cols * 2 + 127) / 128) * 128;
+  const size_t xsz = XT == PSK_F32 ? 4 : 2;
+  const size_t xrow = (size_t)((P.cols * xsz + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
   const size_t budget = PIPE_SMEM_BUDGET;
-  const bool long_chain = (P.cols + P.partials - 1) / P.partials >= 1024;
+  const int64_t chain = ((P.cols + P.partials - 1) / P.partials) * (KIND == REGION_LAYER ? 2 : 1);
+  const bool long_chain = chain >= 1024;
   int sx = long_chain ? 4 : PIPE_SX_MAX;
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
@@ -719,7 +882,7 @@ static int launch_pipe(SoftmaxParams P, cudaStream_t stream) {
   // team and its parity waits run in order
   if (sx < PIPE_SX_MAX && PIPE_SX_MAX * xrow + se * erow <= budget) sx = PIPE_SX_MAX;
   if (se < 2 * PIPE_TEAMS) {  // cannot happen for cols <= 4096; kept as a guard
-    return fail(PSK_E_ARG, "softmax ring does not fit shared memory (cols %lld)", (long long)P.cols);
+    return fail(PSK_E_ARG, "row ring does not fit shared memory (cols %lld)", (long long)P.cols);
   }
   P.sx = sx;
   P.se = se;
@@ -729,29 +892,188 @@ static int launch_pipe(SoftmaxParams P, cudaStream_t stream) {
   P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
   const size_t smem = sx * xrow + se * erow;
   static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)softmax_pipe_kernel<YT, EXPM>, (int)budget, attr);
+  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM>, (int)budget, attr);
   const int64_t sms = device_sm_count();
   const unsigned grid = (unsigned)(P.rows < sms ? P.rows : sms);
-  softmax_pipe_kernel<YT, EXPM><<<grid, PIPE_THREADS, smem, stream>>>(P);
-  return check_launch("softmax region kernel (pipelined)");
+  region_pipe_kernel<KIND, XT, YT, EXPM><<<grid, PIPE_THREADS, smem, stream>>>(P);
+  return check_launch("row region kernel (pipelined)");
 }
 
 template <int XT, int YT, int EXPM>
-static int dispatch_exp(const SoftmaxParams& P, bool vec, cudaStream_t s) {
+static int dispatch_exp(const RegionParams& P, bool vec, cudaStream_t s) {
   if (P.cols > SM_CAP) return launch_stream<XT, YT, EXPM>(P, s);
-  if (XT == PSK_BF16 && vec && P.partials <= 32 && P.cols >= 8) return launch_pipe<YT, EXPM>(P, s);
+  if (XT == PSK_BF16 && vec && P.partials <= 32 && P.cols >= 8)
+    return launch_pipe<REGION_SOFTMAX, PSK_BF16, YT, EXPM>(P, s);
   return vec ? launch_batch<XT, YT, EXPM, true>(P, s) : launch_batch<XT, YT, EXPM, false>(P, s);
 }
 
 template <int XT, int YT>
-static int dispatch_softmax(const SoftmaxParams& P, int exp_mode, bool vec, cudaStream_t s) {
+static int dispatch_softmax(const RegionParams& P, int exp_mode, bool vec, cudaStream_t s) {
   return exp_mode == PSK_EXP_EXACT ? dispatch_exp<XT, YT, PSK_EXP_EXACT>(P, vec, s)
                                    : dispatch_exp<XT, YT, PSK_EXP_FAST>(P, vec, s);
+}
+
+// ------------------------------------------------ norm rows, any shape
+// One row at a time per CTA (grid-stride over rows): the row widened into
+// shared memory as f32, the chains run by warp 0 (lane l takes partials l and
+// l + 32, so up to 64), the partials combined left to right by lane 0, then
+// every thread divides (IEEE division) and applies the scale and bias.  For
+// rows the pipelined kernel does not take: unaligned, wider than 4096, more
+// than 32 partials.
+constexpr int NORM_MAX_COLS = 49152;                 // 192 KB of f32 row in shared memory
+
+template <int T>
+__device__ __forceinline__ float load1(const void* base, int64_t off) {
+  if (T == PSK_F32) return __ldg((const float*)base + off);
+  return bf16_bits_to_f32(__ldg((const uint16_t*)base + off));
+}
+
+template <int KIND, int XT, int YT>
+__global__ void __launch_bounds__(SM_THREADS) norm_row_kernel(const __grid_constant__ RegionParams P) {
+  extern __shared__ __align__(16) float row[];
+  __shared__ float part[SM_MAX_PARTIALS];
+  __shared__ float stat[2];                          // mu, d
+  const int t = threadIdx.x, lane = t & 31;
+  const int cols = (int)P.cols;
+  const int parts = P.partials < cols ? P.partials : cols;
+  const float n_f = (float)cols;                     // exact: cols <= 49152
+  for (int64_t r = blockIdx.x; r < P.rows; r += gridDim.x) {
+    const int64_t xo = r * P.ldx;
+    for (int j = t; j < cols; j += SM_THREADS) row[j] = load1<XT>(P.x, xo + j);
+    __syncthreads();
+    if (t < 32) {
+      float mu = 0.0f;
+      if (KIND == REGION_LAYER) {
+        for (int pp = lane; pp < parts; pp += 32) part[pp] = run_chain(row, cols, pp, parts);
+        __syncwarp();
+        if (lane == 0) {
+          float s1 = part[0];
+          for (int q = 1; q < parts; ++q) s1 = __fadd_rn(s1, part[q]);
+          stat[0] = __fdiv_rn(s1, n_f);
+        }
+        __syncwarp();
+        mu = stat[0];
+        for (int pp = lane; pp < parts; pp += 32)
+          part[pp] = run_chain(row, cols, pp, parts, ChainCenteredSquare{mu});
+      } else {
+        for (int pp = lane; pp < parts; pp += 32) part[pp] = run_chain(row, cols, pp, parts, ChainSquare());
+      }
+      __syncwarp();
+      if (lane == 0) {
+        float ss = part[0];
+        for (int q = 1; q < parts; ++q) ss = __fadd_rn(ss, part[q]);
+        stat[0] = mu;
+        stat[1] = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n_f), P.eps));
+      }
+    }
+    __syncthreads();
+    const float mu = stat[0], d = stat[1];
+    const int64_t yo = r * P.ldy;
+    for (int j = t; j < cols; j += SM_THREADS) {
+      float v = row[j];
+      if (KIND == REGION_LAYER) v = __fsub_rn(v, mu);
+      v = __fdiv_rn(v, d);
+      if (P.gamma) v = __fmul_rn(v, P.param_dtype == PSK_F32 ? __ldg((const float*)P.gamma + j)
+                                                              : bf16_bits_to_f32(__ldg((const uint16_t*)P.gamma + j)));
+      if (KIND == REGION_LAYER && P.beta)
+        v = __fadd_rn(v, P.param_dtype == PSK_F32 ? __ldg((const float*)P.beta + j)
+                                                  : bf16_bits_to_f32(__ldg((const uint16_t*)P.beta + j)));
+      store_y1<YT>(P.y, yo + j, v);
+    }
+    __syncthreads();
+  }
+}
+
+template <int KIND, int XT, int YT>
+static int launch_norm_rows(const RegionParams& P, cudaStream_t stream) {
+  const size_t smem = (size_t)P.cols * sizeof(float);
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)norm_row_kernel<KIND, XT, YT>, (int)(NORM_MAX_COLS * sizeof(float)), attr);
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_row_kernel<KIND, XT, YT>, SM_THREADS, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t cap = (int64_t)device_sm_count() * per_sm;
+  const unsigned grid = (unsigned)(P.rows < cap ? P.rows : cap);
+  norm_row_kernel<KIND, XT, YT><<<grid, SM_THREADS, smem, stream>>>(P);
+  return check_launch("norm region kernel (row at a time)");
+}
+
+template <int KIND, int XT, int YT>
+static int dispatch_norm(const RegionParams& P, bool pipe, cudaStream_t s) {
+  if (pipe) return launch_pipe<KIND, XT, YT, PSK_EXP_EXACT>(P, s);
+  return launch_norm_rows<KIND, XT, YT>(P, s);
+}
+
+template <int KIND>
+static int dispatch_norm_types(const RegionParams& P, int xt, int yt, bool pipe, cudaStream_t s) {
+  if (xt == PSK_BF16 && yt == PSK_BF16) return dispatch_norm<KIND, PSK_BF16, PSK_BF16>(P, pipe, s);
+  if (xt == PSK_BF16 && yt == PSK_F32) return dispatch_norm<KIND, PSK_BF16, PSK_F32>(P, pipe, s);
+  if (xt == PSK_F32 && yt == PSK_BF16) return dispatch_norm<KIND, PSK_F32, PSK_BF16>(P, pipe, s);
+  return dispatch_norm<KIND, PSK_F32, PSK_F32>(P, pipe, s);
 }
 
 }  // namespace psk
 
 using namespace psk;
+
+// Number of partial chains of a declared order, or a refusal (shared by both
+// region entry points).
+static int order_partials(const psk_order& order, int* partials) {
+  *partials = 1;
+  switch (order.kind) {
+    case PSK_ORDER_SEQUENTIAL: return PSK_OK;
+    case PSK_ORDER_BLOCKED:
+      if (order.param < 1) return fail(PSK_E_ORDER, "blocked width %d < 1", order.param);
+      return PSK_OK;
+    case PSK_ORDER_INTERLEAVED:
+      if (order.param < 1 || order.param > SM_MAX_PARTIALS)
+        return fail(PSK_E_ORDER, "interleaved partials %d (1..%d)", order.param, SM_MAX_PARTIALS);
+      *partials = order.param;
+      return PSK_OK;
+    default:
+      return fail(PSK_E_ORDER, "order kind %d", order.kind);
+  }
+}
+
+static bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  const char* a0 = (const char*)a;
+  const char* b0 = (const char*)b;
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+extern "C" int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
+                               int64_t ldx, int64_t ldy, int32_t kind, double eps, const void* gamma,
+                               const void* beta, int32_t param_dtype, psk_order order, void* stream) {
+  clear_error();
+  if (!dtype_ok(xt)) return fail(PSK_E_DTYPE, "x dtype %d", xt);
+  if (!dtype_ok(yt)) return fail(PSK_E_DTYPE, "y dtype %d", yt);
+  if (kind != PSK_NORM_RMS && kind != PSK_NORM_LAYER) return fail(PSK_E_ARG, "norm kind %d", kind);
+  if (!(eps == eps) || eps > 3.4e38 || eps < -3.4e38) return fail(PSK_E_ARG, "eps is not a finite f32 value");
+  if (kind == PSK_NORM_RMS && beta) return fail(PSK_E_ARG, "RMSNorm takes no bias");
+  if ((gamma || beta) && !dtype_ok(param_dtype)) return fail(PSK_E_DTYPE, "parameter dtype %d", param_dtype);
+  if (rows < 0 || cols < 0) return fail(PSK_E_SHAPE, "rows %lld, cols %lld", (long long)rows, (long long)cols);
+  int partials = 1;
+  int rc = order_partials(order, &partials);
+  if (rc) return rc;
+  if (rows == 0 || cols == 0) return PSK_OK;
+  if (cols > NORM_MAX_COLS) return fail(PSK_E_SHAPE, "cols %lld above %d", (long long)cols, NORM_MAX_COLS);
+  if (!x || !y) return fail(PSK_E_NULL, "x or y is NULL");
+  if (ldx < cols || ldy < cols) return fail(PSK_E_SHAPE, "leading dimension below cols");
+  const size_t xbytes = (size_t)((rows - 1) * ldx + cols) * dtype_size(xt);
+  const size_t ybytes = (size_t)((rows - 1) * ldy + cols) * dtype_size(yt);
+  if (overlaps(x, xbytes, y, ybytes) && !(x == y && xt == yt && ldx == ldy))
+    return fail(PSK_E_ALIAS, "y overlaps x and is not the same buffer");
+  const size_t pbytes = (size_t)cols * dtype_size(param_dtype);
+  if ((gamma && overlaps(gamma, pbytes, y, ybytes)) || (beta && overlaps(beta, pbytes, y, ybytes)))
+    return fail(PSK_E_ALIAS, "y overlaps gamma or beta");
+  RegionParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0, 0, 0, gamma, beta, param_dtype, (float)eps};
+  const bool pipe = cols <= SM_CAP && cols >= 8 && cols % 8 == 0 && ldx % 8 == 0 && ldy % 8 == 0 &&
+                    partials <= 32 && (uintptr_t)x % 16 == 0 && (uintptr_t)y % 16 == 0 &&
+                    (uintptr_t)gamma % 16 == 0 && (uintptr_t)beta % 16 == 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  return kind == PSK_NORM_RMS ? dispatch_norm_types<REGION_RMS>(P, xt, yt, pipe, s)
+                              : dispatch_norm_types<REGION_LAYER>(P, xt, yt, pipe, s);
+}
 
 extern "C" int psk_device_status(uint32_t* status, int32_t reset) {
   clear_error();
@@ -775,19 +1097,8 @@ extern "C" int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt
   if (cols > 0x7FFFFFFF) return fail(PSK_E_SHAPE, "cols %lld above 2^31-1", (long long)cols);
   if (exp_mode != PSK_EXP_EXACT && exp_mode != PSK_EXP_FAST) return fail(PSK_E_ARG, "exp_mode %d", exp_mode);
   int partials = 1;
-  switch (order.kind) {
-    case PSK_ORDER_SEQUENTIAL: break;
-    case PSK_ORDER_BLOCKED:
-      if (order.param < 1) return fail(PSK_E_ORDER, "blocked width %d < 1", order.param);
-      break;
-    case PSK_ORDER_INTERLEAVED:
-      if (order.param < 1 || order.param > SM_MAX_PARTIALS)
-        return fail(PSK_E_ORDER, "interleaved partials %d (1..%d)", order.param, SM_MAX_PARTIALS);
-      partials = order.param;
-      break;
-    default:
-      return fail(PSK_E_ORDER, "order kind %d", order.kind);
-  }
+  const int orc = order_partials(order, &partials);
+  if (orc) return orc;
   if (rows == 0 || cols == 0) return PSK_OK;
   if (!x || !y) return fail(PSK_E_NULL, "x or y is NULL");
   if (ldx < cols || ldy < cols) return fail(PSK_E_SHAPE, "leading dimension below cols");
@@ -798,7 +1109,7 @@ extern "C" int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt
   const char* yhi = ylo + ((rows - 1) * ldy + cols) * dtype_size(yt);
   if (xlo < yhi && ylo < xhi && !(x == y && xt == yt && ldx == ldy))
     return fail(PSK_E_ALIAS, "y overlaps x and is not the same buffer");
-  SoftmaxParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0, 0, 0};
+  RegionParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0, 0, 0};
   const bool vec = (cols % 8 == 0) && (ldx % 8 == 0) && (ldy % 8 == 0) && ((uintptr_t)x % 16 == 0) &&
                    ((uintptr_t)y % 16 == 0);
   cudaStream_t s = (cudaStream_t)stream;

@@ -1,5 +1,5 @@
 """Python binding of the C ABI with the same names: psk_group_run,
-psk_softmax_region, psk_adamw_tree (plus the host-only psk_group_check and
+psk_softmax_region, psk_norm_region, psk_adamw_tree (plus the host-only psk_group_check and
 psk_adamw_scalars).  Each function marshals torch tensors (device memory and
 the current stream) or plain host arrays into the C structs and calls the
 library; every step of the hot path runs in the library's kernels.
@@ -104,6 +104,31 @@ def psk_softmax_region(x, y, order=("sequential",), exp_mode: str = "exact", str
     rows, cols = x.shape
     N.check(N.lib().psk_softmax_region(x.data_ptr(), _dtype_code(x), y.data_ptr(), _dtype_code(y), rows, cols,
                                        max(x.stride(0), cols), max(y.stride(0), cols), o, em, _stream_handle(stream)))
+
+
+def psk_norm_region(x, y, kind: str, eps: float, gamma=None, beta=None, order=("sequential",),
+                    stream=None) -> None:
+    """RMSNorm (kind "rms") or LayerNorm ("layer") of the rows of the 2-D
+    tensor x into y; gamma / beta: optional 1-D tensors of x's row length, both
+    of one storage type."""
+    if x.dim() != 2 or y.dim() != 2 or tuple(x.shape) != tuple(y.shape):
+        raise ValueError("x and y must be 2-D tensors of one shape")
+    if x.stride(1) != 1 or y.stride(1) != 1:
+        raise ValueError("rows must be contiguous")
+    params = [t for t in (gamma, beta) if t is not None]
+    for t in params:
+        if t.dim() != 1 or t.numel() != x.shape[1] or (t.numel() > 1 and t.stride(0) != 1):
+            raise ValueError("gamma and beta must be contiguous vectors of the row length")
+    if len(params) == 2 and gamma.dtype != beta.dtype:
+        raise TypeError("gamma and beta must share one storage type")
+    pdt = _dtype_code(params[0]) if params else N.PSK_F32
+    o = N.psk_order(_ORDER[order[0]], int(order[1]) if len(order) > 1 else 0)
+    k = {"rms": N.PSK_NORM_RMS, "layer": N.PSK_NORM_LAYER}[kind]
+    rows, cols = x.shape
+    N.check(N.lib().psk_norm_region(x.data_ptr(), _dtype_code(x), y.data_ptr(), _dtype_code(y), rows, cols,
+                                    max(x.stride(0), cols), max(y.stride(0), cols), k, float(eps),
+                                    gamma.data_ptr() if gamma is not None else None,
+                                    beta.data_ptr() if beta is not None else None, pdt, o, _stream_handle(stream)))
 
 
 def psk_device_status(reset: bool = False) -> int:
