@@ -44,7 +44,7 @@ def _args():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
     p.add_argument("--softmax-exp", choices=["exact", "fast"], default="fast",
                    help="exp of the softmax region inside the step (the other mode is timed beside it)")
-    p.add_argument("--only", choices=["all", "group", "softmax", "adamw"], default="all",
+    p.add_argument("--only", choices=["all", "group", "softmax", "adamw", "norm"], default="all",
                    help="time one case only (profiling captures)")
     p.add_argument("--scale", type=float, default=1.0,
                    help="shrink the group rows, softmax rows and model layers (profiling captures only)")
@@ -153,8 +153,8 @@ def _gpu_uuid(torch, dev):
 _KERNEL_SOURCES = {
     "adamw": ["adamw.cu"],
     "group": ["group.cu", "group_dev.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
-    "softmax_sequential": ["softmax.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
-    "softmax_interleaved8": ["softmax.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+    "softmax_sequential": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+    "softmax_interleaved8": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
 }
 
 
@@ -170,7 +170,7 @@ def _counter(kernel: str, name: str):
     summaries (profiles/kernel_counters.txt), if the kernel's source is
     unchanged since the capture; else None."""
     path = os.path.join(HERE, "profiles", "kernel_counters.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in _KERNEL_SOURCES:
         return None
     h = _source_hash(kernel)
     for line in open(path):
@@ -272,8 +272,25 @@ def run_ours(a, ws, rank, local):
         "softmax_interleaved8": lambda: R.psk_softmax_region(sx, sy, ("interleaved", 8), em),
         "adamw": lambda: R.psk_adamw_tree(leaves, tree.hp),
     }
-    kernels = [k for k in launches if a.only == "all" or k.startswith(a.only)]
     b_all = {"group": b_group, "softmax_sequential": b_soft, "softmax_interleaved8": b_soft, "adamw": b_adam}
+    # the normalization regions (rows beyond the step's path): timed beside
+    # the step, or as the step itself under --only norm
+    norm_launches, norm_rows = {}, 0
+    if a.only in ("all", "norm"):
+        for kind, label in (("rms", "rmsnorm"), ("layer", "layernorm")):
+            nw = W.norm_rows(kind, rows=max(1, int(32768 * sc)))
+            nx = nw.device_x()
+            ny = torch.empty_like(nx)
+            ng, nb = nw.device_params()
+            for oname, order in (("sequential", ("sequential",)), ("interleaved8", ("interleaved", 8))):
+                norm_launches[f"{label}_{oname}"] = (lambda nx=nx, ny=ny, kind=kind, eps=nw.eps, ng=ng, nb=nb,
+                                                     order=order: R.psk_norm_region(nx, ny, kind, eps, ng, nb, order))
+                b_all[f"{label}_{oname}"] = nw.algorithmic_bytes()
+            norm_rows = nw.rows
+        torch.cuda.synchronize()
+    if a.only == "norm":
+        launches = dict(norm_launches)
+    kernels = [k for k in launches if a.only in ("all", "norm") or k.startswith(a.only)]
     bytes_step = sum(b_all[k] for k in kernels)
 
     def step(ev=None):
@@ -328,6 +345,18 @@ def run_ours(a, ws, rank, local):
             torch.cuda.synchronize()
             extra_ms[f"{name}_{other}_exp"] = e0.elapsed_time(e1) / a.steps
 
+    if a.only == "all":
+        for name, fn in norm_launches.items():
+            for _ in range(2):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(a.steps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            extra_ms[name] = e0.elapsed_time(e1) / a.steps
+
     # end to end through the public API with host buffers: per step, copy every
     # input from pinned host memory, run the step, read every result back
     e2e = None
@@ -381,17 +410,21 @@ def run_ours(a, ws, rank, local):
         return
 
     peak, peak_kind = _peaks()
-    kb = {"group": b_group, "softmax_sequential": b_soft, "softmax_interleaved8": b_soft, "adamw": b_adam}
+    kb = dict(b_all)
     kinfo = {}
     for k in kernels:
         gbs = kb[k] / (per_kernel_ms[k] / 1e3) / 1e9
         kinfo[k] = {"ms": round(per_kernel_ms[k], 4), "algorithmic_bytes": int(kb[k]), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4)}
     for k, ms in extra_ms.items():
-        gbs = b_soft / (ms / 1e3) / 1e9
-        kinfo[k] = {"ms": round(ms, 4), "algorithmic_bytes": int(b_soft), "gbs": round(gbs, 1),
+        kbytes = b_all.get(k, b_soft)
+        gbs = kbytes / (ms / 1e3) / 1e9
+        kinfo[k] = {"ms": round(ms, 4), "algorithmic_bytes": int(kbytes), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4), "in_value": False,
-                    "rows_per_s": round(sw.rows / (ms / 1e3), 1)}
+                    "rows_per_s": round((norm_rows if k in norm_launches else sw.rows) / (ms / 1e3), 1)}
+    for k in norm_launches:
+        if k in kernels:
+            kinfo[k]["rows_per_s"] = round(norm_rows / (per_kernel_ms[k] / 1e3), 1)
     if "group" in kinfo:
         kinfo["group"]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (per_kernel_ms["group"] / 1e3), 1)
         kinfo["group"]["node_evals_per_s"] = round(kinfo["group"]["elems_per_s"] * wl.n_ops, 1)
