@@ -537,6 +537,110 @@ __device__ __forceinline__ void load4_param(const void* base, int dtype, int j, 
   }
 }
 
+// Storage of four consecutive norm parameters (one 16- or 8-byte load).
+template <int PT> struct Param4;
+template <> struct Param4<PSK_F32> {
+  float4 q;
+  __device__ __forceinline__ void load(const void* base, int j) { q = __ldg(reinterpret_cast<const float4*>(base) + (j >> 2)); }
+  __device__ __forceinline__ void widen(float* v) const { v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w; }
+};
+template <> struct Param4<PSK_BF16> {
+  uint2 q;
+  __device__ __forceinline__ void load(const void* base, int j) { q = __ldg(reinterpret_cast<const uint2*>(base) + (j >> 2)); }
+  __device__ __forceinline__ void widen(float* v) const {
+    v[0] = __uint_as_float(q.x << 16);
+    v[1] = __uint_as_float(q.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(q.y << 16);
+    v[3] = __uint_as_float(q.y & 0xFFFF0000u);
+  }
+};
+
+// A norm row's epilogue for one team thread (its 8 chunks of 4 columns): bf16
+// scale and bias chunks are loaded first (16 registers each), so they arrive
+// while the thread waits for the row's mean and divisor; f32 ones are loaded
+// chunk by chunk.  Then (x - mu) / d, * gamma, + beta, rounded to the output
+// and stored.  False if the wait gave up.
+// One chunk of a norm row's epilogue: (x - mu) / d, * gamma, + beta, rounded
+// to the output and stored.
+template <int KIND, int YT, int PT>
+__device__ __forceinline__ void norm_chunk(const float* Er, char* yr, int j, const RowDivisor& D, float mu,
+                                           const Param4<PT>* g, const Param4<PT>* b) {
+  const float4 e = *reinterpret_cast<const float4*>(Er + j);
+  float o4[4] = {e.x, e.y, e.z, e.w};
+  if (KIND == REGION_LAYER) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o4[q] = __fsub_rn(o4[q], mu);
+  }
+  divide_n<4>(o4, D);
+  if (g) {
+    float g4[4];
+    g->widen(g4);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o4[q] = __fmul_rn(o4[q], g4[q]);
+  }
+  if (b) {
+    float b4[4];
+    b->widen(b4);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o4[q] = __fadd_rn(o4[q], b4[q]);
+  }
+  if (YT == PSK_F32) {
+    __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o4[0], o4[1], o4[2], o4[3]));
+  } else {
+    uint2 q;
+    q.x = f32x2_to_bf16x2(o4[0], o4[1]);
+    q.y = f32x2_to_bf16x2(o4[2], o4[3]);
+    __stcs(reinterpret_cast<uint2*>(yr) + (j >> 2), q);
+  }
+}
+
+// A norm row's epilogue for one team thread (its 8 chunks of 4 columns).  bf16
+// scale and bias chunks are loaded first (16 registers each), so they arrive
+// while the thread waits for the row's mean and divisor; f32 ones are loaded
+// chunk by chunk.  False if the wait gave up.
+template <int KIND, int YT, int PT>
+__device__ __forceinline__ bool norm_epilogue(const RegionParams& P, const float* Er, char* yr, int tt, int cols,
+                                              uint64_t* ready, uint32_t parity, const float* d_slot,
+                                              const float* mu_slot) {
+  constexpr int NC = PIPE_EPT / 4;
+  const bool hg = P.gamma != nullptr;
+  const bool hb = KIND == REGION_LAYER && P.beta != nullptr;
+  if constexpr (PT == PSK_BF16) {
+    Param4<PT> g[NC], b[NC];
+#pragma unroll
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) {
+        if (hg) g[c4].load(P.gamma, j);
+        if (hb) b[c4].load(P.beta, j);
+      }
+    }
+    if (!mbar_wait(ready, parity)) return false;
+    const RowDivisor D = make_divisor(*d_slot);
+    const float mu = *mu_slot;
+#pragma unroll
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) norm_chunk<KIND, YT, PT>(Er, yr, j, D, mu, hg ? &g[c4] : nullptr, hb ? &b[c4] : nullptr);
+    }
+  } else {
+    if (!mbar_wait(ready, parity)) return false;
+    const RowDivisor D = make_divisor(*d_slot);
+    const float mu = *mu_slot;
+#pragma unroll 2
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) {
+        Param4<PT> g, b;
+        if (hg) g.load(P.gamma, j);
+        if (hb) b.load(P.beta, j);
+        norm_chunk<KIND, YT, PT>(Er, yr, j, D, mu, hg ? &g : nullptr, hb ? &b : nullptr);
+      }
+    }
+  }
+  return true;
+}
+
 template <int KIND, int XT, int YT, int EXPM>
 __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(128) unsigned char pipe_smem[];
@@ -712,40 +816,26 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
     }
     if (o >= 0 && !dead) {
       const int se = o % SE;
-      if (!mbar_wait(&sready[se], (uint32_t)(o / SE) & 1u)) { abort_flag = 1; dead = true; continue; }
-      const float sm = rowsum[se], rs = rowrcp[se];
-      const bool fast_ok = sm >= 1.0f && sm < 0x1p20f;
-      RowDivisor D;
-      if (KIND != REGION_SOFTMAX) D = make_divisor(sm);
+      const uint32_t par = (uint32_t)(o / SE) & 1u;
       const float* Er = E + (size_t)se * estride;
       char* yr = (char*)P.y + ((int64_t)blockIdx.x + (int64_t)o * gridDim.x) * P.ldy * ysz;
+      if (KIND != REGION_SOFTMAX) {
+        const bool ok = P.param_dtype == PSK_BF16
+                            ? norm_epilogue<KIND, YT, PSK_BF16>(P, Er, yr, tt, cols, &sready[se], par, &rowsum[se], &rowrcp[se])
+                            : norm_epilogue<KIND, YT, PSK_F32>(P, Er, yr, tt, cols, &sready[se], par, &rowsum[se], &rowrcp[se]);
+        if (!ok) { abort_flag = 1; dead = true; }
+        continue;
+      }
+      if (!mbar_wait(&sready[se], par)) { abort_flag = 1; dead = true; continue; }
+      const float sm = rowsum[se], rs = rowrcp[se];
+      const bool fast_ok = sm >= 1.0f && sm < 0x1p20f;
 #pragma unroll
       for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
         if (j < cols) {
           const float4 e = *reinterpret_cast<const float4*>(Er + j);
           float o4[4] = {e.x, e.y, e.z, e.w};
-          if (KIND == REGION_SOFTMAX) {
-            row_div_n<4>(o4, sm, rs, fast_ok);
-          } else {
-            if (KIND == REGION_LAYER) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) o4[q] = __fsub_rn(o4[q], rs);
-            }
-            divide_n<4>(o4, D);
-            if (P.gamma) {
-              float g4[4];
-              load4_param(P.gamma, P.param_dtype, j, g4);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) o4[q] = __fmul_rn(o4[q], g4[q]);
-            }
-            if (KIND == REGION_LAYER && P.beta) {
-              float b4[4];
-              load4_param(P.beta, P.param_dtype, j, b4);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) o4[q] = __fadd_rn(o4[q], b4[q]);
-            }
-          }
+          row_div_n<4>(o4, sm, rs, fast_ok);
           if (YT == PSK_F32) {
             __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o4[0], o4[1], o4[2], o4[3]));
           } else {
