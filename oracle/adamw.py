@@ -19,8 +19,26 @@ Readings taken here:
     q  = mh / (sqrt(vh) + eps)
     u  = q + (wd*theta)
     theta1 = theta - (lr*u)
-* the schedule is constant and there is no gradient clipping; bf16 gradients
-  widen exactly.
+* bf16 gradients widen exactly.
+
+Schedules and clipping (the same passage: grad_clip = c scales the gradient
+by min(1, c / (||g||_2 + 1e-6)), the global norm over the tree, as
+clip_grad_norm_; schedules constant(), linear(warmup = w) -- lr t/w for
+t <= w, then lr (total - t)/(total - w) -- and cosine(warmup = w) -- lr t/w,
+then lr 1/2 (1 + cos(pi (t - w)/(total - w))) -- both reaching 0 at total).
+Readings taken here:
+* the scheduled lr is computed exactly (a rational, or cos at 300 bits, whose
+  value is rational only where cos(pi r) is: r in {0, 1/3, 1/2, 2/3, 1}) and
+  rounded once to f32; from t = total on it is 0 (the relu of the pages'
+  piecewise form); warmup 0 has no warmup piece;
+* ||g||^2 is summed in f32 over a declared tree: each leaf's RN(g_j^2) in
+  blocks of 1024 consecutive elements (sequential within a block), the block
+  sums in groups of 64 (sequential), the group sums of a leaf (sequential),
+  then the leaves in tree order (sequential); the pages fix no order, and
+  this one keeps every chain short on the GPU;
+* scale = min(q, 1) with q = RN(c / RN(sqrt(||g||^2) + RN(1e-6))), min as the
+  group's MIN (q < 1 ? q : 1, so a NaN q gives 1); every gradient is then
+  RN(g * scale) in f32 before the step (scale 1 changes no bit).
 """
 
 from __future__ import annotations
@@ -86,3 +104,105 @@ def step_tree(leaves, grad_dtype: str, hp):
     weight_decay t.  Returns a list of (theta', m', v') per leaf."""
     h = hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
     return [step_leaf(th, m, v, g, grad_dtype, h) for th, m, v, g in leaves]
+
+
+# ------------------------------------------------------ schedules and clip
+LR_CONSTANT, LR_LINEAR, LR_COSINE = "constant", "linear", "cosine"
+SQ_BLOCK = 1024      # elements per block of the squared-norm tree
+SQ_GROUP = 64        # blocks per group
+
+
+def lr_factor(kind: str, warmup: int, total: int, t: int):
+    """The schedule's factor at step t, exactly: a Fraction, or an mpmath value
+    (cosine at an irrational point)."""
+    if t < 1:
+        raise ValueError("t counts steps from 1")
+    if kind == LR_CONSTANT:
+        return Fraction(1)
+    if kind not in (LR_LINEAR, LR_COSINE):
+        raise ValueError(f"unknown schedule {kind!r}")
+    if not (0 <= warmup < total):
+        raise ValueError("a schedule needs 0 <= warmup < total")
+    if warmup > 0 and t <= warmup:
+        return Fraction(t, warmup)
+    if t >= total:
+        return Fraction(0)
+    num, den = t - warmup, total - warmup           # r = num / den in (0, 1)
+    if kind == LR_LINEAR:
+        return Fraction(den - num, den)
+    exact = {Fraction(1, 3): Fraction(1, 2), Fraction(1, 2): Fraction(0), Fraction(2, 3): Fraction(-1, 2)}
+    r = Fraction(num, den)
+    if r in exact:
+        return (1 + exact[r]) / 2
+    import mpmath as mp
+
+    with mp.workprec(300):
+        return (1 + mp.cos(mp.pi * mp.mpf(num) / den)) / 2
+
+
+def lr_scheduled(lr: float, kind: str, warmup: int, total: int, t: int) -> np.float32:
+    """RN_f32(lr * factor(t)), the exact product rounded once."""
+    f = lr_factor(kind, warmup, total, t)
+    if isinstance(f, Fraction):
+        return rn_f32(Fraction(lr) * f)
+    import mpmath as mp
+
+    with mp.workprec(300):
+        v = mp.mpf(lr) * f
+        man, exp = mp.frexp(v)
+        q = Fraction(int(mp.floor(man * mp.mpf(2) ** 280)), 1) * Fraction(2) ** (int(exp) - 280)
+    return _rn_decided(q, Fraction(1, 2 ** 250))
+
+
+def _seq_sum_rows(a: np.ndarray) -> np.ndarray:
+    """Sequential f32 sum along axis 1 of a 2-D array (rows in parallel)."""
+    s = a[:, 0].copy()
+    for j in range(1, a.shape[1]):
+        s = (s + a[:, j]).astype(np.float32)
+    return s
+
+
+def grad_sq_norm(grads, grad_dtype: str) -> np.float32:
+    """||g||^2 over the tree in the declared f32 tree (see the module text)."""
+    total = None
+    for g in grads:
+        gf = widen(np.asarray(g), grad_dtype).reshape(-1)
+        if gf.size == 0:
+            continue
+        with np.errstate(all="ignore"):
+            sq = (gf * gf).astype(np.float32)
+            nb = -(-sq.size // SQ_BLOCK)
+            blocks = _seq_sum_rows(np.pad(sq, (0, nb * SQ_BLOCK - sq.size)).reshape(nb, SQ_BLOCK))
+            ng = -(-nb // SQ_GROUP)
+            groups = _seq_sum_rows(np.pad(blocks, (0, ng * SQ_GROUP - nb)).reshape(ng, SQ_GROUP))
+            leaf = groups[0]
+            for v in groups[1:]:
+                leaf = np.float32(leaf + v)
+            total = leaf if total is None else np.float32(total + leaf)
+    return np.float32(0.0) if total is None else np.float32(total)
+
+
+def clip_scale(sq_norm: np.float32, grad_clip: float) -> np.float32:
+    """min(RN(c / RN(sqrt(||g||^2) + RN(1e-6))), 1) in f32."""
+    with np.errstate(all="ignore"):
+        norm = np.sqrt(np.float32(sq_norm))
+        den = np.float32(norm + np.float32(1e-6))
+        q = np.float32(np.float32(grad_clip) / den)
+    return q if q < np.float32(1.0) else np.float32(1.0)
+
+
+def step_tree_scheduled(leaves, grad_dtype: str, hp, kind: str = LR_CONSTANT, warmup: int = 0, total: int = 1,
+                        grad_clip: float = 0.0):
+    """step_tree with the lr schedule and (grad_clip > 0) global-norm clipping.
+    Returns (list of (theta', m', v'), scale or None)."""
+    leaves = list(leaves)
+    h = hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
+    h["lr"] = lr_scheduled(hp.lr, kind, warmup, total, hp.t)
+    scale = None
+    if grad_clip > 0:
+        scale = clip_scale(grad_sq_norm([g for _, _, _, g in leaves], grad_dtype), grad_clip)
+        with np.errstate(all="ignore"):
+            leaves = [(th, m, v, (widen(np.asarray(g), grad_dtype) * scale).astype(np.float32))
+                      for th, m, v, g in leaves]
+        grad_dtype = "f32"
+    return [step_leaf(th, m, v, g, grad_dtype, h) for th, m, v, g in leaves], scale

@@ -9,6 +9,7 @@
 * hand-picked scalars against exact rational arithmetic rounded per operation.
 """
 
+import math
 from fractions import Fraction
 
 import numpy as np
@@ -106,3 +107,88 @@ def test_bf16_grads_widen_exactly():
     a = OA.step_leaf(th, z, z, gb, "bf16", h)
     b = OA.step_leaf(th, z, z, bf16_to_f32(gb), "f32", h)
     assert all(same_bits(x, y) for x, y in zip(a, b))
+
+
+# ------------------------------------------------------ schedules and clip
+
+def test_linear_schedule_closed_forms():
+    lr, w, total = 3e-4, 100, 1000
+    L = np.float32(lr)
+    f = lambda t: OA.lr_scheduled(lr, "linear", w, total, t)  # noqa: E731
+    assert f(w) == L and f(w // 2) == L / 2 and f(w // 4) == L / 4
+    assert f(total) == 0 and f(total + 7) == 0
+    assert f(w + (total - w) // 2) == L / 2                  # half way down: exactly half
+    seq = [f(t) for t in range(1, total + 1)]
+    assert all(a <= b for a, b in zip(seq[:w - 1], seq[1:w]))
+    assert all(a >= b for a, b in zip(seq[w - 1:], seq[w:]))
+    assert OA.lr_scheduled(lr, "linear", 0, 400, 100) == np.float32(3e-4 * 0.75) or \
+        abs(float(OA.lr_scheduled(lr, "linear", 0, 400, 100)) - 2.25e-4) < 1e-11
+
+
+def test_cosine_schedule_closed_forms_and_symmetry():
+    lr, w, total = 1e-3, 50, 1050
+    L = np.float32(lr)
+    f = lambda t: OA.lr_scheduled(lr, "cosine", w, total, t)  # noqa: E731
+    assert f(w) == L and f(total) == 0 and f(w // 2) == L / 2
+    assert f(w + 500) == L / 2                                  # cos(pi/2) = 0
+    assert f(w + 250) == np.float32(lr * 0.75 + 0) or abs(float(f(w + 250)) / (lr * (1 + np.cos(np.pi / 4)) / 2) - 1) < 2 ** -23
+    for d in range(1, 500, 37):                                 # f(w+d) + f(total-d) = lr in exact reals
+        s = float(f(w + d)) + float(f(total - d))
+        assert abs(s - lr) <= float(np.spacing(L)) * 1.01
+    for t in range(w + 1, total, 97):                           # the exact value, rounded once
+        want = lr * 0.5 * (1 + math.cos(math.pi * (t - w) / (total - w)))
+        assert abs(float(f(t)) - want) <= 0.5 * float(np.spacing(np.float32(want))) * 1.0001
+
+
+def test_squared_norm_follows_the_declared_tree():
+    """squares 1, then 2047 times 2^-24: a sequential chain keeps 1 (each
+    1 + 2^-24 ties to 1); blocks of 1024 give 1 and 1024 * 2^-24 = 2^-14, so
+    the leaf's sum is 1 + 2^-14 exactly."""
+    g = np.full(2048, np.float32(2.0 ** -12), dtype=np.float32)
+    g[0] = 1.0
+    assert OA.grad_sq_norm([g], "f32") == np.float32(1 + 2.0 ** -14)
+    # leaves combine in order, groups of 64 blocks inside a leaf
+    big = np.full(64 * 1024 + 5, np.float32(0.5), dtype=np.float32)
+    assert OA.grad_sq_norm([big, g], "f32") == np.float32(big.size * 0.25 + 1 + 2.0 ** -14)
+    assert OA.grad_sq_norm([], "f32") == 0
+
+
+def test_clip_scale_closed_form():
+    """||g|| = 2^-10, c = 2^-12: q = c / (2^-10 + 1e-6), just below 1/4."""
+    g = np.zeros(3000, dtype=np.float32)
+    g[17] = np.float32(2.0 ** -10)
+    sq = OA.grad_sq_norm([g], "f32")
+    assert sq == np.float32(2.0 ** -20)
+    q = OA.clip_scale(sq, 2.0 ** -12)
+    want = Fraction(1, 4096) / (Fraction(1, 1024) + Fraction(float(np.float32(1e-6))))
+    assert abs(Fraction(float(q)) - want) <= Fraction(float(np.spacing(np.float32(0.25)))) / 2
+    assert q < 0.25
+    assert OA.clip_scale(np.float32(4.0), 100.0) == 1.0          # below the threshold: no scaling
+
+
+def test_clipped_scheduled_step_against_torch_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    shapes = [(37, 19), (2500,), (3, 5, 7)]
+    th = [(rng.standard_normal(s) * 0.02).astype(np.float32) for s in shapes]
+    m = [(rng.standard_normal(s) * 1e-3).astype(np.float32) for s in shapes]
+    v = [np.abs(rng.standard_normal(s) * 1e-4).astype(np.float32) for s in shapes]
+    g = [(rng.standard_normal(s) * 0.5).astype(np.float32) for s in shapes]
+    hp = W.AdamWHyper(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, t=7)
+    out, scale = OA.step_tree_scheduled(zip(th, m, v, g), "f32", hp, "cosine", 3, 20, grad_clip=1.0)
+    assert scale < 1
+    params = [torch.nn.Parameter(torch.from_numpy(t.astype(np.float64))) for t in th]
+    for p_, gg in zip(params, g):
+        p_.grad = torch.from_numpy(gg.astype(np.float64))
+    torch.nn.utils.clip_grad_norm_(params, 1.0)
+    opt = torch.optim.AdamW(params, lr=float(OA.lr_scheduled(1e-3, "cosine", 3, 20, 7)), betas=(0.9, 0.999),
+                            eps=1e-8, weight_decay=0.01)
+    for p_, mm, vv in zip(params, m, v):
+        st = opt.state[p_]
+        st["step"] = torch.tensor(6.0, dtype=torch.float64)
+        st["exp_avg"] = torch.from_numpy(mm.astype(np.float64))
+        st["exp_avg_sq"] = torch.from_numpy(vv.astype(np.float64))
+    opt.step()
+    for (t1, m1, v1), p_, mm in zip(out, params, m):
+        assert np.allclose(t1, p_.detach().numpy(), rtol=0, atol=3e-7)
+        assert np.allclose(m1, opt.state[p_]["exp_avg"].numpy(), rtol=3e-6, atol=1e-9)

@@ -109,6 +109,47 @@ def _norm_bias_before_scale(monkeypatch):
     monkeypatch.setattr(ON, "_affine", wrong)
 
 
+def _cosine_without_half(monkeypatch):
+    real = OA.lr_factor
+
+    def wrong(kind, warmup, total, t):
+        f = real(kind, warmup, total, t)
+        return f * 2 if kind == "cosine" and warmup < t < total else f
+
+    monkeypatch.setattr(OA, "lr_factor", wrong)
+
+
+def _linear_decay_from_zero(monkeypatch):
+    real = OA.lr_factor
+
+    def wrong(kind, warmup, total, t):
+        from fractions import Fraction
+        if kind == "linear" and warmup < t < total:
+            return Fraction(total - t, total)
+        return real(kind, warmup, total, t)
+
+    monkeypatch.setattr(OA, "lr_factor", wrong)
+
+
+def _sq_norm_one_chain(monkeypatch):
+    def wrong(grads, grad_dtype):
+        total = np.float32(0)
+        for g in grads:
+            for v in OF.widen(np.asarray(g), grad_dtype).reshape(-1):
+                total = np.float32(total + np.float32(v * v))
+        return total
+
+    monkeypatch.setattr(OA, "grad_sq_norm", wrong)
+
+
+def _clip_without_epsilon(monkeypatch):
+    def wrong(sq_norm, grad_clip):
+        q = np.float32(np.float32(grad_clip) / np.sqrt(np.float32(sq_norm)))
+        return q if q < 1 else np.float32(1)
+
+    monkeypatch.setattr(OA, "clip_scale", wrong)
+
+
 CASES = [
     (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
     (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
@@ -122,6 +163,10 @@ CASES = [
     (_norm_eps_after_sqrt, TN.test_rms_closed_form_with_eps),
     (_norm_no_mean_in_rms, TN.test_rms_of_a_constant_row_is_one),
     (_norm_bias_before_scale, TN.test_gamma_and_beta),
+    (_cosine_without_half, TA.test_cosine_schedule_closed_forms_and_symmetry),
+    (_linear_decay_from_zero, TA.test_linear_schedule_closed_forms),
+    (_sq_norm_one_chain, TA.test_squared_norm_follows_the_declared_tree),
+    (_clip_without_epsilon, TA.test_clip_scale_closed_form),
 ]
 
 
