@@ -18,9 +18,9 @@
  *                       trees; presk "The language", The optimizer).
  *
  * Conventions for every call:
- * - Pointers named ptr/x/y/theta/m/v/grad are DEVICE pointers owned by the
- *   caller; descriptor structs and arrays of them are HOST memory, read during
- *   the call only.  The library allocates no device memory and keeps no state
+ * - Pointers named ptr/x/y/theta/m/v/grad/gamma/beta/workspace are DEVICE
+ *   pointers owned by the caller; descriptor structs and arrays of them are
+ *   HOST memory, read during the call only.  The library allocates no device memory and keeps no state
  *   across calls besides cached device attributes and one device status word
  *   (psk_device_status).
  * - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
@@ -221,8 +221,48 @@ typedef struct { double lr, beta1, beta2, eps, weight_decay; int64_t t; } psk_ad
 int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp, void* stream);
 
 /* Host-only: the nine f32 scalars the step reads, in the order
- * b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd. */
+ * b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd (constant schedule). */
 int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]);
+
+/* ---------------------------------------------- schedules and clipping
+ * presk "The language", The optimizer: with grad_clip = c the gradient is
+ * first scaled by min(1, c / (||g||_2 + 1e-6)), the global norm over the tree;
+ * schedules constant(), linear(warmup = w) -- lr t/w for t <= w, then
+ * lr (total - t)/(total - w) -- and cosine(warmup = w) -- lr t/w, then
+ * lr 1/2 (1 + cos(pi (t - w)/(total - w))) -- both 0 from t = total on.
+ * The scheduled lr is computed exactly from the binary64 arguments and
+ * rounded once to f32 (psk_adamw_lr returns it).  Clipping (grad_clip > 0):
+ *   ||g||^2 = f32 sum of RN(g^2) over a declared tree -- blocks of 1024
+ *   consecutive elements of a leaf (in order), groups of 64 blocks (in
+ *   order), a leaf's groups (in order), the leaves (in order; empty leaves
+ *   skipped);
+ *   q = RN(c / RN(sqrt(||g||^2) + RN(1e-6))), scale = q < 1 ? q : 1;
+ *   every gradient enters the step as RN(g * scale).
+ * warmup 0 has no warmup piece; linear and cosine need
+ * 0 <= warmup < total < 2^52; grad_clip must be finite, 0 = no clipping. */
+typedef enum { PSK_LR_CONSTANT = 0, PSK_LR_LINEAR = 1, PSK_LR_COSINE = 2 } psk_lr_kind;
+typedef struct {
+  int32_t kind;         /* psk_lr_kind */
+  int64_t warmup, total;
+  double grad_clip;     /* c; 0 = none */
+} psk_adamw_schedule;
+
+/* Host-only: the scheduled f32 lr of step hp->t. */
+int psk_adamw_lr(const psk_adamw_hparams* hp, const psk_adamw_schedule* sched, float* lr);
+
+/* Host-only: the DEVICE workspace bytes psk_adamw_tree_ex needs for these
+ * leaves and this schedule (0 without clipping: about 4 bytes per 1024
+ * parameters with it). */
+int psk_adamw_workspace(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_schedule* sched,
+                        uint64_t* bytes);
+
+/* psk_adamw_tree with a schedule (NULL: constant, no clipping) and, when
+ * clipping, a caller-owned 16-byte aligned DEVICE workspace of at least
+ * psk_adamw_workspace bytes (its contents need no initialisation and are
+ * scratch: concurrent calls must not share one).  Clipping adds three short
+ * launches (the squared-norm tree and the scale) before the update. */
+int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                      const psk_adamw_schedule* sched, void* workspace, uint64_t workspace_bytes, void* stream);
 
 /* Host-only, synchronous: the device status word of the pipelined kernels of
  * the current device (0 = no bounded wait ever timed out; bit 0 = a wait gave

@@ -6,8 +6,11 @@ parameter tree, each one CUDA launch through a C ABI (include/psk.h).
 """
 
 from .ops import (  # noqa: F401
+    psk_adamw_lr,
     psk_adamw_scalars,
     psk_adamw_tree,
+    psk_adamw_tree_ex,
+    psk_adamw_workspace,
     psk_device_status,
     psk_group_check,
     psk_group_prepare,

@@ -16,6 +16,7 @@ PSK_F32, PSK_BF16 = 0, 1
 PSK_ORDER_SEQUENTIAL, PSK_ORDER_BLOCKED, PSK_ORDER_INTERLEAVED = 0, 1, 2
 PSK_EXP_EXACT, PSK_EXP_FAST = 0, 1
 PSK_NORM_RMS, PSK_NORM_LAYER = 0, 1
+PSK_LR_CONSTANT, PSK_LR_LINEAR, PSK_LR_COSINE = 0, 1, 2
 PSK_MAX_RANK = 4
 PSK_ADAMW_MAX_LEAVES = 512
 
@@ -25,7 +26,7 @@ ERRORS = {
 }
 
 EXPORTS = ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_norm_region",
-           "psk_adamw_tree",
+           "psk_adamw_tree", "psk_adamw_tree_ex", "psk_adamw_lr", "psk_adamw_workspace",
            "psk_adamw_scalars", "psk_device_status", "psk_last_error")
 
 
@@ -57,6 +58,11 @@ class psk_adamw_hparams(ctypes.Structure):
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("t", ctypes.c_int64)]
 
 
+class psk_adamw_schedule(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("warmup", ctypes.c_int64), ("total", ctypes.c_int64),
+                ("grad_clip", ctypes.c_double)]
+
+
 class PskError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"{ERRORS.get(code, code)}: {msg}")
@@ -86,11 +92,15 @@ def lib() -> ctypes.CDLL:
                                       ctypes.c_int32, psk_order, ctypes.c_void_p]
         L.psk_adamw_tree.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_hparams), ctypes.c_void_p]
         L.psk_adamw_scalars.argtypes = [P(psk_adamw_hparams), P(ctypes.c_float)]
+        L.psk_adamw_lr.argtypes = [P(psk_adamw_hparams), P(psk_adamw_schedule), P(ctypes.c_float)]
+        L.psk_adamw_workspace.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_schedule), P(ctypes.c_uint64)]
+        L.psk_adamw_tree_ex.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_hparams), P(psk_adamw_schedule),
+                                        ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
         L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_last_error.restype = ctypes.c_char_p
         for f in ("psk_group_run", "psk_group_check", "psk_group_prepare", "psk_softmax_region", "psk_norm_region",
                   "psk_adamw_tree",
-                  "psk_adamw_scalars",
+                  "psk_adamw_scalars", "psk_adamw_lr", "psk_adamw_workspace", "psk_adamw_tree_ex",
                   "psk_device_status"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L

@@ -13,6 +13,18 @@
 // Unaligned leaves and ragged tails take a scalar path with the same
 // arithmetic.  Each operation is one IEEE f32 rounding, in the order of the
 // definition, so every parameter is bit-identical to the unfused chain.
+//
+// psk_adamw_tree_ex adds the pages' schedules and global-norm clipping (the
+// same passage: grad_clip = c scales g by min(1, c / (||g||_2 + 1e-6));
+// constant / linear / cosine schedules with warmup).  The scheduled lr is
+// computed on the host exactly (rational arithmetic on binary64 pairs, cos in
+// double-double) and rounded once.  Clipping takes three short launches
+// before the update, in the caller's workspace: ||g||^2 in f32 over a declared
+// tree -- RN(g^2) summed in blocks of 1024 consecutive elements of a leaf (one
+// thread per block), the block sums in groups of 64 and the group sums of a
+// leaf (one CTA per leaf), the leaf sums in tree order (one thread) -- then
+// scale = min(q, 1), q = RN(c / RN(sqrt(||g||^2) + RN(1e-6))), which the
+// update kernel reads and applies as RN(g * scale).
 
 #include <math.h>
 #include <string.h>
@@ -62,8 +74,10 @@ __device__ __forceinline__ float load_grad(const void* g, int32_t gdt, int64_t i
   return bf16_bits_to_f32(__ldcs((const unsigned short*)g + i));
 }
 
-__global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant__ AdamParams P) {
+template <bool CLIP>
+__global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant__ AdamParams P, const float* clip) {
   const int t = threadIdx.x;
+  const float scale = CLIP ? *clip : 1.0f;
   for (int64_t c = blockIdx.x; c < P.n_chunks; c += gridDim.x) {
     // the leaf holding chunk c: last leaf with chunk_begin <= c
     int lo = 0, hi = P.n_leaves - 1;
@@ -89,6 +103,10 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
           g[k] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
                              __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
         }
+        if (CLIP) {
+          g[k].x = __fmul_rn(g[k].x, scale); g[k].y = __fmul_rn(g[k].y, scale);
+          g[k].z = __fmul_rn(g[k].z, scale); g[k].w = __fmul_rn(g[k].w, scale);
+        }
       }
 #pragma unroll
       for (int k = 0; k < AW_VPT; ++k) {
@@ -106,6 +124,7 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
         const int64_t i = base + j;
         float th = L.th[i], m = L.m[i], v = L.v[i];
         float g = load_grad(L.g, L.gdt, i);
+        if (CLIP) g = __fmul_rn(g, scale);
         adamw_one(P.s, th, m, v, g);
         L.th[i] = th;
         L.m[i] = m;
@@ -113,6 +132,114 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
       }
     }
   }
+}
+
+// ------------------------------------------------- clipping: ||g||^2 tree
+constexpr int SQ_BLOCK = 1024;                 // elements per block (one chain)
+constexpr int SQ_GROUP = 64;                   // blocks per group
+constexpr int SQ_THREADS = 256;
+
+struct SqLeaf {
+  const void* g;
+  int64_t numel;
+  int64_t block_begin;   // first block of the leaf in the launch's block array
+  int64_t group_begin;   // first group of the leaf in the launch's group array
+  int32_t gdt;
+  int32_t leaf_index;    // position of the leaf in the whole tree (its leaf-sum slot)
+};
+
+struct SqParams {
+  int32_t n_leaves;
+  int64_t n_blocks;
+  float* block_sums;     // workspace
+  float* group_sums;     // workspace
+  float* leaf_sums;      // workspace, one per leaf of the tree
+  SqLeaf leaf[PSK_ADAMW_MAX_LEAVES];
+};
+
+// One thread per block: RN(g^2) added in index order over the block's (up to)
+// 1024 elements, read 8 (bf16) or 4 (f32) at a time when aligned.
+__global__ void __launch_bounds__(SQ_THREADS) sq_blocks_kernel(const __grid_constant__ SqParams P) {
+  const int64_t b = (int64_t)blockIdx.x * SQ_THREADS + threadIdx.x;
+  if (b >= P.n_blocks) return;
+  int lo = 0, hi = P.n_leaves - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.leaf[mid].block_begin <= b) lo = mid; else hi = mid - 1;
+  }
+  const SqLeaf& L = P.leaf[lo];
+  const int64_t base = (b - L.block_begin) * SQ_BLOCK;
+  const int n = (int)((L.numel - base) < SQ_BLOCK ? (L.numel - base) : SQ_BLOCK);
+  float acc = 0.0f;
+  int j = 0;
+  if (L.gdt == PSK_BF16) {
+    const uint16_t* g = (const uint16_t*)L.g + base;
+    if (((uintptr_t)g & 15u) == 0) {
+      for (; j + 8 <= n; j += 8) {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(g + j));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(w[k] << 16), c = __uint_as_float(w[k] & 0xFFFF0000u);
+          acc = __fadd_rn(acc, __fmul_rn(a, a));
+          acc = __fadd_rn(acc, __fmul_rn(c, c));
+        }
+      }
+    }
+    for (; j < n; ++j) {
+      const float a = bf16_bits_to_f32(__ldcs(g + j));
+      acc = __fadd_rn(acc, __fmul_rn(a, a));
+    }
+  } else {
+    const float* g = (const float*)L.g + base;
+    if (((uintptr_t)g & 15u) == 0) {
+      for (; j + 4 <= n; j += 4) {
+        const float4 q = __ldcs(reinterpret_cast<const float4*>(g + j));
+        acc = __fadd_rn(acc, __fmul_rn(q.x, q.x));
+        acc = __fadd_rn(acc, __fmul_rn(q.y, q.y));
+        acc = __fadd_rn(acc, __fmul_rn(q.z, q.z));
+        acc = __fadd_rn(acc, __fmul_rn(q.w, q.w));
+      }
+    }
+    for (; j < n; ++j) {
+      const float a = __ldcs(g + j);
+      acc = __fadd_rn(acc, __fmul_rn(a, a));
+    }
+  }
+  P.block_sums[b] = acc;   // 0 + x = x: the chain starting from 0 is the chain starting from the first square
+}
+
+// One CTA per leaf: its groups (64 consecutive blocks each, added in order) by
+// the CTA's threads, then the leaf's sum of its group sums in order.
+__global__ void __launch_bounds__(SQ_THREADS) sq_leaves_kernel(const __grid_constant__ SqParams P) {
+  const SqLeaf& L = P.leaf[blockIdx.x];
+  const int64_t nb = (L.numel + SQ_BLOCK - 1) / SQ_BLOCK;
+  const int64_t ng = (nb + SQ_GROUP - 1) / SQ_GROUP;
+  for (int64_t gi = threadIdx.x; gi < ng; gi += SQ_THREADS) {
+    const int64_t b0 = gi * SQ_GROUP;
+    const int64_t b1 = b0 + SQ_GROUP < nb ? b0 + SQ_GROUP : nb;
+    const float* bs = P.block_sums + L.block_begin;
+    float acc = bs[b0];
+    for (int64_t b = b0 + 1; b < b1; ++b) acc = __fadd_rn(acc, bs[b]);
+    P.group_sums[L.group_begin + gi] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float* gs = P.group_sums + L.group_begin;
+    float acc = gs[0];
+    for (int64_t gi = 1; gi < ng; ++gi) acc = __fadd_rn(acc, gs[gi]);
+    P.leaf_sums[L.leaf_index] = acc;
+  }
+}
+
+// One thread: the leaf sums in tree order, then the clip scale.
+__global__ void sq_scale_kernel(const float* leaf_sums, int32_t n_leaves, float clip, float* scale) {
+  float acc = 0.0f;
+  for (int i = 0; i < n_leaves; ++i) acc = i == 0 ? leaf_sums[0] : __fadd_rn(acc, leaf_sums[i]);
+  const float norm = __fsqrt_rn(acc);
+  const float den = __fadd_rn(norm, 1e-6f);
+  const float q = __fdiv_rn(clip, den);
+  *scale = q < 1.0f ? q : 1.0f;
 }
 
 // ------------------------------------------------- host: scalar injection
@@ -162,6 +289,91 @@ static float hd_to_f32(HD v) {
   return v.hi < 0 ? -pick : pick;
 }
 
+// ------------------------------------------------- host: lr schedules
+static HD hd_div(HD a, double b) {      // a / b for an exact binary64 b
+  const double q1 = a.hi / b;
+  const double p = q1 * b, pe = fma(q1, b, -p);
+  const double r = ((a.hi - p) - pe) + a.lo;
+  return hd_norm(q1, r / b);
+}
+static HD hd_add(HD a, HD b) {
+  HD s = hd_two_sum(a.hi, b.hi);
+  return hd_norm(s.hi, s.lo + a.lo + b.lo);
+}
+static const HD HD_PI = {0x1.921fb54442d18p+1, 0x1.1a62633145c07p-53};
+
+// cos(x), 0 <= x <= pi, in double-double (Taylor series after folding x to
+// [0, pi/2]; error far below 2^-100).
+static HD hd_cos(HD x) {
+  bool neg = false;
+  if (x.hi > 0.5 * HD_PI.hi) {
+    x = hd_add(HD_PI, HD{-x.hi, -x.lo});
+    neg = true;
+  }
+  const HD x2 = hd_mul(x, x);
+  HD term{1.0, 0.0}, sum{1.0, 0.0};
+  for (int k = 1; k < 30; ++k) {
+    term = hd_div(hd_mul(term, x2), (double)((2 * k - 1) * (2 * k)));
+    sum = hd_add(sum, (k & 1) ? HD{-term.hi, -term.lo} : term);
+    if (fabs(term.hi) < 0x1p-110) break;
+  }
+  return neg ? HD{-sum.hi, -sum.lo} : sum;
+}
+
+// Exact comparison of two normalised double-double values.
+static int hd_cmp(HD a, HD b) {
+  if (a.hi != b.hi) return a.hi < b.hi ? -1 : 1;
+  if (a.lo != b.lo) return a.lo < b.lo ? -1 : 1;
+  return 0;
+}
+static HD hd_prod(double a, double b) {  // exact
+  const double p = a * b;
+  return hd_norm(p, fma(a, b, -p));
+}
+
+// RN_f32(lr * num / den) exactly, for num, den < 2^53 (lr * num and every
+// candidate midpoint * den are exact double-double products).
+static float rn_f32_rational(double lr, double num, double den) {
+  if (num == 0.0 || lr == 0.0) return 0.0f * (float)lr;
+  const HD a = hd_prod(lr, num);                 // exact
+  const HD q = hd_div(a, den);
+  const float c = (float)q.hi;
+  const int side = hd_cmp(a, hd_prod((double)c, den));       // true value vs c
+  if (side == 0) return c;
+  const float nb = nextafterf(c, side > 0 ? INFINITY : -INFINITY);
+  const double mid = 0.5 * ((double)c + (double)nb);        // exact
+  const int m = hd_cmp(a, hd_prod(mid, den)) * (side > 0 ? 1 : -1);   // > 0: beyond the midpoint
+  if (m > 0) return nb;
+  if (m < 0) return c;
+  uint32_t cb;
+  memcpy(&cb, &c, 4);
+  return (cb & 1u) ? nb : c;                                 // a tie: the even one
+}
+
+// The scheduled learning rate at step t, rounded once to f32.
+static int scheduled_lr(const psk_adamw_hparams* hp, const psk_adamw_schedule* sc, float& out) {
+  const int64_t t = hp->t, w = sc ? sc->warmup : 0, T = sc ? sc->total : 1;
+  const int kind = sc ? sc->kind : PSK_LR_CONSTANT;
+  if (kind == PSK_LR_CONSTANT) { out = (float)hp->lr; return PSK_OK; }
+  if (kind != PSK_LR_LINEAR && kind != PSK_LR_COSINE) return fail(PSK_E_ARG, "schedule kind %d", kind);
+  if (!(w >= 0 && w < T) || T > (int64_t(1) << 52))
+    return fail(PSK_E_ARG, "schedule needs 0 <= warmup < total < 2^52 (warmup %lld, total %lld)", (long long)w,
+                (long long)T);
+  if (w > 0 && t <= w) { out = rn_f32_rational(hp->lr, (double)t, (double)w); return PSK_OK; }
+  if (t >= T) { out = 0.0f; return PSK_OK; }
+  const int64_t num = t - w, den = T - w;       // r = num / den in (0, 1)
+  if (kind == PSK_LR_LINEAR) { out = rn_f32_rational(hp->lr, (double)(den - num), (double)den); return PSK_OK; }
+  // cosine: rational where cos(pi r) is (r = 1/3, 1/2, 2/3), else via double-double
+  if (3 * num == den) { out = rn_f32_rational(hp->lr, 3.0, 4.0); return PSK_OK; }
+  if (2 * num == den) { out = rn_f32_rational(hp->lr, 1.0, 2.0); return PSK_OK; }
+  if (3 * num == 2 * den) { out = rn_f32_rational(hp->lr, 1.0, 4.0); return PSK_OK; }
+  const HD r = hd_div(HD{(double)num, 0.0}, (double)den);
+  const HD c = hd_cos(hd_mul(HD_PI, r));
+  const HD f = hd_mul(hd_add(HD{1.0, 0.0}, c), HD{0.5, 0.0});
+  out = hd_to_f32(hd_mul(HD{hp->lr, 0.0}, f));
+  return PSK_OK;
+}
+
 static int make_scalars(const psk_adamw_hparams* hp, AdamScalars& s) {
   if (!hp) return fail(PSK_E_NULL, "hyperparameters are NULL");
   if (hp->t < 1) return fail(PSK_E_ARG, "t = %lld: steps count from 1", (long long)hp->t);
@@ -181,40 +393,128 @@ static int make_scalars(const psk_adamw_hparams* hp, AdamScalars& s) {
   return PSK_OK;
 }
 
-}  // namespace psk
+// Workspace of the clipped step: the scale, then the block, group and leaf
+// sums of the squared-norm tree, each 16-byte aligned.
+struct Workspace {
+  uint64_t scale_off, blocks_off, groups_off, leaves_off, bytes;
+  int64_t n_blocks, n_groups, n_leaves;
+};
 
-using namespace psk;
+static uint64_t align16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
 
-extern "C" int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]) {
-  clear_error();
-  if (!out) return fail(PSK_E_NULL, "output array is NULL");
-  AdamScalars s;
-  int rc = make_scalars(hp, s);
-  if (rc) return rc;
-  float v[9] = {s.b1, s.b2, s.omb1, s.omb2, s.bc1, s.bc2, s.lr, s.eps, s.wd};
-  memcpy(out, v, sizeof(v));
+static Workspace plan_workspace(const psk_leaf* leaves, int32_t n_leaves, bool clip) {
+  Workspace W{};
+  if (!clip) return W;
+  for (int i = 0; i < n_leaves; ++i) {
+    if (leaves[i].numel <= 0) continue;
+    const int64_t nb = (leaves[i].numel + SQ_BLOCK - 1) / SQ_BLOCK;
+    W.n_blocks += nb;
+    W.n_groups += (nb + SQ_GROUP - 1) / SQ_GROUP;
+    W.n_leaves += 1;
+  }
+  W.scale_off = 0;
+  W.blocks_off = 16;
+  W.groups_off = align16(W.blocks_off + 4 * (uint64_t)W.n_blocks);
+  W.leaves_off = align16(W.groups_off + 4 * (uint64_t)W.n_groups);
+  W.bytes = align16(W.leaves_off + 4 * (uint64_t)W.n_leaves);
+  return W;
+}
+
+static int check_leaves(const psk_leaf* leaves, int32_t n_leaves) {
+  if (n_leaves < 0) return fail(PSK_E_ARG, "n_leaves %d", n_leaves);
+  if (n_leaves > 0 && !leaves) return fail(PSK_E_NULL, "leaf table is NULL");
+  for (int i = 0; i < n_leaves; ++i) {
+    const psk_leaf& L = leaves[i];
+    if (L.numel < 0) return fail(PSK_E_SHAPE, "leaf %d: numel %lld", i, (long long)L.numel);
+    if (!dtype_ok(L.grad_dtype)) return fail(PSK_E_DTYPE, "leaf %d: grad dtype %d", i, L.grad_dtype);
+    if (L.numel > 0 && (!L.theta || !L.m || !L.v || !L.grad)) return fail(PSK_E_NULL, "leaf %d: NULL pointer", i);
+  }
   return PSK_OK;
 }
 
-extern "C" int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp, void* stream) {
-  clear_error();
-  if (n_leaves < 0) return fail(PSK_E_ARG, "n_leaves %d", n_leaves);
-  if (n_leaves > 0 && !leaves) return fail(PSK_E_NULL, "leaf table is NULL");
+static int check_schedule(const psk_adamw_schedule* sc) {
+  if (!sc) return PSK_OK;
+  if (!(sc->grad_clip >= 0.0) || !isfinite(sc->grad_clip)) return fail(PSK_E_ARG, "grad_clip must be finite and >= 0");
+  if (sc->kind != PSK_LR_CONSTANT && sc->kind != PSK_LR_LINEAR && sc->kind != PSK_LR_COSINE)
+    return fail(PSK_E_ARG, "schedule kind %d", sc->kind);
+  return PSK_OK;
+}
+
+// ||g||^2 tree and the clip scale into the workspace (launches only).
+static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace& W, char* ws, float clip,
+                       cudaStream_t stream) {
+  SqParams* P = new SqParams;
+  float* blocks = (float*)(ws + W.blocks_off);
+  float* groups = (float*)(ws + W.groups_off);
+  float* leaf_sums = (float*)(ws + W.leaves_off);
+  int rc = PSK_OK, i = 0, leaf_index = 0;
+  int64_t block0 = 0, group0 = 0;
+  while (i < n_leaves && rc == PSK_OK) {
+    int cnt = 0;
+    int64_t nb_batch = 0, ng_batch = 0;
+    for (; i < n_leaves && cnt < PSK_ADAMW_MAX_LEAVES; ++i) {
+      const psk_leaf& L = leaves[i];
+      if (L.numel == 0) continue;
+      SqLeaf& d = P->leaf[cnt++];
+      d.g = L.grad;
+      d.numel = L.numel;
+      d.gdt = L.grad_dtype;
+      d.block_begin = nb_batch;
+      d.group_begin = ng_batch;
+      d.leaf_index = leaf_index++;
+      const int64_t nb = (L.numel + SQ_BLOCK - 1) / SQ_BLOCK;
+      nb_batch += nb;
+      ng_batch += (nb + SQ_GROUP - 1) / SQ_GROUP;
+    }
+    if (cnt == 0) continue;
+    P->n_leaves = cnt;
+    P->n_blocks = nb_batch;
+    P->block_sums = blocks + block0;
+    P->group_sums = groups + group0;
+    P->leaf_sums = leaf_sums;
+    sq_blocks_kernel<<<(unsigned)((nb_batch + SQ_THREADS - 1) / SQ_THREADS), SQ_THREADS, 0, stream>>>(*P);
+    rc = check_launch("squared-norm blocks kernel");
+    if (rc) break;
+    sq_leaves_kernel<<<cnt, SQ_THREADS, 0, stream>>>(*P);
+    rc = check_launch("squared-norm leaves kernel");
+    block0 += nb_batch;
+    group0 += ng_batch;
+  }
+  delete P;
+  if (rc) return rc;
+  sq_scale_kernel<<<1, 1, 0, stream>>>(leaf_sums, (int32_t)W.n_leaves, clip, (float*)(ws + W.scale_off));
+  return check_launch("clip scale kernel");
+}
+
+static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                     const psk_adamw_schedule* sc, void* workspace, uint64_t workspace_bytes, void* stream) {
+  int rc = check_leaves(leaves, n_leaves);
+  if (rc) return rc;
+  rc = check_schedule(sc);
+  if (rc) return rc;
   AdamParams* P = new AdamParams;   // host staging of the kernel parameter
-  int rc = make_scalars(hp, P->s);
-  for (int i = 0; i < n_leaves && rc == PSK_OK; ++i) {
-    const psk_leaf& L = leaves[i];
-    if (L.numel < 0) rc = fail(PSK_E_SHAPE, "leaf %d: numel %lld", i, (long long)L.numel);
-    else if (!dtype_ok(L.grad_dtype)) rc = fail(PSK_E_DTYPE, "leaf %d: grad dtype %d", i, L.grad_dtype);
-    else if (L.numel > 0 && (!L.theta || !L.m || !L.v || !L.grad)) rc = fail(PSK_E_NULL, "leaf %d: NULL pointer", i);
+  rc = make_scalars(hp, P->s);
+  if (rc == PSK_OK) rc = scheduled_lr(hp, sc, P->s.lr);
+  const bool clip = sc && sc->grad_clip > 0.0;
+  const Workspace W = plan_workspace(leaves, n_leaves, clip);
+  if (rc == PSK_OK && clip) {
+    if (!workspace) rc = fail(PSK_E_NULL, "clipping needs a workspace of %llu bytes", (unsigned long long)W.bytes);
+    else if (workspace_bytes < W.bytes)
+      rc = fail(PSK_E_ARG, "workspace of %llu bytes, clipping needs %llu", (unsigned long long)workspace_bytes,
+                (unsigned long long)W.bytes);
+    else if ((uintptr_t)workspace % 16 != 0) rc = fail(PSK_E_ARG, "workspace must be 16-byte aligned");
   }
   int sms = 1, per_sm = 1, dev = 0;
   if (rc == PSK_OK) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel, AW_THREADS, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel<false>, AW_THREADS, 0);
     if (per_sm < 1) per_sm = 1;
   }
+  cudaStream_t s = (cudaStream_t)stream;
+  const float* scale = clip ? (const float*)((char*)workspace + W.scale_off) : nullptr;
+  if (rc == PSK_OK && clip && W.n_leaves > 0) rc = launch_clip(leaves, n_leaves, W, (char*)workspace,
+                                                               (float)sc->grad_clip, s);
   // one launch per PSK_ADAMW_MAX_LEAVES non-empty leaves (one launch for the trees here)
   int i = 0;
   while (i < n_leaves && rc == PSK_OK) {
@@ -238,9 +538,58 @@ extern "C" int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const ps
     P->n_chunks = chunks;
     int64_t cap = (int64_t)sms * per_sm;
     unsigned grid = (unsigned)(chunks < cap ? chunks : cap);
-    adamw_kernel<<<grid, AW_THREADS, 0, (cudaStream_t)stream>>>(*P);
+    if (clip) adamw_kernel<true><<<grid, AW_THREADS, 0, s>>>(*P, scale);
+    else adamw_kernel<false><<<grid, AW_THREADS, 0, s>>>(*P, nullptr);
     rc = check_launch("adamw tree kernel");
   }
   delete P;
   return rc;
+}
+
+}  // namespace psk
+
+using namespace psk;
+
+extern "C" int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]) {
+  clear_error();
+  if (!out) return fail(PSK_E_NULL, "output array is NULL");
+  AdamScalars s;
+  int rc = make_scalars(hp, s);
+  if (rc) return rc;
+  float v[9] = {s.b1, s.b2, s.omb1, s.omb2, s.bc1, s.bc2, s.lr, s.eps, s.wd};
+  memcpy(out, v, sizeof(v));
+  return PSK_OK;
+}
+
+extern "C" int psk_adamw_lr(const psk_adamw_hparams* hp, const psk_adamw_schedule* sched, float* lr) {
+  clear_error();
+  if (!lr) return fail(PSK_E_NULL, "output is NULL");
+  AdamScalars s;
+  int rc = make_scalars(hp, s);
+  if (rc == PSK_OK) rc = check_schedule(sched);
+  if (rc == PSK_OK) rc = scheduled_lr(hp, sched, *lr);
+  return rc;
+}
+
+extern "C" int psk_adamw_workspace(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_schedule* sched,
+                                   uint64_t* bytes) {
+  clear_error();
+  if (!bytes) return fail(PSK_E_NULL, "output is NULL");
+  int rc = check_leaves(leaves, n_leaves);
+  if (rc == PSK_OK) rc = check_schedule(sched);
+  if (rc) return rc;
+  *bytes = plan_workspace(leaves, n_leaves, sched && sched->grad_clip > 0.0).bytes;
+  return PSK_OK;
+}
+
+extern "C" int psk_adamw_tree(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp, void* stream) {
+  clear_error();
+  return adamw_run(leaves, n_leaves, hp, nullptr, nullptr, 0, stream);
+}
+
+extern "C" int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                                 const psk_adamw_schedule* sched, void* workspace, uint64_t workspace_bytes,
+                                 void* stream) {
+  clear_error();
+  return adamw_run(leaves, n_leaves, hp, sched, workspace, workspace_bytes, stream);
 }

@@ -153,13 +153,52 @@ def psk_adamw_scalars(hp):
     return np.array(list(out), dtype=np.float32)
 
 
-def psk_adamw_tree(leaves, hp, stream=None) -> None:
-    """leaves: list of (theta, m, v, grad) tensors, updated in place."""
+def _leaf_table(leaves):
     n = len(leaves)
     arr = (N.psk_leaf * max(n, 1))()
     for i, (th, m, v, g) in enumerate(leaves):
         arr[i].theta, arr[i].m, arr[i].v, arr[i].grad = th.data_ptr(), m.data_ptr(), v.data_ptr(), g.data_ptr()
         arr[i].grad_dtype = _dtype_code(g)
         arr[i].numel = int(th.numel())
+    return arr, n
+
+
+_LR = {"constant": N.PSK_LR_CONSTANT, "linear": N.PSK_LR_LINEAR, "cosine": N.PSK_LR_COSINE}
+
+
+def _schedule(kind="constant", warmup=0, total=1, grad_clip=0.0) -> N.psk_adamw_schedule:
+    return N.psk_adamw_schedule(_LR[kind], int(warmup), int(total), float(grad_clip))
+
+
+def psk_adamw_tree(leaves, hp, stream=None) -> None:
+    """leaves: list of (theta, m, v, grad) tensors, updated in place."""
+    arr, n = _leaf_table(leaves)
     h = _hparams(hp)
     N.check(N.lib().psk_adamw_tree(arr, n, ctypes.byref(h), _stream_handle(stream)))
+
+
+def psk_adamw_lr(hp, kind="constant", warmup=0, total=1) -> np.float32:
+    """The scheduled f32 lr of step hp.t (host only)."""
+    h, sc, out = _hparams(hp), _schedule(kind, warmup, total), ctypes.c_float(0)
+    N.check(N.lib().psk_adamw_lr(ctypes.byref(h), ctypes.byref(sc), ctypes.byref(out)))
+    return np.float32(out.value)
+
+
+def psk_adamw_workspace(leaves, kind="constant", warmup=0, total=1, grad_clip=0.0) -> int:
+    """Device workspace bytes psk_adamw_tree_ex needs (0 without clipping)."""
+    arr, n = _leaf_table(leaves)
+    sc, out = _schedule(kind, warmup, total, grad_clip), ctypes.c_uint64(0)
+    N.check(N.lib().psk_adamw_workspace(arr, n, ctypes.byref(sc), ctypes.byref(out)))
+    return int(out.value)
+
+
+def psk_adamw_tree_ex(leaves, hp, kind="constant", warmup=0, total=1, grad_clip=0.0, workspace=None,
+                      stream=None) -> None:
+    """psk_adamw_tree with a schedule and global-norm clipping; workspace: a
+    device tensor of at least psk_adamw_workspace bytes (needed when clipping)."""
+    arr, n = _leaf_table(leaves)
+    h, sc = _hparams(hp), _schedule(kind, warmup, total, grad_clip)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    N.check(N.lib().psk_adamw_tree_ex(arr, n, ctypes.byref(h), ctypes.byref(sc), ws_ptr, ws_bytes,
+                                      _stream_handle(stream)))

@@ -180,3 +180,44 @@ def test_group_prepare_refuses_as_check(native):
     with pytest.raises(native.PskError) as e:                                             # transposed: races
         ops.psk_group_prepare(W.encode([("IN", 0), ("NEG",)]), None, [(x, (1, 4))], x)
     assert e.value.name == "PSK_E_ALIAS"
+
+
+def test_scheduled_lr_equals_oracle(native):
+    """The host's exact schedule (binary64 pairs, double-double cos) against the
+    oracle's (rationals, mpmath): the same f32 for every step, including lrs
+    and lengths whose quotients fall on or next to f32 rounding midpoints."""
+    from reduction_groups_gb300 import ops
+
+    rng = np.random.default_rng(17)
+    cases = [(3e-4, "linear", 100, 1000), (1e-3, "cosine", 50, 1050), (2.0 ** -10, "linear", 2 ** 12, 2 ** 20),
+             (2.0 ** -7 * 3, "cosine", 0, 3 * 2 ** 10), (6e-4, "cosine", 2000, 100000), (1.0, "linear", 0, 7),
+             (0.1, "constant", 0, 1)]
+    for lr, kind, w, total in cases:
+        ts = sorted(set([1, 2, w, w + 1, total - 1, total, total + 3, max(1, w // 2), w + (total - w) // 3,
+                         w + (total - w) // 2, w + 2 * (total - w) // 3] +
+                        [int(t) for t in rng.integers(1, total + 5, 300)]))
+        for t in ts:
+            if t < 1:
+                continue
+            hp = W.AdamWHyper(lr=lr, t=int(t))
+            got = ops.psk_adamw_lr(hp, kind, w, total)
+            want = OA.lr_scheduled(lr, kind, w, total, int(t))
+            assert got.view(np.uint32) == np.float32(want).view(np.uint32), (lr, kind, w, total, t, got, want)
+
+
+def test_adamw_workspace_and_schedule_refusals(native):
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    leaves = [tuple(torch.zeros(n) for _ in range(4)) for n in (5, 0, 3000, 70000)]
+    assert ops.psk_adamw_workspace(leaves) == 0
+    nb = 1 + 3 + 69                                   # blocks of 1024
+    ng = 1 + 1 + 2                                    # groups of 64 blocks
+    want = 16 + ((4 * nb + 15) // 16) * 16 + ((4 * ng + 15) // 16) * 16 + ((4 * 3 + 15) // 16) * 16
+    assert ops.psk_adamw_workspace(leaves, grad_clip=1.0) == want
+    hp = W.AdamWHyper(t=3)
+    with pytest.raises(native.PskError) as e:
+        ops.psk_adamw_lr(hp, "linear", 10, 10)
+    assert e.value.name == "PSK_E_ARG"
+    with pytest.raises(native.PskError):
+        ops.psk_adamw_workspace(leaves, grad_clip=float("nan"))

@@ -1,0 +1,128 @@
+"""Parity of the scheduled, clipped AdamW step (psk_adamw_tree_ex) with the
+oracle, bit for bit: the squared-norm tree, the clip scale, the scheduled lr
+and every updated parameter."""
+
+import numpy as np
+import pytest
+
+import oracle.adamw as OA
+from oracle.f32 import bf16_to_f32, f32_to_bf16
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import reduction_groups_gb300 as R
+
+    return R
+
+
+def _to_dev(a, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _to_host(t):
+    if t.dtype == torch.bfloat16:
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _workspace(dev, leaves, **sched):
+    n = dev.psk_adamw_workspace(leaves, **sched)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+
+
+def _check(leaves, want):
+    for (th, m, v, g), (wt, wm, wv) in zip(leaves, want):
+        assert np.array_equal(_to_host(th).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v).view(np.uint32), wv.view(np.uint32))
+
+
+@pytest.mark.parametrize("kind,w,total", [("cosine", 3, 40), ("linear", 0, 25), ("constant", 0, 1)])
+@pytest.mark.parametrize("clip", [0.0, 1e-2, 1e3])
+def test_gpt_tree_scheduled_and_clipped_bitwise(dev, kind, w, total, clip):
+    """clip 1e-2 scales every gradient (scale < 1), 1e3 leaves them (scale 1)."""
+    tree = W.gpt_adamw_leaves()
+    host = [tree.host_leaf(i) for i in range(len(tree.leaves))]
+    want, scale = OA.step_tree_scheduled(host, tree.grad_dtype, tree.hp, kind, w, total, grad_clip=clip)
+    leaves = [tuple(_to_dev(a, tree.grad_dtype if k == 3 else "f32") for k, a in enumerate(h)) for h in host]
+    ws = _workspace(dev, leaves, kind=kind, warmup=w, total=total, grad_clip=clip)
+    dev.psk_adamw_tree_ex(leaves, tree.hp, kind, w, total, clip, ws)
+    torch.cuda.synchronize()
+    _check(leaves, want)
+    if clip > 0:
+        got = ws[:4].cpu().numpy().view(np.float32)[0]
+        assert got.view(np.uint32) == np.float32(scale).view(np.uint32)
+        assert (scale < 1) == (clip < 1)
+
+
+def test_ragged_unaligned_bf16_leaves_clipped(dev):
+    rng = np.random.default_rng(9)
+    hp = W.AdamWHyper(lr=1e-3, t=5)
+    sizes = [1, 3, 1023, 1025, 4097, 64 * 1024 + 3, 0, 10007]
+    host, leaves = [], []
+    for n in sizes:
+        th = (rng.standard_normal(n + 1) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n + 1) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n + 1) * 1e-4).astype(np.float32)
+        g = f32_to_bf16((rng.standard_normal(n + 1) * 0.3).astype(np.float32))
+        host.append((th[1:], m[1:], v[1:], g[1:]))
+        leaves.append(tuple(_to_dev(a, "bf16" if k == 3 else "f32")[1:] for k, a in enumerate((th, m, v, g))))
+    want, scale = OA.step_tree_scheduled(host, "bf16", hp, "linear", 2, 9, grad_clip=0.5)
+    assert scale < 1
+    ws = _workspace(dev, leaves, kind="linear", warmup=2, total=9, grad_clip=0.5)
+    dev.psk_adamw_tree_ex(leaves, hp, "linear", 2, 9, 0.5, ws)
+    torch.cuda.synchronize()
+    _check(leaves, want)
+
+
+def test_two_layer_llama_tree_clipped_sampled(dev):
+    """A 2-layer Llama-style tree (~200M parameters, bf16 gradients): the scale
+    against the oracle's squared-norm tree over every gradient, and sampled
+    parameters against the oracle's step."""
+    tree = W.llama_adamw_leaves(layers=2)
+    leaves = [tree.device_leaf(i) for i in range(len(tree.leaves))]
+    grads = [_to_host(g) for (_, _, _, g) in leaves]
+    scale = OA.clip_scale(OA.grad_sq_norm(grads, "bf16"), 1.0)
+    rng = np.random.default_rng(12)
+    picks, before = [], []
+    for (th, m, v, g) in leaves:
+        n = th.numel()
+        idx = np.unique(np.concatenate([np.arange(min(n, 4)), np.arange(max(0, n - 4), n),
+                                        rng.integers(0, n, min(n, 8192))]))
+        it = torch.from_numpy(idx).cuda()
+        picks.append(it)
+        before.append(tuple(_to_host(a[it]) for a in (th, m, v, g)))
+    h = OA.hyper_f32(tree.hp.lr, tree.hp.beta1, tree.hp.beta2, tree.hp.eps, tree.hp.weight_decay, tree.hp.t)
+    h["lr"] = OA.lr_scheduled(tree.hp.lr, "cosine", 100, 5000, tree.hp.t)
+    ws = _workspace(dev, leaves, kind="cosine", warmup=100, total=5000, grad_clip=1.0)
+    dev.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000, 1.0, ws)
+    torch.cuda.synchronize()
+    assert ws[:4].cpu().numpy().view(np.float32)[0].view(np.uint32) == scale.view(np.uint32)
+    for (th, m, v, g), it, (bt, bm, bv, bg) in zip(leaves, picks, before):
+        gs = (bf16_to_f32(bg) * scale).astype(np.float32)
+        wt, wm, wv = OA.step_leaf(bt, bm, bv, gs, "f32", h)
+        assert np.array_equal(_to_host(th[it]).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m[it]).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v[it]).view(np.uint32), wv.view(np.uint32))
+
+
+def test_clip_needs_a_workspace(dev):
+    leaves = [tuple(torch.zeros(100, device="cuda") for _ in range(4))]
+    hp = W.AdamWHyper(t=1)
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_adamw_tree_ex(leaves, hp, grad_clip=1.0)
+    assert e.value.name == "PSK_E_NULL"
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_adamw_tree_ex(leaves, hp, grad_clip=1.0, workspace=small)
+    assert e.value.name == "PSK_E_ARG"
