@@ -275,7 +275,7 @@ def run_ours(a, ws, rank, local):
     b_all = {"group": b_group, "softmax_sequential": b_soft, "softmax_interleaved8": b_soft, "adamw": b_adam}
     # the normalization regions (rows beyond the step's path): timed beside
     # the step, or as the step itself under --only norm
-    norm_launches, norm_rows = {}, 0
+    extra_launches, norm_rows = {}, 0
     if a.only in ("all", "norm"):
         for kind, label in (("rms", "rmsnorm"), ("layer", "layernorm")):
             nw = W.norm_rows(kind, rows=max(1, int(32768 * sc)))
@@ -283,13 +283,13 @@ def run_ours(a, ws, rank, local):
             ny = torch.empty_like(nx)
             ng, nb = nw.device_params()
             for oname, order in (("sequential", ("sequential",)), ("interleaved8", ("interleaved", 8))):
-                norm_launches[f"{label}_{oname}"] = (lambda nx=nx, ny=ny, kind=kind, eps=nw.eps, ng=ng, nb=nb,
+                extra_launches[f"{label}_{oname}"] = (lambda nx=nx, ny=ny, kind=kind, eps=nw.eps, ng=ng, nb=nb,
                                                      order=order: R.psk_norm_region(nx, ny, kind, eps, ng, nb, order))
                 b_all[f"{label}_{oname}"] = nw.algorithmic_bytes()
             norm_rows = nw.rows
         torch.cuda.synchronize()
     if a.only == "norm":
-        launches = dict(norm_launches)
+        launches = dict(extra_launches)
     kernels = [k for k in launches if a.only in ("all", "norm") or k.startswith(a.only)]
     bytes_step = sum(b_all[k] for k in kernels)
 
@@ -345,8 +345,17 @@ def run_ours(a, ws, rank, local):
             torch.cuda.synchronize()
             extra_ms[f"{name}_{other}_exp"] = e0.elapsed_time(e1) / a.steps
 
-    if a.only == "all":
-        for name, fn in norm_launches.items():
+    # the clipped step with a cosine schedule on the same tree (clipping reads
+    # every gradient once more before the update), beside the step
+    clip_ws = None
+    if a.only in ("all", "adamw"):
+        clip_ws = torch.empty(max(16, R.psk_adamw_workspace(leaves, "cosine", 100, 5000, 1.0)), dtype=torch.uint8,
+                              device="cuda")
+        extra_launches["adamw_clip_cosine"] = lambda: R.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000, 1.0,
+                                                                         clip_ws)
+        b_all["adamw_clip_cosine"] = b_adam + tree.n_params * (2 if tree.grad_dtype == "bf16" else 4)
+    if a.only in ("all", "adamw"):
+        for name, fn in extra_launches.items():
             for _ in range(2):
                 fn()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -421,8 +430,11 @@ def run_ours(a, ws, rank, local):
         gbs = kbytes / (ms / 1e3) / 1e9
         kinfo[k] = {"ms": round(ms, 4), "algorithmic_bytes": int(kbytes), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4), "in_value": False,
-                    "rows_per_s": round((norm_rows if k in norm_launches else sw.rows) / (ms / 1e3), 1)}
-    for k in norm_launches:
+                    "rows_per_s": round((norm_rows if k in extra_launches else sw.rows) / (ms / 1e3), 1)}
+        if k == "adamw_clip_cosine":
+            del kinfo[k]["rows_per_s"]
+            kinfo[k]["params_per_s"] = round(tree.n_params / (ms / 1e3), 1)
+    for k in extra_launches:
         if k in kernels:
             kinfo[k]["rows_per_s"] = round(norm_rows / (per_kernel_ms[k] / 1e3), 1)
     if "group" in kinfo:
