@@ -264,6 +264,20 @@ int psk_adamw_workspace(const psk_leaf* leaves, int32_t n_leaves, const psk_adam
 int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
                       const psk_adamw_schedule* sched, void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* psk_adamw_tree_ex without a caller workspace: when clipping, its scratch
+ * is a fixed buffer of PSK_ADAMW_STATIC_WORKSPACE bytes inside the library's
+ * device module (one per device, reserved when the module loads), so the call
+ * allocates nothing and needs no workspace argument.  The pages have no
+ * counterpart: it exists for callers that cannot hand the library device
+ * memory.  Limits: trees whose clipping scratch exceeds the buffer (about
+ * 2 * 10^9 parameters) are refused with PSK_E_ARG; calls that overlap in time
+ * on one device (other streams, other threads) share the buffer and race, so
+ * they must be serialised (one stream, or events).  Without clipping it is
+ * psk_adamw_tree_ex. */
+#define PSK_ADAMW_STATIC_WORKSPACE (8u << 20)
+int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                          const psk_adamw_schedule* sched, void* stream);
+
 /* Host-only, synchronous: the device status word of the pipelined kernels of
  * the current device (0 = no bounded wait ever timed out; bit 0 = a wait gave
  * up and the kernel wound down, its output then unspecified).  reset != 0

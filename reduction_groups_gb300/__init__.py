@@ -10,6 +10,7 @@ from .ops import (  # noqa: F401
     psk_adamw_scalars,
     psk_adamw_tree,
     psk_adamw_tree_ex,
+    psk_adamw_tree_static,
     psk_adamw_workspace,
     psk_device_status,
     psk_group_check,

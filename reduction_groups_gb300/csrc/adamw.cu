@@ -29,6 +29,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace psk {
@@ -546,9 +548,48 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
   return rc;
 }
 
+// Scratch of psk_adamw_tree_static: one fixed buffer in the library's module
+// per device, reserved when the module loads; its address comes from
+// cudaGetSymbolAddress, once per device.  Every value in it is written before
+// it is read, so nothing is cleared.
+static __device__ __align__(256) unsigned char g_adamw_static_ws[PSK_ADAMW_STATIC_WORKSPACE];
+
+static int static_workspace(void** ptr) {
+  static void* addr[PSK_MAX_DEVICES] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= PSK_MAX_DEVICES)
+    return fail(PSK_E_CUDA, "no current CUDA device below %d", PSK_MAX_DEVICES);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_adamw_static_ws) != cudaSuccess) {
+    addr[dev] = nullptr;
+    return check_launch("static workspace address");
+  }
+  *ptr = addr[dev];
+  return PSK_OK;
+}
+
 }  // namespace psk
 
 using namespace psk;
+
+extern "C" int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                                     const psk_adamw_schedule* sched, void* stream) {
+  clear_error();
+  const bool clip = sched && sched->grad_clip > 0.0;
+  if (!clip) return adamw_run(leaves, n_leaves, hp, sched, nullptr, 0, stream);
+  int rc = check_leaves(leaves, n_leaves);
+  if (rc == PSK_OK) rc = check_schedule(sched);
+  if (rc) return rc;
+  const Workspace W = plan_workspace(leaves, n_leaves, true);
+  if (W.bytes > (uint64_t)PSK_ADAMW_STATIC_WORKSPACE)
+    return fail(PSK_E_ARG, "clipping this tree needs %llu bytes of scratch, the fixed buffer holds %llu",
+                (unsigned long long)W.bytes, (unsigned long long)PSK_ADAMW_STATIC_WORKSPACE);
+  void* ws = nullptr;
+  rc = static_workspace(&ws);
+  if (rc) return rc;
+  return adamw_run(leaves, n_leaves, hp, sched, ws, PSK_ADAMW_STATIC_WORKSPACE, stream);
+}
 
 extern "C" int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]) {
   clear_error();

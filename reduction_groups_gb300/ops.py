@@ -202,3 +202,11 @@ def psk_adamw_tree_ex(leaves, hp, kind="constant", warmup=0, total=1, grad_clip=
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     N.check(N.lib().psk_adamw_tree_ex(arr, n, ctypes.byref(h), ctypes.byref(sc), ws_ptr, ws_bytes,
                                       _stream_handle(stream)))
+
+
+def psk_adamw_tree_static(leaves, hp, kind="constant", warmup=0, total=1, grad_clip=0.0, stream=None) -> None:
+    """psk_adamw_tree_ex whose clipping scratch is the library's fixed device
+    buffer (no workspace argument; overlapping calls on one device race)."""
+    arr, n = _leaf_table(leaves)
+    h, sc = _hparams(hp), _schedule(kind, warmup, total, grad_clip)
+    N.check(N.lib().psk_adamw_tree_static(arr, n, ctypes.byref(h), ctypes.byref(sc), _stream_handle(stream)))

@@ -2,6 +2,7 @@
 every entry point include/psk.h declares, validates programs exactly as the
 oracle's definition does, and injects the AdamW scalars the oracle computes."""
 
+import ctypes
 import os
 import re
 
@@ -221,3 +222,21 @@ def test_adamw_workspace_and_schedule_refusals(native):
     assert e.value.name == "PSK_E_ARG"
     with pytest.raises(native.PskError):
         ops.psk_adamw_workspace(leaves, grad_clip=float("nan"))
+
+
+def test_static_scratch_refuses_trees_beyond_its_buffer(native):
+    """The fixed buffer's size check happens on the host, before any device
+    work: a tree needing more clipping scratch is refused (no device here, so a
+    check that let it through would fail with PSK_E_CUDA instead)."""
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import _native as N
+
+    t = torch.zeros(4)
+    arr = (N.psk_leaf * 1)()
+    arr[0].theta = arr[0].m = arr[0].v = arr[0].grad = t.data_ptr()
+    arr[0].grad_dtype = N.PSK_F32
+    arr[0].numel = 3 * 10 ** 9                     # never dereferenced: refused first
+    h = N.psk_adamw_hparams(3e-4, 0.9, 0.999, 1e-8, 0.01, 1)
+    sc = N.psk_adamw_schedule(N.PSK_LR_CONSTANT, 0, 1, 1.0)
+    rc = N.lib().psk_adamw_tree_static(arr, 1, ctypes.byref(h), ctypes.byref(sc), None)
+    assert N.ERRORS.get(rc) == "PSK_E_ARG" and "fixed buffer" in N.lib().psk_last_error().decode()
