@@ -177,6 +177,22 @@ __global__ void __launch_bounds__(SQ_THREADS) sq_blocks_kernel(const __grid_cons
   if (L.gdt == PSK_BF16) {
     const uint16_t* g = (const uint16_t*)L.g + base;
     if (((uintptr_t)g & 15u) == 0) {
+      // four 16-byte loads in flight per thread; the adds keep index order
+      for (; j + 32 <= n; j += 32) {
+        uint4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = __ldcs(reinterpret_cast<const uint4*>(g + j) + u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float a = __uint_as_float(w[k] << 16), c = __uint_as_float(w[k] & 0xFFFF0000u);
+            acc = __fadd_rn(acc, __fmul_rn(a, a));
+            acc = __fadd_rn(acc, __fmul_rn(c, c));
+          }
+        }
+      }
       for (; j + 8 <= n; j += 8) {
         const uint4 q = __ldcs(reinterpret_cast<const uint4*>(g + j));
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -195,6 +211,18 @@ __global__ void __launch_bounds__(SQ_THREADS) sq_blocks_kernel(const __grid_cons
   } else {
     const float* g = (const float*)L.g + base;
     if (((uintptr_t)g & 15u) == 0) {
+      for (; j + 16 <= n; j += 16) {
+        float4 q[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q[u] = __ldcs(reinterpret_cast<const float4*>(g + j) + u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc = __fadd_rn(acc, __fmul_rn(q[u].x, q[u].x));
+          acc = __fadd_rn(acc, __fmul_rn(q[u].y, q[u].y));
+          acc = __fadd_rn(acc, __fmul_rn(q[u].z, q[u].z));
+          acc = __fadd_rn(acc, __fmul_rn(q[u].w, q[u].w));
+        }
+      }
       for (; j + 4 <= n; j += 4) {
         const float4 q = __ldcs(reinterpret_cast<const float4*>(g + j));
         acc = __fadd_rn(acc, __fmul_rn(q.x, q.x));
