@@ -150,6 +150,25 @@ def _clip_without_epsilon(monkeypatch):
     monkeypatch.setattr(OA, "clip_scale", wrong)
 
 
+def _mask_keeps_emptied_rows(monkeypatch):
+    real = OS._apply_mask
+
+    def wrong(xf, mask):
+        xm, emptied = real(xf, mask)
+        return xm, np.zeros_like(emptied)
+
+    monkeypatch.setattr(OS, "_apply_mask", wrong)
+
+
+def _backward_sign_flipped(monkeypatch):
+    def wrong(y, ct, y_dtype, ct_dtype, dx_dtype, order=("sequential",)):
+        yf, cf = OF.widen(np.asarray(y), y_dtype), OF.widen(np.asarray(ct), ct_dtype)
+        s = OS.row_sum((cf * yf).astype(np.float32), order)
+        return OF.store((yf * (s[:, None] - cf).astype(np.float32)).astype(np.float32), dx_dtype)
+
+    monkeypatch.setattr(OS, "softmax_backward", wrong)
+
+
 CASES = [
     (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
     (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
@@ -167,6 +186,8 @@ CASES = [
     (_linear_decay_from_zero, TA.test_linear_schedule_closed_forms),
     (_sq_norm_one_chain, TA.test_squared_norm_follows_the_declared_tree),
     (_clip_without_epsilon, TA.test_clip_scale_closed_form),
+    (_mask_keeps_emptied_rows, TS.test_mask_emptied_rows_give_zeros_and_full_mask_changes_nothing),
+    (_backward_sign_flipped, TS.test_backward_one_hot_cotangent_closed_form),
 ]
 
 

@@ -118,3 +118,68 @@ def test_nan_and_empty_rows():
     assert e.shape == (4, 0)
     one = OS.softmax_region(np.array([[3.5]], dtype=np.float32), "f32", "f32", SEQ)
     assert one[0, 0] == 1.0
+
+
+# ------------------------------------------------------------ masked softmax
+
+@pytest.mark.parametrize("order", [SEQ, ("interleaved", 3)])
+def test_masked_equals_scores_with_minus_infinity(order):
+    """The pages' definition: the bits of the softmax of the scores with -inf
+    at every refused position (rows the mask does not empty)."""
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((30, 77)) * 3).astype(np.float32)
+    mask = (rng.random((30, 77)) < 0.6).astype(np.uint8)
+    mask[:, 5] = 1
+    got = OS.softmax_region(x, "f32", "f32", order, mask=mask)
+    want = OS.softmax_region(np.where(mask != 0, x, -np.inf).astype(np.float32), "f32", "f32", order)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert np.all(got[mask == 0] == 0)
+    row = (rng.random(77) < 0.5).astype(np.uint8)
+    row[0] = 1
+    assert np.array_equal(OS.softmax_region(x, "f32", "f32", order, mask=row),
+                          OS.softmax_region(x, "f32", "f32", order, mask=np.tile(row, (30, 1))))
+
+
+def test_mask_emptied_rows_give_zeros_and_full_mask_changes_nothing():
+    rng = np.random.default_rng(42)
+    x = (rng.standard_normal((6, 40)) * 3).astype(np.float32)
+    mask = np.ones((6, 40), dtype=np.uint8)
+    mask[2] = 0
+    y = OS.softmax_region(x, "f32", "f32", SEQ, mask=mask)
+    assert np.all(y[2] == 0) and not np.signbit(y[2]).any()
+    assert np.array_equal(np.delete(y, 2, axis=0), np.delete(OS.softmax_region(x, "f32", "f32", SEQ), 2, axis=0))
+    x2 = x.copy()
+    x2[4, :] = -np.inf                          # allowed but -inf everywhere: NaN, as without a mask
+    y2 = OS.softmax_region(x2, "f32", "f32", SEQ, mask=np.ones(40, np.uint8))
+    assert np.isnan(y2[4]).all()
+
+
+# ----------------------------------------------------------- softmax backward
+
+def test_backward_one_hot_cotangent_closed_form():
+    """ct = e_k: s = y_k exactly, dx_j = RN(y_j * -y_k) (j != k),
+    dx_k = RN(y_k * RN(1 - y_k))."""
+    rng = np.random.default_rng(43)
+    y = OS.softmax_region((rng.standard_normal((4, 33)) * 2).astype(np.float32), "f32", "f32", SEQ)
+    for k in (0, 7, 32):
+        ct = np.zeros_like(y)
+        ct[:, k] = 1.0
+        dx = OS.softmax_backward(y, ct, "f32", "f32", "f32")
+        want = (y * -y[:, k:k + 1]).astype(np.float32)
+        want[:, k] = (y[:, k] * (np.float32(1) - y[:, k]).astype(np.float32)).astype(np.float32)
+        assert np.array_equal(dx.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("order", [SEQ, ("interleaved", 8)])
+def test_backward_against_torch_autograd_float64(order):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(44)
+    x = (rng.standard_normal((16, 300)) * 2).astype(np.float32)
+    ct = rng.standard_normal((16, 300)).astype(np.float32)
+    xt = torch.from_numpy(x.astype(np.float64)).requires_grad_(True)
+    torch.softmax(xt, dim=1).backward(torch.from_numpy(ct.astype(np.float64)))
+    y = OS.softmax_region(x, "f32", "f32", order)
+    dx = OS.softmax_backward(y, ct, "f32", "f32", "f32", order)
+    want = xt.grad.numpy()
+    assert np.all(np.abs(dx - want) <= 1e-6 * np.abs(want) + 1e-8)
+    assert np.all(np.abs(dx.astype(np.float64).sum(axis=1)) < 1e-6)   # sum_j y_j (ct_j - s) = 0 in exact reals
