@@ -172,6 +172,29 @@ typedef enum { PSK_EXP_EXACT = 0, PSK_EXP_FAST = 1 } psk_exp_mode;
 int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
                        int64_t ldx, int64_t ldy, psk_order order, int32_t exp_mode, void* stream);
 
+/* The masked softmax region (presk "Native execution", numerics: a mask is
+ * an index buffer of 0 and 1; the masked softmax takes its maximum from the
+ * allowed positions and its sum over them, writes 0 where it refuses, and a
+ * row it empties gives zeros -- otherwise the bits of the softmax of the
+ * scores with -inf at the refused positions).  mask: DEVICE bytes, nonzero
+ * allows; ldm = 0 applies one mask row of cols bytes to every row, ldm >= cols
+ * gives each row its own.  Other arguments as psk_softmax_region; y must not
+ * overlap the mask; cols up to 49152. */
+int psk_softmax_masked(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
+                       int64_t ldx, int64_t ldy, const uint8_t* mask, int64_t ldm, psk_order order,
+                       int32_t exp_mode, void* stream);
+
+/* The softmax region's backward (presk "The language", automatic
+ * differentiation: softmax's rule is y (ct - sum_axis(ct y))): per row
+ * s = sum_j RN(ct_j y_j) in the declared order, dx_j = RN(y_j RN(ct_j - s)),
+ * rounded to dxt.  y (the forward's output), ct (the cotangent) and dx are
+ * DEVICE rows with leading dimensions ldy, ldc, ldd >= cols; dx may be y or ct
+ * in place (same type and leading dimension), no other overlap; cols up to
+ * 49152. */
+int psk_softmax_backward(const void* y, int32_t yt, const void* ct, int32_t ct_t, void* dx, int32_t dxt,
+                         int64_t rows, int64_t cols, int64_t ldy, int64_t ldc, int64_t ldd, psk_order order,
+                         void* stream);
+
 /* ==================================================== psk_norm_region
  * The normalization regions over rows of `cols` elements, each a last-axis
  * reduction and its pointwise epilogue in one launch (poot "Fusion and

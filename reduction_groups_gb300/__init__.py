@@ -17,6 +17,8 @@ from .ops import (  # noqa: F401
     psk_group_prepare,
     psk_group_run,
     psk_norm_region,
+    psk_softmax_backward,
+    psk_softmax_masked,
     psk_softmax_region,
 )
 from ._native import PskError  # noqa: F401

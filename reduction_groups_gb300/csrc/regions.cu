@@ -25,8 +25,9 @@
 //                        CTA, warp 0 runs the chains;
 //   softmax_stream_kernel softmax rows longer than 4096, in chunks (exp
 //                        recomputed in the output pass, bit-identical);
-//   norm_row_kernel      other norm rows: one row at a time per CTA, held in
-//                        shared memory as f32.
+//   region_row_kernel    other norm rows, masked softmax rows and backward
+//                        rows: one row at a time per CTA, held in shared
+//                        memory as f32.
 
 #include "common.cuh"
 #include "crmath.cuh"
@@ -39,8 +40,8 @@ constexpr int SM_EPT = 16;                      // row elements per thread when 
 constexpr int SM_CAP = SM_THREADS * SM_EPT;     // 4096
 constexpr int SM_MAX_PARTIALS = 64;
 
-// Region kinds of the pipelined kernel.
-enum : int { REGION_SOFTMAX = 0, REGION_RMS = 1, REGION_LAYER = 2 };
+// Region kinds of the row kernels.
+enum : int { REGION_SOFTMAX = 0, REGION_RMS = 1, REGION_LAYER = 2, REGION_SOFTMAX_BWD = 3 };
 
 struct RegionParams {
   const void* x;
@@ -55,6 +56,13 @@ struct RegionParams {
   const void* beta;     // bias per column (LayerNorm), NULL if none
   int32_t param_dtype;  // storage type of gamma and beta
   float eps;            // RN_f32 of the eps argument
+  // masked softmax
+  const uint8_t* mask;  // 0 refuses, nonzero allows; NULL if none
+  int64_t ldm;          // mask row stride (0: one mask row for every row)
+  // softmax backward (x is y)
+  const void* ct;       // cotangent rows
+  int64_t ldc;
+  int32_t ct_dtype;
 };
 
 // NaN-propagating max (exact; the order of a max reduction changes no bit
@@ -641,18 +649,82 @@ __device__ __forceinline__ bool norm_epilogue(const RegionParams& P, const float
   return true;
 }
 
+// A backward row's epilogue for one team thread: y and ct (back from L2: the
+// producer read them moments ago) loaded before the wait for the row's sum
+// when they are bf16, chunk by chunk when f32; dx = RN(y RN(ct - s)).
+template <int XT, int YT>
+__device__ __forceinline__ bool bwd_epilogue(const RegionParams& P, char* yr, int64_t row, int tt, int cols,
+                                             uint64_t* ready, uint32_t parity, const float* s_slot) {
+  constexpr int NC = PIPE_EPT / 4;
+  const void* ybase = (const char*)P.x + row * P.ldx * (XT == PSK_F32 ? 4 : 2);
+  const void* cbase = (const char*)P.ct + row * P.ldc * (XT == PSK_F32 ? 4 : 2);
+  auto finish = [&](int j, const float* y4, const float* c4v, float s) {
+    float o4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o4[q] = __fmul_rn(y4[q], __fsub_rn(c4v[q], s));
+    if (YT == PSK_F32) {
+      __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o4[0], o4[1], o4[2], o4[3]));
+    } else {
+      uint2 q;
+      q.x = f32x2_to_bf16x2(o4[0], o4[1]);
+      q.y = f32x2_to_bf16x2(o4[2], o4[3]);
+      __stcs(reinterpret_cast<uint2*>(yr) + (j >> 2), q);
+    }
+  };
+  if constexpr (XT == PSK_BF16) {
+    Param4<PSK_BF16> yv[NC], cv[NC];
+#pragma unroll
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) { yv[c4].load(ybase, j); cv[c4].load(cbase, j); }
+    }
+    if (!mbar_wait(ready, parity)) return false;
+    const float s = *s_slot;
+#pragma unroll
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) {
+        float y4[4], c4v[4];
+        yv[c4].widen(y4);
+        cv[c4].widen(c4v);
+        finish(j, y4, c4v, s);
+      }
+    }
+  } else {
+    if (!mbar_wait(ready, parity)) return false;
+    const float s = *s_slot;
+#pragma unroll 2
+    for (int c4 = 0; c4 < NC; ++c4) {
+      const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+      if (j < cols) {
+        Param4<PSK_F32> yv, cv;
+        yv.load(ybase, j);
+        cv.load(cbase, j);
+        float y4[4], c4v[4];
+        yv.widen(y4);
+        cv.widen(c4v);
+        finish(j, y4, c4v, s);
+      }
+    }
+  }
+  return true;
+}
+
 template <int KIND, int XT, int YT, int EXPM>
 __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(128) unsigned char pipe_smem[];
   __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
   __shared__ float rowsum[PIPE_SE_MAX], rowrcp[PIPE_SE_MAX];   // softmax: s, RN(1/s); norms: d, mu
   __shared__ float red[PIPE_TEAMS][2][PIPE_TW];
+  __shared__ int red_any[PIPE_TEAMS][2][PIPE_TW];            // masked softmax: does the row allow a position
   __shared__ volatile int abort_flag;
 
   constexpr uint32_t XSZ = XT == PSK_F32 ? 4u : 2u;
+  constexpr bool BWD = KIND == REGION_SOFTMAX_BWD;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cols = (int)P.cols;
-  const uint32_t xbytes = (uint32_t)cols * XSZ;
+  const uint32_t rbytes = (uint32_t)cols * XSZ;               // one stored row
+  const uint32_t xbytes = BWD ? 2u * rbytes : rbytes;         // backward: the row of y, then the row of ct
   const uint32_t xslot = ((xbytes + 127u) / 128u) * 128u;     // ring slot stride in bytes
   const int SX = P.sx, SE = P.se, LAG = P.se / PIPE_TEAMS - 1;
   unsigned char* X = pipe_smem;
@@ -676,12 +748,18 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       int issued = 0;
       const unsigned char* src = (const unsigned char*)P.x + (int64_t)blockIdx.x * P.ldx * XSZ;
       const int64_t step = (int64_t)gridDim.x * P.ldx * XSZ;
+      const unsigned char* csrc = BWD ? (const unsigned char*)P.ct + (int64_t)blockIdx.x * P.ldc * XSZ : nullptr;
+      const int64_t cstep = (int64_t)gridDim.x * P.ldc * XSZ;
       for (int i = 0; i < n_local; ++i) {
         const int s = i % SX;
         if (i >= SX && !mbar_wait(&xempty[s], (uint32_t)((i / SX) - 1) & 1u)) { abort_flag = 1; break; }
         if (abort_flag) break;
         mbar_arrive_expect_tx(&xfull[s], xbytes);
-        bulk_copy_g2s(X + (size_t)s * xslot, src, xbytes, &xfull[s]);
+        bulk_copy_g2s(X + (size_t)s * xslot, src, rbytes, &xfull[s]);
+        if (BWD) {
+          bulk_copy_g2s(X + (size_t)s * xslot + rbytes, csrc, rbytes, &xfull[s]);
+          csrc += cstep;
+        }
         src += step;
         issued = i + 1;
       }
@@ -719,7 +797,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         }
         return sum;
       };
-      if (KIND == REGION_SOFTMAX) {
+      if (KIND == REGION_SOFTMAX || BWD) {
         const float sum = combine(act ? run_chain(Er, cols, p, parts) : 0.0f);
         if (act && p == 0) {
           rowsum[se] = sum;
@@ -761,15 +839,41 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
     dead = dead || abort_flag;
     if (i < n_local) {
       const int s = i % SX;
+      // masked softmax: the row's mask words, loaded before the wait for x
+      const bool masked = KIND == REGION_SOFTMAX && P.mask != nullptr;
+      uint32_t mk[PIPE_EPT / 4];
+      if (masked) {
+        const uint8_t* mrow = P.mask + ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * P.ldm;
+#pragma unroll
+        for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+          const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+          mk[c4] = j < cols ? __ldg(reinterpret_cast<const uint32_t*>(mrow + j)) : 0u;
+        }
+      }
       if (!dead && !mbar_wait(&xfull[s], (uint32_t)(i / SX) & 1u)) { abort_flag = 1; dead = true; }
       const unsigned char* xs = X + (size_t)s * xslot;
       float v[PIPE_EPT];
       float m = -INFINITY;
+      int any = 0;
 #pragma unroll
       for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
         if (j < cols && !dead) {
           load4<XT>(xs, j, &v[4 * c4]);
+          if (BWD) {                                           // p = RN(ct y)
+            float c[4];
+            load4<XT>(xs + rbytes, j, c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[4 * c4 + q] = __fmul_rn(c[q], v[4 * c4 + q]);
+          }
+          if (masked) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool allow = ((mk[c4] >> (8 * q)) & 0xFFu) != 0u;
+              any |= allow;
+              if (!allow) v[4 * c4 + q] = -INFINITY;
+            }
+          }
         } else {
           v[4 * c4 + 0] = v[4 * c4 + 1] = v[4 * c4 + 2] = v[4 * c4 + 3] = -INFINITY;
         }
@@ -782,12 +886,22 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (lane == 0) red[team][k & 1][tw] = m;
+        if (masked) {
+          any = __any_sync(0xffffffffu, any);
+          if (lane == 0) red_any[team][k & 1][tw] = any;
+        }
       }
       named_barrier(1 + team, PIPE_TT);                      // every team thread has read x
       if (KIND == REGION_SOFTMAX) {
         m = red[team][k & 1][0];
 #pragma unroll
         for (int q = 1; q < PIPE_TW; ++q) m = max_nan(m, red[team][k & 1][q]);
+        if (masked) {
+          int team_any = 0;
+#pragma unroll
+          for (int q = 0; q < PIPE_TW; ++q) team_any |= red_any[team][k & 1][q];
+          if (!team_any) m = 0.0f;                           // a row the mask empties: every exp is 0
+        }
       }
       if (tt == 0) mbar_arrive(&xempty[s]);
       const int se = i % SE;
@@ -819,6 +933,13 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       const uint32_t par = (uint32_t)(o / SE) & 1u;
       const float* Er = E + (size_t)se * estride;
       char* yr = (char*)P.y + ((int64_t)blockIdx.x + (int64_t)o * gridDim.x) * P.ldy * ysz;
+      if (BWD) {
+        if (!bwd_epilogue<XT, YT>(P, yr, blockIdx.x + (int64_t)o * gridDim.x, tt, cols, &sready[se], par, &rowsum[se])) {
+          abort_flag = 1;
+          dead = true;
+        }
+        continue;
+      }
       if (KIND != REGION_SOFTMAX) {
         const bool ok = P.param_dtype == PSK_BF16
                             ? norm_epilogue<KIND, YT, PSK_BF16>(P, Er, yr, tt, cols, &sready[se], par, &rowsum[se], &rowrcp[se])
@@ -835,7 +956,11 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         if (j < cols) {
           const float4 e = *reinterpret_cast<const float4*>(Er + j);
           float o4[4] = {e.x, e.y, e.z, e.w};
-          row_div_n<4>(o4, sm, rs, fast_ok);
+          if (sm == 0.0f) {                                  // a zero sum only in a row the mask empties
+            o4[0] = o4[1] = o4[2] = o4[3] = 0.0f;
+          } else {
+            row_div_n<4>(o4, sm, rs, fast_ok);
+          }
           if (YT == PSK_F32) {
             __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(o4[0], o4[1], o4[2], o4[3]));
           } else {
@@ -960,12 +1085,13 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const int pad = P.partials < 4 ? 4 : ((P.partials + 3) / 4) * 4;
   P.estride = (int)(((P.cols + 31) / 32) * 32 + pad);
   const size_t xsz = XT == PSK_F32 ? 4 : 2;
-  const size_t xrow = (size_t)((P.cols * xsz + 127) / 128) * 128;
+  const size_t xrow = (size_t)((P.cols * xsz * (KIND == REGION_SOFTMAX_BWD ? 2 : 1) + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
   const size_t budget = PIPE_SMEM_BUDGET;
   const int64_t chain = ((P.cols + P.partials - 1) / P.partials) * (KIND == REGION_LAYER ? 2 : 1);
   const bool long_chain = chain >= 1024;
   int sx = long_chain ? 4 : PIPE_SX_MAX;
+  if (sx * xrow + 2 * PIPE_TEAMS * erow > budget) sx = 4;   // wide x slots (backward: y and ct) leave room for 8 value rows
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
   // x slots stay a multiple of the team count, so that each slot serves one
@@ -1003,14 +1129,15 @@ static int dispatch_softmax(const RegionParams& P, int exp_mode, bool vec, cudaS
                                    : dispatch_exp<XT, YT, PSK_EXP_FAST>(P, vec, s);
 }
 
-// ------------------------------------------------ norm rows, any shape
-// One row at a time per CTA (grid-stride over rows): the row widened into
-// shared memory as f32, the chains run by warp 0 (lane l takes partials l and
-// l + 32, so up to 64), the partials combined left to right by lane 0, then
-// every thread divides (IEEE division) and applies the scale and bias.  For
-// rows the pipelined kernel does not take: unaligned, wider than 4096, more
-// than 32 partials.
-constexpr int NORM_MAX_COLS = 49152;                 // 192 KB of f32 row in shared memory
+// ------------------------------------------------ row regions, any shape
+// One row at a time per CTA (grid-stride over rows): the row's values in
+// shared memory as f32 -- softmax: the (masked) scores, then e = exp(x - m);
+// backward: RN(ct y); norms: x -- the chains run by warp 0 (lane l takes
+// partials l and l + 32, so up to 64), the partials combined left to right by
+// lane 0, then every thread writes its outputs (IEEE division).  For rows the
+// pipelined kernel does not take: unaligned, f32 masked scores, wider than
+// 4096 (up to 49152), more than 32 partials.
+constexpr int ROW_MAX_COLS = 49152;                  // 192 KB of f32 row in shared memory
 
 template <int T>
 __device__ __forceinline__ float load1(const void* base, int64_t off) {
@@ -1018,18 +1145,51 @@ __device__ __forceinline__ float load1(const void* base, int64_t off) {
   return bf16_bits_to_f32(__ldg((const uint16_t*)base + off));
 }
 
-template <int KIND, int XT, int YT>
-__global__ void __launch_bounds__(SM_THREADS) norm_row_kernel(const __grid_constant__ RegionParams P) {
+__device__ __forceinline__ float load1_rt(const void* base, int dtype, int64_t off) {
+  return dtype == PSK_F32 ? __ldg((const float*)base + off) : bf16_bits_to_f32(__ldg((const uint16_t*)base + off));
+}
+
+template <int KIND, int XT, int YT, int EXPM>
+__global__ void __launch_bounds__(SM_THREADS) region_row_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(16) float row[];
   __shared__ float part[SM_MAX_PARTIALS];
-  __shared__ float stat[2];                          // mu, d
-  const int t = threadIdx.x, lane = t & 31;
+  __shared__ float red[SM_THREADS / 32];
+  __shared__ float stat[2];                          // norms: mu, d; softmax: s; backward: s
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   const int cols = (int)P.cols;
   const int parts = P.partials < cols ? P.partials : cols;
   const float n_f = (float)cols;                     // exact: cols <= 49152
   for (int64_t r = blockIdx.x; r < P.rows; r += gridDim.x) {
     const int64_t xo = r * P.ldx;
-    for (int j = t; j < cols; j += SM_THREADS) row[j] = load1<XT>(P.x, xo + j);
+    if (KIND == REGION_SOFTMAX) {
+      // masked scores and their maximum; a row the mask empties gets m = 0
+      const uint8_t* mrow = P.mask ? P.mask + r * P.ldm : nullptr;
+      float m = -INFINITY;
+      int any = 0;
+      for (int j = t; j < cols; j += SM_THREADS) {
+        float v = load1<XT>(P.x, xo + j);
+        if (mrow) {
+          const bool allow = mrow[j] != 0;
+          any |= allow;
+          if (!allow) v = -INFINITY;
+        }
+        row[j] = v;
+        m = max_nan(m, v);
+      }
+      for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) red[wid] = m;
+      any = __syncthreads_or(any);
+      m = red[0];
+      for (int q = 1; q < SM_THREADS / 32; ++q) m = max_nan(m, red[q]);
+      if (mrow && !any) m = 0.0f;
+      for (int j = t; j < cols; j += SM_THREADS) row[j] = region_exp<EXPM>(__fsub_rn(row[j], m));
+    } else if (KIND == REGION_SOFTMAX_BWD) {
+      const int64_t co = r * P.ldc;
+      for (int j = t; j < cols; j += SM_THREADS)
+        row[j] = __fmul_rn(load1_rt(P.ct, P.ct_dtype, co + j), load1<XT>(P.x, xo + j));
+    } else {
+      for (int j = t; j < cols; j += SM_THREADS) row[j] = load1<XT>(P.x, xo + j);
+    }
     __syncthreads();
     if (t < 32) {
       float mu = 0.0f;
@@ -1045,15 +1205,17 @@ __global__ void __launch_bounds__(SM_THREADS) norm_row_kernel(const __grid_const
         mu = stat[0];
         for (int pp = lane; pp < parts; pp += 32)
           part[pp] = run_chain(row, cols, pp, parts, ChainCenteredSquare{mu});
-      } else {
+      } else if (KIND == REGION_RMS) {
         for (int pp = lane; pp < parts; pp += 32) part[pp] = run_chain(row, cols, pp, parts, ChainSquare());
+      } else {
+        for (int pp = lane; pp < parts; pp += 32) part[pp] = run_chain(row, cols, pp, parts);
       }
       __syncwarp();
       if (lane == 0) {
         float ss = part[0];
         for (int q = 1; q < parts; ++q) ss = __fadd_rn(ss, part[q]);
         stat[0] = mu;
-        stat[1] = __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n_f), P.eps));
+        stat[1] = (KIND == REGION_RMS || KIND == REGION_LAYER) ? __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n_f), P.eps)) : ss;
       }
     }
     __syncthreads();
@@ -1061,37 +1223,41 @@ __global__ void __launch_bounds__(SM_THREADS) norm_row_kernel(const __grid_const
     const int64_t yo = r * P.ldy;
     for (int j = t; j < cols; j += SM_THREADS) {
       float v = row[j];
-      if (KIND == REGION_LAYER) v = __fsub_rn(v, mu);
-      v = __fdiv_rn(v, d);
-      if (P.gamma) v = __fmul_rn(v, P.param_dtype == PSK_F32 ? __ldg((const float*)P.gamma + j)
-                                                              : bf16_bits_to_f32(__ldg((const uint16_t*)P.gamma + j)));
-      if (KIND == REGION_LAYER && P.beta)
-        v = __fadd_rn(v, P.param_dtype == PSK_F32 ? __ldg((const float*)P.beta + j)
-                                                  : bf16_bits_to_f32(__ldg((const uint16_t*)P.beta + j)));
+      if (KIND == REGION_SOFTMAX) {
+        v = d == 0.0f ? 0.0f : __fdiv_rn(v, d);       // a zero sum only in a row the mask empties
+      } else if (KIND == REGION_SOFTMAX_BWD) {
+        const float y = load1<XT>(P.x, xo + j), c = load1_rt(P.ct, P.ct_dtype, r * P.ldc + j);
+        v = __fmul_rn(y, __fsub_rn(c, d));
+      } else {
+        if (KIND == REGION_LAYER) v = __fsub_rn(v, mu);
+        v = __fdiv_rn(v, d);
+        if (P.gamma) v = __fmul_rn(v, load1_rt(P.gamma, P.param_dtype, j));
+        if (KIND == REGION_LAYER && P.beta) v = __fadd_rn(v, load1_rt(P.beta, P.param_dtype, j));
+      }
       store_y1<YT>(P.y, yo + j, v);
     }
     __syncthreads();
   }
 }
 
-template <int KIND, int XT, int YT>
-static int launch_norm_rows(const RegionParams& P, cudaStream_t stream) {
+template <int KIND, int XT, int YT, int EXPM>
+static int launch_region_rows(const RegionParams& P, cudaStream_t stream) {
   const size_t smem = (size_t)P.cols * sizeof(float);
   static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)norm_row_kernel<KIND, XT, YT>, (int)(NORM_MAX_COLS * sizeof(float)), attr);
+  smem_limit_once((const void*)region_row_kernel<KIND, XT, YT, EXPM>, (int)(ROW_MAX_COLS * sizeof(float)), attr);
   int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_row_kernel<KIND, XT, YT>, SM_THREADS, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, region_row_kernel<KIND, XT, YT, EXPM>, SM_THREADS, smem);
   if (per_sm < 1) per_sm = 1;
   const int64_t cap = (int64_t)device_sm_count() * per_sm;
   const unsigned grid = (unsigned)(P.rows < cap ? P.rows : cap);
-  norm_row_kernel<KIND, XT, YT><<<grid, SM_THREADS, smem, stream>>>(P);
-  return check_launch("norm region kernel (row at a time)");
+  region_row_kernel<KIND, XT, YT, EXPM><<<grid, SM_THREADS, smem, stream>>>(P);
+  return check_launch("row region kernel (row at a time)");
 }
 
 template <int KIND, int XT, int YT>
 static int dispatch_norm(const RegionParams& P, bool pipe, cudaStream_t s) {
   if (pipe) return launch_pipe<KIND, XT, YT, PSK_EXP_EXACT>(P, s);
-  return launch_norm_rows<KIND, XT, YT>(P, s);
+  return launch_region_rows<KIND, XT, YT, PSK_EXP_EXACT>(P, s);
 }
 
 template <int KIND>
@@ -1100,6 +1266,26 @@ static int dispatch_norm_types(const RegionParams& P, int xt, int yt, bool pipe,
   if (xt == PSK_BF16 && yt == PSK_F32) return dispatch_norm<KIND, PSK_BF16, PSK_F32>(P, pipe, s);
   if (xt == PSK_F32 && yt == PSK_BF16) return dispatch_norm<KIND, PSK_F32, PSK_BF16>(P, pipe, s);
   return dispatch_norm<KIND, PSK_F32, PSK_F32>(P, pipe, s);
+}
+
+// masked softmax: the pipelined kernel for bf16 scores with 4-byte aligned
+// mask rows, the row kernel otherwise
+template <int XT, int YT, int EXPM>
+static int dispatch_masked_exp(const RegionParams& P, bool pipe, cudaStream_t s) {
+  if (XT == PSK_BF16 && pipe) return launch_pipe<REGION_SOFTMAX, PSK_BF16, YT, EXPM>(P, s);
+  return launch_region_rows<REGION_SOFTMAX, XT, YT, EXPM>(P, s);
+}
+
+template <int XT, int YT>
+static int dispatch_masked(const RegionParams& P, int exp_mode, bool pipe, cudaStream_t s) {
+  return exp_mode == PSK_EXP_EXACT ? dispatch_masked_exp<XT, YT, PSK_EXP_EXACT>(P, pipe, s)
+                                   : dispatch_masked_exp<XT, YT, PSK_EXP_FAST>(P, pipe, s);
+}
+
+template <int XT, int YT>
+static int dispatch_bwd(const RegionParams& P, bool pipe, cudaStream_t s) {
+  if (pipe) return launch_pipe<REGION_SOFTMAX_BWD, XT, YT, PSK_EXP_EXACT>(P, s);
+  return launch_region_rows<REGION_SOFTMAX_BWD, XT, YT, PSK_EXP_EXACT>(P, s);
 }
 
 }  // namespace psk
@@ -1146,7 +1332,7 @@ extern "C" int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, i
   int rc = order_partials(order, &partials);
   if (rc) return rc;
   if (rows == 0 || cols == 0) return PSK_OK;
-  if (cols > NORM_MAX_COLS) return fail(PSK_E_SHAPE, "cols %lld above %d", (long long)cols, NORM_MAX_COLS);
+  if (cols > ROW_MAX_COLS) return fail(PSK_E_SHAPE, "cols %lld above %d", (long long)cols, ROW_MAX_COLS);
   if (!x || !y) return fail(PSK_E_NULL, "x or y is NULL");
   if (ldx < cols || ldy < cols) return fail(PSK_E_SHAPE, "leading dimension below cols");
   const size_t xbytes = (size_t)((rows - 1) * ldx + cols) * dtype_size(xt);
@@ -1207,4 +1393,73 @@ extern "C" int psk_softmax_region(const void* x, int32_t xt, void* y, int32_t yt
   if (xt == PSK_BF16 && yt == PSK_F32) return dispatch_softmax<PSK_BF16, PSK_F32>(P, exp_mode, vec, s);
   if (xt == PSK_F32 && yt == PSK_BF16) return dispatch_softmax<PSK_F32, PSK_BF16>(P, exp_mode, vec, s);
   return dispatch_softmax<PSK_F32, PSK_F32>(P, exp_mode, vec, s);
+}
+
+extern "C" int psk_softmax_masked(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows, int64_t cols,
+                                  int64_t ldx, int64_t ldy, const uint8_t* mask, int64_t ldm, psk_order order,
+                                  int32_t exp_mode, void* stream) {
+  clear_error();
+  if (!dtype_ok(xt)) return fail(PSK_E_DTYPE, "x dtype %d", xt);
+  if (!dtype_ok(yt)) return fail(PSK_E_DTYPE, "y dtype %d", yt);
+  if (rows < 0 || cols < 0) return fail(PSK_E_SHAPE, "rows %lld, cols %lld", (long long)rows, (long long)cols);
+  if (exp_mode != PSK_EXP_EXACT && exp_mode != PSK_EXP_FAST) return fail(PSK_E_ARG, "exp_mode %d", exp_mode);
+  int partials = 1;
+  const int orc = order_partials(order, &partials);
+  if (orc) return orc;
+  if (rows == 0 || cols == 0) return PSK_OK;
+  if (cols > ROW_MAX_COLS) return fail(PSK_E_SHAPE, "masked rows of %lld columns (max %d)", (long long)cols, ROW_MAX_COLS);
+  if (!x || !y || !mask) return fail(PSK_E_NULL, "x, y or mask is NULL");
+  if (ldx < cols || ldy < cols) return fail(PSK_E_SHAPE, "leading dimension below cols");
+  if (ldm != 0 && ldm < cols) return fail(PSK_E_SHAPE, "mask leading dimension %lld (0 or >= cols)", (long long)ldm);
+  const size_t xbytes = (size_t)((rows - 1) * ldx + cols) * dtype_size(xt);
+  const size_t ybytes = (size_t)((rows - 1) * ldy + cols) * dtype_size(yt);
+  const size_t mbytes = (size_t)(ldm == 0 ? cols : (rows - 1) * ldm + cols);
+  if (overlaps(x, xbytes, y, ybytes) && !(x == y && xt == yt && ldx == ldy))
+    return fail(PSK_E_ALIAS, "y overlaps x and is not the same buffer");
+  if (overlaps(mask, mbytes, y, ybytes)) return fail(PSK_E_ALIAS, "y overlaps the mask");
+  RegionParams P{x, y, rows, cols, ldx, ldy, partials, 1, 0, 0, 0};
+  P.mask = mask;
+  P.ldm = ldm;
+  const bool pipe = cols <= SM_CAP && cols >= 8 && cols % 8 == 0 && ldx % 8 == 0 && ldy % 8 == 0 &&
+                    partials <= 32 && (uintptr_t)x % 16 == 0 && (uintptr_t)y % 16 == 0 &&
+                    (uintptr_t)mask % 4 == 0 && ldm % 4 == 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (xt == PSK_BF16 && yt == PSK_BF16) return dispatch_masked<PSK_BF16, PSK_BF16>(P, exp_mode, pipe, s);
+  if (xt == PSK_BF16 && yt == PSK_F32) return dispatch_masked<PSK_BF16, PSK_F32>(P, exp_mode, pipe, s);
+  if (xt == PSK_F32 && yt == PSK_BF16) return dispatch_masked<PSK_F32, PSK_BF16>(P, exp_mode, pipe, s);
+  return dispatch_masked<PSK_F32, PSK_F32>(P, exp_mode, pipe, s);
+}
+
+extern "C" int psk_softmax_backward(const void* y, int32_t yt, const void* ct, int32_t ct_t, void* dx, int32_t dxt,
+                                    int64_t rows, int64_t cols, int64_t ldy, int64_t ldc, int64_t ldd,
+                                    psk_order order, void* stream) {
+  clear_error();
+  if (!dtype_ok(yt) || !dtype_ok(ct_t) || !dtype_ok(dxt)) return fail(PSK_E_DTYPE, "storage type of y, ct or dx");
+  if (rows < 0 || cols < 0) return fail(PSK_E_SHAPE, "rows %lld, cols %lld", (long long)rows, (long long)cols);
+  int partials = 1;
+  const int orc = order_partials(order, &partials);
+  if (orc) return orc;
+  if (rows == 0 || cols == 0) return PSK_OK;
+  if (cols > ROW_MAX_COLS) return fail(PSK_E_SHAPE, "rows of %lld columns (max %d)", (long long)cols, ROW_MAX_COLS);
+  if (!y || !ct || !dx) return fail(PSK_E_NULL, "y, ct or dx is NULL");
+  if (ldy < cols || ldc < cols || ldd < cols) return fail(PSK_E_SHAPE, "leading dimension below cols");
+  const size_t ybytes = (size_t)((rows - 1) * ldy + cols) * dtype_size(yt);
+  const size_t cbytes = (size_t)((rows - 1) * ldc + cols) * dtype_size(ct_t);
+  const size_t dbytes = (size_t)((rows - 1) * ldd + cols) * dtype_size(dxt);
+  if (overlaps(dx, dbytes, y, ybytes) && !(dx == y && dxt == yt && ldd == ldy))
+    return fail(PSK_E_ALIAS, "dx overlaps y and is not the same buffer");
+  if (overlaps(dx, dbytes, ct, cbytes) && !(dx == ct && dxt == ct_t && ldd == ldc))
+    return fail(PSK_E_ALIAS, "dx overlaps ct and is not the same buffer");
+  RegionParams P{y, dx, rows, cols, ldy, ldd, partials, 1, 0, 0, 0};
+  P.ct = ct;
+  P.ldc = ldc;
+  P.ct_dtype = ct_t;
+  const bool pipe = ct_t == yt && cols <= SM_CAP && cols >= 8 && cols % 8 == 0 && ldy % 8 == 0 && ldc % 8 == 0 &&
+                    ldd % 8 == 0 && partials <= 32 && (uintptr_t)y % 16 == 0 && (uintptr_t)ct % 16 == 0 &&
+                    (uintptr_t)dx % 16 == 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (yt == PSK_BF16 && dxt == PSK_BF16) return dispatch_bwd<PSK_BF16, PSK_BF16>(P, pipe, s);
+  if (yt == PSK_BF16 && dxt == PSK_F32) return dispatch_bwd<PSK_BF16, PSK_F32>(P, pipe, s);
+  if (yt == PSK_F32 && dxt == PSK_BF16) return dispatch_bwd<PSK_F32, PSK_BF16>(P, pipe, s);
+  return dispatch_bwd<PSK_F32, PSK_F32>(P, pipe, s);
 }

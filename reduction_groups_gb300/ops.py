@@ -106,6 +106,50 @@ def psk_softmax_region(x, y, order=("sequential",), exp_mode: str = "exact", str
                                        max(x.stride(0), cols), max(y.stride(0), cols), o, em, _stream_handle(stream)))
 
 
+def _rows2d(*ts):
+    for t in ts:
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("row regions take 2-D tensors with contiguous rows")
+    if len({tuple(t.shape) for t in ts}) != 1:
+        raise ValueError("the row tensors must share one shape")
+
+
+def psk_softmax_masked(x, y, mask, order=("sequential",), exp_mode: str = "exact", stream=None) -> None:
+    """Masked softmax of the rows of x into y; mask: a uint8/bool device tensor
+    of shape [cols] (every row) or [rows, cols] (contiguous rows), nonzero
+    allows."""
+    import torch
+
+    _rows2d(x, y)
+    rows, cols = x.shape
+    if mask.dtype not in (torch.uint8, torch.bool):
+        raise TypeError("the mask must be uint8 or bool")
+    if mask.dim() == 1:
+        if mask.numel() != cols or (cols > 1 and mask.stride(0) != 1):
+            raise ValueError("a mask row must hold cols contiguous values")
+        ldm = 0
+    else:
+        if tuple(mask.shape) != (rows, cols) or mask.stride(1) != 1:
+            raise ValueError("a full mask must be [rows, cols] with contiguous rows")
+        ldm = max(mask.stride(0), cols)
+    o = N.psk_order(_ORDER[order[0]], int(order[1]) if len(order) > 1 else 0)
+    em = {"exact": N.PSK_EXP_EXACT, "fast": N.PSK_EXP_FAST}[exp_mode]
+    N.check(N.lib().psk_softmax_masked(x.data_ptr(), _dtype_code(x), y.data_ptr(), _dtype_code(y), rows, cols,
+                                       max(x.stride(0), cols), max(y.stride(0), cols), mask.data_ptr(), ldm, o, em,
+                                       _stream_handle(stream)))
+
+
+def psk_softmax_backward(y, ct, dx, order=("sequential",), stream=None) -> None:
+    """dx = y (ct - sum(ct y)) per row (the softmax region's backward)."""
+    _rows2d(y, ct, dx)
+    rows, cols = y.shape
+    o = N.psk_order(_ORDER[order[0]], int(order[1]) if len(order) > 1 else 0)
+    N.check(N.lib().psk_softmax_backward(y.data_ptr(), _dtype_code(y), ct.data_ptr(), _dtype_code(ct),
+                                         dx.data_ptr(), _dtype_code(dx), rows, cols, max(y.stride(0), cols),
+                                         max(ct.stride(0), cols), max(dx.stride(0), cols), o,
+                                         _stream_handle(stream)))
+
+
 def psk_norm_region(x, y, kind: str, eps: float, gamma=None, beta=None, order=("sequential",),
                     stream=None) -> None:
     """RMSNorm (kind "rms") or LayerNorm ("layer") of the rows of the 2-D

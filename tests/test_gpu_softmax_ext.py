@@ -1,0 +1,133 @@
+"""Parity of the masked softmax region and the softmax backward (through the
+C ABI) with the CPU oracle, bit for bit (exact exp; the fast exp within the
+region's stated tolerance)."""
+
+import numpy as np
+import pytest
+
+import oracle.softmax as OS
+from oracle.f32 import bf16_to_f32, f32_to_bf16
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import reduction_groups_gb300 as R
+
+    return R
+
+
+def _to_dev(a, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _to_host(t):
+    if t.dtype == torch.bfloat16:
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _same(a, b, dtype):
+    if dtype == "bf16":
+        a = bf16_to_f32(a)
+        b = bf16_to_f32(b)
+    return (a.view(np.uint32) == b.view(np.uint32)) | (np.isnan(a) & np.isnan(b))
+
+
+def _empty(shape, dtype):
+    return torch.full(shape, float("nan"), dtype=torch.bfloat16 if dtype == "bf16" else torch.float32, device="cuda")
+
+
+ORDERS = [("sequential",), ("interleaved", 8), ("interleaved", 3), ("interleaved", 40)]
+
+
+@pytest.mark.parametrize("order", ORDERS, ids=lambda o: "-".join(map(str, o)))
+@pytest.mark.parametrize("shape,xt,full", [((300, 512), "bf16", True), ((300, 512), "bf16", False),
+                                           ((2000, 4096), "bf16", True), ((37, 999), "bf16", True),
+                                           ((64, 640), "f32", False), ((5, 10000), "bf16", True)])
+def test_masked_softmax_bitwise(dev, order, shape, xt, full):
+    rows, cols = shape
+    wl = W.softmax_rows(rows, cols)
+    x = wl.host_x() if xt == "bf16" else bf16_to_f32(wl.host_x())
+    rng = np.random.default_rng(rows + cols)
+    mask = (rng.random((rows, cols) if full else (cols,)) < 0.7).astype(np.uint8)
+    if full:
+        mask[1] = 0                                    # a row the mask empties
+        mask[2] = 0
+        mask[2, cols - 1] = 1                          # one allowed position, the last
+        ii = np.arange(min(rows, cols))
+        mask[ii[3:], :] = (np.arange(cols)[None, :] <= ii[3:, None]).astype(np.uint8)   # causal rows
+    want = OS.softmax_region(x, xt, "bf16", order, mask=mask)
+    y = _empty((rows, cols), "bf16")
+    dev.psk_softmax_masked(_to_dev(x, xt), y, torch.from_numpy(mask).cuda(), order, "exact")
+    torch.cuda.synchronize()
+    ok = _same(_to_host(y), want, "bf16")
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} differ"
+    assert dev.psk_device_status() == 0
+
+
+def test_masked_softmax_fast_exp_and_bool_mask(dev):
+    wl = W.softmax_rows(256, 4096)
+    x = wl.host_x()
+    rng = np.random.default_rng(6)
+    mask = rng.random((256, 4096)) < 0.5
+    mask[7] = False
+    for order in (("sequential",), ("interleaved", 8)):
+        want = OS.softmax_region(x, "bf16", "f32", order, mask=mask)
+        y = _empty((256, 4096), "f32")
+        dev.psk_softmax_masked(_to_dev(x, "bf16"), y, torch.from_numpy(mask).cuda(), order, "fast")
+        torch.cuda.synchronize()
+        got = _to_host(y)
+        assert np.all(got[~mask] == 0) and np.all(got[7] == 0)
+        rel = np.abs(got.astype(np.float64) - want) / np.maximum(np.abs(want), 1e-38)
+        assert rel.max() <= 1e-6
+
+
+@pytest.mark.parametrize("order", ORDERS, ids=lambda o: "-".join(map(str, o)))
+@pytest.mark.parametrize("shape,yt,ct_t,dxt", [((300, 512), "bf16", "bf16", "bf16"), ((2000, 4096), "bf16", "bf16", "f32"),
+                                               ((64, 640), "f32", "f32", "f32"), ((37, 999), "bf16", "f32", "bf16"),
+                                               ((5, 10000), "f32", "bf16", "f32"), ((600, 16), "bf16", "bf16", "bf16")])
+def test_softmax_backward_bitwise(dev, order, shape, yt, ct_t, dxt):
+    rows, cols = shape
+    rng = np.random.default_rng(cols)
+    y32 = OS.softmax_region((rng.standard_normal((rows, cols)) * 2).astype(np.float32), "f32", "f32")
+    ct32 = rng.standard_normal((rows, cols)).astype(np.float32)
+    y = f32_to_bf16(y32) if yt == "bf16" else y32
+    ct = f32_to_bf16(ct32) if ct_t == "bf16" else ct32
+    want = OS.softmax_backward(y, ct, yt, ct_t, dxt, order)
+    dx = _empty((rows, cols), dxt)
+    dev.psk_softmax_backward(_to_dev(y, yt), _to_dev(ct, ct_t), dx, order)
+    torch.cuda.synchronize()
+    ok = _same(_to_host(dx), want, dxt)
+    assert ok.all(), f"{(~ok).sum()} of {ok.size} differ"
+    assert dev.psk_device_status() == 0
+
+
+def test_softmax_backward_in_place_and_refusals(dev):
+    rng = np.random.default_rng(3)
+    y = OS.softmax_region((rng.standard_normal((40, 256)) * 2).astype(np.float32), "f32", "f32")
+    ct = rng.standard_normal((40, 256)).astype(np.float32)
+    want = OS.softmax_backward(y, ct, "f32", "f32", "f32", ("interleaved", 8))
+    ctd = _to_dev(ct, "f32")
+    dev.psk_softmax_backward(_to_dev(y, "f32"), ctd, ctd, ("interleaved", 8))   # dx written over ct
+    torch.cuda.synchronize()
+    assert _same(_to_host(ctd), want, "f32").all()
+    buf = torch.zeros(40 * 256 + 8, dtype=torch.float32, device="cuda")
+    yd = buf[:40 * 256].view(40, 256)
+    shifted = buf[8:].view(40, 256)                 # overlaps y, not in place: refused before any launch
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_softmax_backward(yd, ctd, shifted, ("sequential",))
+    assert e.value.name == "PSK_E_ALIAS"
+    x = _to_dev(f32_to_bf16(y), "bf16")
+    m = torch.ones(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(dev.PskError) as e:
+        dev.psk_softmax_masked(x, x.clone(), m, ("interleaved", 65))
+    assert e.value.name == "PSK_E_ORDER"
