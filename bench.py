@@ -288,6 +288,20 @@ def run_ours(a, ws, rank, local):
                 b_all[f"{label}_{oname}"] = nw.algorithmic_bytes()
             norm_rows = nw.rows
         torch.cuda.synchronize()
+    if a.only in ("all", "softmax"):
+        # the masked softmax (one mask row for every row, 70 % allowed) and the
+        # softmax backward on the softmax region's shape
+        mrow = (torch.rand(sw.cols, device="cuda", generator=torch.Generator(device="cuda").manual_seed(7))
+                < 0.7).to(torch.uint8)
+        extra_launches["softmax_masked_interleaved8"] = lambda: R.psk_softmax_masked(sx, sy, mrow, ("interleaved", 8),
+                                                                                     em)
+        b_all["softmax_masked_interleaved8"] = b_soft
+        bct = torch.empty_like(sx).normal_(generator=torch.Generator(device="cuda").manual_seed(8))
+        bdx = torch.empty_like(sx)
+        for oname, order in (("sequential", ("sequential",)), ("interleaved8", ("interleaved", 8))):
+            extra_launches[f"softmax_backward_{oname}"] = (lambda order=order: R.psk_softmax_backward(sy, bct, bdx,
+                                                                                                     order))
+            b_all[f"softmax_backward_{oname}"] = 3 * sw.rows * sw.cols * 2
     if a.only == "norm":
         launches = dict(extra_launches)
     kernels = [k for k in launches if a.only in ("all", "norm") or k.startswith(a.only)]
@@ -354,7 +368,7 @@ def run_ours(a, ws, rank, local):
         extra_launches["adamw_clip_cosine"] = lambda: R.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000, 1.0,
                                                                          clip_ws)
         b_all["adamw_clip_cosine"] = b_adam + tree.n_params * (2 if tree.grad_dtype == "bf16" else 4)
-    if a.only in ("all", "adamw"):
+    if a.only in ("all", "adamw", "softmax"):
         for name, fn in extra_launches.items():
             for _ in range(2):
                 fn()
@@ -430,7 +444,7 @@ def run_ours(a, ws, rank, local):
         gbs = kbytes / (ms / 1e3) / 1e9
         kinfo[k] = {"ms": round(ms, 4), "algorithmic_bytes": int(kbytes), "gbs": round(gbs, 1),
                     "frac_of_hbm_peak": round(gbs / peak, 4), "in_value": False,
-                    "rows_per_s": round((norm_rows if k in extra_launches else sw.rows) / (ms / 1e3), 1)}
+                    "rows_per_s": round((norm_rows if k.startswith(("rms", "layer")) else sw.rows) / (ms / 1e3), 1)}
         if k == "adamw_clip_cosine":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["params_per_s"] = round(tree.n_params / (ms / 1e3), 1)

@@ -180,7 +180,9 @@ __device__ __forceinline__ float row_div(float e, float s, float rs, bool fast_o
 
 // N quotients e_q / s at once: Markstein's correction for all, one test for
 // the whole group, and the per-element path (IEEE division where the
-// correction's operand range is left) only for a group that needs it.
+// correction's operand range is left) only for a group that needs it.  The
+// dividends are exp values (>= +0): +0, a masked position's, gives +0 through
+// the correction as well.
 template <int N>
 __device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast_ok) {
   float y[N];
@@ -191,7 +193,7 @@ __device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast
     const float qq = e * rs;
     const float r = fmaf(-qq, s, e);
     y[q] = fmaf(r, rs, qq);
-    bad = bad || !(e >= 0x1p-100f);
+    bad = bad || !(e >= 0x1p-100f || e == 0.0f);
   }
   if (bad) {
 #pragma unroll
@@ -710,7 +712,7 @@ __device__ __forceinline__ bool bwd_epilogue(const RegionParams& P, char* yr, in
   return true;
 }
 
-template <int KIND, int XT, int YT, int EXPM>
+template <int KIND, int XT, int YT, int EXPM, bool MASK>
 __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(128) unsigned char pipe_smem[];
   __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
@@ -840,7 +842,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
     if (i < n_local) {
       const int s = i % SX;
       // masked softmax: the row's mask words, loaded before the wait for x
-      const bool masked = KIND == REGION_SOFTMAX && P.mask != nullptr;
+      constexpr bool masked = KIND == REGION_SOFTMAX && MASK;
       uint32_t mk[PIPE_EPT / 4];
       if (masked) {
         const uint8_t* mrow = P.mask + ((int64_t)blockIdx.x + (int64_t)i * gridDim.x) * P.ldm;
@@ -956,7 +958,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         if (j < cols) {
           const float4 e = *reinterpret_cast<const float4*>(Er + j);
           float o4[4] = {e.x, e.y, e.z, e.w};
-          if (sm == 0.0f) {                                  // a zero sum only in a row the mask empties
+          if (MASK && sm == 0.0f) {                          // a zero sum only in a row the mask empties
             o4[0] = o4[1] = o4[2] = o4[3] = 0.0f;
           } else {
             row_div_n<4>(o4, sm, rs, fast_ok);
@@ -1080,7 +1082,7 @@ static int launch_stream(const RegionParams& P, cudaStream_t stream) {
 // order over 4096 columns) is the bottleneck, so it gets the value ring first
 // (x ring down to 4 slots); otherwise the x ring comes first.  Chain groups
 // take G <= 4 consecutive rows (one per team).
-template <int KIND, int XT, int YT, int EXPM>
+template <int KIND, int XT, int YT, int EXPM, bool MASK = false>
 static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const int pad = P.partials < 4 ? 4 : ((P.partials + 3) / 4) * 4;
   P.estride = (int)(((P.cols + 31) / 32) * 32 + pad);
@@ -1108,10 +1110,10 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
   const size_t smem = sx * xrow + se * erow;
   static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM>, (int)budget, attr);
+  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK>, (int)budget, attr);
   const int64_t sms = device_sm_count();
   const unsigned grid = (unsigned)(P.rows < sms ? P.rows : sms);
-  region_pipe_kernel<KIND, XT, YT, EXPM><<<grid, PIPE_THREADS, smem, stream>>>(P);
+  region_pipe_kernel<KIND, XT, YT, EXPM, MASK><<<grid, PIPE_THREADS, smem, stream>>>(P);
   return check_launch("row region kernel (pipelined)");
 }
 
@@ -1272,7 +1274,7 @@ static int dispatch_norm_types(const RegionParams& P, int xt, int yt, bool pipe,
 // mask rows, the row kernel otherwise
 template <int XT, int YT, int EXPM>
 static int dispatch_masked_exp(const RegionParams& P, bool pipe, cudaStream_t s) {
-  if (XT == PSK_BF16 && pipe) return launch_pipe<REGION_SOFTMAX, PSK_BF16, YT, EXPM>(P, s);
+  if (XT == PSK_BF16 && pipe) return launch_pipe<REGION_SOFTMAX, PSK_BF16, YT, EXPM, true>(P, s);
   return launch_region_rows<REGION_SOFTMAX, XT, YT, EXPM>(P, s);
 }
 
