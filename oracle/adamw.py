@@ -19,7 +19,9 @@ Readings taken here:
     q  = mh / (sqrt(vh) + eps)
     u  = q + (wd*theta)
     theta1 = theta - (lr*u)
-* bf16 gradients widen exactly.
+* bf16 gradients widen exactly; a leaf stored in bf16 at rest (theta, m and v
+  in bf16) widens exactly, runs the same f32 chain and rounds each of
+  theta', m', v' once to bf16 (round to nearest even).
 
 Schedules and clipping (the same passage: grad_clip = c scales the gradient
 by min(1, c / (||g||_2 + 1e-6)), the global norm over the tree, as
@@ -48,7 +50,7 @@ from fractions import Fraction
 
 import numpy as np
 
-from .f32 import rn_f32, widen
+from .f32 import f32_to_bf16, rn_f32, widen
 
 
 def _rn_decided(q: Fraction, rel_err: Fraction) -> np.float32:
@@ -81,8 +83,15 @@ def hyper_f32(lr: float, beta1: float, beta2: float, eps: float, weight_decay: f
     }
 
 
-def step_leaf(theta: np.ndarray, m: np.ndarray, v: np.ndarray, grad: np.ndarray, grad_dtype: str, h: dict):
-    """One AdamW step over one leaf; returns (theta', m', v') as new f32 arrays."""
+def step_leaf(theta: np.ndarray, m: np.ndarray, v: np.ndarray, grad: np.ndarray, grad_dtype: str, h: dict,
+              param_dtype: str = "f32"):
+    """One AdamW step over one leaf; returns (theta', m', v') as new arrays in
+    the leaf's storage type (f32 values, or bf16 bits rounded once from the
+    f32 results: a parameter at rest in bf16, presk "Native execution",
+    params, keeps its moments in the same type, the tree type of adamw.init)."""
+    if param_dtype == "bf16":
+        t1, m1, v1 = step_leaf(widen(theta, "bf16"), widen(m, "bf16"), widen(v, "bf16"), grad, grad_dtype, h)
+        return f32_to_bf16(t1), f32_to_bf16(m1), f32_to_bf16(v1)
     th = np.asarray(theta, dtype=np.float32)
     m = np.asarray(m, dtype=np.float32)
     v = np.asarray(v, dtype=np.float32)

@@ -192,3 +192,23 @@ def test_clipped_scheduled_step_against_torch_float64():
     for (t1, m1, v1), p_, mm in zip(out, params, m):
         assert np.allclose(t1, p_.detach().numpy(), rtol=0, atol=3e-7)
         assert np.allclose(m1, opt.state[p_]["exp_avg"].numpy(), rtol=3e-6, atol=1e-9)
+
+
+def test_bf16_leaf_at_rest_is_the_f32_chain_rounded_once():
+    """A bf16 leaf: widen theta, m, v exactly, the f32 step, one RNE per output
+    (checked against PyTorch's own bf16 rounding of the f32 results)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(51)
+    n = 4000
+    th32 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m32 = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    v32 = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    to_b = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    thb, mb, vb = to_b(th32), to_b(m32), to_b(v32)
+    h = OA.hyper_f32(1e-3, 0.9, 0.999, 1e-8, 0.01, 4)
+    got = OA.step_leaf(thb, mb, vb, g, "f32", h, param_dtype="bf16")
+    wide = lambda b: (b.astype(np.uint32) << 16).view(np.float32)  # noqa: E731
+    want32 = OA.step_leaf(wide(thb), wide(mb), wide(vb), g, "f32", h)
+    for a, w in zip(got, want32):
+        assert a.dtype == np.uint16 and np.array_equal(a, to_b(w))
