@@ -228,15 +228,19 @@ int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, int64_t rows
  *   theta' = theta - lr ((m^ / (sqrt(v^) + eps)) + wd theta)
  * The scalars b1, b2, 1-b1, 1-b2, 1-b1^t, 1-b2^t, lr, eps, wd are computed
  * from the binary64 hyperparameters on the host and rounded once to f32
- * (psk_adamw_scalars returns them).  theta, m, v are f32; grad is f32 or bf16
- * (widened exactly).  t >= 1; 0 < beta < 1; leaves must not overlap. */
+ * (psk_adamw_scalars returns them).  theta, m, v are f32, or bf16 per leaf
+ * (param_dtype); grad is f32 or bf16 (widened exactly).  t >= 1;
+ * 0 < beta < 1; leaves must not overlap. */
 #define PSK_ADAMW_MAX_LEAVES 512
 typedef struct {
-  float* theta;
-  float* m;
-  float* v;
+  void* theta;          /* param_dtype */
+  void* m;              /* param_dtype */
+  void* v;              /* param_dtype */
   const void* grad;
   int32_t grad_dtype;   /* psk_dtype */
+  int32_t param_dtype;  /* psk_dtype of theta, m and v: PSK_F32 (0, the default) or PSK_BF16, a leaf stored in
+                           bf16 at rest (presk "Native execution", params): widened exactly, stepped in f32,
+                           each of theta', m', v' rounded once to bf16 */
   int64_t numel;        /* >= 0; 0 skips the leaf */
 } psk_leaf;
 typedef struct { double lr, beta1, beta2, eps, weight_decay; int64_t t; } psk_adamw_hparams;

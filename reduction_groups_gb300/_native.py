@@ -51,7 +51,8 @@ class psk_order(ctypes.Structure):
 
 class psk_leaf(ctypes.Structure):
     _fields_ = [("theta", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
-                ("grad", ctypes.c_void_p), ("grad_dtype", ctypes.c_int32), ("numel", ctypes.c_int64)]
+                ("grad", ctypes.c_void_p), ("grad_dtype", ctypes.c_int32), ("param_dtype", ctypes.c_int32),
+                ("numel", ctypes.c_int64)]
 
 
 class psk_adamw_hparams(ctypes.Structure):

@@ -40,15 +40,43 @@ constexpr int AW_CHUNK = 4096;                 // elements per chunk
 constexpr int AW_VPT = AW_CHUNK / (AW_THREADS * 4);   // float4 vectors per thread per chunk
 
 struct LeafDesc {
-  float* th;
-  float* m;
-  float* v;
+  void* th;
+  void* m;
+  void* v;
   const void* g;
   int64_t numel;
   int64_t chunk_begin;   // first chunk of this leaf in the launch
-  int32_t gdt;
-  int32_t vec;           // 16-byte aligned theta/m/v and 8/16-byte aligned grad
+  int8_t gdt;            // storage type of the gradient
+  int8_t pdt;            // storage type of theta, m, v
+  int8_t vec;            // theta/m/v and grad aligned for 16-byte (f32) or 8-byte (bf16) vectors
 };
+static_assert(sizeof(LeafDesc) == 56, "512 leaf descriptors must fit the 32 KB kernel parameter space");
+
+// Four consecutive stored values at element i, widened / rounded back.
+__device__ __forceinline__ float4 load4_any(const void* p, int32_t dt, int64_t i) {
+  if (dt == PSK_F32) return __ldcs((const float4*)((const float*)p + i));
+  const uint2 q = __ldcs((const uint2*)((const unsigned short*)p + i));
+  return make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
+                     __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void store4_any(void* p, int32_t dt, int64_t i, float4 v) {
+  if (dt == PSK_F32) {
+    __stcs((float4*)((float*)p + i), v);
+  } else {
+    uint2 q;
+    q.x = f32x2_to_bf16x2(v.x, v.y);
+    q.y = f32x2_to_bf16x2(v.z, v.w);
+    __stcs((uint2*)((unsigned short*)p + i), q);
+  }
+}
+__device__ __forceinline__ float load1_any(const void* p, int32_t dt, int64_t i) {
+  if (dt == PSK_F32) return ((const float*)p)[i];
+  return bf16_bits_to_f32(((const unsigned short*)p)[i]);
+}
+__device__ __forceinline__ void store1_any(void* p, int32_t dt, int64_t i, float v) {
+  if (dt == PSK_F32) ((float*)p)[i] = v;
+  else ((unsigned short*)p)[i] = f32_to_bf16_bits(v);
+}
 
 struct AdamScalars { float b1, b2, omb1, omb2, bc1, bc2, lr, eps, wd; };
 
@@ -76,7 +104,10 @@ __device__ __forceinline__ float load_grad(const void* g, int32_t gdt, int64_t i
   return bf16_bits_to_f32(__ldcs((const unsigned short*)g + i));
 }
 
-template <bool CLIP>
+// theta, m, v stored as PDT (a template parameter: the host launches the f32
+// leaves and the bf16 leaves of a tree separately, so each kernel keeps one
+// load and store path); the gradient's type is a per-chunk uniform branch.
+template <bool CLIP, int PDT>
 __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant__ AdamParams P, const float* clip) {
   const int t = threadIdx.x;
   const float scale = CLIP ? *clip : 1.0f;
@@ -95,9 +126,9 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
 #pragma unroll
       for (int k = 0; k < AW_VPT; ++k) {
         const int64_t i = base + (int64_t)(k * AW_THREADS + t) * 4;
-        th[k] = __ldcs((const float4*)(L.th + i));
-        m[k] = __ldcs((const float4*)(L.m + i));
-        v[k] = __ldcs((const float4*)(L.v + i));
+        th[k] = load4_any(L.th, PDT, i);
+        m[k] = load4_any(L.m, PDT, i);
+        v[k] = load4_any(L.v, PDT, i);
         if (L.gdt == PSK_F32) {
           g[k] = __ldcs((const float4*)((const float*)L.g + i));
         } else {
@@ -117,20 +148,20 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
         adamw_one(P.s, th[k].z, m[k].z, v[k].z, g[k].z);
         adamw_one(P.s, th[k].w, m[k].w, v[k].w, g[k].w);
         const int64_t i = base + (int64_t)(k * AW_THREADS + t) * 4;
-        __stcs((float4*)(L.th + i), th[k]);
-        __stcs((float4*)(L.m + i), m[k]);
-        __stcs((float4*)(L.v + i), v[k]);
+        store4_any(L.th, PDT, i, th[k]);
+        store4_any(L.m, PDT, i, m[k]);
+        store4_any(L.v, PDT, i, v[k]);
       }
     } else {
       for (int64_t j = t; j < n; j += AW_THREADS) {
         const int64_t i = base + j;
-        float th = L.th[i], m = L.m[i], v = L.v[i];
+        float th = load1_any(L.th, PDT, i), m = load1_any(L.m, PDT, i), v = load1_any(L.v, PDT, i);
         float g = load_grad(L.g, L.gdt, i);
         if (CLIP) g = __fmul_rn(g, scale);
         adamw_one(P.s, th, m, v, g);
-        L.th[i] = th;
-        L.m[i] = m;
-        L.v[i] = v;
+        store1_any(L.th, PDT, i, th);
+        store1_any(L.m, PDT, i, m);
+        store1_any(L.v, PDT, i, v);
       }
     }
   }
@@ -457,6 +488,7 @@ static int check_leaves(const psk_leaf* leaves, int32_t n_leaves) {
     const psk_leaf& L = leaves[i];
     if (L.numel < 0) return fail(PSK_E_SHAPE, "leaf %d: numel %lld", i, (long long)L.numel);
     if (!dtype_ok(L.grad_dtype)) return fail(PSK_E_DTYPE, "leaf %d: grad dtype %d", i, L.grad_dtype);
+    if (!dtype_ok(L.param_dtype)) return fail(PSK_E_DTYPE, "leaf %d: parameter dtype %d", i, L.param_dtype);
     if (L.numel > 0 && (!L.theta || !L.m || !L.v || !L.grad)) return fail(PSK_E_NULL, "leaf %d: NULL pointer", i);
   }
   return PSK_OK;
@@ -538,29 +570,32 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
   if (rc == PSK_OK) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel<false>, AW_THREADS, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel<false, PSK_F32>, AW_THREADS, 0);
     if (per_sm < 1) per_sm = 1;
   }
   cudaStream_t s = (cudaStream_t)stream;
   const float* scale = clip ? (const float*)((char*)workspace + W.scale_off) : nullptr;
   if (rc == PSK_OK && clip && W.n_leaves > 0) rc = launch_clip(leaves, n_leaves, W, (char*)workspace,
                                                                (float)sc->grad_clip, s);
-  // one launch per PSK_ADAMW_MAX_LEAVES non-empty leaves (one launch for the trees here)
+  // one launch per PSK_ADAMW_MAX_LEAVES non-empty leaves of each parameter
+  // storage type (one launch for the trees here)
+  for (int pdt = PSK_F32; pdt <= PSK_BF16 && rc == PSK_OK; ++pdt) {
   int i = 0;
   while (i < n_leaves && rc == PSK_OK) {
     int cnt = 0;
     int64_t chunks = 0;
     for (; i < n_leaves && cnt < PSK_ADAMW_MAX_LEAVES; ++i) {
       const psk_leaf& L = leaves[i];
-      if (L.numel == 0) continue;
+      if (L.numel == 0 || L.param_dtype != pdt) continue;
       LeafDesc& d = P->leaf[cnt++];
       d.th = L.theta; d.m = L.m; d.v = L.v; d.g = L.grad;
       d.numel = L.numel;
       d.chunk_begin = chunks;
-      d.gdt = L.grad_dtype;
-      const uintptr_t ga = L.grad_dtype == PSK_F32 ? 16 : 8;
-      d.vec = ((uintptr_t)L.theta % 16 == 0) && ((uintptr_t)L.m % 16 == 0) && ((uintptr_t)L.v % 16 == 0) &&
-              ((uintptr_t)L.grad % ga == 0);
+      d.gdt = (int8_t)L.grad_dtype;
+      d.pdt = (int8_t)L.param_dtype;
+      const uintptr_t ga = L.grad_dtype == PSK_F32 ? 16 : 8, pa = L.param_dtype == PSK_F32 ? 16 : 8;
+      d.vec = (int8_t)(((uintptr_t)L.theta % pa == 0) && ((uintptr_t)L.m % pa == 0) && ((uintptr_t)L.v % pa == 0) &&
+                       ((uintptr_t)L.grad % ga == 0));
       chunks += (L.numel + AW_CHUNK - 1) / AW_CHUNK;
     }
     if (cnt == 0) continue;
@@ -568,9 +603,15 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
     P->n_chunks = chunks;
     int64_t cap = (int64_t)sms * per_sm;
     unsigned grid = (unsigned)(chunks < cap ? chunks : cap);
-    if (clip) adamw_kernel<true><<<grid, AW_THREADS, 0, s>>>(*P, scale);
-    else adamw_kernel<false><<<grid, AW_THREADS, 0, s>>>(*P, nullptr);
+    if (pdt == PSK_F32) {
+      if (clip) adamw_kernel<true, PSK_F32><<<grid, AW_THREADS, 0, s>>>(*P, scale);
+      else adamw_kernel<false, PSK_F32><<<grid, AW_THREADS, 0, s>>>(*P, nullptr);
+    } else {
+      if (clip) adamw_kernel<true, PSK_BF16><<<grid, AW_THREADS, 0, s>>>(*P, scale);
+      else adamw_kernel<false, PSK_BF16><<<grid, AW_THREADS, 0, s>>>(*P, nullptr);
+    }
     rc = check_launch("adamw tree kernel");
+  }
   }
   delete P;
   return rc;

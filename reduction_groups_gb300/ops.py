@@ -203,6 +203,9 @@ def _leaf_table(leaves):
     for i, (th, m, v, g) in enumerate(leaves):
         arr[i].theta, arr[i].m, arr[i].v, arr[i].grad = th.data_ptr(), m.data_ptr(), v.data_ptr(), g.data_ptr()
         arr[i].grad_dtype = _dtype_code(g)
+        arr[i].param_dtype = _dtype_code(th)
+        if _dtype_code(m) != arr[i].param_dtype or _dtype_code(v) != arr[i].param_dtype:
+            raise TypeError("theta, m and v of a leaf must share one storage type")
         arr[i].numel = int(th.numel())
     return arr, n
 

@@ -126,3 +126,36 @@ def test_clip_needs_a_workspace(dev):
     with pytest.raises(dev.PskError) as e:
         dev.psk_adamw_tree_ex(leaves, hp, grad_clip=1.0, workspace=small)
     assert e.value.name == "PSK_E_ARG"
+
+
+def test_mixed_bf16_and_f32_leaves_at_rest(dev):
+    """Leaves stored in bf16 at rest next to f32 ones, clipped and scheduled,
+    aligned and not: every output against the oracle, bit for bit."""
+    rng = np.random.default_rng(61)
+    hp = W.AdamWHyper(lr=1e-3, t=9)
+    specs = [(4096, "bf16", "bf16"), (10007, "bf16", "f32"), (4096, "f32", "bf16"), (3, "bf16", "bf16"),
+             (70000, "bf16", "bf16"), (513, "f32", "f32")]
+    host, leaves, pdts = [], [], []
+    for n, pdt, gdt in specs:
+        th = (rng.standard_normal(n + 1) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n + 1) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n + 1) * 1e-4).astype(np.float32)
+        g = (rng.standard_normal(n + 1) * 0.1).astype(np.float32)
+        arrs = [f32_to_bf16(a) if pdt == "bf16" else a for a in (th, m, v)] + [f32_to_bf16(g) if gdt == "bf16" else g]
+        off = 1 if n % 2 else 0                        # odd sizes: unaligned views
+        host.append(tuple(a[off:off + n] for a in arrs))
+        leaves.append(tuple(_to_dev(a, pdt if k < 3 else gdt)[off:off + n] for k, a in enumerate(arrs)))
+        pdts.append((pdt, gdt))
+    h = OA.hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
+    h["lr"] = OA.lr_scheduled(hp.lr, "linear", 2, 30, hp.t)
+    widened = [OA.widen(np.asarray(g), gdt) for (_, _, _, g), (_, gdt) in zip(host, pdts)]
+    scale = OA.clip_scale(OA.grad_sq_norm(widened, "f32"), 0.5)
+    ws = torch.empty(max(16, dev.psk_adamw_workspace(leaves, "linear", 2, 30, 0.5)), dtype=torch.uint8, device="cuda")
+    dev.psk_adamw_tree_ex(leaves, hp, "linear", 2, 30, 0.5, ws)
+    torch.cuda.synchronize()
+    for (th, m, v, g), (pdt, gdt), (bt, bm, bv, bg), gw in zip(leaves, pdts, host, widened):
+        want = OA.step_leaf(bt, bm, bv, (gw * scale).astype(np.float32), "f32", h, param_dtype=pdt)
+        for got_t, w in zip((th, m, v), want):
+            got = _to_host(got_t)
+            assert np.array_equal(got.view(np.uint16 if pdt == "bf16" else np.uint32),
+                                  w.view(np.uint16 if pdt == "bf16" else np.uint32))
