@@ -176,3 +176,63 @@ def erf_f32(x: np.ndarray) -> np.ndarray:
         y = flat_y.reshape(x.shape)
     # odd symmetry: copy x's sign (keeps erf(-0) = -0 and NaN as NaN)
     return np.copysign(y, x).astype(np.float32)
+
+
+# -------------------------------------------------------------------- log
+
+def _log_exact(x: np.float32) -> np.float32:
+    with localcontext() as ctx:
+        ctx.prec = 60
+        v = Decimal(float(x)).ln()
+    q = Fraction(v)
+    _check_decided(q, 60)
+    return rn_f32(q)
+
+
+def log_f32(x: np.ndarray) -> np.ndarray:
+    """Correctly rounded binary32 natural logarithm, elementwise: log(+-0) =
+    -inf, log(x < 0) = NaN, log(+inf) = +inf, log(1) = +0, NaN stays NaN."""
+    x = np.asarray(x, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        yd = np.log(x.astype(np.float64))
+        y = yd.astype(np.float32)
+    amb = _ambiguous(np.abs(yd))
+    if amb.any():
+        flat_x = x.reshape(-1)
+        flat_y = y.reshape(-1)
+        for i in np.flatnonzero(amb.reshape(-1)):
+            flat_y[i] = _log_exact(flat_x[i])
+        y = flat_y.reshape(x.shape)
+    return y
+
+
+# -------------------------------------------------------------------- tanh
+
+def _tanh_exact(a: np.float32) -> np.float32:
+    """tanh(a) = (e^(2a) - 1) / (e^(2a) + 1) at 120 digits, a >= 0 (the
+    cancellation in the numerator costs at most 45 of them)."""
+    with localcontext() as ctx:
+        ctx.prec = 120
+        e2 = (Decimal(float(a)) * 2).exp()
+        v = (e2 - 1) / (e2 + 1)
+    q = Fraction(v)
+    _check_decided(q, 60)
+    return rn_f32(q)
+
+
+def tanh_f32(x: np.ndarray) -> np.ndarray:
+    """Correctly rounded binary32 tanh, elementwise (odd: tanh(+-0) = +-0,
+    tanh(+-inf) = +-1, NaN stays NaN)."""
+    x = np.asarray(x, dtype=np.float32)
+    ax = np.abs(x)
+    with np.errstate(under="ignore", invalid="ignore"):
+        yd = np.tanh(ax.astype(np.float64))
+        y = yd.astype(np.float32)
+    amb = _ambiguous(yd)
+    if amb.any():
+        flat_x = ax.reshape(-1)
+        flat_y = y.reshape(-1)
+        for i in np.flatnonzero(amb.reshape(-1)):
+            flat_y[i] = _tanh_exact(flat_x[i])
+        y = flat_y.reshape(x.shape)
+    return np.copysign(y, x).astype(np.float32)

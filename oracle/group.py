@@ -13,7 +13,8 @@ argument in the low 24 bits):
 
   operand tokens  IN k (input k), IMM k (immediate k), REF k (op node k's value)
   binary ops      ADD SUB MUL DIV MAX MIN    (a b OP -> OP(a, b))
-  unary ops       NEG ABS EXP EXPC GELU SQRT SQRTA ERF
+  unary ops       NEG ABS EXP EXPC GELU SQRT SQRTA ERF RECIP LOG TANH
+  ternary op      SELECT                     (c a b SELECT -> a where c != 0, else b)
 
 Readings of the pages taken here:
 * the 64-node cap ("past sixty-four nodes the group stops growing") counts op
@@ -27,7 +28,17 @@ Readings of the pages taken here:
   rounded (``oracle.crmath``);
 * broadcasting: each input gives an element stride per output axis, 0 where
   it is broadcast (trailing-axis alignment, presk "The language",
-  Broadcasting; a length-1 column [R, 1] is read with stride (1, 0)).
+  Broadcasting; a length-1 column [R, 1] is read with stride (1, 0));
+* the op set beyond the configurations' follows poot "Fusion and Planning",
+  Pointwise chains (the unaries Neg, Exp, Log, Sqrt, Recip, Tanh and Erf, and
+  Select): RECIP is the IEEE quotient 1/a, LOG and TANH are correctly rounded
+  like EXP and ERF; SELECT's condition is an I32 region input (the operand
+  just before the two branches must be an IN token of an "i32" input), c != 0
+  picks a, and the select moves the picked value's bits without arithmetic,
+  so a NaN or an infinity in the other branch never reaches the result.  An
+  I32 input is read by SELECT conditions only; any other use is refused.
+  Sigmoid is not an op of its own: it is written as the chain
+  1 / (1 + exp(-a)).
 """
 
 from __future__ import annotations
@@ -41,11 +52,13 @@ OP = {
     "IN": 0x01, "IMM": 0x02, "REF": 0x03,
     "ADD": 0x10, "SUB": 0x11, "MUL": 0x12, "DIV": 0x13, "MAX": 0x14, "MIN": 0x15,
     "NEG": 0x20, "ABS": 0x21, "EXP": 0x22, "EXPC": 0x23, "GELU": 0x24,
-    "SQRT": 0x25, "SQRTA": 0x26, "ERF": 0x27,
+    "SQRT": 0x25, "SQRTA": 0x26, "ERF": 0x27, "RECIP": 0x28, "LOG": 0x29, "TANH": 0x2A,
+    "SELECT": 0x30,
 }
 NAME = {v: k for k, v in OP.items()}
 BINARY = {"ADD", "SUB", "MUL", "DIV", "MAX", "MIN"}
-UNARY = {"NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF"}
+UNARY = {"NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF", "RECIP", "LOG", "TANH"}
+TERNARY = {"SELECT"}
 MAX_NODES = 64
 MAX_TOKENS = 1024
 
@@ -56,15 +69,18 @@ class ProgramError(ValueError):
     """A program that is not a group: refused, never run."""
 
 
-def decode(tokens, n_inputs: int, n_imm: int):
+def decode(tokens, n_inputs: int, n_imm: int, input_dtypes=None):
     """Validate a token program and return [(name, arg)].  Refuses: an empty
     program or no op node; more than 64 op nodes; an unknown opcode; an operand
     index out of range; a REF to a node not yet computed; a stack underflow; a
-    final stack that is not exactly the root."""
+    final stack that is not exactly the root; a SELECT whose condition is not an
+    input token.  With ``input_dtypes`` also refuses a condition input that is
+    not "i32" and an "i32" input read as anything but a condition."""
     toks = [int(t) for t in np.asarray(tokens, dtype=np.uint32).reshape(-1)]
     if not toks or len(toks) > MAX_TOKENS:
         raise ProgramError("program length out of range")
     prog, depth, nodes = [], 0, 0
+    kinds = []   # per stack slot: ("IN", k) for an input token, None otherwise
     for pos, t in enumerate(toks):
         code, arg = t >> 24, t & 0xFFFFFF
         name = NAME.get(code)
@@ -74,19 +90,33 @@ def decode(tokens, n_inputs: int, n_imm: int):
             if arg >= n_inputs:
                 raise ProgramError(f"token {pos}: input {arg} of {n_inputs}")
             depth += 1
+            kinds.append(("IN", arg))
         elif name == "IMM":
             if arg >= n_imm:
                 raise ProgramError(f"token {pos}: immediate {arg} of {n_imm}")
             depth += 1
+            kinds.append(None)
         elif name == "REF":
             if arg >= nodes:
                 raise ProgramError(f"token {pos}: REF {arg} before it exists")
             depth += 1
+            kinds.append(None)
         else:
-            need = 2 if name in BINARY else 1
+            need = 3 if name in TERNARY else (2 if name in BINARY else 1)
             if depth < need:
                 raise ProgramError(f"token {pos}: {name} needs {need} operands")
+            ops = kinds[len(kinds) - need:]
+            del kinds[len(kinds) - need:]
+            if name in TERNARY and ops[0] is None:
+                raise ProgramError(f"token {pos}: a SELECT condition must be an input token")
+            if input_dtypes is not None:
+                for j, o in enumerate(ops):
+                    is_cond = name in TERNARY and j == 0
+                    if o is not None and (input_dtypes[o[1]] == "i32") != is_cond:
+                        raise ProgramError(f"token {pos}: input {o[1]} is "
+                                           + ("not i32" if is_cond else "i32 and only a SELECT condition reads it"))
             depth -= need - 1
+            kinds.append(None)
             nodes += 1
             if nodes > MAX_NODES:
                 raise ProgramError("more than 64 op nodes")
@@ -146,16 +176,32 @@ def apply_op(name: str, a: np.ndarray, b: np.ndarray | None = None) -> np.ndarra
             r = np.sqrt(np.abs(a))
         elif name == "ERF":
             r = crmath.erf_f32(a)
+        elif name == "RECIP":
+            r = np.float32(1.0) / a
+        elif name == "LOG":
+            r = crmath.log_f32(a)
+        elif name == "TANH":
+            r = crmath.tanh_f32(a)
         else:
             raise ProgramError(f"not an op: {name}")
     return np.asarray(r, dtype=np.float32)
 
 
+def select(c: np.ndarray, a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """SELECT: a where the i32 condition is nonzero, else b; the picked value's
+    bits are moved, never computed on."""
+    return np.where(np.asarray(c) != 0, a, b).astype(np.float32)
+
+
 def broadcast_input(arr: np.ndarray, dtype: str, strides, out_shape) -> np.ndarray:
-    """The f32 value each output element reads from a stored input: element
-    (i0, i1, ...) reads arr.flat[sum_k i_k * strides[k]]."""
+    """The value each output element reads from a stored input: element
+    (i0, i1, ...) reads arr.flat[sum_k i_k * strides[k]] (f32 for "f32" and
+    "bf16" storage, int32 for an "i32" condition input)."""
     out_shape = tuple(int(s) for s in out_shape)
-    vals = widen(np.asarray(arr).reshape(-1), dtype)
+    if dtype == "i32":
+        vals = np.asarray(arr).reshape(-1).astype(np.int32)
+    else:
+        vals = widen(np.asarray(arr).reshape(-1), dtype)
     if len(out_shape) == 0:
         return vals[:1].reshape(())
     off = np.zeros(out_shape, dtype=np.int64)
@@ -169,10 +215,11 @@ def broadcast_input(arr: np.ndarray, dtype: str, strides, out_shape) -> np.ndarr
 def evaluate(tokens, imm, inputs, out_shape, out_dtype: str, return_nodes: bool = False):
     """Run a group program node by node.
 
-    inputs: list of (stored array, dtype "f32"|"bf16", strides per output axis).
-    Returns the root in storage form (f32 array, or bf16 bit patterns)."""
+    inputs: list of (stored array, dtype "f32"|"bf16"|"i32", strides per
+    output axis).  Returns the root in storage form (f32 array, or bf16 bit
+    patterns)."""
     imm = np.asarray(imm, dtype=np.float32).reshape(-1)
-    prog = decode(tokens, len(inputs), len(imm))
+    prog = decode(tokens, len(inputs), len(imm), [dt for _, dt, _ in inputs])
     out_shape = tuple(int(s) for s in out_shape)
     vals = [broadcast_input(a, dt, st, out_shape) for a, dt, st in inputs]
     stack, nodes = [], []
@@ -187,6 +234,13 @@ def evaluate(tokens, imm, inputs, out_shape, out_dtype: str, return_nodes: bool 
             b = stack.pop()
             a = stack.pop()
             r = apply_op(name, a, b)
+            nodes.append(r)
+            stack.append(r)
+        elif name in TERNARY:
+            b = stack.pop()
+            a = stack.pop()
+            c = stack.pop()
+            r = select(c, a, b)
             nodes.append(r)
             stack.append(r)
         else:

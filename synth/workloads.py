@@ -27,10 +27,11 @@ OPCODES = {
     "IN": 0x01, "IMM": 0x02, "REF": 0x03,
     "ADD": 0x10, "SUB": 0x11, "MUL": 0x12, "DIV": 0x13, "MAX": 0x14, "MIN": 0x15,
     "NEG": 0x20, "ABS": 0x21, "EXP": 0x22, "EXPC": 0x23, "GELU": 0x24,
-    "SQRT": 0x25, "SQRTA": 0x26, "ERF": 0x27,
+    "SQRT": 0x25, "SQRTA": 0x26, "ERF": 0x27, "RECIP": 0x28, "LOG": 0x29, "TANH": 0x2A,
+    "SELECT": 0x30,
 }
 BINARY_OPS = ("ADD", "SUB", "MUL", "DIV", "MAX", "MIN")
-UNARY_OPS = ("NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF")
+UNARY_OPS = ("NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF", "RECIP", "LOG", "TANH")
 
 
 def tok(name: str, arg: int = 0) -> int:

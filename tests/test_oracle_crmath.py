@@ -100,3 +100,62 @@ def test_exp_error_bound_half_ulp_vs_binary64():
     ulp = np.spacing(np.abs(crmath.exp_f32(x))).astype(np.float64)
     assert np.all(np.abs(y - ref) <= 0.5 * ulp * (1 + 1e-6))
     assert math.isclose(float(crmath.exp_f32(np.float32(1.0))), math.e, rel_tol=1e-7)
+
+
+# ---------------------------------------------------------------- log, tanh
+
+def test_log_correctly_rounded_across_binades():
+    x = np.abs(_sample_binades(-149 + 23, 127, 12, 21))
+    x = np.concatenate([x, np.linspace(0.5, 2.0, 2001, dtype=np.float32)])
+    assert same_bits(crmath.log_f32(x), _cr(mpmath.log, x))
+
+
+def test_log_subnormals_specials_and_powers_of_two():
+    tiny = np.array([1e-45, 3e-45, 1e-40, 1e-38, 1.1754942e-38], dtype=np.float32)
+    assert same_bits(crmath.log_f32(tiny), _cr(mpmath.log, tiny))
+    sp = crmath.log_f32(np.array([0.0, -0.0, -1.0, -np.inf, np.inf, np.nan, 1.0], dtype=np.float32))
+    assert np.isneginf(sp[0]) and np.isneginf(sp[1]) and np.isnan(sp[2]) and np.isnan(sp[3])
+    assert np.isposinf(sp[4]) and np.isnan(sp[5]) and sp.view(np.uint32)[6] == 0
+    # log(2^k) is k ln2 rounded once
+    k = np.arange(-149, 128)
+    x = np.ldexp(np.float32(1.0), k).astype(np.float32)
+    ln2 = mpf_fraction(mpmath.log(2))
+    assert same_bits(crmath.log_f32(x), np.array([rn32(int(v) * ln2) for v in k], dtype=np.float32))
+
+
+def test_log_rare_boundary_cases_resolved_exactly():
+    x = np.linspace(0.25, 8.0, 400_001, dtype=np.float32)
+    amb = crmath._ambiguous(np.abs(np.log(x.astype(np.float64))))
+    assert amb.sum() >= 3
+    xa = x[amb]
+    assert same_bits(crmath.log_f32(xa), _cr(mpmath.log, xa))
+
+
+def test_tanh_correctly_rounded_across_binades():
+    x = _sample_binades(-40, 4, 30, 22)
+    assert same_bits(crmath.tanh_f32(x), _cr(mpmath.tanh, x))
+
+
+def test_tanh_small_arguments_saturation_and_specials():
+    # below 2^-12 the cubic term is under half an ulp: tanh rounds to x
+    rng = np.random.default_rng(23)
+    tiny = np.concatenate([np.array([1e-45, 1e-40, 2.0 ** -13, 2.0 ** -12 * 0.999], dtype=np.float32),
+                           rng.uniform(0, 2.0 ** -12, 200).astype(np.float32)])
+    assert same_bits(crmath.tanh_f32(tiny), tiny)
+    assert same_bits(crmath.tanh_f32(tiny), _cr(mpmath.tanh, tiny))
+    big = np.array([9.0, 9.0109, 9.011, 9.5, 20.0, 1e30], dtype=np.float32)
+    assert same_bits(crmath.tanh_f32(big), _cr(mpmath.tanh, big))
+    assert crmath.tanh_f32(np.float32(9.5)) == 1.0
+    sp = crmath.tanh_f32(np.array([0.0, -0.0, np.inf, -np.inf, np.nan], dtype=np.float32))
+    assert sp.view(np.uint32)[0] == 0 and sp.view(np.uint32)[1] == 0x80000000
+    assert sp[2] == 1.0 and sp[3] == -1.0 and np.isnan(sp[4])
+    x = rng.standard_normal(20000).astype(np.float32) * 3
+    assert same_bits(crmath.tanh_f32(-x), -crmath.tanh_f32(x))
+
+
+def test_tanh_rare_boundary_cases_resolved_exactly():
+    x = np.linspace(0, 9.5, 400_001, dtype=np.float32)
+    amb = crmath._ambiguous(np.tanh(x.astype(np.float64)))
+    assert amb.sum() >= 3
+    xa = x[amb]
+    assert same_bits(crmath.tanh_f32(xa), _cr(mpmath.tanh, xa))

@@ -22,7 +22,7 @@ from synth import workloads as W
 from tests.exact import f32_binop, mpf_fraction, rn32, same_bits, sqrt32
 
 BIN = ["ADD", "SUB", "MUL", "DIV", "MAX", "MIN"]
-UN = ["NEG", "ABS", "SQRT", "SQRTA"]
+UN = ["NEG", "ABS", "SQRT", "SQRTA", "RECIP"]
 
 
 def _exact_node(name, a, b=None):
@@ -38,6 +38,8 @@ def _exact_node(name, a, b=None):
         return np.float32(-a)
     if name == "ABS":
         return np.float32(abs(a))
+    if name == "RECIP":
+        return f32_binop("DIV", np.float32(1.0), a)
     if name in ("SQRT", "SQRTA"):
         v = abs(a) if name == "SQRTA" else a
         if np.isnan(v) or v < 0:
@@ -224,3 +226,84 @@ def test_cap_of_64_nodes():
         OG.decode(W.encode([("IN", 0)] + [("NEG",)] * 65), 1, 0)
     with pytest.raises(OG.ProgramError):
         OG.decode(np.array([0x7F000000], dtype=np.uint32), 1, 0)
+
+
+# ------------------------------------------------- SELECT, LOG, TANH, sigmoid
+
+def _select_program():
+    # c a b SELECT with a = x * 2 and b = log(y): each branch a node of its own
+    return W.encode([("IN", 0), ("IN", 1), ("IMM", 0), ("MUL",), ("IN", 2), ("LOG",), ("SELECT",)])
+
+
+def test_select_moves_the_picked_bits_and_never_the_other_branch():
+    c = np.array([1, 0, 7, 0, -1, 0, 1, 0], dtype=np.int32)
+    x = np.array([1.5, np.nan, np.inf, 2.0, -0.0, 1e38, 3.0, np.float32(-np.inf)], dtype=np.float32)
+    y = np.array([-1.0, 4.0, np.nan, 0.0, 5.0, -2.0, -np.inf, 1.0], dtype=np.float32)
+    inputs = [(c, "i32", (1,)), (x, "f32", (1,)), (y, "f32", (1,))]
+    out = OG.evaluate(_select_program(), [2.0], inputs, (8,), "f32")
+    want = []
+    for ci, xi, yi in zip(c, x, y):
+        if ci != 0:
+            want.append(f32_binop("MUL", xi, np.float32(2.0)))
+        else:
+            want.append(rn32(mpf_fraction(__import__("mpmath").log(float(yi)))) if 0 < yi < np.inf
+                        else {0.0: -np.inf, np.inf: np.inf}.get(float(yi), np.nan) if yi >= 0 else np.nan)
+    assert same_bits(out, np.array(want, dtype=np.float32))
+    # an unpicked NaN or infinity never reaches the result (x[1] NaN, y[6] = -inf);
+    # a picked one does (x[2] = inf doubled, log(0) = -inf)
+    assert np.isfinite(out[1]) and np.isfinite(out[6])
+    assert np.isposinf(out[2]) and np.isneginf(out[3])
+
+
+def test_select_of_bf16_branches_equals_the_stored_branch():
+    rng = np.random.default_rng(31)
+    a = f32_to_bf16(rng.standard_normal(64).astype(np.float32))
+    b = f32_to_bf16(rng.standard_normal(64).astype(np.float32))
+    c = rng.integers(0, 2, 64).astype(np.int32)
+    toks = W.encode([("IN", 0), ("IN", 1), ("IN", 2), ("SELECT",)])
+    out = OG.evaluate(toks, [], [(c, "i32", (1,)), (a, "bf16", (1,)), (b, "bf16", (1,))], (64,), "bf16")
+    assert np.array_equal(out, np.where(c != 0, a, b))
+
+
+def test_select_condition_broadcast_row_mask():
+    rng = np.random.default_rng(32)
+    m = rng.integers(0, 2, 5).astype(np.int32)
+    x = rng.standard_normal((3, 5)).astype(np.float32)
+    toks = W.encode([("IN", 0), ("IN", 1), ("IMM", 0), ("SELECT",)])
+    out = OG.evaluate(toks, [-7.0], [(m, "i32", (0, 1)), (x, "f32", (5, 1))], (3, 5), "f32")
+    assert same_bits(out, np.where(m[None, :] != 0, x, np.float32(-7.0)))
+
+
+@pytest.mark.parametrize("seq,dtypes", [
+    ([("IN", 0), ("IN", 1), ("IN", 1), ("SELECT",)], ["f32", "f32"]),          # condition not i32
+    ([("IMM", 0), ("IN", 1), ("IN", 1), ("SELECT",)], ["i32", "f32"]),         # condition not an input token
+    ([("IN", 1), ("NEG",), ("IN", 1), ("IN", 1), ("SELECT",)], ["i32", "f32"]),  # condition a node
+    ([("IN", 0), ("NEG",)], ["i32"]),                                          # i32 read as a value
+    ([("IN", 0), ("IN", 0), ("IN", 1), ("SELECT",)], ["i32", "f32"]),          # i32 as a branch
+    ([("IN", 0), ("IN", 1), ("SELECT",)], ["i32", "f32"]),                     # two operands
+])
+def test_select_typing_is_refused(seq, dtypes):
+    with pytest.raises(OG.ProgramError):
+        OG.decode(W.encode(seq), len(dtypes), 1, dtypes)
+
+
+def test_log_tanh_and_sigmoid_chain_against_mpmath():
+    import mpmath
+
+    mpmath.mp.prec = 200
+    rng = np.random.default_rng(33)
+    x = np.concatenate([rng.standard_normal(300).astype(np.float32) * 4,
+                        np.array([0.0, -0.0, 1e-30, 20.0, -20.0, -90.0, 90.0], dtype=np.float32)])
+    # sigmoid(x) = 1 / (1 + exp(-x)), four nodes; then log(sigmoid) and tanh(x)
+    sig = W.encode([("IN", 0), ("NEG",), ("EXP",), ("IMM", 0), ("ADD",), ("RECIP",)])
+    s, nodes = OG.evaluate(sig, [1.0], [(x, "f32", (1,))], x.shape, "f32", return_nodes=True)
+    for xi, e, d, si in zip(x, nodes[1], nodes[2], s):
+        assert e == rn32(mpf_fraction(mpmath.exp(-mpmath.mpf(float(xi))))) or (np.isinf(e) and float(xi) < -88)
+        assert d == f32_binop("ADD", np.float32(1.0), e)
+        assert same_bits(np.float32(si), f32_binop("DIV", np.float32(1.0), d))
+    ls = OG.evaluate(W.encode([("IN", 0), ("LOG",)]), [], [(s, "f32", (1,))], x.shape, "f32")
+    want = [rn32(mpf_fraction(mpmath.log(float(v)))) if v > 0 else np.float32(-np.inf) for v in s]
+    assert same_bits(ls, np.array(want, dtype=np.float32))
+    th = OG.evaluate(W.encode([("IN", 0), ("TANH",)]), [], [(x, "f32", (1,))], x.shape, "f32")
+    want = [rn32(mpf_fraction(mpmath.tanh(float(v)))) if v != 0 else v for v in x]
+    assert same_bits(th, np.array(want, dtype=np.float32))

@@ -169,6 +169,37 @@ def _backward_sign_flipped(monkeypatch):
     monkeypatch.setattr(OS, "softmax_backward", wrong)
 
 
+def _log_in_binary32(monkeypatch):
+    def wrong(x):
+        with np.errstate(all="ignore"):
+            return np.log(np.asarray(x, dtype=np.float32))
+
+    monkeypatch.setattr(OC, "log_f32", wrong)
+
+
+def _tanh_through_exp_in_binary32(monkeypatch):
+    def wrong(x):
+        x = np.asarray(x, dtype=np.float32)
+        with np.errstate(all="ignore"):
+            e = np.exp(np.float32(2) * x)
+            return ((e - np.float32(1)) / (e + np.float32(1))).astype(np.float32)
+
+    monkeypatch.setattr(OC, "tanh_f32", wrong)
+
+
+def _select_by_arithmetic(monkeypatch):
+    def wrong(c, a, b):
+        k = (np.asarray(c) != 0).astype(np.float32)
+        with np.errstate(all="ignore"):
+            return (k * a + (np.float32(1) - k) * b).astype(np.float32)
+
+    monkeypatch.setattr(OG, "select", wrong)
+
+
+def _select_picks_on_zero(monkeypatch):
+    monkeypatch.setattr(OG, "select", lambda c, a, b: np.where(np.asarray(c) == 0, a, b).astype(np.float32))
+
+
 CASES = [
     (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
     (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
@@ -188,6 +219,10 @@ CASES = [
     (_clip_without_epsilon, TA.test_clip_scale_closed_form),
     (_mask_keeps_emptied_rows, TS.test_mask_emptied_rows_give_zeros_and_full_mask_changes_nothing),
     (_backward_sign_flipped, TS.test_backward_one_hot_cotangent_closed_form),
+    (_log_in_binary32, TC.test_log_correctly_rounded_across_binades),
+    (_tanh_through_exp_in_binary32, TC.test_tanh_correctly_rounded_across_binades),
+    (_select_by_arithmetic, TG.test_select_moves_the_picked_bits_and_never_the_other_branch),
+    (_select_picks_on_zero, TG.test_select_condition_broadcast_row_mask),
 ]
 
 
