@@ -57,7 +57,9 @@ extern "C" {
 #define PSK_E_ARG (-9)            /* any other argument out of range */
 
 /* ------------------------------------------------------- storage types */
-typedef enum { PSK_F32 = 0, PSK_BF16 = 1 } psk_dtype;
+/* PSK_I32 (32-bit integers) is a fusion group's input type for SELECT
+ * conditions only; every other argument of every entry point refuses it. */
+typedef enum { PSK_F32 = 0, PSK_BF16 = 1, PSK_I32 = 2 } psk_dtype;
 
 /* ======================================================== psk_group_run
  * Program format (postfix; one uint32 token per item; opcode in bits 31..24,
@@ -72,6 +74,19 @@ typedef enum { PSK_F32 = 0, PSK_BF16 = 1 } psk_dtype;
  *   EXPC                      exp(min(max(a, -4), 4))
  *   GELU                      a * (0.5 * (1 + erf(a * RN(1/sqrt 2))))
  *   SQRT SQRTA                sqrt(a) / sqrt(|a|), IEEE
+ *   RECIP                     1 / a, IEEE (one rounding)
+ *   LOG TANH                  correctly rounded natural log / tanh
+ *   SELECT                    c a b SELECT -> a where c != 0, else b; pops b,
+ *                             then a, then c.  The condition c must be an IN
+ *                             token of a PSK_I32 input, and a PSK_I32 input is
+ *                             read only as a condition (else PSK_E_DTYPE at
+ *                             run).  The picked value's bits are moved, never
+ *                             computed on: a NaN or an infinity in the other
+ *                             branch never reaches the result (poot "Fusion
+ *                             and Planning", Pointwise chains: Select is a
+ *                             bit-moving select on an I32 region input).
+ * The op set follows the same passage's unaries (Neg, Exp, Log, Sqrt, Recip,
+ * Tanh, Erf) and Select; sigmoid is the chain 1 / (1 + exp(-a)).
  * A valid program has 1..64 op nodes (the cap at which a group stops
  * growing, PSK-Realize "What a group is"), at most 1024 tokens, REFs only to
  * nodes already computed, operands in range, and leaves exactly one value (the
@@ -93,6 +108,10 @@ typedef enum { PSK_F32 = 0, PSK_BF16 = 1 } psk_dtype;
 #define PSK_OP_SQRT 0x25
 #define PSK_OP_SQRTA 0x26
 #define PSK_OP_ERF 0x27
+#define PSK_OP_RECIP 0x28
+#define PSK_OP_LOG 0x29
+#define PSK_OP_TANH 0x2A
+#define PSK_OP_SELECT 0x30
 #define PSK_MAX_NODES 64
 #define PSK_MAX_TOKENS 1024
 #define PSK_MAX_INPUTS 16
@@ -113,7 +132,7 @@ typedef struct {
  * in elements and must be >= 0. */
 typedef struct {
   const void* ptr;
-  int32_t dtype;              /* psk_dtype */
+  int32_t dtype;              /* psk_dtype: PSK_F32, PSK_BF16, or PSK_I32 for a SELECT condition */
   int64_t stride[PSK_MAX_RANK];
 } psk_input;
 
@@ -135,8 +154,10 @@ int psk_group_run(const psk_program* prog, const psk_input* inputs, int32_t n_in
                   const psk_output* out, void* stream);
 
 /* Host-only check of a program (no launch, no device needed): returns 0, the
- * number of op nodes and the most f32 values (inputs and node results) one
- * element keeps live at once, or the refusal psk_group_run would give. */
+ * number of op nodes and the most values (inputs and node results) one
+ * element keeps live at once, or the refusal psk_group_run would give for the
+ * program's structure.  Input types (the PSK_I32 rule of SELECT) need the
+ * input descriptors and are checked by psk_group_prepare / psk_group_run. */
 int psk_group_check(const psk_program* prog, int32_t n_inputs, int32_t* n_nodes, int32_t* n_values);
 
 /* Host-only, synchronous, needs no device: everything psk_group_run does

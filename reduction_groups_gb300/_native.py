@@ -12,7 +12,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libpsk.so")
 
-PSK_F32, PSK_BF16 = 0, 1
+PSK_F32, PSK_BF16, PSK_I32 = 0, 1, 2
 PSK_ORDER_SEQUENTIAL, PSK_ORDER_BLOCKED, PSK_ORDER_INTERLEAVED = 0, 1, 2
 PSK_EXP_EXACT, PSK_EXP_FAST = 0, 1
 PSK_NORM_RMS, PSK_NORM_LAYER = 0, 1

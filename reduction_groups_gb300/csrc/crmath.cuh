@@ -128,6 +128,21 @@ PSK_HD dd dd_div_d(dd a, double b) {  // a / b, b a small exact value
   return dd{s, e};
 }
 
+PSK_HD dd dd_neg(dd a) { return dd{-a.hi, -a.lo}; }
+
+// a / b in double-double: three quotient digits, each from the residual
+// a - q b evaluated in double-double (relative error below 2^-100).
+PSK_HD dd dd_div(dd a, dd b) {
+  double q1 = a.hi / b.hi;
+  dd r = dd_add(a, dd_neg(dd_mul(b, dd{q1, 0.0})));
+  double q2 = r.hi / b.hi;
+  r = dd_add(r, dd_neg(dd_mul(b, dd{q2, 0.0})));
+  double q3 = r.hi / b.hi;
+  double s, e;
+  fast_two_sum_d(q1, q2, s, e);
+  return dd_add(dd{s, e}, dd{q3, 0.0});
+}
+
 // ------------------------------------------------------------ rounding
 // RN_f32 of a binary64 value y known to within rel*|y|; ok = false when the
 // interval of possible exact values reaches a binary32 rounding boundary.
@@ -174,12 +189,12 @@ PSK_HD float dd_to_f32(dd v) {
 
 // ====================================================================== exp
 
-// Tier 3: double-double.  exp(x) = 2^k exp(r), r = x - k ln2, Taylor to 2^-106.
-PSK_NOINLINE float exp_tier3(float xf) {
+// exp(x) = 2^k exp(r), r = x - k ln2, with exp(r) by its Taylor series in
+// double-double (to 2^-106); returns exp(r) and k.
+PSK_HD dd exp_dd_reduced(double x, int& k) {
   const dd LN2 = {PSK_DD_LN2_HI, PSK_DD_LN2_LO};
-  double x = (double)xf;
-  double k = rint(x * PSK_DD_INV_LN2);
-  dd kl = dd_mul(LN2, dd{k, 0.0});
+  double kd = rint(x * PSK_DD_INV_LN2);
+  dd kl = dd_mul(LN2, dd{kd, 0.0});
   dd r = dd_add(dd{x, 0.0}, dd{-kl.hi, -kl.lo});
   dd term = {1.0, 0.0}, sum = {1.0, 0.0};
   for (int n = 1; n < 40; ++n) {
@@ -187,7 +202,14 @@ PSK_NOINLINE float exp_tier3(float xf) {
     sum = dd_add(sum, term);
     if (fabs(term.hi) < 0x1p-110 * fabs(sum.hi)) break;
   }
-  int ki = (int)k;
+  k = (int)kd;
+  return sum;
+}
+
+// Tier 3: double-double.
+PSK_NOINLINE float exp_tier3(float xf) {
+  int ki;
+  dd sum = exp_dd_reduced((double)xf, ki);
   return dd_to_f32(dd{ldexp(sum.hi, ki), ldexp(sum.lo, ki)});
 }
 
@@ -325,38 +347,48 @@ PSK_NOINLINE float erf_tier2(float af) {
   return ok ? res : erf_tier3(af);
 }
 
-// Tier 1 core, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375).  p2: coefficients
-// 0..3 of the 128 Taylor polynomials (width 1/32, centres i/32) as float pairs
-// [k][interval][hi, lo]; h: coefficients 4..D as floats [k - 4][interval]
-// (psk_erf_p2 / psk_erf_h, or copies in shared memory).
-// erf(a) = (R + d)(1 + delta), |delta| < 2^-42.
+// Tier 1 core of a function tabulated as Taylor polynomials about i/32
+// (interval width 1/32), N intervals, degree D, coefficients 0..NPAIR-1 as
+// float pairs [k][interval][hi, lo] in p2 and NPAIR..D as floats
+// [k - NPAIR][interval] in h.  Returns R + d = f(a)(1 + delta).
 //
-// t = a - i/32 (exact, |t| <= 1/64).  Coefficients 4..D by Horner in binary32
-// (their terms stay below 2^-18 of erf(a)); then V_k = c_k + t V_{k+1} for
-// k = 3..0 in float-float, each product split exactly (two_prod) and each
-// sum renormalised (Fast2Sum: |c_k| >= |t V_{k+1}| or c_k = 0 on every
-// interval, checked when the tables are generated).
-PSK_HD void erf_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
+// t = a - i/32 (exact, |t| <= 1/64).  Coefficients NPAIR..D by Horner in
+// binary32 (their terms stay below 2^-18 of f(a)); then V_k = c_k + t V_{k+1}
+// for k = NPAIR-1..0 in float-float, each product split exactly (two_prod)
+// and each sum renormalised: by Fast2Sum where |c_k| >= |t V_{k+1}| or
+// c_k = 0 holds on every interval (checked when the tables are generated),
+// by TwoSum at the steps set in TWOSUM (bit k: step k).
+template <int N, int D, int NPAIR, int TWOSUM>
+PSK_HD void taylor32_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
   const int i = (int)rintf(a * 32.0f);
   const float t = fmaf((float)i, -0.03125f, a);   // exact
-  float H = h[(PSK_ERF_D32 - PSK_ERF_NPAIR) * PSK_ERF_N32 + i];
+  float H = h[(D - NPAIR) * N + i];
 #pragma unroll
-  for (int k = PSK_ERF_D32 - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
+  for (int k = D - 1; k >= NPAIR; --k) H = fmaf(H, t, h[(k - NPAIR) * N + i]);
   float p, pe, vh, vl, ch, cl;
   two_prod(t, H, p, pe);
-  load_pair(p2 + (PSK_ERF_NPAIR - 1) * 2 * PSK_ERF_N32, i, ch, cl);
-  fast_two_sum(ch, p, vh, vl);
+  load_pair(p2 + (NPAIR - 1) * 2 * N, i, ch, cl);
+  if (TWOSUM & (1 << (NPAIR - 1))) two_sum(ch, p, vh, vl);
+  else fast_two_sum(ch, p, vh, vl);
   vl = vl + (pe + cl);
 #pragma unroll
-  for (int k = PSK_ERF_NPAIR - 2; k >= 0; --k) {
+  for (int k = NPAIR - 2; k >= 0; --k) {
     two_prod(t, vh, p, pe);
     pe = fmaf(t, vl, pe);
-    load_pair(p2 + k * 2 * PSK_ERF_N32, i, ch, cl);
-    fast_two_sum(ch, p, vh, vl);
+    load_pair(p2 + k * 2 * N, i, ch, cl);
+    if (TWOSUM & (1 << k)) two_sum(ch, p, vh, vl);
+    else fast_two_sum(ch, p, vh, vl);
     vl = vl + (pe + cl);
   }
   R = vh + vl;
   d = vl - (R - vh);
+}
+
+// erf tier 1, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375): p2 / h are
+// psk_erf_p2 / psk_erf_h or copies in shared memory.  Relative error below
+// 2^-42 (the coefficients' terms from 4 on stay below 2^-18 of erf(a)).
+PSK_HD void erf_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
+  taylor32_tier1_core<PSK_ERF_N32, PSK_ERF_D32, PSK_ERF_NPAIR, 0>(a, p2, h, R, d);
 }
 
 PSK_HD bool erf_tier1(float a, const float* p2, const float* h, float& out) {
@@ -381,6 +413,148 @@ PSK_HD float erf_cr(float x, const float* p2, const float* h) {
   float r;
   if (!(inr && erf_tier1(a, p2, h, r))) r = erf_abs_rest(a);
   return copysignf(r, x);
+}
+
+// ===================================================================== tanh
+// tanh(a) rounds to a below 2^-12 (a^3/3 is under half an ulp there) and to 1
+// from PSK_TANH_ONE_FROM (1 - tanh(a) <= 2^-25); between, tier 1 is the
+// Taylor table (psk_tanh_p2 / psk_tanh_h, erf's layout) and tier 3 the
+// double-double (1 - e^-2a) / (1 + e^-2a) (cancellation costs at most 11 of
+// its 106 bits).
+
+// Tier 3: 2^-12 <= a < PSK_TANH_ONE_FROM.
+PSK_NOINLINE float tanh_tier3(float af) {
+  int k;
+  dd E = exp_dd_reduced(-2.0 * (double)af, k);
+  E = dd{ldexp(E.hi, k), ldexp(E.lo, k)};        // e^-2a >= 2^-27: no underflow
+  dd num = dd_add(dd{1.0, 0.0}, dd_neg(E));
+  dd den = dd_add(dd{1.0, 0.0}, E);
+  return dd_to_f32(dd_div(num, den));
+}
+
+PSK_HD void tanh_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
+  taylor32_tier1_core<PSK_TANH_N32, PSK_TANH_D32, PSK_ERF_NPAIR, PSK_TANH_TWOSUM_MASK>(a, p2, h, R, d);
+}
+
+PSK_HD bool tanh_tier1(float a, const float* p2, const float* h, float& out) {
+  float d;
+  tanh_tier1_core(a, p2, h, out, d);
+  return tier1_decided(out, d);
+}
+
+// tanh of a = |x| where tier 1 does not reach or decide: NaN, small
+// arguments, saturation, the undecided rest by tier 3.
+PSK_NOINLINE float tanh_abs_rest(float a) {
+  if (!(a == a)) return a + a;
+  if (a < 0x1p-12f) return a;
+  if (a >= PSK_TANH_ONE_FROM) return 1.0f;
+  return tanh_tier3(a);
+}
+
+// Correctly rounded tanh (odd; tanh(+-0) = +-0, tanh(+-inf) = +-1).
+PSK_HD float tanh_cr(float x, const float* p2, const float* h) {
+  const float a = fabsf(x);
+  const bool inr = a >= 0x1p-12f && a < PSK_TANH_ONE_FROM;
+  float r;
+  if (!(inr && tanh_tier1(a, p2, h, r))) r = tanh_abs_rest(a);
+  return copysignf(r, x);
+}
+
+// ====================================================================== log
+// x = 2^e m, m in [1, 2); on the intervals above sqrt 2 (table flag s = 1) m
+// is read as m/2 and e as e + 1, so that log(x) = e' ln2 + log(m') with
+// m' in [0.707, 1.414).  The table entry of m's top nine bits gives c (a
+// multiple of 2^-10 near 1/m, so r = m c - 1 is exact and |r| < 2^-9) and
+// T = -log(c 2^s), so log(x) = e' ln2 + T + log1p(r).  Entries 0 and 511 (m
+// next to 1 and 2) have c = 1 and 1/2, T = 0: near x = 1 the result is
+// log1p(r) with no cancellation.
+
+// Tier 3: log(m') = 2 atanh(u), u = (m' - 1)/(m' + 1) (|u| < 0.172), by its
+// series in double-double; x positive, finite, normal.
+PSK_NOINLINE float log_tier3(float xf, int ebias) {
+  int e = (int)((f2u(xf) >> 23) & 0xffu) - 127 + ebias;
+  double m = (double)u2f((f2u(xf) & 0x007fffffu) | 0x3f800000u);
+  if (m > 0x1.6a09e667f3bcdp+0) { m *= 0.5; e += 1; }
+  dd u = dd_div_d(dd{m - 1.0, 0.0}, m + 1.0);    // m - 1 and m + 1 exact
+  dd u2 = dd_mul(u, u);
+  dd term = u, sum = u;
+  for (int n = 1; n < 40; ++n) {
+    term = dd_mul(term, u2);
+    dd t = dd_div_d(term, (double)(2 * n + 1));
+    sum = dd_add(sum, t);
+    if (fabs(t.hi) < 0x1p-110 * fabs(sum.hi)) break;
+  }
+  const dd LN2 = {PSK_DD_LN2_HI, PSK_DD_LN2_LO};
+  dd r = dd_add(dd_mul(LN2, dd{(double)e, 0.0}), dd{2.0 * sum.hi, 2.0 * sum.lo});
+  return dd_to_f32(r);
+}
+
+// Entry i of the log table: (c, T hi, T lo, s), one 16-byte load on the
+// device (the table is 16-byte aligned).
+PSK_HD void load_quad(const float* tab4, int i, float& c, float& th, float& tl, float& s) {
+#if defined(PSK_HOST_BUILD)
+  c = tab4[4 * i]; th = tab4[4 * i + 1]; tl = tab4[4 * i + 2]; s = tab4[4 * i + 3];
+#else
+  const float4 q = *reinterpret_cast<const float4*>(tab4 + 4 * i);
+  c = q.x; th = q.y; tl = q.z; s = q.w;
+#endif
+}
+
+// Tier 1 core: x positive, finite and normal (a subnormal is passed scaled
+// by 2^24 with ebias = -24).  log(x) = R + d to a relative error below
+// 2^-40:
+//   log1p(r) = r - r^2/2 + r^3 (1/3 - r/4 + r^2/5)   (dropped: r^6/6 < 2^-56),
+// r^2 split exactly (two_prod).  T hi, r, -r^2/2, e' L1 and e' L2 (exact: L1
+// and L2 carry 16 bits, |e'| < 2^8) are added exactly, each by Fast2Sum (the
+// table holds T = 0 or |T hi| >= |r|; |r^2/2| < |T hi + r|; e' L1 is 0 or
+// above 0.69 > |log m'|; |e' L2| < 2^-11 |e' L1 + log m'|); the rest -- the
+// Fast2Sum errors, T lo, e' L3, the product error of r^2 and the cubic tail,
+// each below 2^-19 of the result -- is summed in binary32.
+PSK_HD void log_tier1_core(float x, int ebias, const float* tab4, float& R, float& d) {
+  const uint32_t u = f2u(x);
+  const int i = (int)((u >> 14) & 511u);
+  const float m = u2f((u & 0x007fffffu) | 0x3f800000u);
+  float c, th, tl, sf;
+  load_quad(tab4, i, c, th, tl, sf);
+  const float ef = (float)((int)(u >> 23) - 127 + ebias) + sf;
+  const float r = fmaf(m, c, -1.0f);               // exact
+  float s2, se;
+  two_prod(r, r, s2, se);
+  const float hs = -0.5f * s2;                     // exact
+  float a1, b1, a2, b2, a3, b3, H, b4;
+  fast_two_sum(th, r, a1, b1);
+  fast_two_sum(a1, hs, a2, b2);
+  fast_two_sum(ef * PSK_LOG_L1, a2, a3, b3);
+  fast_two_sum(a3, ef * PSK_LOG_L2, H, b4);
+  const float p = fmaf(fmaf(r, 0.2f, -0.25f), r, 0x1.555556p-2f);
+  const float tail = fmaf(-0.5f, se, (s2 * r) * p);
+  const float low = ((b1 + b2) + (b3 + b4)) + (fmaf(ef, PSK_LOG_L3, tl) + tail);
+  fast_two_sum(H, low, R, d);
+}
+
+// log of x outside tier 1's reach or undecided by it: NaN, zero, negative,
+// infinite, 1 (exactly 0) and the undecided rest by tier 3.
+PSK_NOINLINE float log_rest(float x) {
+  if (!(x == x)) return x + x;
+  if (x == 0.0f) return -INFINITY;
+  if (x < 0.0f) return u2f(0x7fc00000u);
+  if (isinf(x)) return x;
+  if (x == 1.0f) return 0.0f;
+  return x < 0x1p-126f ? log_tier3(x * 0x1p24f, -24) : log_tier3(x, 0);
+}
+
+// Correctly rounded natural logarithm.
+PSK_HD float log_cr(float x, const float* tab4) {
+  const bool inr = x > 0.0f && x < INFINITY && x != 1.0f;
+  float r = 0.0f;
+  bool ok = false;
+  if (inr) {
+    const bool sub = x < 0x1p-126f;
+    float d;
+    log_tier1_core(sub ? x * 0x1p24f : x, sub ? -24 : 0, tab4, r, d);
+    ok = tier1_decided(r, d);
+  }
+  return ok ? r : log_rest(x);
 }
 
 // ================================================ division by a fixed b

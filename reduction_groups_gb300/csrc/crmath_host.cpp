@@ -9,24 +9,38 @@ using namespace psk;
 
 extern "C" {
 
-// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful
+// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr
 void psk_host_unary(int which, const float* x, float* y, long n) {
   for (long i = 0; i < n; ++i) {
     switch (which) {
       case 0: y[i] = exp_cr(x[i], psk_exp_tab2); break;
       case 1: y[i] = erf_cr(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0]); break;
+      case 3: y[i] = log_cr(x[i], psk_log_tab); break;
+      case 4: y[i] = tanh_cr(x[i], &psk_tanh_p2[0][0], &psk_tanh_h[0][0]); break;
       default: y[i] = exp_faithful(x[i]); break;
     }
   }
 }
 
 // Tier-by-tier: tier 1 with its decision flag (inputs must be in its range),
-// tiers 2 and 3 on their own.  which: 0 exp, 1 erf.
+// tiers 2 and 3 on their own.  which: 0 exp, 1 erf, 2 log (tiers 1 and 3;
+// normal positive x), 3 tanh (tiers 1 and 3; 2^-12 <= x < its saturation).
 void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char* ok, long n) {
   for (long i = 0; i < n; ++i) {
     float r = 0.0f;
     bool k = true;
-    if (tier == 1) {
+    if (which == 2) {
+      if (tier == 1) {
+        float d;
+        log_tier1_core(x[i], 0, psk_log_tab, r, d);
+        k = tier1_decided(r, d);
+      } else {
+        r = log_tier3(x[i], 0);
+      }
+    } else if (which == 3) {
+      if (tier == 1) k = tanh_tier1(x[i], &psk_tanh_p2[0][0], &psk_tanh_h[0][0], r);
+      else r = tanh_tier3(x[i]);
+    } else if (tier == 1) {
       k = which == 0 ? exp_tier1(x[i], psk_exp_tab2, r)
                      : erf_tier1(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0], r);
     } else if (tier == 2) {
@@ -40,11 +54,18 @@ void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char*
 }
 
 // Tier-1 approximations before rounding, as binary64 (R + d) 2^n, to
-// measure their error against a reference.  which: 0 exp, 1 erf.
+// measure their error against a reference.  which: 0 exp, 1 erf, 2 log
+// (normal positive x), 3 tanh.
 void psk_host_tier1_value(int which, const float* x, double* y, long n) {
   for (long i = 0; i < n; ++i) {
     float R, d;
-    if (which == 0) {
+    if (which == 2) {
+      log_tier1_core(x[i], 0, psk_log_tab, R, d);
+      y[i] = (double)R + (double)d;
+    } else if (which == 3) {
+      tanh_tier1_core(x[i], &psk_tanh_p2[0][0], &psk_tanh_h[0][0], R, d);
+      y[i] = (double)R + (double)d;
+    } else if (which == 0) {
       int e;
       exp_tier1_core(x[i], psk_exp_tab2, R, d, e);
       y[i] = ldexp((double)R + (double)d, e);

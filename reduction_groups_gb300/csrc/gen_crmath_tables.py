@@ -1,4 +1,5 @@
-"""Writes crmath_tables.inc: the constant tables of the device exp / erf.
+"""Writes crmath_tables.inc: the constant tables of the device exp / erf /
+log / tanh.
 
 Run by hand (needs mpmath, 300-bit arithmetic); the generated file is
 committed, so building the library does not need mpmath.
@@ -17,6 +18,16 @@ Tables:
   interleaved) and 4..D32 as floats, D32 the least degree whose truncation
   stays below 2^-48 relative on every interval; the binary64 path uses 32
   intervals of width 1/8 centred at i/8, degree 12 (below 2^-61).
+* tanh: Taylor polynomials about c = i/32 in the erf layout (width 1/32,
+  coefficients 0..3 as float pairs, the rest as floats), up to the least
+  binary32 from which tanh rounds to 1; coefficient k is P_k(tanh c)/k! with
+  P_0(T) = T and P_{k+1}(T) = (1 - T^2) P_k'(T) (d tanh/dx = 1 - tanh^2).
+* log: 512 intervals by the top nine significand bits of x, each with
+  c (a multiple of 2^-10 near 1/m, exactly 1 and 1/2 on the two intervals
+  touching m = 1 and m = 2), s (1 where the interval lies above sqrt 2: the
+  significand is then read as m/2 and the exponent as e + 1) and
+  T = -log(c 2^s) as a float pair, stored as (c, T hi, T lo, s); r = m c - 1
+  is exact in binary32 (checked) and below 2^-9 in magnitude.
 """
 
 import mpmath as mp
@@ -114,6 +125,119 @@ def check_fast2sum(c32hi, D32):
                 v = mp.mpf(c32hi[k][i]) + tv
 
 
+def fast2sum_failures(hi, npair, n_int, factor, t_lo0):
+    """The pair steps k (0..npair-1) at which Fast2Sum's exact condition
+    |c_k| >= |t V_{k+1}| (times `factor`) or c_k = 0 fails on some interval of
+    a table of n_int intervals (interval 0 starting at t_lo0); those steps
+    add with the branch-free TwoSum instead, which is exact in any order."""
+    D = len(hi) - 1
+    bad = set()
+    for i in range(n_int):
+        ts = [mp.mpf(j) / 4096 for j in range(0, 65)] if i == 0 else \
+             [mp.mpf(j) / 4096 for j in range(-64, 65)]
+        if i == 0:
+            ts = [max(t, t_lo0) for t in ts]
+        for t in ts:
+            v = mp.mpf(0)
+            for k in range(D, -1, -1):
+                tv = t * v
+                if k <= npair - 1:
+                    ck = mp.mpf(hi[k][i])
+                    if not (ck == 0 or abs(ck) >= abs(tv) * factor):
+                        bad.add(k)
+                v = mp.mpf(hi[k][i]) + tv
+    return bad
+
+
+def tanh_taylor(c, D):
+    """tanh Taylor coefficients about c through degree D (integer derivative
+    polynomials evaluated at tanh c)."""
+    T = mp.tanh(c)
+    poly = [0, 1]                       # P_0(T) = T, coefficients by power
+    out = [T]
+    for k in range(1, D + 1):
+        der = [j * poly[j] for j in range(1, len(poly))]            # P'
+        nxt = [0] * (len(der) + 2)
+        for j, a in enumerate(der):                                 # (1 - T^2) P'
+            nxt[j] += a
+            nxt[j + 2] -= a
+        poly = nxt
+        val = mp.mpf(0)
+        for a in reversed(poly):
+            val = val * T + a
+        out.append(val / mp.factorial(k))
+    return out
+
+
+def tanh_one_from():
+    """Least binary32 a with RN(tanh a) = 1, i.e. 1 - tanh(a) <= 2^-25."""
+    import struct
+    nxt = lambda v, d: struct.unpack("f", struct.pack("I", struct.unpack("I", struct.pack("f", v))[0] + d))[0]
+    done = lambda a: 1 - mp.tanh(a) <= mp.mpf(2) ** -25
+    a = struct.unpack("f", struct.pack("f", float(mp.atanh(1 - mp.mpf(2) ** -25))))[0]
+    while not done(a):
+        a = nxt(a, 1)
+    while done(nxt(a, -1)):
+        a = nxt(a, -1)
+    return a
+
+
+TANH_LO = mp.mpf(2) ** -12     # below, tanh(a) rounds to a
+
+
+def tanh_degree(n_int):
+    for D in range(5, 16):
+        ok = True
+        for i in range(n_int):
+            c = i * W32
+            cs = tanh_taylor(c, D + 2)
+            h = W32 / 2
+            if i == 0:
+                tail = 2 * (abs(cs[D + 1]) * h ** D + abs(cs[D + 2]) * h ** (D + 1)) * h
+                lo_a = h
+            else:
+                tail = 2 * (abs(cs[D + 1]) * h ** (D + 1) + abs(cs[D + 2]) * h ** (D + 2))
+                lo_a = c - h
+            if tail >= mp.mpf(2) ** -48 * mp.tanh(lo_a):
+                ok = False
+                break
+        if ok:
+            return D
+    raise AssertionError("no degree below 16")
+
+
+def log_table():
+    """(c, T hi, T lo, s) per interval, the largest |r|, and checks."""
+    rows = []
+    rmax = mp.mpf(0)
+    sqrt2 = mp.sqrt(2)
+    for i in range(512):
+        m_lo = 1 + mp.mpf(i) / 512
+        m_hi = 1 + mp.mpf(i + 1) / 512 - mp.mpf(2) ** -23     # last binary32 in the interval
+        mid = 1 + (mp.mpf(i) + mp.mpf(0.5)) / 512
+        s = 1 if mid > sqrt2 else 0
+        if i == 0:
+            c = mp.mpf(1)
+        elif i == 511:
+            c = mp.mpf(1) / 2
+        else:
+            c = mp.nint(1024 / mid) / 1024
+        rloc = mp.mpf(0)
+        for m in (m_lo, m_hi):
+            r = m * c - 1
+            # exact in binary32: a multiple of 2^-33 below 2^-9 (24 bits)
+            assert abs(r) < mp.mpf(2) ** -9, (i, float(r))
+            assert mp.floor(r * 2 ** 33) == r * 2 ** 33
+            rloc = max(rloc, abs(r))
+        rmax = max(rmax, rloc)
+        T = -mp.log(c * 2 ** s)
+        th, tl = split_f32(T)
+        # T hi + r is added by Fast2Sum: T = 0 or |T hi| >= |r|
+        assert th == 0 or abs(th) >= rloc, (i, th, float(rloc))
+        rows.append((float(c), th, tl, float(s)))
+    return rows, rmax
+
+
 def main():
     out = []
     w = out.append
@@ -205,6 +329,49 @@ def main():
     w(f"PSK_TAB double psk_erf_c64[{D64 + 1}][32] = {{")
     for k in range(D64 + 1):
         w("  {" + ", ".join(fmt64(v) for v in c64[k]) + "},")
+    w("};")
+
+    # tanh, binary32 path: the erf layout over [0, tanh's saturation point]
+    one = tanh_one_from()
+    n_t = int(mp.nint(mp.mpf(one) * 32)) + 1
+    Dt = tanh_degree(n_t)
+    thi = [[0.0] * n_t for _ in range(Dt + 1)]
+    tlo = [[0.0] * n_t for _ in range(N_PAIR)]
+    for i in range(n_t):
+        tc = tanh_taylor(i * W32, Dt)
+        for k in range(Dt + 1):
+            if k < N_PAIR:
+                thi[k][i], tlo[k][i] = split_f32(tc[k])
+            else:
+                thi[k][i] = f32(tc[k])
+    bad = fast2sum_failures(thi, N_PAIR, n_t, mp.mpf(1.001), TANH_LO)
+    w(f"#define PSK_TANH_ONE_FROM {fmt32(one)}")
+    w(f"#define PSK_TANH_TWOSUM_MASK {sum(1 << k for k in bad)}   // pair steps added with TwoSum")
+    w(f"#define PSK_TANH_N32 {n_t}")
+    w(f"#define PSK_TANH_D32 {Dt}")
+    w(f"PSK_GTAB float psk_tanh_p2[{N_PAIR}][{2 * n_t}] = {{   // coefficients 0..{N_PAIR - 1}: (hi, lo) per interval")
+    for k in range(N_PAIR):
+        w("  {" + ", ".join(f"{fmt32(thi[k][i])}, {fmt32(tlo[k][i])}" for i in range(n_t)) + "},")
+    w("};")
+    w(f"PSK_GTAB float psk_tanh_h[{Dt + 1 - N_PAIR}][{n_t}] = {{   // coefficients {N_PAIR}..{Dt}")
+    for k in range(N_PAIR, Dt + 1):
+        w("  {" + ", ".join(fmt32(v) for v in thi[k]) + "},")
+    w("};")
+
+    # log, binary32 path.  e' ln2 = e' L1 + e' L2 + e' L3: L1 and L2 carry
+    # 16 significant bits each, so e' L1 and e' L2 are exact for |e'| < 2^8.
+    ln2 = mp.log(2)
+    L1 = trunc_bits(ln2, 16)
+    L2 = trunc_bits(ln2 - L1, 16)
+    L3 = rn(ln2 - L1 - L2, 24)
+    w(f"#define PSK_LOG_L1 {fmt32(L1)}")
+    w(f"#define PSK_LOG_L2 {fmt32(L2)}")
+    w(f"#define PSK_LOG_L3 {fmt32(L3)}")
+    rows, rmax = log_table()
+    w(f"// largest |r| = 2^{float(mp.log(rmax, 2)):.3f}")
+    w("PSK_GTAB float psk_log_tab[2048] = {   // per interval: c, T hi, T lo, s")
+    for i0 in range(0, 512, 2):
+        w("  " + ", ".join(", ".join(fmt32(v) for v in rows[i]) for i in (i0, i0 + 1)) + ",")
     w("};")
     print("\n".join(out))
 

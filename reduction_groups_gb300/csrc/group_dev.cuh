@@ -53,6 +53,27 @@ __device__ __forceinline__ void load_tables(MathTables& t) {
     t.erf_h[i] = (&psk_erf_h[0][0])[i];
 }
 
+// log and tanh tables, staged per CTA only by kernels with such nodes.
+struct LogTables {
+  float4 tab[512];                                             // (c, T hi, T lo, s) per interval
+};
+struct TanhTables {
+  float2 p2[PSK_ERF_NPAIR * PSK_TANH_N32];                     // coefficients 0..3 as (hi, lo)
+  float h[(PSK_TANH_D32 + 1 - PSK_ERF_NPAIR) * PSK_TANH_N32];  // coefficients 4..D
+};
+
+__device__ __forceinline__ void load_log_tables(LogTables& t) {
+  const float4* src = reinterpret_cast<const float4*>(psk_log_tab);
+  for (int i = threadIdx.x; i < 512; i += blockDim.x) t.tab[i] = src[i];
+}
+
+__device__ __forceinline__ void load_tanh_tables(TanhTables& t) {
+  const float2* p2 = reinterpret_cast<const float2*>(&psk_tanh_p2[0][0]);
+  for (int i = threadIdx.x; i < PSK_ERF_NPAIR * PSK_TANH_N32; i += blockDim.x) t.p2[i] = p2[i];
+  for (int i = threadIdx.x; i < (PSK_TANH_D32 + 1 - PSK_ERF_NPAIR) * PSK_TANH_N32; i += blockDim.x)
+    t.h[i] = (&psk_tanh_h[0][0])[i];
+}
+
 template <int V> struct Vec { float v[V]; };
 
 template <int V>
@@ -87,14 +108,27 @@ __device__ __forceinline__ void vec_coords(const GroupParams& P, uint64_t v, uin
   }
 }
 
-// Input k at the vector's coordinates: contiguous inputs load 16 B (f32) or
-// 8 B (bf16) at once, broadcast ones one element, the rest gather.
+// Input k at the vector's coordinates: contiguous inputs load 16 B (f32,
+// i32) or 8 B (bf16) at once, broadcast ones one element, the rest gather.
+// An i32 input (a SELECT condition) keeps its bits in the value's register.
 template <int V, int DT, int MODE>
 __device__ __forceinline__ Vec<V> load_in(const GroupInput& in, uint32_t i0, uint32_t i1, uint32_t i2, uint32_t i3) {
   const int64_t off = (int64_t)i0 * in.stride[0] + (int64_t)i1 * in.stride[1] + (int64_t)i2 * in.stride[2] +
                       (int64_t)i3 * in.stride[3];
   Vec<V> r;
-  if (DT == PSK_F32) {
+  if (DT == PSK_I32) {
+    const uint32_t* p = (const uint32_t*)in.ptr + off;
+    if (V == 4 && MODE == IN_CONTIG) {
+      const uint4 q = __ldg((const uint4*)p);
+      r.v[0] = __uint_as_float(q.x); r.v[1 % V] = __uint_as_float(q.y);
+      r.v[2 % V] = __uint_as_float(q.z); r.v[3 % V] = __uint_as_float(q.w);
+    } else if (MODE == IN_BCAST) {
+      r = splat<V>(__uint_as_float(__ldg(p)));
+    } else {
+#pragma unroll
+      for (int j = 0; j < V; ++j) r.v[j] = __uint_as_float(__ldg(p + j * in.stride[3]));
+    }
+  } else if (DT == PSK_F32) {
     const float* p = (const float*)in.ptr + off;
     if (V == 4 && MODE == IN_CONTIG) {
       const float4 q = __ldg((const float4*)p);
@@ -158,7 +192,17 @@ PSK_NODE1(node_neg, -a)
 PSK_NODE1(node_abs, fabsf(a))
 PSK_NODE1(node_sqrt, __fsqrt_rn(a))
 PSK_NODE1(node_sqrta, __fsqrt_rn(fabsf(a)))
+PSK_NODE1(node_recip, __frcp_rn(a))
 #undef PSK_NODE1
+
+// SELECT: C holds the condition's i32 bits; the picked operand is moved as is.
+template <int V>
+__device__ __forceinline__ Vec<V> node_select(const Vec<V>& C, const Vec<V>& A, const Vec<V>& B) {
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) r.v[j] = __float_as_uint(C.v[j]) != 0u ? A.v[j] : B.v[j];
+  return r;
+}
 
 // exp, exp(clamp(a, -4, 4)), erf and gelu: one out-of-line copy each, called
 // by every such node (the kernel's code stays small enough for the
@@ -209,6 +253,47 @@ __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
     if (!(inr[j] && tier1_decided(R[j], d[j]))) e = erf_abs_rest(fabsf(tt[j]));
     e = copysignf(e, tt[j]);
     r.v[j] = GELU ? __fmul_rn(A.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, e))) : e;
+  }
+  return r;
+}
+
+// log: tier 1 for positive finite x other than 1 (subnormals scaled by
+// 2^24), the rest and undecided elements out of line.
+template <int V>
+__device__ __noinline__ Vec<V> node_log(Vec<V> A, const LogTables& tab) {
+  float R[V], d[V];
+  bool inr[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const float a = A.v[j];
+    inr[j] = a > 0.0f && a < INFINITY && a != 1.0f;
+    const bool sub = a < 0x1p-126f;
+    log_tier1_core(inr[j] ? (sub ? a * 0x1p24f : a) : 2.0f, (inr[j] && sub) ? -24 : 0,
+                   reinterpret_cast<const float*>(tab.tab), R[j], d[j]);
+  }
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) r.v[j] = (inr[j] && tier1_decided(R[j], d[j])) ? R[j] : log_rest(A.v[j]);
+  return r;
+}
+
+// tanh: tier 1 on 2^-12 <= |a| < PSK_TANH_ONE_FROM, the rest out of line.
+template <int V>
+__device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
+  float R[V], d[V];
+  bool inr[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const float aa = fabsf(A.v[j]);
+    inr[j] = aa >= 0x1p-12f && aa < PSK_TANH_ONE_FROM;
+    tanh_tier1_core(inr[j] ? aa : 0.5f, reinterpret_cast<const float*>(tab.p2), tab.h, R[j], d[j]);
+  }
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    float t = R[j];
+    if (!(inr[j] && tier1_decided(R[j], d[j]))) t = tanh_abs_rest(fabsf(A.v[j]));
+    r.v[j] = copysignf(t, A.v[j]);
   }
   return r;
 }

@@ -15,13 +15,17 @@ from . import _native as N
 
 
 def _dtype_code(t) -> int:
+    """The psk_dtype of a tensor; which entry point takes which type is the
+    library's to check (int32 is a group's SELECT condition type only)."""
     import torch
 
     if t.dtype == torch.float32:
         return N.PSK_F32
     if t.dtype == torch.bfloat16:
         return N.PSK_BF16
-    raise TypeError(f"storage type {t.dtype} is not f32 or bf16")
+    if t.dtype == torch.int32:
+        return N.PSK_I32
+    raise TypeError(f"storage type {t.dtype} is not f32, bf16 or int32")
 
 
 def _stream_handle(stream) -> int:
@@ -81,7 +85,8 @@ def psk_group_prepare(tokens, imm, inputs, out) -> None:
 
 def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
     """inputs: list of (tensor, strides) with one element stride per output axis
-    (0 = broadcast); out: a contiguous row-major tensor (f32 or bf16)."""
+    (0 = broadcast), f32 or bf16 values or int32 SELECT conditions; out: a
+    contiguous row-major tensor (f32 or bf16)."""
     p, keep = _program(tokens, imm)
     arr, n, o = _group_args(inputs, out)
     N.check(N.lib().psk_group_run(ctypes.byref(p), arr, n, ctypes.byref(o), _stream_handle(stream)))

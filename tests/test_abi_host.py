@@ -44,7 +44,7 @@ def test_opcodes_agree_across_header_oracle_and_inputs():
 
 def _rand_program(rng, n_in, n_imm, valid=True):
     ops_b = ["ADD", "SUB", "MUL", "DIV", "MAX", "MIN"]
-    ops_u = ["NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF"]
+    ops_u = ["NEG", "ABS", "EXP", "EXPC", "GELU", "SQRT", "SQRTA", "ERF", "RECIP", "LOG", "TANH"]
     seq, depth, nodes = [], 0, 0
     n_ops = int(rng.integers(1, 70))
     while nodes < n_ops:
@@ -62,6 +62,10 @@ def _rand_program(rng, n_in, n_imm, valid=True):
             depth += 1
         elif r < 0.6:
             seq.append((str(rng.choice(ops_u)),))
+            nodes += 1
+        elif r < 0.68 and depth >= 3:
+            seq.append(("SELECT",))     # valid only where the condition slot holds an IN token
+            depth -= 2
             nodes += 1
         else:
             seq.append((str(rng.choice(ops_b)),))
@@ -166,6 +170,46 @@ def test_group_prepare_compiles_every_op_and_layout(native):
                 col = torch.zeros(8, 1, dtype=din)
                 out = torch.zeros(8, cols, dtype=dout)
                 ops.psk_group_prepare(toks, imm, [(x, (cols * step, step)), (row, (0, 1)), (col, (1, 0))], out)
+
+
+def test_group_prepare_compiles_the_extended_op_set(native):
+    """RECIP, LOG, TANH and SELECT with an int32 condition in every access
+    mode, and the sigmoid chain."""
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    seq = [("IN", 0), ("IN", 1), ("RECIP",), ("IN", 1), ("LOG",), ("SELECT",), ("TANH",),
+           ("IN", 1), ("NEG",), ("EXP",), ("IMM", 0), ("ADD",), ("RECIP",), ("ADD",)]
+    toks = W.encode(seq)
+    for din in (torch.float32, torch.bfloat16):
+        for cols, cstride in ((16, (16, 1)), (16, (0, 1)), (15, (15, 1)), (16, (1, 0))):
+            c = torch.zeros(8, cols, dtype=torch.int32)
+            x = torch.zeros(8, cols, dtype=din)
+            out = torch.zeros(8, cols, dtype=torch.float32)
+            ops.psk_group_prepare(toks, np.array([1.0], np.float32), [(c, cstride), (x, (cols, 1))], out)
+
+
+def test_select_typing_refusals(native):
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    c = torch.zeros(4, 4, dtype=torch.int32)
+    x = torch.zeros(4, 4)
+    out = torch.zeros(4, 4)
+    sel = W.encode([("IN", 0), ("IN", 1), ("IN", 1), ("SELECT",)])
+    ops.psk_group_prepare(sel, None, [(c, (4, 1)), (x, (4, 1))], out)
+    with pytest.raises(native.PskError) as e:                      # condition is f32
+        ops.psk_group_prepare(sel, None, [(x, (4, 1)), (x, (4, 1))], out)
+    assert e.value.name == "PSK_E_DTYPE" and "condition" in str(e.value)
+    with pytest.raises(native.PskError) as e:                      # i32 read as a value
+        ops.psk_group_prepare(W.encode([("IN", 0), ("NEG",)]), None, [(c, (4, 1))], out)
+    assert e.value.name == "PSK_E_DTYPE"
+    with pytest.raises(native.PskError) as e:                      # condition is a node
+        ops.psk_group_check(W.encode([("IN", 1), ("NEG",), ("IN", 1), ("IN", 1), ("SELECT",)]), 2)
+    assert e.value.name == "PSK_E_PROGRAM" and "condition" in str(e.value)
+    with pytest.raises(native.PskError) as e:                      # an i32 output
+        ops.psk_group_prepare(sel, None, [(c, (4, 1)), (x, (4, 1))], torch.zeros(4, 4, dtype=torch.int32))
+    assert e.value.name == "PSK_E_DTYPE"
 
 
 def test_group_prepare_refuses_as_check(native):

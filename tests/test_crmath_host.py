@@ -155,3 +155,80 @@ def test_tier1_relative_error_below_the_decision_bound(hm):
     ref = erf64(xa.astype(np.float64))
     rel = np.abs(value(1, xa) / ref - 1)
     assert rel.max() < 2.0 ** -42, np.log2(rel.max())
+
+
+# ---------------------------------------------------------------- log, tanh
+
+def _positive_normals(n, seed):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0x00800000, 0x7F800000, n, dtype=np.uint64).astype(np.uint32).view(np.float32)
+
+
+def test_log_composed_equals_oracle(hm):
+    from oracle.crmath import log_f32
+
+    unary, _ = hm
+    rng = np.random.default_rng(41)
+    x = np.concatenate([_positive_normals(1_000_000, 42), (1 + rng.uniform(-2 ** -7, 2 ** -7, 300_000)).astype(np.float32),
+                        rng.uniform(0, 2.0 ** -126, 20_000).astype(np.float32),
+                        np.array([0.0, -0.0, -1.0, -1e-45, np.inf, -np.inf, np.nan, 1.0, 1e-45, 2.0, 0.5,
+                                  np.sqrt(2), 3.4028235e38, 1.1754942e-38], dtype=np.float32)])
+    assert same_bits(unary(3, x), log_f32(x))
+
+
+def test_tanh_composed_equals_oracle(hm):
+    from oracle.crmath import tanh_f32
+
+    unary, _ = hm
+    rng = np.random.default_rng(43)
+    x = np.concatenate([rng.uniform(-10, 10, 1_000_000).astype(np.float32), _all_binades(-30, 3, 4000, 44),
+                        rng.uniform(-2 ** -11, 2 ** -11, 20_000).astype(np.float32),
+                        np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, 2 ** -12, 9.010913, 9.0109135, 9.5,
+                                  -9.5, 1e30], dtype=np.float32)])
+    assert same_bits(unary(4, x), tanh_f32(x))
+
+
+def test_log_tanh_tier1_keeps_only_correct_roundings_and_tier3_alone(hm):
+    from oracle.crmath import log_f32, tanh_f32
+
+    _, tier = hm
+    x = _positive_normals(2_000_000, 45)
+    y, ok = tier(2, 1, x)
+    assert same_bits(y[ok], log_f32(x[ok]))
+    assert 1 - ok.mean() < 2.0 ** -12
+    bad = x[~ok][:2000]
+    y3, _ = tier(2, 3, np.concatenate([bad, x[:20000]]))
+    assert same_bits(y3, log_f32(np.concatenate([bad, x[:20000]])))
+    rng = np.random.default_rng(46)
+    a = rng.uniform(2.0 ** -12, 9.0109, 2_000_000).astype(np.float32)
+    y, ok = tier(3, 1, a)
+    assert same_bits(y[ok], tanh_f32(a[ok]))
+    assert 1 - ok.mean() < 2.0 ** -12
+    bad = a[~ok][:2000]
+    y3, _ = tier(3, 3, np.concatenate([bad, a[:20000]]))
+    assert same_bits(y3, tanh_f32(np.concatenate([bad, a[:20000]])))
+
+
+def test_log_tanh_tier1_relative_error(hm):
+    """Tier 1's decision assumes a relative error below 2^-40; over every float
+    of their tier-1 ranges the bounds are 2^-42.1 (log, worst just above 1,
+    where the cubic tail is largest against the result) and 2^-46.1 (tanh)."""
+    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
+
+    def value(which, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty(x.shape, dtype=np.float64)
+        L.psk_host_tier1_value(ctypes.c_int(which), ctypes.c_void_p(x.ctypes.data), ctypes.c_void_p(y.ctypes.data),
+                               ctypes.c_long(x.size))
+        return y
+
+    rng = np.random.default_rng(47)
+    x = np.concatenate([_positive_normals(1_000_000, 48), (1 + rng.uniform(-2 ** -8, 2 ** -8, 1_000_000)).astype(np.float32),
+                        (np.sqrt(2) * (1 + rng.uniform(-2 ** -8, 2 ** -8, 200_000))).astype(np.float32)])
+    x = x[x != 1]
+    rel = np.abs(value(2, x) / np.log(x.astype(np.float64)) - 1)
+    assert rel.max() < 2.0 ** -41.5, np.log2(rel.max())
+    a = np.concatenate([rng.uniform(2.0 ** -12, 9.0109, 1_000_000), np.exp2(rng.uniform(-12, 3, 500_000))]).astype(np.float32)
+    a = a[(a >= 2.0 ** -12) & (a < 9.0109)]
+    rel = np.abs(value(3, a) / np.tanh(a.astype(np.float64)) - 1)
+    assert rel.max() < 2.0 ** -44, np.log2(rel.max())
