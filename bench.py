@@ -302,6 +302,15 @@ def run_ours(a, ws, rank, local):
             extra_launches[f"softmax_backward_{oname}"] = (lambda order=order: R.psk_softmax_backward(sy, bct, bdx,
                                                                                                      order))
             b_all[f"softmax_backward_{oname}"] = 3 * sw.rows * sw.cols * 2
+    if a.only in ("all", "group"):
+        # the extended op set (LOG, TANH, RECIP, SELECT on an int32 mask) on the
+        # group's shape
+        xw = W.select_group(rows=max(1, int(8192 * sc)))
+        x_in = xw.device_inputs()
+        x_args = [(t, s_.strides) for t, s_ in zip(x_in, xw.inputs)]
+        x_out = torch.empty(xw.out_shape, dtype=torch.bfloat16, device="cuda")
+        extra_launches["group_select_log_tanh"] = lambda: R.psk_group_run(xw.tokens, xw.imm, x_args, x_out)
+        b_all["group_select_log_tanh"] = xw.algorithmic_bytes()
     if a.only == "norm":
         launches = dict(extra_launches)
     kernels = [k for k in launches if a.only in ("all", "norm") or k.startswith(a.only)]
@@ -368,7 +377,7 @@ def run_ours(a, ws, rank, local):
         extra_launches["adamw_clip_cosine"] = lambda: R.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000, 1.0,
                                                                          clip_ws)
         b_all["adamw_clip_cosine"] = b_adam + tree.n_params * (2 if tree.grad_dtype == "bf16" else 4)
-    if a.only in ("all", "adamw", "softmax"):
+    if a.only in ("all", "adamw", "softmax", "group"):
         for name, fn in extra_launches.items():
             for _ in range(2):
                 fn()
@@ -448,6 +457,9 @@ def run_ours(a, ws, rank, local):
         if k == "adamw_clip_cosine":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["params_per_s"] = round(tree.n_params / (ms / 1e3), 1)
+        if k == "group_select_log_tanh":
+            del kinfo[k]["rows_per_s"]
+            kinfo[k]["elems_per_s"] = round(xw.out_shape[0] * xw.out_shape[1] / (ms / 1e3), 1)
     for k in extra_launches:
         if k in kernels:
             kinfo[k]["rows_per_s"] = round(norm_rows / (per_kernel_ms[k] / 1e3), 1)

@@ -51,8 +51,8 @@ class InputSpec:
     name: str
     shape: tuple          # stored shape (contiguous, row-major)
     strides: tuple        # element stride per OUTPUT axis (0 = broadcast)
-    dtype: str            # "f32" | "bf16"
-    dist: tuple           # ("normal", std) | ("uniform", lo, hi) | ("const", value)
+    dtype: str            # "f32" | "bf16" | "i32"
+    dist: tuple           # ("normal", std) | ("uniform", lo, hi) | ("const", value) | ("bernoulli", p)
 
 
 @dataclass
@@ -81,6 +81,10 @@ class GroupWorkload:
         for i, spec in enumerate(self.inputs):
             dt = torch.bfloat16 if spec.dtype == "bf16" else torch.float32
             kind = spec.dist[0]
+            if kind == "bernoulli":
+                u = G.device_uniform(spec.shape, 0.0, 1.0, self.seed, i, device, torch.float32)
+                out.append((u < spec.dist[1]).to(torch.int32))
+                continue
             if kind == "normal":
                 t = G.device_normal(spec.shape, spec.dist[1], self.seed, i, device, dt)
             elif kind == "uniform":
@@ -94,13 +98,15 @@ class GroupWorkload:
         """Bytes a fused launch must move: every stored input once, the output once."""
         b = 0
         for spec in self.inputs:
-            b += int(np.prod(spec.shape, dtype=np.int64)) * (2 if spec.dtype == "bf16" else 4)
+            b += int(np.prod(spec.shape, dtype=np.int64)) * (2 if spec.dtype == "bf16" else 4)   # i32: 4
         b += int(np.prod(self.out_shape, dtype=np.int64)) * (2 if self.out_dtype == "bf16" else 4)
         return b
 
 
 def _host_draw(spec: InputSpec, seed: int, tensor_id: int) -> np.ndarray:
     kind = spec.dist[0]
+    if kind == "bernoulli":
+        return (G.host_uniform(spec.shape, 0.0, 1.0, seed, tensor_id) < spec.dist[1]).astype(np.int32)
     if kind == "normal":
         v = G.host_normal(spec.shape, spec.dist[1], seed, tensor_id)
     elif kind == "uniform":
@@ -125,6 +131,21 @@ def small_group(rows: int = 64, cols: int = 64) -> GroupWorkload:
     ]
     return GroupWorkload("small_group", SEED_BASE + 0, encode(prog),
                          np.array([1.7], dtype=np.float32), inputs, (rows, cols), "f32", 5)
+
+
+def select_group(rows: int = 8192, cols: int = 8192, seed: int = SEED_BASE + 7) -> GroupWorkload:
+    """The extended op set on one group: y = select(mask, log(sigmoid(x)),
+    tanh(x)) with sigmoid as 1 / (1 + exp(-x)); x bf16 [rows, cols] ~N(0, 3),
+    mask an int32 row vector [cols] (70 % ones) broadcast down the rows; bf16
+    out.  Seven nodes: NEG EXP ADD RECIP LOG TANH SELECT."""
+    prog = [("IN", 1), ("IN", 0), ("NEG",), ("EXP",), ("IMM", 0), ("ADD",), ("RECIP",), ("LOG",),
+            ("IN", 0), ("TANH",), ("SELECT",)]
+    inputs = [
+        InputSpec("x", (rows, cols), (cols, 1), "bf16", ("normal", 3.0)),
+        InputSpec("mask", (cols,), (0, 1), "i32", ("bernoulli", 0.7)),
+    ]
+    return GroupWorkload("select_group", seed, encode(prog), np.array([1.0], dtype=np.float32), inputs,
+                         (rows, cols), "bf16", 7)
 
 
 CAP_OPS = ("ADD", "MUL", "SUB", "MAX", "EXPC", "GELU", "SQRTA")
