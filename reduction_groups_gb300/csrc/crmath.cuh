@@ -9,9 +9,9 @@
 // Each function has three tiers (Ziv's strategy: evaluate with an error bound,
 // keep the result when the bound decides the rounding, else retry more
 // accurately):
-//   1. binary32 float-float arithmetic, relative error below 2^-40; the result
+//   1. binary32 float-float arithmetic, relative error below 2^-41; the result
 //      is kept when it lies more than the error bound away from every rounding
-//      boundary (one call in about 2^15 fails the test);
+//      boundary (one call in about 2^14 fails the test);
 //   2. binary64, relative error below 2^-50, kept unless within 2^-48 of a
 //      boundary (one call in about 2^25 of the calls reaching it);
 //   3. double-double Taylor series, error below 2^-95.
@@ -288,13 +288,15 @@ PSK_HD void exp_tier1_core(float x, const float* tab2, float& R, float& d, int& 
   d = lo - (R - h);
 }
 
-// Keep R when |d| plus the error bound stays below half an ulp of R (R not a
-// power of two, whose lower neighbour is nearer).  With a relative error
-// below 2^-40 this decides the rounding of the exact value.
+// Keep R when R + d (1 + 2^-14) still rounds to R (R finite): fma rounds the
+// exact sum once, so this tests |d| against the half-gap to R's neighbour on
+// d's side -- the smaller gap below a power of two included -- with a margin
+// of 2^-14 of it, in two instructions.  An approximation R + d of relative
+// error below 2^-41 lies within 2^-16 of a half-gap above (2^-15 of the one
+// below a power of two) of the exact value, so a kept R is its correct
+// rounding.
 PSK_HD bool tier1_decided(float R, float d) {
-  uint32_t rb = f2u(R);
-  float hu = u2f((rb & 0x7f800000u) - (24u << 23));
-  return ((rb & 0x007fffffu) != 0u) && (fabsf(d) <= hu * 0.99996948f);
+  return fmaf(d, 0x1.0004p+0f, R) == R;
 }
 
 PSK_HD bool exp_tier1(float x, const float* tab2, float& out) {
@@ -418,9 +420,9 @@ PSK_HD float erf_cr(float x, const float* p2, const float* h) {
 // ===================================================================== tanh
 // tanh(a) rounds to a below 2^-12 (a^3/3 is under half an ulp there) and to 1
 // from PSK_TANH_ONE_FROM (1 - tanh(a) <= 2^-25); between, tier 1 is the
-// Taylor table (psk_tanh_p2 / psk_tanh_h, erf's layout) and tier 3 the
-// double-double (1 - e^-2a) / (1 + e^-2a) (cancellation costs at most 11 of
-// its 106 bits).
+// Taylor table (psk_tanh_p2 / psk_tanh_h, erf's layout), tier 2 the math
+// library's binary64 tanh and tier 3 the double-double (1 - e^-2a) /
+// (1 + e^-2a) (cancellation costs at most 11 of its 106 bits).
 
 // Tier 3: 2^-12 <= a < PSK_TANH_ONE_FROM.
 PSK_NOINLINE float tanh_tier3(float af) {
@@ -442,13 +444,22 @@ PSK_HD bool tanh_tier1(float a, const float* p2, const float* h, float& out) {
   return tier1_decided(out, d);
 }
 
+// Tier 2: the math library's binary64 tanh (within a few ulp of binary64,
+// relative error below 2^-50), kept unless within 2^-48 of a rounding
+// boundary; else tier 3.  2^-12 <= a < PSK_TANH_ONE_FROM.
+PSK_NOINLINE float tanh_tier2(float af) {
+  bool ok;
+  const float r = round_checked(tanh((double)af), 0x1p-48, ok);
+  return ok ? r : tanh_tier3(af);
+}
+
 // tanh of a = |x| where tier 1 does not reach or decide: NaN, small
-// arguments, saturation, the undecided rest by tier 3.
+// arguments, saturation, the undecided rest by tiers 2 and 3.
 PSK_NOINLINE float tanh_abs_rest(float a) {
   if (!(a == a)) return a + a;
   if (a < 0x1p-12f) return a;
   if (a >= PSK_TANH_ONE_FROM) return 1.0f;
-  return tanh_tier3(a);
+  return tanh_tier2(a);
 }
 
 // Correctly rounded tanh (odd; tanh(+-0) = +-0, tanh(+-inf) = +-1).
@@ -502,7 +513,7 @@ PSK_HD void load_quad(const float* tab4, int i, float& c, float& th, float& tl, 
 
 // Tier 1 core: x positive, finite and normal (a subnormal is passed scaled
 // by 2^24 with ebias = -24).  log(x) = R + d to a relative error below
-// 2^-40:
+// 2^-41 (at most 2^-42.1 over every positive normal float):
 //   log1p(r) = r - r^2/2 + r^3 (1/3 - r/4 + r^2/5)   (dropped: r^6/6 < 2^-56),
 // r^2 split exactly (two_prod).  T hi, r, -r^2/2, e' L1 and e' L2 (exact: L1
 // and L2 carry 16 bits, |e'| < 2^8) are added exactly, each by Fast2Sum (the
@@ -532,15 +543,25 @@ PSK_HD void log_tier1_core(float x, int ebias, const float* tab4, float& R, floa
   fast_two_sum(H, low, R, d);
 }
 
+// Tier 2: the math library's binary64 log (within a few ulp of binary64,
+// relative error below 2^-50), kept unless within 2^-48 of a rounding
+// boundary; else tier 3.  x positive, finite, not 1.
+PSK_NOINLINE float log_tier2(float x) {
+  bool ok;
+  const float r = round_checked(log((double)x), 0x1p-48, ok);
+  if (ok) return r;
+  return x < 0x1p-126f ? log_tier3(x * 0x1p24f, -24) : log_tier3(x, 0);
+}
+
 // log of x outside tier 1's reach or undecided by it: NaN, zero, negative,
-// infinite, 1 (exactly 0) and the undecided rest by tier 3.
+// infinite, 1 (exactly 0) and the undecided rest by tiers 2 and 3.
 PSK_NOINLINE float log_rest(float x) {
   if (!(x == x)) return x + x;
   if (x == 0.0f) return -INFINITY;
   if (x < 0.0f) return u2f(0x7fc00000u);
   if (isinf(x)) return x;
   if (x == 1.0f) return 0.0f;
-  return x < 0x1p-126f ? log_tier3(x * 0x1p24f, -24) : log_tier3(x, 0);
+  return log_tier2(x);
 }
 
 // Correctly rounded natural logarithm.

@@ -23,8 +23,8 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
 }
 
 // Tier-by-tier: tier 1 with its decision flag (inputs must be in its range),
-// tiers 2 and 3 on their own.  which: 0 exp, 1 erf, 2 log (tiers 1 and 3;
-// normal positive x), 3 tanh (tiers 1 and 3; 2^-12 <= x < its saturation).
+// tiers 2 and 3 on their own.  which: 0 exp, 1 erf, 2 log (normal positive
+// x other than 1), 3 tanh (2^-12 <= x < its saturation).
 void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char* ok, long n) {
   for (long i = 0; i < n; ++i) {
     float r = 0.0f;
@@ -35,11 +35,11 @@ void psk_host_tier(int which, int tier, const float* x, float* y, unsigned char*
         log_tier1_core(x[i], 0, psk_log_tab, r, d);
         k = tier1_decided(r, d);
       } else {
-        r = log_tier3(x[i], 0);
+        r = tier == 2 ? log_tier2(x[i]) : log_tier3(x[i], 0);
       }
     } else if (which == 3) {
       if (tier == 1) k = tanh_tier1(x[i], &psk_tanh_p2[0][0], &psk_tanh_h[0][0], r);
-      else r = tanh_tier3(x[i]);
+      else r = tier == 2 ? tanh_tier2(x[i]) : tanh_tier3(x[i]);
     } else if (tier == 1) {
       k = which == 0 ? exp_tier1(x[i], psk_exp_tab2, r)
                      : erf_tier1(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0], r);

@@ -207,13 +207,14 @@ __device__ __forceinline__ Vec<V> node_select(const Vec<V>& C, const Vec<V>& A, 
 // exp, exp(clamp(a, -4, 4)), erf and gelu: one out-of-line copy each, called
 // by every such node (the kernel's code stays small enough for the
 // instruction cache).  The tier-1 cores of the V elements run side by side
-// (independent chains for the scheduler); undecided elements go on to the
-// slower tiers.
+// (independent chains for the scheduler); one branch per call sends the
+// undecided elements on to the slower tiers.
 template <int V, bool CLAMP>
 __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
   float a[V], R[V], d[V];
   int n[V];
-  bool inr[V];
+  bool ok[V];
+  bool all = true;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     a[j] = A.v[j];
@@ -221,15 +222,18 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
       a[j] = a[j] > -4.0f ? a[j] : -4.0f;
       a[j] = a[j] < 4.0f ? a[j] : 4.0f;
     }
-    inr[j] = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range (NaN clamps to -4)
-    exp_tier1_core(inr[j] ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
+    const bool inr = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range (NaN clamps to -4)
+    exp_tier1_core(inr ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
+    ok[j] = inr && tier1_decided(R[j], d[j]);
+    all = all && ok[j];
   }
   Vec<V> r;
 #pragma unroll
-  for (int j = 0; j < V; ++j) {
-    float o = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
-    if (!(inr[j] && tier1_decided(R[j], d[j]))) o = exp_tier2(a[j]);
-    r.v[j] = o;
+  for (int j = 0; j < V; ++j) r.v[j] = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
+  if (!all) {   // one branch per call; the elements tier 1 left undecided
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      if (!ok[j]) r.v[j] = exp_tier2(a[j]);
   }
   return r;
 }
@@ -238,20 +242,26 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
 template <int V, bool GELU>
 __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
   float tt[V], R[V], d[V];
-  bool inr[V];
+  bool ok[V];
+  bool all = true;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     tt[j] = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
     const float aa = fabsf(tt[j]);
-    inr[j] = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
-    erf_tier1_core(inr[j] ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h, R[j], d[j]);
+    const bool inr = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
+    erf_tier1_core(inr ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h, R[j], d[j]);
+    ok[j] = inr && tier1_decided(R[j], d[j]);
+    all = all && ok[j];
+  }
+  if (!all) {
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      if (!ok[j]) R[j] = erf_abs_rest(fabsf(tt[j]));
   }
   Vec<V> r;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
-    float e = R[j];
-    if (!(inr[j] && tier1_decided(R[j], d[j]))) e = erf_abs_rest(fabsf(tt[j]));
-    e = copysignf(e, tt[j]);
+    const float e = copysignf(R[j], tt[j]);
     r.v[j] = GELU ? __fmul_rn(A.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, e))) : e;
   }
   return r;
@@ -262,18 +272,26 @@ __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
 template <int V>
 __device__ __noinline__ Vec<V> node_log(Vec<V> A, const LogTables& tab) {
   float R[V], d[V];
-  bool inr[V];
+  bool ok[V];
+  bool all = true;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     const float a = A.v[j];
-    inr[j] = a > 0.0f && a < INFINITY && a != 1.0f;
+    const bool inr = a > 0.0f && a < INFINITY && a != 1.0f;
     const bool sub = a < 0x1p-126f;
-    log_tier1_core(inr[j] ? (sub ? a * 0x1p24f : a) : 2.0f, (inr[j] && sub) ? -24 : 0,
+    log_tier1_core(inr ? (sub ? a * 0x1p24f : a) : 2.0f, (inr && sub) ? -24 : 0,
                    reinterpret_cast<const float*>(tab.tab), R[j], d[j]);
+    ok[j] = inr && tier1_decided(R[j], d[j]);
+    all = all && ok[j];
   }
   Vec<V> r;
 #pragma unroll
-  for (int j = 0; j < V; ++j) r.v[j] = (inr[j] && tier1_decided(R[j], d[j])) ? R[j] : log_rest(A.v[j]);
+  for (int j = 0; j < V; ++j) r.v[j] = R[j];
+  if (!all) {
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      if (!ok[j]) r.v[j] = log_rest(A.v[j]);
+  }
   return r;
 }
 
@@ -281,20 +299,24 @@ __device__ __noinline__ Vec<V> node_log(Vec<V> A, const LogTables& tab) {
 template <int V>
 __device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
   float R[V], d[V];
-  bool inr[V];
+  bool ok[V];
+  bool all = true;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     const float aa = fabsf(A.v[j]);
-    inr[j] = aa >= 0x1p-12f && aa < PSK_TANH_ONE_FROM;
-    tanh_tier1_core(inr[j] ? aa : 0.5f, reinterpret_cast<const float*>(tab.p2), tab.h, R[j], d[j]);
+    const bool inr = aa >= 0x1p-12f && aa < PSK_TANH_ONE_FROM;
+    tanh_tier1_core(inr ? aa : 0.5f, reinterpret_cast<const float*>(tab.p2), tab.h, R[j], d[j]);
+    ok[j] = inr && tier1_decided(R[j], d[j]);
+    all = all && ok[j];
+  }
+  if (!all) {
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      if (!ok[j]) R[j] = tanh_abs_rest(fabsf(A.v[j]));
   }
   Vec<V> r;
 #pragma unroll
-  for (int j = 0; j < V; ++j) {
-    float t = R[j];
-    if (!(inr[j] && tier1_decided(R[j], d[j]))) t = tanh_abs_rest(fabsf(A.v[j]));
-    r.v[j] = copysignf(t, A.v[j]);
-  }
+  for (int j = 0; j < V; ++j) r.v[j] = copysignf(R[j], A.v[j]);
   return r;
 }
 

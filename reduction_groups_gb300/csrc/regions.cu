@@ -89,18 +89,25 @@ __device__ __forceinline__ void region_exp8(float* v) {
   } else {
     float R[8], d[8];
     int n[8];
-    bool inr[8];
+    bool ok[8];
+    bool all = true;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      inr[q] = fabsf(v[q]) <= 87.0f;
-      exp_tier1_core(inr[q] ? v[q] : 0.0f, psk_exp_tab2, R[q], d[q], n[q]);
+      const bool inr = fabsf(v[q]) <= 87.0f;
+      exp_tier1_core(inr ? v[q] : 0.0f, psk_exp_tab2, R[q], d[q], n[q]);
+      ok[q] = inr && tier1_decided(R[q], d[q]);
+      all = all && ok[q];
+    }
+    float out[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) out[q] = u2f((uint32_t)((int32_t)f2u(R[q]) + n[q] * (1 << 23)));
+    if (!all) {   // one branch for the eight; the undecided elements
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (!ok[q]) out[q] = exp_tier2(v[q]);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float out = u2f((uint32_t)((int32_t)f2u(R[q]) + n[q] * (1 << 23)));
-      if (!(inr[q] && tier1_decided(R[q], d[q]))) out = exp_tier2(v[q]);
-      v[q] = out;
-    }
+    for (int q = 0; q < 8; ++q) v[q] = out[q];
   }
 }
 

@@ -82,7 +82,7 @@ def test_tier1_keeps_only_correct_roundings(hm):
     x = rng.uniform(-87, 87, 2_000_000).astype(np.float32)
     y, ok = tier(0, 1, x)
     assert same_bits(y[ok], exp_f32(x[ok]))
-    assert 1 - ok.mean() < 2.0 ** -12          # about one call in 2^15 falls through
+    assert 1 - ok.mean() < 2.0 ** -12          # about one call in 2^14 falls through
     a = rng.uniform(2.0 ** -60, 3.919, 2_000_000).astype(np.float32)
     y, ok = tier(1, 1, a)
     assert same_bits(y[ok], erf_f32(a[ok]))
@@ -126,7 +126,7 @@ def test_division_through_reciprocal_equals_ieee():
 
 
 def test_tier1_relative_error_below_the_decision_bound(hm):
-    """Tier 1's decision assumes a relative error below 2^-40.  The value it
+    """Tier 1's decision assumes a relative error below 2^-41.  The value it
     returns, (R + d) 2^n, against binary64 exp and erf (errors below 2^-52) on
     every binade, uniform reals and the reduction's worst points (|r| at its
     ln2/2048 limit); measured over every float of their tier-1 ranges the
@@ -188,7 +188,7 @@ def test_tanh_composed_equals_oracle(hm):
     assert same_bits(unary(4, x), tanh_f32(x))
 
 
-def test_log_tanh_tier1_keeps_only_correct_roundings_and_tier3_alone(hm):
+def test_log_tanh_tier1_keeps_only_correct_roundings_and_tiers_2_3_alone(hm):
     from oracle.crmath import log_f32, tanh_f32
 
     _, tier = hm
@@ -196,21 +196,24 @@ def test_log_tanh_tier1_keeps_only_correct_roundings_and_tier3_alone(hm):
     y, ok = tier(2, 1, x)
     assert same_bits(y[ok], log_f32(x[ok]))
     assert 1 - ok.mean() < 2.0 ** -12
-    bad = x[~ok][:2000]
-    y3, _ = tier(2, 3, np.concatenate([bad, x[:20000]]))
-    assert same_bits(y3, log_f32(np.concatenate([bad, x[:20000]])))
+    bad = np.concatenate([x[~ok][:2000], x[:20000]])
+    bad = bad[bad != 1]
+    for t in (2, 3):
+        y3, _ = tier(2, t, bad)
+        assert same_bits(y3, log_f32(bad))
     rng = np.random.default_rng(46)
     a = rng.uniform(2.0 ** -12, 9.0109, 2_000_000).astype(np.float32)
     y, ok = tier(3, 1, a)
     assert same_bits(y[ok], tanh_f32(a[ok]))
     assert 1 - ok.mean() < 2.0 ** -12
-    bad = a[~ok][:2000]
-    y3, _ = tier(3, 3, np.concatenate([bad, a[:20000]]))
-    assert same_bits(y3, tanh_f32(np.concatenate([bad, a[:20000]])))
+    bad = np.concatenate([a[~ok][:2000], a[:20000]])
+    for t in (2, 3):
+        y3, _ = tier(3, t, bad)
+        assert same_bits(y3, tanh_f32(bad))
 
 
 def test_log_tanh_tier1_relative_error(hm):
-    """Tier 1's decision assumes a relative error below 2^-40; over every float
+    """Tier 1's decision assumes a relative error below 2^-41; over every float
     of their tier-1 ranges the bounds are 2^-42.1 (log, worst just above 1,
     where the cubic tail is largest against the result) and 2^-46.1 (tanh)."""
     L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
