@@ -261,9 +261,10 @@ PSK_HD void load_pair(const float* tab2, int j, float& hi, float& lo) {
 //   ql = c (1 + r1) + r1^2 (1/2 + r1/6)
 // (dropped: r^4/24, c^2/2 and c r1^2/2, each below 2^-45), and
 //   exp(x) 2^-n = Th + Th r1 + [Th ql + Tl (1 + r1)]
-// (dropped: Tl ql < 2^-45), where Th r1 is split exactly (two_prod) and added
-// to Th exactly (Fast2Sum, |Th r1| < Th), and the bracket (< 2^-20.5) takes one
-// rounding of its own.
+// (dropped: Tl ql < 2^-45), where Th r1 is split exactly (two_prod) and the
+// bracket (< 2^-20.5) takes one rounding of its own; R = RN(Th + RN(m1 +
+// low)) and the residual d = ((Th - R) + m1) + low, whose first two steps
+// are exact (Th - R by Sterbenz; the sum below ulp(R) on the grid of m1).
 PSK_HD void exp_tier1_core(float x, const float* tab2, float& R, float& d, int& n) {
   const float kf = rintf(x * PSK_EXP_INV_L);
   const int k = (int)kf;
@@ -281,11 +282,8 @@ PSK_HD void exp_tier1_core(float x, const float* tab2, float& R, float& d, int& 
   two_prod(Th, r1, m1, e1);
   const float t = fmaf(Tl, r1, Tl + e1);
   const float low = fmaf(Th, ql, t);
-  float h, l;
-  fast_two_sum(Th, m1, h, l);
-  const float lo = l + low;
-  R = h + lo;
-  d = lo - (R - h);
+  R = Th + (m1 + low);
+  d = ((Th - R) + m1) + low;   // Th - R exact (Sterbenz), + m1 exact but for < 2^-47
 }
 
 // Keep R when R + d (1 + 2^-14) still rounds to R (R finite): fma rounds the
@@ -362,8 +360,9 @@ PSK_NOINLINE float erf_tier2(float af) {
 // by TwoSum at the steps set in TWOSUM (bit k: step k).
 template <int N, int D, int NPAIR, int TWOSUM>
 PSK_HD void taylor32_tier1_core(float a, const float* p2, const float* h, float& R, float& d) {
-  const int i = (int)rintf(a * 32.0f);
-  const float t = fmaf((float)i, -0.03125f, a);   // exact
+  const float fi = rintf(a * 32.0f);
+  const int i = (int)fi;
+  const float t = fmaf(fi, -0.03125f, a);   // exact
   float H = h[(D - NPAIR) * N + i];
 #pragma unroll
   for (int k = D - 1; k >= NPAIR; --k) H = fmaf(H, t, h[(k - NPAIR) * N + i]);
