@@ -130,7 +130,7 @@ def test_tier1_relative_error_below_the_decision_bound(hm):
     returns, (R + d) 2^n, against binary64 exp and erf (errors below 2^-52) on
     every binade, uniform reals and the reduction's worst points (|r| at its
     ln2/2048 limit); measured over every float of their tier-1 ranges the
-    bounds are 2^-43.2 (exp) and 2^-45.8 (erf)."""
+    bounds are 2^-43.3 (exp) and 2^-45.8 (erf)."""
     from scipy.special import erf as erf64
 
     L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
