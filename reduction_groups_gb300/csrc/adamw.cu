@@ -136,13 +136,14 @@ __global__ void __launch_bounds__(AW_THREADS) adamw_kernel(const __grid_constant
           g[k] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u),
                              __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u));
         }
+      }
+      // every load of the chunk is in flight before the first use of one
+#pragma unroll
+      for (int k = 0; k < AW_VPT; ++k) {
         if (CLIP) {
           g[k].x = __fmul_rn(g[k].x, scale); g[k].y = __fmul_rn(g[k].y, scale);
           g[k].z = __fmul_rn(g[k].z, scale); g[k].w = __fmul_rn(g[k].w, scale);
         }
-      }
-#pragma unroll
-      for (int k = 0; k < AW_VPT; ++k) {
         adamw_one(P.s, th[k].x, m[k].x, v[k].x, g[k].x);
         adamw_one(P.s, th[k].y, m[k].y, v[k].y, g[k].y);
         adamw_one(P.s, th[k].z, m[k].z, v[k].z, g[k].z);
@@ -190,19 +191,10 @@ struct SqParams {
   SqLeaf leaf[PSK_ADAMW_MAX_LEAVES];
 };
 
-// One thread per block: RN(g^2) added in index order over the block's (up to)
-// 1024 elements, read 8 (bf16) or 4 (f32) at a time when aligned.
-__global__ void __launch_bounds__(SQ_THREADS) sq_blocks_kernel(const __grid_constant__ SqParams P) {
-  const int64_t b = (int64_t)blockIdx.x * SQ_THREADS + threadIdx.x;
-  if (b >= P.n_blocks) return;
-  int lo = 0, hi = P.n_leaves - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.leaf[mid].block_begin <= b) lo = mid; else hi = mid - 1;
-  }
-  const SqLeaf& L = P.leaf[lo];
-  const int64_t base = (b - L.block_begin) * SQ_BLOCK;
-  const int n = (int)((L.numel - base) < SQ_BLOCK ? (L.numel - base) : SQ_BLOCK);
+// RN(g^2) added in index order over one block's (up to 1024) elements by
+// one thread, read 8 (bf16) or 4 (f32) at a time when aligned: blocks that
+// are short or unaligned, and warps holding any such block.
+__device__ float block_sq_lane(const SqLeaf& L, int64_t base, int n) {
   float acc = 0.0f;
   int j = 0;
   if (L.gdt == PSK_BF16) {
@@ -267,7 +259,117 @@ __global__ void __launch_bounds__(SQ_THREADS) sq_blocks_kernel(const __grid_cons
       acc = __fadd_rn(acc, __fmul_rn(a, a));
     }
   }
-  P.block_sums[b] = acc;   // 0 + x = x: the chain starting from 0 is the chain starting from the first square
+  return acc;   // 0 + x = x: the chain starting from 0 is the chain starting from the first square
+}
+
+// Full, 16-byte aligned blocks: the warp's 32 blocks (lane l owns block
+// b0 + l) are fetched cooperatively in stages of 32 elements per block --
+// each 16-byte piece by one lane, `cp.async` into shared memory, the pieces of
+// one block adjacent so a warp instruction reads whole 32-byte sectors -- and
+// each lane then adds its own block's squares in index order from shared
+// memory.  One lane per block reading its own 2 KB would issue 32 separate
+// sectors per warp instruction and run at the L1's one wavefront per cycle.
+constexpr int SQ_CH = 32;                                  // elements per block per stage
+constexpr int SQ_STAGES = 3;
+constexpr int SQ_SLOT = 144;                               // bytes per block per stage (128 + 16: no bank conflict)
+constexpr int SQ_BLK_THREADS = 128;
+constexpr int SQ_WARP_SMEM = SQ_STAGES * 32 * SQ_SLOT;
+constexpr int SQ_BLK_SMEM = (SQ_BLK_THREADS / 32) * SQ_WARP_SMEM;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+
+__device__ float block_sq_warp(const unsigned char* g, int gdt, unsigned char* S) {
+  const int lane = threadIdx.x & 31, q = lane & 7;
+  const uint64_t gp = (uint64_t)(uintptr_t)g;
+  const int esz = gdt == PSK_BF16 ? 2 : 4;
+  // lane copies piece q of blocks 4 i + lane / 8, i = 0..7 (a bf16 stage of a
+  // block is 4 pieces, an f32 one 8)
+  const unsigned char* src[8];
+  int step[8];
+  bool ok[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int sb = 4 * i + (lane >> 3);
+    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)gp, sb);
+    const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(gp >> 32), sb);
+    const int e = __shfl_sync(0xffffffffu, esz, sb);
+    src[i] = (const unsigned char*)(uintptr_t)(((uint64_t)hi << 32) | lo) + q * 16;
+    step[i] = SQ_CH * e;
+    ok[i] = q * 16 < SQ_CH * e;
+  }
+  auto issue = [&](int it) {
+    unsigned char* st = S + (it % SQ_STAGES) * (32 * SQ_SLOT);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (ok[i]) cp_async16(st + (4 * i + (lane >> 3)) * SQ_SLOT + q * 16, src[i] + (size_t)it * step[i]);
+    cp_async_commit();
+  };
+  constexpr int NIT = SQ_BLOCK / SQ_CH;
+  issue(0);
+  issue(1);
+  float acc = 0.0f;
+  for (int it = 0; it < NIT; ++it) {
+    if (it + 2 < NIT) issue(it + 2);
+    else cp_async_commit();                                // an empty group keeps the count
+    cp_async_wait_2();                                     // this lane's copies of stage `it` landed
+    __syncwarp();                                          // ... and every other lane's
+    const unsigned char* mine = S + (it % SQ_STAGES) * (32 * SQ_SLOT) + lane * SQ_SLOT;
+    if (gdt == PSK_BF16) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(mine + 16 * u);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(w[k] << 16), c = __uint_as_float(w[k] & 0xFFFF0000u);
+          acc = __fadd_rn(acc, __fmul_rn(a, a));
+          acc = __fadd_rn(acc, __fmul_rn(c, c));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 f = *reinterpret_cast<const float4*>(mine + 16 * u);
+        acc = __fadd_rn(acc, __fmul_rn(f.x, f.x));
+        acc = __fadd_rn(acc, __fmul_rn(f.y, f.y));
+        acc = __fadd_rn(acc, __fmul_rn(f.z, f.z));
+        acc = __fadd_rn(acc, __fmul_rn(f.w, f.w));
+      }
+    }
+    __syncwarp();                                          // stage read before a later copy reuses it
+  }
+  return acc;
+}
+
+// One thread per block (SQ_BLK_THREADS blocks per CTA): the warp-cooperative
+// path when all 32 blocks of a warp are full and 16-byte aligned, else each
+// lane alone.
+__global__ void __launch_bounds__(SQ_BLK_THREADS) sq_blocks_kernel(const __grid_constant__ SqParams P) {
+  extern __shared__ __align__(16) unsigned char sq_smem[];
+  const int64_t b = (int64_t)blockIdx.x * SQ_BLK_THREADS + threadIdx.x;
+  const bool have = b < P.n_blocks;
+  int lo = 0;
+  if (have) {
+    int hi = P.n_leaves - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P.leaf[mid].block_begin <= b) lo = mid; else hi = mid - 1;
+    }
+  }
+  const SqLeaf& L = P.leaf[lo];
+  const int64_t base = have ? (b - L.block_begin) * SQ_BLOCK : 0;
+  const int n = have ? (int)((L.numel - base) < SQ_BLOCK ? (L.numel - base) : SQ_BLOCK) : 0;
+  const unsigned char* g = have ? (const unsigned char*)L.g + base * (L.gdt == PSK_BF16 ? 2 : 4) : nullptr;
+  const bool full = have && n == SQ_BLOCK && ((uintptr_t)g & 15u) == 0;
+  float acc;
+  if (__all_sync(0xffffffffu, full)) acc = block_sq_warp(g, L.gdt, sq_smem + (threadIdx.x >> 5) * SQ_WARP_SMEM);
+  else acc = have ? block_sq_lane(L, base, n) : 0.0f;
+  if (have) P.block_sums[b] = acc;
 }
 
 // One CTA per leaf: its groups (64 consecutive blocks each, added in order) by
@@ -534,7 +636,10 @@ static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace
     P->block_sums = blocks + block0;
     P->group_sums = groups + group0;
     P->leaf_sums = leaf_sums;
-    sq_blocks_kernel<<<(unsigned)((nb_batch + SQ_THREADS - 1) / SQ_THREADS), SQ_THREADS, 0, stream>>>(*P);
+    static bool smem_set[PSK_MAX_DEVICES];
+    smem_limit_once((const void*)sq_blocks_kernel, SQ_BLK_SMEM, smem_set);
+    sq_blocks_kernel<<<(unsigned)((nb_batch + SQ_BLK_THREADS - 1) / SQ_BLK_THREADS), SQ_BLK_THREADS, SQ_BLK_SMEM,
+                       stream>>>(*P);
     rc = check_launch("squared-norm blocks kernel");
     if (rc) break;
     sq_leaves_kernel<<<cnt, SQ_THREADS, 0, stream>>>(*P);

@@ -159,3 +159,37 @@ def test_mixed_bf16_and_f32_leaves_at_rest(dev):
             got = _to_host(got_t)
             assert np.array_equal(got.view(np.uint16 if pdt == "bf16" else np.uint32),
                                   w.view(np.uint16 if pdt == "bf16" else np.uint32))
+
+
+def test_clip_norm_over_mixed_gradient_types_in_one_warp(dev):
+    """Leaves of whole 1024-element blocks whose gradients alternate f32 and
+    bf16, so the squared-norm pass's warp-cooperative loads mix both types and
+    several leaves in one warp, plus a ragged leaf (the per-lane path): the
+    clip scale and every updated parameter bit for bit."""
+    rng = np.random.default_rng(21)
+    hp = W.AdamWHyper(lr=2e-3, t=7)
+    sizes = [1024, 3072, 2048, 1024, 32 * 1024, 5 * 1024, 1024 * 40, 777, 4096]
+    host, leaves, gf32 = [], [], []
+    for i, n in enumerate(sizes):
+        gdt = "bf16" if i % 2 else "f32"
+        th = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        g32 = (rng.standard_normal(n) * (0.1 + i)).astype(np.float32)
+        g = f32_to_bf16(g32) if gdt == "bf16" else g32
+        host.append((th, m, v, g, gdt))
+        gf32.append(bf16_to_f32(g) if gdt == "bf16" else g)
+        leaves.append((_to_dev(th, "f32"), _to_dev(m, "f32"), _to_dev(v, "f32"), _to_dev(g, gdt)))
+    scale = OA.clip_scale(OA.grad_sq_norm(gf32, "f32"), 0.25)
+    assert scale < 1
+    ws = _workspace(dev, leaves, kind="linear", warmup=2, total=20, grad_clip=0.25)
+    dev.psk_adamw_tree_ex(leaves, hp, "linear", 2, 20, 0.25, ws)
+    torch.cuda.synchronize()
+    assert ws[:4].cpu().numpy().view(np.float32)[0].view(np.uint32) == scale.view(np.uint32)
+    h = OA.hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
+    h["lr"] = OA.lr_scheduled(hp.lr, "linear", 2, 20, hp.t)
+    for (th, m, v, g), (bt, bm, bv, bg, gdt), g32 in zip(leaves, host, gf32):
+        wt, wm, wv = OA.step_leaf(bt, bm, bv, (g32 * scale).astype(np.float32), "f32", h)
+        assert np.array_equal(_to_host(th).view(np.uint32), wt.view(np.uint32))
+        assert np.array_equal(_to_host(m).view(np.uint32), wm.view(np.uint32))
+        assert np.array_equal(_to_host(v).view(np.uint32), wv.view(np.uint32))
