@@ -41,6 +41,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    p.add_argument("--e2e-copy-streams", type=int, default=1,
+                   help="streams per copy direction in the end-to-end leg (units alternate between them)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
     p.add_argument("--softmax-exp", choices=["exact", "fast"], default="fast",
                    help="exp of the softmax region inside the step (the other mode is timed beside it)")
@@ -390,49 +392,93 @@ def run_ours(a, ws, rank, local):
             extra_ms[name] = e0.elapsed_time(e1) / a.steps
 
     # end to end through the public API with host buffers: per step, copy every
-    # input from pinned host memory, run the step, read every result back
+    # input from pinned host memory, run the step, read every result back.
+    # The step is cut into units (the group, the softmax region, AdamW over
+    # consecutive leaf slices: leaves update independently, so the slices give
+    # the one-launch step's bits); each unit's inputs go up on one stream, its
+    # kernels run on a second once they have landed, its results come down on
+    # a third, so copies in both directions overlap each other and the kernels.
     e2e = None
     if not a.no_e2e and a.only == "all":
         host_g = [t.cpu().pin_memory() for t in g_in]
         host_gout = torch.empty(g_out.shape, dtype=g_out.dtype, pin_memory=True)
         host_sx = sx.cpu().pin_memory()
-        host_sy = torch.empty(sy.shape, dtype=sy.dtype, pin_memory=True)
+        sy2 = torch.empty_like(sy)
+        host_sy = [torch.empty(sy.shape, dtype=sy.dtype, pin_memory=True) for _ in range(2)]
         host_leaves = [tuple(t.cpu().pin_memory() for t in leaf) for leaf in leaves]
         h2d = sum(t.numel() * t.element_size() for t in host_g) + host_sx.numel() * 2 + \
             sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf)
-        d2h = host_gout.numel() * 2 + 2 * host_sy.numel() * 2 + \
+        d2h = host_gout.numel() * 2 + 2 * host_sy[0].numel() * 2 + \
             sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf[:3])
+        # AdamW slices of about a tenth of the parameters each, in leaf order
+        slices, cur, acc_n = [], [], 0
+        per = max(1, tree.n_params // 10)
+        for i, leaf in enumerate(leaves):
+            cur.append(i)
+            acc_n += leaf[0].numel()
+            if acc_n >= per:
+                slices.append(cur)
+                cur, acc_n = [], 0
+        if cur:
+            slices.append(cur)
+        units = []      # (copies in, kernels, copies out) as (device, host) pairs and a launch list
+        units.append(([(d_, h_) for d_, h_ in zip(g_in, host_g)],
+                      [lambda st: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out, st)],
+                      [(g_out, host_gout)]))
+        units.append(([(sx, host_sx)],
+                      [lambda st: R.psk_softmax_region(sx, sy, ("sequential",), em, st),
+                       lambda st: R.psk_softmax_region(sx, sy2, ("interleaved", 8), em, st)],
+                      [(sy, host_sy[0]), (sy2, host_sy[1])]))
+        for sl in slices:
+            units.append(([(d_, h_) for i in sl for d_, h_ in zip(leaves[i], host_leaves[i])],
+                          [lambda st, sl=sl: R.psk_adamw_tree([leaves[i] for i in sl], tree.hp, st)],
+                          [(d_, h_) for i in sl for d_, h_ in zip(leaves[i][:3], host_leaves[i][:3])]))
+        n_cs = a.e2e_copy_streams
+        s_ins = [torch.cuda.Stream() for _ in range(n_cs)]
+        s_outs = [torch.cuda.Stream() for _ in range(n_cs)]
+        s_cmp = torch.cuda.Stream()
+        ev = [[torch.cuda.Event() for _ in range(3)] for _ in units]    # per unit: in, computed, out
+        out_done = [None] * len(units)                                    # last step's "out" events
+
+        def e2e_step(after):
+            for u, (cin, cmp, cout) in enumerate(units):
+                s_in, s_out = s_ins[u % n_cs], s_outs[u % n_cs]
+                e_in, e_cmp, e_out = ev[u]
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(after)
+                    if out_done[u] is not None:
+                        s_in.wait_event(out_done[u])   # the previous step's results of this unit are read
+                    for d_, h_ in cin:
+                        d_.copy_(h_, non_blocking=True)
+                    e_in.record(s_in)
+                s_cmp.wait_event(e_in)
+                for fn in cmp:
+                    fn(s_cmp)
+                e_cmp.record(s_cmp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(e_cmp)
+                    for d_, h_ in cout:
+                        h_.copy_(d_, non_blocking=True)
+                    e_out.record(s_out)
+                out_done[u] = e_out
+
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
-        def e2e_step():
-            for d_, h_ in zip(g_in, host_g):
-                d_.copy_(h_, non_blocking=True)
-            sx.copy_(host_sx, non_blocking=True)
-            for dl, hl in zip(leaves, host_leaves):
-                for d_, h_ in zip(dl, hl):
-                    d_.copy_(h_, non_blocking=True)
-            R.psk_group_run(wl.tokens, wl.imm, g_args, g_out)
-            host_gout.copy_(g_out, non_blocking=True)
-            R.psk_softmax_region(sx, sy, ("sequential",), em)
-            host_sy.copy_(sy, non_blocking=True)
-            R.psk_softmax_region(sx, sy, ("interleaved", 8), em)
-            host_sy.copy_(sy, non_blocking=True)
-            R.psk_adamw_tree(leaves, tree.hp)
-            for dl, hl in zip(leaves, host_leaves):
-                for d_, h_ in zip(dl[:3], hl[:3]):
-                    h_.copy_(d_, non_blocking=True)
-
-        e2e_step()
+        cur_stream = torch.cuda.current_stream()
+        s2.record(cur_stream)
+        e2e_step(s2)
         torch.cuda.synchronize()
         barrier()
-        s2.record()
+        s2.record(cur_stream)
         for _ in range(a.steps):
-            e2e_step()
-        e2.record()
+            e2e_step(s2)
+        for u in range(len(units)):
+            cur_stream.wait_event(out_done[u])
+        e2.record(cur_stream)
         torch.cuda.synchronize()
         ms = max_over_ranks(s2.elapsed_time(e2))
         e2e = {"value": round(job_value(bytes_step, a.steps, ws, ms), 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / a.steps, 3)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / a.steps, 3),
+               "streams": f"inputs and results on {n_cs} streams per direction, kernels on one, overlapped per unit"}
 
     if rank != 0:
         if ws > 1:
