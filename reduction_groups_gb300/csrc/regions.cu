@@ -1082,13 +1082,15 @@ static int launch_stream(const RegionParams& P, cudaStream_t stream) {
   return check_launch("softmax region kernel (streaming rows)");
 }
 
-// Ring depths from the shared-memory budget.  Eight bf16 rows in flight per
-// SM cover HBM latency; the value ring holds SE = 4 (LAG + 1) rows, about
-// 4 LAG of them in their chains.  A long chain (>= 1024 dependent adds per
-// row: cols / P, twice that for LayerNorm's two chains; e.g. the sequential
-// order over 4096 columns) is the bottleneck, so it gets the value ring first
-// (x ring down to 4 slots); otherwise the x ring comes first.  Chain groups
-// take G <= 4 consecutive rows (one per team).
+// Ring depths from the shared-memory budget.  The value ring holds SE =
+// 4 (LAG + 1) rows, about 4 LAG of them in their chains, and a team waits for
+// the sums of the rows it produced LAG iterations earlier: the deeper the
+// value ring, the less the teams wait, for long chains (the sequential order
+// over 4096 columns) and short ones alike (interleaved(8) over 4096 columns:
+// 0.247 ms at LAG 1 with 8 x slots, 0.205 ms at LAG 2 with 4).  So the value
+// ring comes first, the x ring keeping 4 slots (four rows ahead per SM cover
+// HBM latency), and the x ring takes 8 only where that costs no value slot.
+// Chain groups take G <= 4 consecutive rows (one per team).
 template <int KIND, int XT, int YT, int EXPM, bool MASK = false>
 static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const int pad = P.partials < 4 ? 4 : ((P.partials + 3) / 4) * 4;
@@ -1097,10 +1099,7 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const size_t xrow = (size_t)((P.cols * xsz * (KIND == REGION_SOFTMAX_BWD ? 2 : 1) + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
   const size_t budget = PIPE_SMEM_BUDGET;
-  const int64_t chain = ((P.cols + P.partials - 1) / P.partials) * (KIND == REGION_LAYER ? 2 : 1);
-  const bool long_chain = chain >= 1024;
-  int sx = long_chain ? 4 : PIPE_SX_MAX;
-  if (sx * xrow + 2 * PIPE_TEAMS * erow > budget) sx = 4;   // wide x slots (backward: y and ct) leave room for 8 value rows
+  int sx = 4;
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
   // x slots stay a multiple of the team count, so that each slot serves one
