@@ -131,3 +131,53 @@ def test_softmax_backward_in_place_and_refusals(dev):
     with pytest.raises(dev.PskError) as e:
         dev.psk_softmax_masked(x, x.clone(), m, ("interleaved", 65))
     assert e.value.name == "PSK_E_ORDER"
+
+
+# ---------------------------------------------------- one-chain long rows
+# Rows of 2048 < cols <= 4096 summed in one chain (sequential, blocked): partial
+# last chain groups, rows past 512-column boundaries, enough rows per CTA that
+# the rings wrap many times, both output types and both exp modes.
+
+@pytest.mark.parametrize("rows,cols", [(1, 4096), (3, 2056), (5, 3000), (152 * 2 + 9, 4096), (152 * 40 + 13, 2064),
+                                       (152 * 36 + 151, 4096)])
+@pytest.mark.parametrize("order", [("sequential",), ("blocked", 64)])
+def test_one_chain_long_rows_bitwise(dev, rows, cols, order):
+    wl = W.softmax_rows(rows, cols)
+    x = wl.host_x()
+    dev.psk_device_status(reset=True)
+    for yt in ("bf16", "f32"):
+        want = OS.softmax_region(x, "bf16", yt, order)
+        y = _empty((rows, cols), yt)
+        dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, "exact")
+        torch.cuda.synchronize()
+        ok = _same(_to_host(y), want, yt)
+        assert ok.all(), f"{(~ok).sum()} of {ok.size} differ"
+        dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, "fast")
+        torch.cuda.synchronize()
+        got = _to_host(y)
+        g = bf16_to_f32(got) if yt == "bf16" else got
+        w = bf16_to_f32(want) if yt == "bf16" else want
+        tol = 2.0 ** -7 if yt == "bf16" else 4e-6
+        assert np.all(np.abs(g.astype(np.float64) - w) <= tol * np.abs(w) + 2.0 ** -140)
+    assert dev.psk_device_status() == 0
+
+
+def test_one_chain_long_rows_specials(dev):
+    """-inf entries, a NaN row, an +inf row, an all -inf row and entries far
+    below the row max, at 4096 columns in the sequential order."""
+    rng = np.random.default_rng(31)
+    rows, cols = 40, 4096
+    x = (rng.standard_normal((rows, cols)) * 3).astype(np.float32)
+    x[0, ::7] = -np.inf
+    x[1, 5:400] = np.linspace(-120.0, -80.0, 395)
+    x[1, 0] = 10.0
+    x[2, :] = -np.inf
+    x[3, 3000] = np.nan
+    x[4, 4095] = np.inf
+    x[5, 511:514] = 50.0
+    xs = f32_to_bf16(x)
+    want = OS.softmax_region(xs, "bf16", "f32", ("sequential",))
+    y = _empty((rows, cols), "f32")
+    dev.psk_softmax_region(_to_dev(xs, "bf16"), y, ("sequential",), "exact")
+    torch.cuda.synchronize()
+    assert _same(_to_host(y), want, "f32").all()
