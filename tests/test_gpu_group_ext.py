@@ -196,3 +196,23 @@ def test_extended_ops_are_refused_with_wrong_types(dev):
     with pytest.raises(dev.PskError) as e:
         dev.psk_group_run(W.encode([("IN", 0), ("LOG",)]), [], [(c, (8, 1))], torch.empty(8, 8, device="cuda"))
     assert e.value.name == "PSK_E_DTYPE"
+
+
+def test_select_group_full_size_sampled_rows(dev):
+    """The select/log/tanh group at its full size [8192, 8192] (int32 row mask,
+    bf16 in and out), launched as the benchmark launches it; sampled rows
+    against the oracle."""
+    wl = W.select_group()
+    dins = wl.device_inputs()
+    out = torch.empty(wl.out_shape, dtype=torch.bfloat16, device="cuda")
+    dev.psk_group_run(wl.tokens, wl.imm, [(t, s.strides) for t, s in zip(dins, wl.inputs)], out)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 4095, 8191] + list(np.random.default_rng(2).integers(0, 8192, 8)))
+    idx = torch.from_numpy(rows).cuda()
+    x = _to_host(dins[0][idx])
+    mask = dins[1].cpu().numpy()
+    assert mask.dtype == np.int32 and 0.6 < mask.mean() < 0.8
+    ins = [(x, "bf16", (8192, 1)), (mask, "i32", (0, 1))]
+    want = OG.evaluate(wl.tokens, wl.imm, ins, (len(rows), 8192), "bf16")
+    ok = _same(_to_host(out[idx]), want, "bf16")
+    assert ok.all(), f"{(~ok).sum()} differ"
