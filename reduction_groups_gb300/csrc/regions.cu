@@ -1099,7 +1099,11 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const size_t xrow = (size_t)((P.cols * xsz * (KIND == REGION_SOFTMAX_BWD ? 2 : 1) + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
   const size_t budget = PIPE_SMEM_BUDGET;
-  int sx = 4;
+  // the correctly rounded exp makes a team's row work long enough that with
+  // short chains the sums are ready in time, and the x ring's depth pays
+  // instead (interleaved(8): 0.466 ms with SX = 8, SE = 8; 0.500 with 4, 12)
+  const int64_t chain = (P.cols + P.partials - 1) / P.partials;
+  int sx = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && chain < 1024) ? PIPE_SX_MAX : 4;
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
   // x slots stay a multiple of the team count, so that each slot serves one
