@@ -333,6 +333,16 @@ int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, const psk_ad
  * mean a pipeline bug, and this lets a caller detect it without a hang. */
 int psk_device_status(uint32_t* status, int32_t reset);
 
+/* Test hook for the bounded waits (no counterpart on the pages): from the
+ * next launch on, the pipelined row-region kernels of the current device stop
+ * producing at local row `row` of every CTA, as if that row's copy had been
+ * lost.  Every wait for it gives up after about two seconds of clock, the
+ * kernel sets bit 0 of the status word and winds down (its output then
+ * unspecified), and the device stays usable.  row = -1 (the default) turns
+ * it off.  Host-only, synchronous; for tests, never for production use.
+ * PSK_E_ARG for row < -1. */
+int psk_test_drop_row(int64_t row);
+
 /* Thread-local description of the last refusal of this thread ("" if none). */
 const char* psk_last_error(void);
 

@@ -20,5 +20,6 @@ from .ops import (  # noqa: F401
     psk_softmax_backward,
     psk_softmax_masked,
     psk_softmax_region,
+    psk_test_drop_row,
 )
 from ._native import PskError  # noqa: F401

@@ -15,6 +15,11 @@ namespace psk {
 // psk_device_status() on the host.
 __device__ unsigned int g_pipe_status;
 
+// Test hook (psk_test_drop_row): the local row at which every pipelined
+// region CTA's producer stops, as if that row's copy were lost, so that the
+// bounded waits run out; -1 (the default) never.
+__device__ long long g_pipe_drop_row = -1;
+
 constexpr unsigned int PIPE_TIMEOUT = 1u;
 constexpr long long PIPE_WAIT_CYCLES = 4000000000LL;   // ~2 s at 2 GHz: far beyond any legitimate wait
 

@@ -759,8 +759,10 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       const int64_t step = (int64_t)gridDim.x * P.ldx * XSZ;
       const unsigned char* csrc = BWD ? (const unsigned char*)P.ct + (int64_t)blockIdx.x * P.ldc * XSZ : nullptr;
       const int64_t cstep = (int64_t)gridDim.x * P.ldc * XSZ;
+      const long long drop = g_pipe_drop_row;
       for (int i = 0; i < n_local; ++i) {
         const int s = i % SX;
+        if (i == drop) break;                               // test hook: the copies from here on are "lost"
         if (i >= SX && !mbar_wait(&xempty[s], (uint32_t)((i / SX) - 1) & 1u)) { abort_flag = 1; break; }
         if (abort_flag) break;
         mbar_arrive_expect_tx(&xfull[s], xbytes);
@@ -1361,6 +1363,14 @@ extern "C" int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, i
   cudaStream_t s = (cudaStream_t)stream;
   return kind == PSK_NORM_RMS ? dispatch_norm_types<REGION_RMS>(P, xt, yt, pipe, s)
                               : dispatch_norm_types<REGION_LAYER>(P, xt, yt, pipe, s);
+}
+
+extern "C" int psk_test_drop_row(int64_t row) {
+  clear_error();
+  if (row < -1) return fail(PSK_E_ARG, "row %lld (-1 or a local row index)", (long long)row);
+  const long long v = row;
+  if (cudaMemcpyToSymbol(g_pipe_drop_row, &v, sizeof(v)) != cudaSuccess) return check_launch("test hook write");
+  return PSK_OK;
 }
 
 extern "C" int psk_device_status(uint32_t* status, int32_t reset) {

@@ -187,6 +187,12 @@ def psk_device_status(reset: bool = False) -> int:
     return v.value
 
 
+def psk_test_drop_row(row: int) -> None:
+    """Test hook: the pipelined row-region kernels stop producing at local row
+    `row` of every CTA (their bounded waits then run out); -1 turns it off."""
+    N.check(N.lib().psk_test_drop_row(int(row)))
+
+
 def _hparams(hp) -> N.psk_adamw_hparams:
     h = N.psk_adamw_hparams()
     h.lr, h.beta1, h.beta2 = float(hp.lr), float(hp.beta1), float(hp.beta2)

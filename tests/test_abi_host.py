@@ -212,6 +212,14 @@ def test_select_typing_refusals(native):
     assert e.value.name == "PSK_E_DTYPE"
 
 
+def test_test_hook_refuses_bad_rows(native):
+    from reduction_groups_gb300 import ops
+
+    with pytest.raises(native.PskError) as e:
+        ops.psk_test_drop_row(-2)
+    assert e.value.name == "PSK_E_ARG"
+
+
 def test_group_prepare_refuses_as_check(native):
     torch = pytest.importorskip("torch")
     from reduction_groups_gb300 import ops

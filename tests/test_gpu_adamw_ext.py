@@ -69,20 +69,27 @@ def test_ragged_unaligned_bf16_leaves_clipped(dev):
     rng = np.random.default_rng(9)
     hp = W.AdamWHyper(lr=1e-3, t=5)
     sizes = [1, 3, 1023, 1025, 4097, 64 * 1024 + 3, 0, 10007]
-    host, leaves = [], []
+    host, leaves, fulls = [], [], []
     for n in sizes:
-        th = (rng.standard_normal(n + 1) * 0.02).astype(np.float32)
-        m = (rng.standard_normal(n + 1) * 1e-3).astype(np.float32)
-        v = np.abs(rng.standard_normal(n + 1) * 1e-4).astype(np.float32)
-        g = f32_to_bf16((rng.standard_normal(n + 1) * 0.3).astype(np.float32))
-        host.append((th[1:], m[1:], v[1:], g[1:]))
-        leaves.append(tuple(_to_dev(a, "bf16" if k == 3 else "f32")[1:] for k, a in enumerate((th, m, v, g))))
+        # one element before and 64 after each leaf: canaries the step must not touch
+        th = (rng.standard_normal(n + 65) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n + 65) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n + 65) * 1e-4).astype(np.float32)
+        g = f32_to_bf16((rng.standard_normal(n + 65) * 0.3).astype(np.float32))
+        host.append((th[1:n + 1], m[1:n + 1], v[1:n + 1], g[1:n + 1]))
+        full = tuple(_to_dev(a, "bf16" if k == 3 else "f32") for k, a in enumerate((th, m, v, g)))
+        fulls.append((full, (th, m, v)))
+        leaves.append(tuple(t[1:n + 1] for t in full))
     want, scale = OA.step_tree_scheduled(host, "bf16", hp, "linear", 2, 9, grad_clip=0.5)
     assert scale < 1
     ws = _workspace(dev, leaves, kind="linear", warmup=2, total=9, grad_clip=0.5)
     dev.psk_adamw_tree_ex(leaves, hp, "linear", 2, 9, 0.5, ws)
     torch.cuda.synchronize()
     _check(leaves, want)
+    for (full, orig), n in zip(fulls, sizes):
+        for t, o in zip(full[:3], orig):
+            h = _to_host(t)
+            assert h[0] == o[0] and np.array_equal(h[n + 1:], o[n + 1:]), "a store landed outside a leaf"
 
 
 def test_two_layer_llama_tree_clipped_sampled(dev):

@@ -7,6 +7,7 @@ import pytest
 
 import oracle.norm as ON
 from synth import workloads as W
+from tests.guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -55,11 +56,13 @@ def _case(rows, cols, kind, xt, yt, pt, seed, eps=None):
 
 def _run(dev, wl, x, g, b, order, y=None):
     xd = _to_dev(x, wl.x_dtype)
-    if y is None:
-        y = torch.full(x.shape, float("nan"), dtype=torch.bfloat16 if wl.y_dtype == "bf16" else torch.float32,
-                       device="cuda")
+    gy = None
+    if y is None:                # NaN-poisoned, canaries around it
+        gy = guarded(x.shape, torch.bfloat16 if wl.y_dtype == "bf16" else torch.float32)
+        y = gy.tensor
     dev.psk_norm_region(xd, y, wl.kind, wl.eps, _to_dev(g, wl.param_dtype), _to_dev(b, wl.param_dtype), order)
     torch.cuda.synchronize()
+    assert gy is None or gy.intact(), "a store landed outside the output"
     return _to_host(y)
 
 

@@ -15,6 +15,7 @@ import oracle.group as OG
 import oracle.softmax as OS
 from oracle.f32 import bf16_to_f32, f32_to_bf16
 from synth import workloads as W
+from tests.guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +57,11 @@ def _run_group(R, wl, inputs_host, out_shape=None):
     out_shape = out_shape or wl.out_shape
     dts = [dt for _, dt in inputs_host]
     dins = [(_to_dev(a, dt), spec.strides) for (a, dt), spec in zip(inputs_host, wl.inputs)]
-    out = torch.empty(out_shape, dtype=torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32, device="cuda")
-    out.fill_(float("nan"))     # poisoned: every element must be written
+    g = guarded(out_shape, torch.bfloat16 if wl.out_dtype == "bf16" else torch.float32)
+    out = g.tensor              # poisoned: every element must be written; canaries around it
     R.psk_group_run(wl.tokens, wl.imm, dins, out)
     torch.cuda.synchronize()
+    assert g.intact(), "a store landed outside the output"
     return _to_host(out)
 
 
@@ -134,9 +136,11 @@ def test_random_programs_all_ops_bitwise(dev, seed):
     col = (rng.standard_normal(R_) * 2).astype(np.float32)
     inputs = [(x, "f32", (C_, 1)), (rowv, "f32", (0, 1)), (col, "f32", (1, 0))]
     want = OG.evaluate(toks, imm, inputs, (R_, C_), "f32")
-    out = torch.empty((R_, C_), dtype=torch.float32, device="cuda")
+    g = guarded((R_, C_), torch.float32)
+    out = g.tensor
     dev.psk_group_run(toks, imm, [(_to_dev(a, dt), st) for a, dt, st in inputs], out)
     torch.cuda.synchronize()
+    assert g.intact()
     ok = _same(_to_host(out), want, "f32")
     assert ok.all(), f"{(~ok).sum()} differ"
 
@@ -177,9 +181,11 @@ def test_rank4_broadcast_and_gather_layouts(dev):
     sg = (5 * 7 * 24, 7 * 24, 24, 2)
     inputs = [(a, "f32", sa), (b, "f32", sb), (big, "f32", sg)]
     want = OG.evaluate(toks, [], inputs, shape, "bf16")
-    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    g = guarded(shape, torch.bfloat16)
+    out = g.tensor
     dev.psk_group_run(toks, [], [(_to_dev(x, dt), st) for x, dt, st in inputs], out)
     torch.cuda.synchronize()
+    assert g.intact()
     assert _same(_to_host(out), want, "bf16").all()
 
 
@@ -250,9 +256,11 @@ def test_softmax_exact_bitwise(dev, order, shape):
     x = wl.host_x()
     want = OS.softmax_region(x, "bf16", "bf16", order)
     xd = _to_dev(x, "bf16")
-    y = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    gy = guarded(shape, torch.bfloat16)
+    y = gy.tensor
     dev.psk_softmax_region(xd, y, order, "exact")
     torch.cuda.synchronize()
+    assert gy.intact(), "a store landed outside the output"
     ok = _same(_to_host(y), want, "bf16")
     assert ok.all(), f"{(~ok).sum()} differ"
 
@@ -275,11 +283,13 @@ def test_softmax_many_rows_per_cta_bitwise(dev, rows, cols, order, yt):
     wl = W.softmax_rows(rows, cols)
     x = wl.host_x()
     want = OS.softmax_region(x, "bf16", yt, order)
-    y = torch.empty((rows, cols), dtype=torch.bfloat16 if yt == "bf16" else torch.float32, device="cuda")
+    gy = guarded((rows, cols), torch.bfloat16 if yt == "bf16" else torch.float32)
+    y = gy.tensor
     dev.psk_device_status(reset=True)
     for mode in ("exact", "fast"):
         dev.psk_softmax_region(_to_dev(x, "bf16"), y, order, mode)
         torch.cuda.synchronize()
+        assert gy.intact(), "a store landed outside the output"
         got = _to_host(y)
         if mode == "exact":
             ok = _same(got, want, yt)

@@ -8,6 +8,7 @@ import pytest
 import oracle.softmax as OS
 from oracle.f32 import bf16_to_f32, f32_to_bf16
 from synth import workloads as W
+from tests.guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +43,23 @@ def _same(a, b, dtype):
     return (a.view(np.uint32) == b.view(np.uint32)) | (np.isnan(a) & np.isnan(b))
 
 
+_GUARDS = []
+
+
 def _empty(shape, dtype):
-    return torch.full(shape, float("nan"), dtype=torch.bfloat16 if dtype == "bf16" else torch.float32, device="cuda")
+    """A NaN-poisoned output with canaries around it (checked at teardown)."""
+    g = guarded(shape, torch.bfloat16 if dtype == "bf16" else torch.float32)
+    _GUARDS.append(g)
+    return g.tensor
+
+
+@pytest.fixture(autouse=True)
+def _canaries_intact():
+    _GUARDS.clear()
+    yield
+    torch.cuda.synchronize()
+    assert all(g.intact() for g in _GUARDS), "a store landed outside an output"
+    _GUARDS.clear()
 
 
 ORDERS = [("sequential",), ("interleaved", 8), ("interleaved", 3), ("interleaved", 40)]
@@ -181,3 +197,29 @@ def test_one_chain_long_rows_specials(dev):
     dev.psk_softmax_region(_to_dev(xs, "bf16"), y, ("sequential",), "exact")
     torch.cuda.synchronize()
     assert _same(_to_host(y), want, "f32").all()
+
+
+# ------------------------------------------------------ bounded waits
+def test_lost_copy_times_out_and_the_device_recovers(dev):
+    """The test hook makes every CTA's producer stop at its third row, as if
+    the copy were lost: the waits for it run out (about two seconds), the
+    kernel records the timeout in the status word and winds down, and the
+    next launch on the same context is correct again."""
+    rows, cols = 152 * 6, 512
+    wl = W.softmax_rows(rows, cols)
+    x = wl.host_x()
+    xd = _to_dev(x, "bf16")
+    y = _empty((rows, cols), "bf16")
+    dev.psk_device_status(reset=True)
+    try:
+        dev.psk_test_drop_row(2)
+        dev.psk_softmax_region(xd, y, ("interleaved", 8), "fast")
+        torch.cuda.synchronize()
+    finally:
+        dev.psk_test_drop_row(-1)
+    assert dev.psk_device_status(reset=True) & 1
+    want = OS.softmax_region(x, "bf16", "bf16", ("sequential",))
+    dev.psk_softmax_region(xd, y, ("sequential",), "exact")
+    torch.cuda.synchronize()
+    assert _same(_to_host(y), want, "bf16").all()
+    assert dev.psk_device_status() == 0
