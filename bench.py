@@ -46,6 +46,9 @@ def _args():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
     p.add_argument("--softmax-exp", choices=["exact", "fast"], default="fast",
                    help="exp of the softmax region inside the step (the other mode is timed beside it)")
+    p.add_argument("--group-math", choices=["exact", "fast"], default="fast",
+                   help="realization of the group's exp / erf / gelu nodes inside the step (the other mode is "
+                        "timed beside it)")
     p.add_argument("--only", choices=["all", "group", "softmax", "adamw", "norm"], default="all",
                    help="time one case only (profiling captures)")
     p.add_argument("--scale", type=float, default=1.0,
@@ -268,8 +271,9 @@ def run_ours(a, ws, rank, local):
     b_soft = sw.algorithmic_bytes()
     b_adam = tree.n_params * tree.bytes_per_param()
     em = a.softmax_exp
+    gm = a.group_math
     launches = {
-        "group": lambda: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out),
+        "group": lambda: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out, math=gm),
         "softmax_sequential": lambda: R.psk_softmax_region(sx, sy, ("sequential",), em),
         "softmax_interleaved8": lambda: R.psk_softmax_region(sx, sy, ("interleaved", 8), em),
         "adamw": lambda: R.psk_adamw_tree(leaves, tree.hp),
@@ -305,6 +309,11 @@ def run_ours(a, ws, rank, local):
                                                                                                      order))
             b_all[f"softmax_backward_{oname}"] = 3 * sw.rows * sw.cols * 2
     if a.only in ("all", "group"):
+        # the 64-node group in the other math mode, beside the step
+        g_other = "exact" if gm == "fast" else "fast"
+        extra_launches[f"group_{g_other}_math"] = lambda: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out,
+                                                                          math=g_other)
+        b_all[f"group_{g_other}_math"] = b_group
         # the extended op set (LOG, TANH, RECIP, SELECT on an int32 mask) on the
         # group's shape
         xw = W.select_group(rows=max(1, int(8192 * sc)))
@@ -423,7 +432,7 @@ def run_ours(a, ws, rank, local):
             slices.append(cur)
         units = []      # (copies in, kernels, copies out) as (device, host) pairs and a launch list
         units.append(([(d_, h_) for d_, h_ in zip(g_in, host_g)],
-                      [lambda st: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out, st)],
+                      [lambda st: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out, st, math=gm)],
                       [(g_out, host_gout)]))
         units.append(([(sx, host_sx)],
                       [lambda st: R.psk_softmax_region(sx, sy, ("sequential",), em, st),
@@ -506,6 +515,9 @@ def run_ours(a, ws, rank, local):
         if k == "group_select_log_tanh":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["elems_per_s"] = round(xw.out_shape[0] * xw.out_shape[1] / (ms / 1e3), 1)
+        if k.startswith("group_") and k.endswith("_math"):
+            del kinfo[k]["rows_per_s"]
+            kinfo[k]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (ms / 1e3), 1)
     for k in extra_launches:
         if k in kernels:
             kinfo[k]["rows_per_s"] = round(norm_rows / (per_kernel_ms[k] / 1e3), 1)
@@ -519,7 +531,7 @@ def run_ours(a, ws, rank, local):
         kinfo["adamw"]["params_per_s"] = round(tree.n_params / (per_kernel_ms["adamw"] / 1e3), 1)
     dom = max(kernels, key=lambda k: per_kernel_ms[k])
     ipeak, mhz = _issue_peak()
-    winst = _counter("group", "warp_instructions") if "group" in kernels and a.scale == 1.0 else None
+    winst = _counter("group", f"warp_instructions_{gm}") if "group" in kernels and a.scale == 1.0 else None
     if winst is not None:
         ach = winst / (per_kernel_ms["group"] / 1e3) / 1e9
         kinfo["group"]["issue_rate_gwarp_instr_s"] = round(ach, 1)
@@ -553,7 +565,7 @@ def run_ours(a, ws, rank, local):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded device draws, shapes of the workloads)",
         "config": {"workload": "64-node group bf16 [8192,8192] + softmax region bf16 [32768,4096] "
                                "(sequential, interleaved(8)) + AdamW tree of a Llama-style 1.1B model",
-                   "softmax_exp": em, "l2": "inputs larger than L2 (no flush needed)",
+                   "softmax_exp": em, "group_math": gm, "l2": "inputs larger than L2 (no flush needed)",
                    "bytes_per_step": int(bytes_step), "parallelism": f"replicas x{ws}"},
         "kernels": kinfo, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         "gpu_launches": len(kernels) * a.steps,

@@ -171,6 +171,21 @@ int psk_group_check(const psk_program* prog, int32_t n_inputs, int32_t* n_nodes,
  * with the compiler's message. */
 int psk_group_prepare(const psk_program* prog, const psk_input* inputs, int32_t n_inputs, const psk_output* out);
 
+/* psk_group_run / psk_group_prepare with a math mode (a psk_exp_mode, below):
+ * PSK_EXP_EXACT is psk_group_run itself (every node correctly rounded);
+ * PSK_EXP_FAST is a declared fast realization of the EXP, EXPC, ERF and GELU
+ * nodes: exp within one f32 ulp and erf within two of the correctly rounded
+ * values (measured over every float of their ranges), gelu's f32 chain
+ * unchanged around the faster erf (so its error is erf's, two ulp of 1,
+ * scaled by |a| / 2, which near gelu's negative tail is large relative to a
+ * tiny result).  LOG and TANH stay correctly rounded.  Not bit-identical to
+ * the oracle; on the 64-node workload 4 outputs in 10^6 differ, by one bf16
+ * ulp.  PSK_E_ARG for another mode; otherwise as psk_group_run. */
+int psk_group_run_ex(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
+                     const psk_output* out, int32_t math_mode, void* stream);
+int psk_group_prepare_ex(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
+                         const psk_output* out, int32_t math_mode);
+
 /* ================================================== psk_softmax_region
  * y[r, :] = softmax(x[r, :]) over rows of `cols` elements: m = max_j x[r,j]
  * (NaN propagates), e_j = exp(x[r,j] - m), s = the sum of e_j in the declared

@@ -612,6 +612,69 @@ PSK_HD float exp_faithful(float x) {
   return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
 }
 
+// ====================================== faithful exp and erf for groups
+// A group's declared fast realization of its EXP, EXP-clamp, ERF and GELU
+// nodes (math mode FAST): each within two f32 ulp of the correctly rounded
+// value (measured over their ranges by the host tests), not correctly
+// rounded and not bit-identical to the oracle.
+
+// exp on |x| <= 88 without special cases: Cody-Waite reduction to |r| <=
+// ln2/2, degree-7 Taylor polynomial, 2^k applied to the exponent field (k in
+// [-127, 127]: normal results down to x = -87.3; below, the bit add would
+// leave the normal range, so callers clamp or use exp_fast).
+PSK_HD float exp_fast_mid(float x) {
+  const float kf = rintf(x * PSK_FEXP_INV_LN2);
+  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);         // exact: ln2 hi carries 16 bits
+  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  return u2f((uint32_t)((int32_t)f2u(p) + ((int)kf << 23)));
+}
+
+// exp over every f32: x clamped to [-104.5, 89] (beyond, the result is 0 or
+// infinity either way), 2^k applied in two exact halves and one rounding at
+// the end (subnormal and overflowing results included), NaN passed through.
+PSK_HD float exp_fast(float x) {
+  const float xc = fminf(fmaxf(x, -104.5f), 89.0f);
+  const float kf = rintf(xc * PSK_FEXP_INV_LN2);
+  float r = fmaf(-kf, PSK_FEXP_LN2_HI, xc);
+  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  const int k = (int)kf;                           // -151 .. 128
+  const int k1 = k >> 1, k2 = k - k1;              // each in [-76, 64]: 2^k1, 2^k2 normal
+  const float y = (p * u2f((uint32_t)(k1 + 127) << 23)) * u2f((uint32_t)(k2 + 127) << 23);
+  return x == x ? y : x;
+}
+
+// erf of a = |x| from the correctly rounded erf's Taylor tables (their
+// binary32 coefficients, the pairs' high parts) by plain binary32 Horner; a
+// past PSK_ERF_ONE_FROM gives 1.  p2 / h as for erf_tier1_core.
+PSK_HD float erf_fast_abs(float a, const float* p2, const float* h) {
+  const float ac = fminf(a, 3.9f);
+  const float fi = rintf(ac * 32.0f);
+  const int i = (int)fi;
+  const float t = fmaf(fi, -0.03125f, ac);         // exact
+  float H = h[(PSK_ERF_D32 - PSK_ERF_NPAIR) * PSK_ERF_N32 + i];
+#pragma unroll
+  for (int k = PSK_ERF_D32 - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
+#pragma unroll
+  for (int k = PSK_ERF_NPAIR - 1; k >= 0; --k) H = fmaf(H, t, p2[k * 2 * PSK_ERF_N32 + 2 * i]);
+  return a >= PSK_ERF_ONE_FROM ? 1.0f : H;
+}
+
 // The same faithful exp for x <= 0, NaN or -inf (the softmax region's
 // x - max), without branches: 2^k is applied as 2^(k+64) and then 2^-64 (one
 // rounding, in the second product, where the result is subnormal; exact

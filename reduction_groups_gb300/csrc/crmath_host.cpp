@@ -9,7 +9,8 @@ using namespace psk;
 
 extern "C" {
 
-// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr
+// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
+// 6 erf_fast (signed), 7 exp_fast_mid
 void psk_host_unary(int which, const float* x, float* y, long n) {
   for (long i = 0; i < n; ++i) {
     switch (which) {
@@ -17,6 +18,14 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
       case 1: y[i] = erf_cr(x[i], &psk_erf_p2[0][0], &psk_erf_h[0][0]); break;
       case 3: y[i] = log_cr(x[i], psk_log_tab); break;
       case 4: y[i] = tanh_cr(x[i], &psk_tanh_p2[0][0], &psk_tanh_h[0][0]); break;
+      case 5: y[i] = exp_fast(x[i]); break;
+      case 6: {
+        const float a = fabsf(x[i]);
+        const float r = a == a ? erf_fast_abs(a, &psk_erf_p2[0][0], &psk_erf_h[0][0]) : a;
+        y[i] = copysignf(r, x[i]);
+        break;
+      }
+      case 7: y[i] = exp_fast_mid(x[i]); break;
       default: y[i] = exp_faithful(x[i]); break;
     }
   }

@@ -320,6 +320,45 @@ __device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
   return r;
 }
 
+// The fast realization (math mode FAST) of the same four nodes: faithful exp
+// (at most one ulp; the clamped argument needs no special cases) and erf (at
+// most two ulp) from the same tables; gelu's chain is unchanged around it.
+template <int V, bool CLAMP>
+__device__ __noinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    float a = A.v[j];
+    if (CLAMP) {
+      a = a > -4.0f ? a : -4.0f;
+      a = a < 4.0f ? a : 4.0f;
+      r.v[j] = exp_fast_mid(a);
+    } else {
+      r.v[j] = exp_fast(a);
+    }
+  }
+  return r;
+}
+
+template <int V, bool GELU>
+__device__ __noinline__ Vec<V> node_erf_fast_any(Vec<V> A, const MathTables& tab) {
+  Vec<V> r;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const float t = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
+    const float aa = fabsf(t);
+    float e = erf_fast_abs(aa, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h);
+    e = t == t ? copysignf(e, t) : t;
+    r.v[j] = GELU ? __fmul_rn(A.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, e))) : e;
+  }
+  return r;
+}
+
+template <int V> __device__ __forceinline__ Vec<V> node_exp_fast(const Vec<V>& a, const MathTables&) { return node_exp_fast_any<V, false>(a); }
+template <int V> __device__ __forceinline__ Vec<V> node_expc_fast(const Vec<V>& a, const MathTables&) { return node_exp_fast_any<V, true>(a); }
+template <int V> __device__ __forceinline__ Vec<V> node_erf_fast(const Vec<V>& a, const MathTables& t) { return node_erf_fast_any<V, false>(a, t); }
+template <int V> __device__ __forceinline__ Vec<V> node_gelu_fast(const Vec<V>& a, const MathTables& t) { return node_erf_fast_any<V, true>(a, t); }
+
 template <int V> __device__ __forceinline__ Vec<V> node_exp(const Vec<V>& a, const MathTables& t) { return node_exp_any<V, false>(a, t); }
 template <int V> __device__ __forceinline__ Vec<V> node_expc(const Vec<V>& a, const MathTables& t) { return node_exp_any<V, true>(a, t); }
 template <int V> __device__ __forceinline__ Vec<V> node_erf(const Vec<V>& a, const MathTables& t) { return node_erf_any<V, false>(a, t); }

@@ -75,21 +75,25 @@ def _group_args(inputs, out):
     return arr, n, o
 
 
-def psk_group_prepare(tokens, imm, inputs, out) -> None:
+_MATH = {"exact": 0, "fast": 1}
+
+
+def psk_group_prepare(tokens, imm, inputs, out, math: str = "exact") -> None:
     """Validate and compile (cached) the kernel psk_group_run would launch for
     these arguments; needs no device (tensors are inspected, not read)."""
     p, keep = _program(tokens, imm)
     arr, n, o = _group_args(inputs, out)
-    N.check(N.lib().psk_group_prepare(ctypes.byref(p), arr, n, ctypes.byref(o)))
+    N.check(N.lib().psk_group_prepare_ex(ctypes.byref(p), arr, n, ctypes.byref(o), _MATH[math]))
 
 
-def psk_group_run(tokens, imm, inputs, out, stream=None) -> None:
+def psk_group_run(tokens, imm, inputs, out, stream=None, math: str = "exact") -> None:
     """inputs: list of (tensor, strides) with one element stride per output axis
     (0 = broadcast), f32 or bf16 values or int32 SELECT conditions; out: a
-    contiguous row-major tensor (f32 or bf16)."""
+    contiguous row-major tensor (f32 or bf16).  math "exact" (every node
+    correctly rounded) or "fast" (faithful exp / erf in EXP, EXPC, ERF, GELU)."""
     p, keep = _program(tokens, imm)
     arr, n, o = _group_args(inputs, out)
-    N.check(N.lib().psk_group_run(ctypes.byref(p), arr, n, ctypes.byref(o), _stream_handle(stream)))
+    N.check(N.lib().psk_group_run_ex(ctypes.byref(p), arr, n, ctypes.byref(o), _MATH[math], _stream_handle(stream)))
 
 
 _ORDER = {"sequential": N.PSK_ORDER_SEQUENTIAL, "blocked": N.PSK_ORDER_BLOCKED,

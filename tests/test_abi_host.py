@@ -212,6 +212,21 @@ def test_select_typing_refusals(native):
     assert e.value.name == "PSK_E_DTYPE"
 
 
+def test_group_prepare_compiles_the_fast_math_mode(native):
+    torch = pytest.importorskip("torch")
+    from reduction_groups_gb300 import ops
+
+    toks = W.encode([("IN", 0), ("EXP",), ("EXPC",), ("ERF",), ("GELU",), ("LOG",), ("TANH",)])
+    x = torch.zeros(8, 16)
+    ops.psk_group_prepare(toks, None, [(x, (16, 1))], torch.zeros(8, 16), math="fast")
+    ops.psk_group_prepare(toks, None, [(x, (16, 1))], torch.zeros(8, 16, dtype=torch.bfloat16), math="fast")
+    from reduction_groups_gb300 import _native as N
+
+    p, keep = ops._program(toks, None)
+    arr, n, o = ops._group_args([(x, (16, 1))], torch.zeros(8, 16))
+    assert N.lib().psk_group_prepare_ex(ctypes.byref(p), arr, n, ctypes.byref(o), 7) == -9   # PSK_E_ARG
+
+
 def test_test_hook_refuses_bad_rows(native):
     from reduction_groups_gb300 import ops
 

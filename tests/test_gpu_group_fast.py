@@ -1,0 +1,128 @@
+"""The fast math mode of groups (psk_group_run_ex, PSK_EXP_FAST) against the
+correctly rounded oracle, within its declared tolerance: EXP and EXPC nodes
+within one f32 ulp, ERF within two, GELU within two ulp of its result plus
+erf's two ulp of 1 carried through its chain (|a| 2^-23), the same NaNs and
+infinities everywhere; on the 64-node workload every output within one bf16
+ulp of the oracle's and almost all identical.
+"""
+
+import numpy as np
+import pytest
+
+import oracle.group as OG
+from oracle.f32 import bf16_to_f32
+from synth import workloads as W
+from tests.guard import guarded
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import reduction_groups_gb300 as R
+
+    return R
+
+
+def _to_dev(a, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _to_host(t):
+    if t.dtype == torch.bfloat16:
+        return t.cpu().view(torch.int16).numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def _ordinal(bits, sign_bit):
+    b = bits.astype(np.int64)
+    mag = b & (sign_bit - 1)
+    return np.where(b & sign_bit, -mag, mag)
+
+
+def _ulps32(a, b):
+    return np.abs(_ordinal(a.view(np.uint32), 1 << 31) - _ordinal(b.view(np.uint32), 1 << 31))
+
+
+def _inputs(op, n, rng):
+    if op in ("EXP",):
+        x = rng.uniform(-110, 95, n)
+    elif op == "EXPC":
+        x = rng.uniform(-6, 6, n)
+    else:
+        x = rng.uniform(-6, 6, n)
+    x = x.astype(np.float32)
+    x[: n // 4] = rng.integers(0, 2 ** 32, n // 4, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    x[:16] = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 88.72283935546875, 88.7228317,
+                       -103.97208, 3.9192059, 2 ** -60, 2 ** -61, 87.0, -87.0, 1.0], dtype=np.float32)
+    return x
+
+
+@pytest.mark.parametrize("op,ulps", [("EXP", 1), ("EXPC", 1), ("ERF", 2), ("GELU", 2)])
+def test_fast_node_within_its_tolerance(dev, op, ulps):
+    rng = np.random.default_rng(81)
+    n = (1 << 22) + 5
+    x = _inputs(op, n, rng)
+    toks = W.encode([("IN", 0), (op,)])
+    want = OG.evaluate(toks, [], [(x, "f32", (1,))], (n,), "f32")
+    g = guarded((n,), torch.float32)
+    dev.psk_group_run(toks, [], [(_to_dev(x, "f32"), (1,))], g.tensor, math="fast")
+    torch.cuda.synchronize()
+    assert g.intact()
+    got = _to_host(g.tensor)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(np.isinf(got[fin]), np.isinf(want[fin]))
+    u = _ulps32(got[fin], want[fin])
+    if op == "GELU":
+        # erf's two ulp of 1 pass through 0.5 (1 + e) and the product by a
+        slack = np.abs(x[fin].astype(np.float64)) * 2.0 ** -23
+        bad = (u > ulps) & (np.abs(got[fin].astype(np.float64) - want[fin]) > slack)
+        assert not bad.any(), f"{bad.sum()} beyond tolerance, e.g. x={x[fin][bad][:4]}"
+    else:
+        assert u.max() <= ulps, f"max {u.max()} ulp at x={x[fin][np.argmax(u)]}"
+
+
+@pytest.mark.parametrize("shape", [(96, 200), (37, 53), (130, 1024)])
+def test_fast_cap_group_within_one_bf16_ulp(dev, shape):
+    wl = W.cap_group(*shape)
+    ins = wl.host_inputs()
+    want = OG.evaluate(wl.tokens, wl.imm, [(a, dt, s.strides) for (a, dt), s in zip(ins, wl.inputs)], wl.out_shape,
+                       "bf16")
+    g = guarded(wl.out_shape, torch.bfloat16)
+    dins = [(_to_dev(a, dt), s.strides) for (a, dt), s in zip(ins, wl.inputs)]
+    dev.psk_group_run(wl.tokens, wl.imm, dins, g.tensor, math="fast")
+    torch.cuda.synchronize()
+    assert g.intact()
+    got = _to_host(g.tensor)
+    both_nan = np.isnan(bf16_to_f32(got)) & np.isnan(bf16_to_f32(want))
+    d = np.abs(_ordinal(got, 1 << 15) - _ordinal(want, 1 << 15))
+    d[both_nan] = 0
+    assert d.max() <= 1 and (d > 0).mean() < 1e-3
+
+
+def test_fast_cap_group_full_size_sampled_rows(dev):
+    """The 64-node workload at full size [8192, 8192] in the fast mode, as the
+    benchmark launches it; sampled rows within one bf16 ulp of the oracle."""
+    wl = W.cap_group()
+    dins = wl.device_inputs()
+    out = torch.empty(wl.out_shape, dtype=torch.bfloat16, device="cuda")
+    dev.psk_group_run(wl.tokens, wl.imm, [(t, s.strides) for t, s in zip(dins, wl.inputs)], out, math="fast")
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 4095, 8191] + list(np.random.default_rng(3).integers(0, 8192, 12)))
+    idx = torch.from_numpy(rows).cuda()
+    x = _to_host(dins[0][idx])
+    ins = [(x, "bf16", (8192, 1)), (_to_host(dins[1]), "bf16", (0, 1)), (_to_host(dins[2]).reshape(-1)[rows], "bf16", (1, 0)),
+           (_to_host(dins[3]).reshape(1), "bf16", (0, 0))]
+    want = OG.evaluate(wl.tokens, wl.imm, ins, (len(rows), 8192), "bf16")
+    got = _to_host(out[idx])
+    both_nan = np.isnan(bf16_to_f32(got)) & np.isnan(bf16_to_f32(want))
+    d = np.abs(_ordinal(got, 1 << 15) - _ordinal(want, 1 << 15))
+    d[both_nan] = 0
+    assert d.max() <= 1 and (d > 0).mean() < 1e-3
