@@ -323,8 +323,10 @@ __device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
 // The fast realization (math mode FAST) of the same four nodes: faithful exp
 // (at most one ulp; the clamped argument needs no special cases) and erf (at
 // most two ulp) from the same tables; gelu's chain is unchanged around it.
+// Short enough to inline at every node (1.22 -> 1.11 ms on the 64-node group
+// against one out-of-line copy each).
 template <int V, bool CLAMP>
-__device__ __noinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
+__device__ __forceinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
   Vec<V> r;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
@@ -341,7 +343,7 @@ __device__ __noinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
 }
 
 template <int V, bool GELU>
-__device__ __noinline__ Vec<V> node_erf_fast_any(Vec<V> A, const MathTables& tab) {
+__device__ __forceinline__ Vec<V> node_erf_fast_any(Vec<V> A, const MathTables& tab) {
   Vec<V> r;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
