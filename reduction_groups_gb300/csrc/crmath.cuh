@@ -660,16 +660,20 @@ PSK_HD float exp_fast(float x) {
 }
 
 // erf of a = |x| from the correctly rounded erf's Taylor tables (their
-// binary32 coefficients, the pairs' high parts) by plain binary32 Horner; a
+// binary32 coefficients, the pairs' high parts) by plain binary32 Horner of
+// degree DF (4 is enough for two ulp: the higher terms stay below 2^-30 of
+// erf on an interval of width 1/32; measured over every float of [0, 5]); a
 // past PSK_ERF_ONE_FROM gives 1.  p2 / h as for erf_tier1_core.
+constexpr int ERF_FAST_DEGREE = 4;
+template <int DF = ERF_FAST_DEGREE>
 PSK_HD float erf_fast_abs(float a, const float* p2, const float* h) {
   const float ac = fminf(a, 3.9f);
   const float fi = rintf(ac * 32.0f);
   const int i = (int)fi;
   const float t = fmaf(fi, -0.03125f, ac);         // exact
-  float H = h[(PSK_ERF_D32 - PSK_ERF_NPAIR) * PSK_ERF_N32 + i];
+  float H = h[(DF - PSK_ERF_NPAIR) * PSK_ERF_N32 + i];
 #pragma unroll
-  for (int k = PSK_ERF_D32 - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
+  for (int k = DF - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
 #pragma unroll
   for (int k = PSK_ERF_NPAIR - 1; k >= 0; --k) H = fmaf(H, t, p2[k * 2 * PSK_ERF_N32 + 2 * i]);
   return a >= PSK_ERF_ONE_FROM ? 1.0f : H;

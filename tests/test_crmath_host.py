@@ -235,3 +235,33 @@ def test_log_tanh_tier1_relative_error(hm):
     a = a[(a >= 2.0 ** -12) & (a < 9.0109)]
     rel = np.abs(value(3, a) / np.tanh(a.astype(np.float64)) - 1)
     assert rel.max() < 2.0 ** -44, np.log2(rel.max())
+
+
+# ------------------------------------------- the groups' fast math mode
+
+def _ulps(a, b):
+    def ordv(x):
+        b_ = x.view(np.int32).astype(np.int64)
+        return np.where(b_ < 0, -(b_ & 0x7FFFFFFF), b_)
+    return np.abs(ordv(a) - ordv(b))
+
+
+def test_fast_exp_and_erf_within_their_bounds(hm):
+    """The fast mode's exp (one ulp) and erf (two ulp) against the correctly
+    rounded oracle; measured over every float of their ranges the bounds are
+    exactly 1 and 2."""
+    unary, _ = hm
+    rng = np.random.default_rng(61)
+    sp = np.array([0.0, -0.0, np.inf, -np.inf, 88.72, 88.73, 89.0, -87.3, -103.97, -104.5, 1e-30, -1e-45],
+                  dtype=np.float32)
+    x = np.concatenate([rng.uniform(-110, 95, 1_000_000).astype(np.float32), _all_binades(-40, 6, 2000, 62), sp])
+    y, ref = unary(5, x), exp_f32(x)
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    assert _ulps(y, ref).max() <= 1
+    xm = rng.uniform(-4, 4, 500_000).astype(np.float32)
+    assert _ulps(unary(7, xm), exp_f32(xm)).max() <= 1
+    a = np.concatenate([rng.uniform(-6, 6, 1_000_000).astype(np.float32), _all_binades(-149 + 23, 2, 2000, 63), sp])
+    y, ref = unary(6, a), erf_f32(a)
+    ok = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    assert _ulps(y[ok], ref[ok]).max() <= 2
