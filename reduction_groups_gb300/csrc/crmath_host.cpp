@@ -4,14 +4,24 @@
 
 #define PSK_HOST_BUILD 1
 #include "crmath.cuh"
+#include "pair.cuh"
 
 using namespace psk;
 
 extern "C" {
 
 // which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
-// 6 erf_fast (signed), 7 exp_fast_mid
+// 6 erf_fast (signed), 7 exp_fast_mid, 8 the softmax region's pair exp
+// (x <= 0, taken two at a time)
 void psk_host_unary(int which, const float* x, float* y, long n) {
+  if (which == 8) {
+    for (long i = 0; i < n; i += 2) {
+      const f2 r = exp2_faithful_nonpos(f2{x[i], i + 1 < n ? x[i + 1] : 0.0f});
+      y[i] = r.x;
+      if (i + 1 < n) y[i + 1] = r.y;
+    }
+    return;
+  }
   for (long i = 0; i < n; ++i) {
     switch (which) {
       case 0: y[i] = exp_cr(x[i], psk_exp_tab2); break;
@@ -104,6 +114,26 @@ long psk_host_div_check(unsigned long seed, long n, float a_lo_exp, float a_hi_e
     if (div_by_recip(fa, fb, rb) != ieee) ++bad;
   }
   return bad;
+}
+
+// The pair exp against the correctly rounded exp over the floats t <= 0
+// whose bit patterns are 0x80000000 + i * stride for i * stride <= span
+// (t = -0 down to -(span)); returns the largest distance in ulps and stores
+// the first input that reaches it.
+long psk_host_exp_pair_maxulp(uint32_t span, uint32_t stride, float* worst) {
+  long maxd = 0;
+  for (uint64_t i = 0; i <= span; i += 2 * (uint64_t)stride) {
+    const float a = u2f(0x80000000u + (uint32_t)i);
+    const float b = u2f(0x80000000u + (uint32_t)(i + stride <= span ? i + stride : i));
+    const f2 r = exp2_faithful_nonpos(f2{a, b});
+    const float ra[2] = {r.x, r.y}, ta[2] = {a, b};
+    for (int q = 0; q < 2; ++q) {
+      const float want = exp_cr(ta[q], psk_exp_tab2);
+      const long d = labs((long)f2u(ra[q]) - (long)f2u(want));
+      if (d > maxd) { maxd = d; if (worst) *worst = ta[q]; }
+    }
+  }
+  return maxd;
 }
 
 }  // extern "C"

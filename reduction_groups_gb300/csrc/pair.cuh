@@ -1,0 +1,70 @@
+// Pairs of binary32 values for the sm_100-class packed f32x2 instructions
+// (fma / add / mul .rn.f32x2: one issue slot, two IEEE operations, each
+// rounded to nearest even with gradual underflow, exactly as two scalar
+// operations), and the softmax region's fast exp written on pairs.
+//
+// The same source compiles as plain C++ for the host (PSK_HOST_BUILD), where a
+// pair operation is the two scalar operations; the host tests measure the
+// pair exp's error over the floats of its range on that build.
+
+#pragma once
+
+#include "crmath.cuh"
+
+namespace psk {
+
+#if defined(PSK_HOST_BUILD)
+struct f2 {
+  float x, y;
+};
+PSK_HD f2 f2_fma(f2 a, f2 b, f2 c) { return f2{fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y)}; }
+PSK_HD f2 f2_add(f2 a, f2 b) { return f2{a.x + b.x, a.y + b.y}; }
+PSK_HD f2 f2_mul(f2 a, f2 b) { return f2{a.x * b.x, a.y * b.y}; }
+// max with NaN propagation (either operand NaN gives NaN)
+PSK_HD float fmax_nan(float a, float b) { return (a != a || b != b) ? (a + b) : (a > b ? a : b); }
+#else
+typedef float2 f2;
+PSK_HD f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+PSK_HD f2 f2_add(f2 a, f2 b) { return __fadd2_rn(a, b); }
+PSK_HD f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
+PSK_HD float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+#endif
+PSK_HD f2 f2_splat(float v) { return f2{v, v}; }
+
+// exp of a pair of t <= 0 (NaN and -inf allowed: the softmax region's x - max),
+// faithful: within one ulp of exp(t), subnormal results included.
+//   t is held at -104.5 (exp below it rounds to +0; -inf, whose reduction
+//   would be NaN, becomes that; NaN stays NaN);
+//   k = nearest integer to t / ln2 by one fma with 1.5 * 2^23 (the sum lands in
+//   the binade whose ulp is 1, so its low bits hold k);
+//   r = t - k ln2 in two fmas (Cody-Waite; ln2's high part has 16 bits, so
+//   k * hi is exact for |k| <= 151), |r| <= ln2 / 2;
+//   e^r by its degree-7 Taylor polynomial (Horner);
+//   2^k applied as 2^(k+64), an exact scaling, then 2^-64, the one rounding
+//   where the result is subnormal.  The exponent field of 2^(k+64) is the
+//   sum's bit pattern shifted left by 23 (its high bits fall out) plus 191.
+// Every step but the clamp and the exponent field is a pair operation.
+constexpr float PAIR_EXP_MAGIC = 12582912.0f;   // 1.5 * 2^23
+PSK_HD f2 exp2_faithful_nonpos(f2 t) {
+  const f2 tc{fmax_nan(t.x, -104.5f), fmax_nan(t.y, -104.5f)};
+  const f2 z = f2_fma(tc, f2_splat(PSK_FEXP_INV_LN2), f2_splat(PAIR_EXP_MAGIC));
+  const f2 kf = f2_add(z, f2_splat(-PAIR_EXP_MAGIC));
+  f2 r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_HI), tc);
+  r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_LO), r);
+  f2 p = f2_splat(1.0f / 5040.0f);
+  p = f2_fma(p, r, f2_splat(1.0f / 720.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 120.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 24.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 6.0f));
+  p = f2_fma(p, r, f2_splat(0.5f));
+  p = f2_fma(p, r, f2_splat(1.0f));
+  p = f2_fma(p, r, f2_splat(1.0f));
+  const f2 s{u2f(f2u(z.x) * (1u << 23) + (191u << 23)), u2f(f2u(z.y) * (1u << 23) + (191u << 23))};
+  return f2_mul(f2_mul(p, s), f2_splat(0x1p-64f));
+}
+
+}  // namespace psk

@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "crmath.cuh"
 #include "pipe.cuh"
+#include "pair.cuh"
 
 namespace psk {
 
@@ -70,6 +71,14 @@ struct RegionParams {
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// The same on a pair of bf16 values (exact: the max of widened bf16 values
+// is a bf16 value).
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -521,7 +530,8 @@ constexpr int PIPE_TT = PIPE_TW * 32;                        // threads per team
 constexpr int PIPE_EPT = SM_CAP / PIPE_TT;                   // row elements per team thread (32)
 constexpr int PIPE_KW = 3;                                   // chain warps
 constexpr int PIPE_THREADS = (PIPE_CW + PIPE_KW + 1) * 32;   // + producer warp
-constexpr int PIPE_SX_MAX = 8;                               // x ring slots
+constexpr int PIPE_SX_MAX = 16;                              // x ring slots (barrier arrays)
+constexpr int PIPE_SX_DEEP = 8;                              // the deep x ring of the default depths
 constexpr int PIPE_SE_MAX = 16;                              // value ring slots (a multiple of the teams)
 constexpr size_t PIPE_SMEM_BUDGET = 225 * 1024;              // dynamic shared memory of one CTA
 
@@ -730,6 +740,9 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
 
   constexpr uint32_t XSZ = XT == PSK_F32 ? 4u : 2u;
   constexpr bool BWD = KIND == REGION_SOFTMAX_BWD;
+  // fast softmax over bf16 rows: the max on the stored pairs, exp and the
+  // division on f32 pairs
+  constexpr bool FASTSM = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_FAST && XT == PSK_BF16 && !MASK;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cols = (int)P.cols;
   const uint32_t rbytes = (uint32_t)cols * XSZ;               // one stored row
@@ -863,9 +876,20 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       }
       if (!dead && !mbar_wait(&xfull[s], (uint32_t)(i / SX) & 1u)) { abort_flag = 1; dead = true; }
       const unsigned char* xs = X + (size_t)s * xslot;
-      float v[PIPE_EPT];
+      float v[FASTSM ? 1 : PIPE_EPT];
+      uint2 xw[FASTSM ? PIPE_EPT / 4 : 1];                   // fast softmax: the row's bf16 pairs as stored
       float m = -INFINITY;
       int any = 0;
+      if constexpr (FASTSM) {
+        uint32_t mb = 0xFF80FF80u;                           // (-inf, -inf)
+#pragma unroll
+        for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+          const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+          xw[c4] = (j < cols && !dead) ? *reinterpret_cast<const uint2*>(xs + 2 * j) : make_uint2(0xFF80FF80u, 0xFF80FF80u);
+          mb = bf16x2_max_nan(mb, bf16x2_max_nan(xw[c4].x, xw[c4].y));
+        }
+        m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
+      } else {
 #pragma unroll
       for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
@@ -893,6 +917,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
           for (int q = 0; q < 4; ++q) m = max_nan(m, v[4 * c4 + q]);
         }
       }
+      }
       if (KIND == REGION_SOFTMAX) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -917,7 +942,21 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       if (tt == 0) mbar_arrive(&xempty[s]);
       const int se = i % SE;
       float* Er = E + (size_t)se * estride;
-      if (!dead) {
+      if (FASTSM && !dead) {
+        // e = exp(x - m) two at a time: x - m as x + (-m) (the same rounding)
+        const f2 nm = f2_splat(-m);
+#pragma unroll
+        for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+          const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+          if (j < cols) {
+            const f2 a = exp2_faithful_nonpos(f2_add(
+                f2{__uint_as_float(xw[c4].x << 16), __uint_as_float(xw[c4].x & 0xFFFF0000u)}, nm));
+            const f2 b = exp2_faithful_nonpos(f2_add(
+                f2{__uint_as_float(xw[c4].y << 16), __uint_as_float(xw[c4].y & 0xFFFF0000u)}, nm));
+            *reinterpret_cast<float4*>(Er + j) = make_float4(a.x, a.y, b.x, b.y);
+          }
+        }
+      } else if (!dead) {
 #pragma unroll
         for (int h = 0; h < PIPE_EPT / 8; ++h) {
           float u[8];
@@ -961,6 +1000,32 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       if (!mbar_wait(&sready[se], par)) { abort_flag = 1; dead = true; continue; }
       const float sm = rowsum[se], rs = rowrcp[se];
       const bool fast_ok = sm >= 1.0f && sm < 0x1p20f;
+      if (FASTSM && fast_ok) {
+        // Markstein's correction two at a time; exp values below 2^-100 are
+        // not sent to IEEE division here (their quotient may be an ulp off,
+        // within the fast realization's tolerance)
+        const f2 rs2 = f2_splat(rs), ns2 = f2_splat(-sm);
+#pragma unroll
+        for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
+          const int j = c4 * (PIPE_TT * 4) + 4 * tt;
+          if (j < cols) {
+            const float4 e = *reinterpret_cast<const float4*>(Er + j);
+            const f2 ea{e.x, e.y}, eb{e.z, e.w};
+            const f2 qa = f2_mul(ea, rs2), qb = f2_mul(eb, rs2);
+            const f2 ya = f2_fma(f2_fma(qa, ns2, ea), rs2, qa);
+            const f2 yb = f2_fma(f2_fma(qb, ns2, eb), rs2, qb);
+            if (YT == PSK_F32) {
+              __stcs(reinterpret_cast<float4*>(yr) + (j >> 2), make_float4(ya.x, ya.y, yb.x, yb.y));
+            } else {
+              uint2 q;
+              q.x = f32x2_to_bf16x2(ya.x, ya.y);
+              q.y = f32x2_to_bf16x2(yb.x, yb.y);
+              __stcs(reinterpret_cast<uint2*>(yr) + (j >> 2), q);
+            }
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
         const int j = c4 * (PIPE_TT * 4) + 4 * tt;
@@ -1105,12 +1170,24 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   // short chains the sums are ready in time, and the x ring's depth pays
   // instead (interleaved(8): 0.466 ms with SX = 8, SE = 8; 0.500 with 4, 12)
   const int64_t chain = (P.cols + P.partials - 1) / P.partials;
-  int sx = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && chain < 1024) ? PIPE_SX_MAX : 4;
+  int sx = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && chain < 1024) ? PIPE_SX_DEEP : 4;
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
   // x slots stay a multiple of the team count, so that each slot serves one
   // team and its parity waits run in order
-  if (sx < PIPE_SX_MAX && PIPE_SX_MAX * xrow + se * erow <= budget) sx = PIPE_SX_MAX;
+  if (sx < PIPE_SX_DEEP && PIPE_SX_DEEP * xrow + se * erow <= budget) sx = PIPE_SX_DEEP;
+  // PSK_PIPE_RINGS="sx,se" in the environment overrides both depths (a tuning
+  // aid; ignored unless both are multiples of the team count, se >= 2 teams,
+  // sx within the barrier arrays and the rings within the budget)
+  static const char* rings = getenv("PSK_PIPE_RINGS");
+  if (rings) {
+    int a = 0, b = 0;
+    if (sscanf(rings, "%d,%d", &a, &b) == 2 && a >= PIPE_TEAMS && a <= PIPE_SX_MAX && a % PIPE_TEAMS == 0 &&
+        b >= 2 * PIPE_TEAMS && b <= PIPE_SE_MAX && b % PIPE_TEAMS == 0 && a * xrow + b * erow <= budget) {
+      sx = a;
+      se = b;
+    }
+  }
   if (se < 2 * PIPE_TEAMS) {  // cannot happen for cols <= 4096; kept as a guard
     return fail(PSK_E_ARG, "row ring does not fit shared memory (cols %lld)", (long long)P.cols);
   }
