@@ -234,6 +234,78 @@ struct ChainCenteredSquare {    // RN(RN(v - mu)^2)
   }
 };
 
+// A chain continued over f(E[j]), f(E[j+P]), ... for j < end, in index
+// order (j is left past the last element added).  Loads run ahead of the
+// dependent adds in a register ring of D16 blocks of 16 (P = 1) or D8 blocks
+// of 8 (P > 1), D - 1 blocks ahead (no moves: each block's registers are
+// refilled right after it is added), so the chain runs at the add latency
+// while the shared-memory latency stays below that of the blocks ahead.
+template <int D16, int D8, class F>
+__device__ __forceinline__ float chain_range(float acc, const float* E, int& j, int end, int P, F f) {
+#define PSK_ADD4(q) acc = __fadd_rn(acc, f(q.x)); acc = __fadd_rn(acc, f(q.y)); \
+                    acc = __fadd_rn(acc, f(q.z)); acc = __fadd_rn(acc, f(q.w));
+  if (P == 1) {
+    constexpr int D = D16;
+    for (; (j & 3) != 0 && j < end; ++j) acc = __fadd_rn(acc, f(E[j]));
+    if (j + D * 16 <= end) {
+      float4 r[D][4];
+#pragma unroll
+      for (int d = 0; d < D; ++d)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[d][q] = *(const float4*)&E[j + 16 * d + 4 * q];
+      for (; j + 2 * D * 16 <= end; j += D * 16) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) { PSK_ADD4(r[d][q]) }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) r[d][q] = *(const float4*)&E[j + 16 * (d + D) + 4 * q];
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < D; ++d)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) { PSK_ADD4(r[d][q]) }
+      j += D * 16;
+    }
+  } else {
+    constexpr int D = D8;
+    if (j + (8 * D - 1) * P < end) {
+      float r[D][8];
+#pragma unroll
+      for (int d = 0; d < D; ++d)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r[d][i] = E[j + (8 * d + i) * P];
+      for (; j + (16 * D - 1) * P < end; j += 8 * D * P) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, f(r[d][i]));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[d][i] = E[j + (8 * (d + D) + i) * P];
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < D; ++d)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = __fadd_rn(acc, f(r[d][i]));
+      j += 8 * D * P;
+    }
+  }
+#undef PSK_ADD4
+  for (; j < end; j += P) acc = __fadd_rn(acc, f(E[j]));
+  return acc;
+}
+
+// The same through chain_range's register ring (the pipelined kernel's chain
+// warps, whose shared-memory loads compete with the teams' traffic).
+template <int D16, int D8, class F>
+__device__ __forceinline__ float run_chain_deep(const float* E, int n, int p, int P, F f) {
+  float acc = f(E[p]);
+  int j = p + P;
+  return chain_range<D16, D8>(acc, E, j, n, P, f);
+}
+
 // One chain: acc over f(E[p]), f(E[p+P]), ... (n elements in the row), in
 // index order.  The loads of the next block are issued before the dependent
 // adds of the current one (registers double-buffered), so the chain runs at
@@ -822,7 +894,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         return sum;
       };
       if (KIND == REGION_SOFTMAX || BWD) {
-        const float sum = combine(act ? run_chain(Er, cols, p, parts) : 0.0f);
+        const float sum = combine(act ? run_chain_deep<3, 4>(Er, cols, p, parts, ChainIdentity()) : 0.0f);
         if (act && p == 0) {
           rowsum[se] = sum;
           rowrcp[se] = __frcp_rn(sum);
@@ -831,12 +903,12 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         float mu = 0.0f;
         float ss;
         if (KIND == REGION_LAYER) {
-          const float s1 = combine(act ? run_chain(Er, cols, p, parts) : 0.0f);
+          const float s1 = combine(act ? run_chain_deep<3, 4>(Er, cols, p, parts, ChainIdentity()) : 0.0f);
           mu = __fdiv_rn(s1, n_f);
           mu = __shfl_sync(0xffffffffu, mu, (lane - p) & 31);   // the row's mean, to every lane of the row
-          ss = combine(act ? run_chain(Er, cols, p, parts, ChainCenteredSquare{mu}) : 0.0f);
+          ss = combine(act ? run_chain_deep<3, 4>(Er, cols, p, parts, ChainCenteredSquare{mu}) : 0.0f);
         } else {
-          ss = combine(act ? run_chain(Er, cols, p, parts, ChainSquare()) : 0.0f);
+          ss = combine(act ? run_chain_deep<3, 4>(Er, cols, p, parts, ChainSquare()) : 0.0f);
         }
         if (act && p == 0) {
           const float var = __fdiv_rn(ss, n_f);
