@@ -157,9 +157,9 @@ def _gpu_uuid(torch, dev):
 # generated from group.cu and compiled at run time from the device headers)
 _KERNEL_SOURCES = {
     "adamw": ["adamw.cu"],
-    "group": ["group.cu", "group_dev.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
-    "softmax_sequential": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
-    "softmax_interleaved8": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc"],
+    "group": ["group.cu", "group_dev.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
+    "softmax_sequential": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
+    "softmax_interleaved8": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
 }
 
 

@@ -12,11 +12,12 @@ extern "C" {
 
 // which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
 // 6 erf_fast (signed), 7 exp_fast_mid, 8 the softmax region's pair exp
-// (x <= 0, taken two at a time)
+// (x <= 0, taken two at a time), 9 the groups' pair exp (|x| <= 87)
 void psk_host_unary(int which, const float* x, float* y, long n) {
-  if (which == 8) {
+  if (which == 8 || which == 9) {
     for (long i = 0; i < n; i += 2) {
-      const f2 r = exp2_faithful_nonpos(f2{x[i], i + 1 < n ? x[i + 1] : 0.0f});
+      const f2 a{x[i], i + 1 < n ? x[i + 1] : 0.0f};
+      const f2 r = which == 8 ? exp2_faithful_nonpos(a) : exp2_faithful_mid(a);
       y[i] = r.x;
       if (i + 1 < n) y[i + 1] = r.y;
     }
@@ -131,6 +132,28 @@ long psk_host_exp_pair_maxulp(uint32_t span, uint32_t stride, float* worst) {
       const float want = exp_cr(ta[q], psk_exp_tab2);
       const long d = labs((long)f2u(ra[q]) - (long)f2u(want));
       if (d > maxd) { maxd = d; if (worst) *worst = ta[q]; }
+    }
+  }
+  return maxd;
+}
+
+// The groups' pair exp (exp2_faithful_mid) against the correctly rounded
+// exp over the floats of [-a, a] whose bit patterns (of |x|) are multiples of
+// stride, both signs; returns the largest distance in ulps.
+long psk_host_exp_mid_maxulp(float a, uint32_t stride, float* worst) {
+  long maxd = 0;
+  const uint32_t top = f2u(a);
+  for (uint64_t i = 0; i <= top; i += 2 * (uint64_t)stride) {
+    for (uint32_t sign = 0; sign <= 0x80000000u; sign += 0x80000000u) {
+      const float xa = u2f(sign | (uint32_t)i);
+      const float xb = u2f(sign | (uint32_t)(i + stride <= top ? i + stride : i));
+      const f2 r = exp2_faithful_mid(f2{xa, xb});
+      const float ra[2] = {r.x, r.y}, ta[2] = {xa, xb};
+      for (int q = 0; q < 2; ++q) {
+        const long d = labs((long)f2u(ra[q]) - (long)f2u(exp_cr(ta[q], psk_exp_tab2)));
+        if (d > maxd) { maxd = d; if (worst) *worst = ta[q]; }
+      }
+      if (sign) break;
     }
   }
   return maxd;

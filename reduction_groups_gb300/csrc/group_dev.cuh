@@ -9,6 +9,7 @@
 #include "../../include/psk.h"
 #include "devcommon.cuh"
 #include "crmath.cuh"
+#include "pair.cuh"
 
 namespace psk {
 
@@ -75,6 +76,12 @@ __device__ __forceinline__ void load_tanh_tables(TanhTables& t) {
 }
 
 template <int V> struct Vec { float v[V]; };
+
+// The EXP-clamp node's min(max(a, -4), 4) with the group's selects
+// (max(a, b) = a > b ? a : b): fmaxf / fminf give the same value for every a
+// (a NaN gives -4 either way; the bounds are not zeros), in one min / max
+// instruction each.
+__device__ __forceinline__ float clamp_pm4(float a) { return fminf(fmaxf(a, -4.0f), 4.0f); }
 
 template <int V>
 __device__ __forceinline__ Vec<V> splat(float q) {
@@ -219,8 +226,7 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
   for (int j = 0; j < V; ++j) {
     a[j] = A.v[j];
     if (CLAMP) {
-      a[j] = a[j] > -4.0f ? a[j] : -4.0f;
-      a[j] = a[j] < 4.0f ? a[j] : 4.0f;
+      a[j] = clamp_pm4(a[j]);
     }
     const bool inr = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range (NaN clamps to -4)
     exp_tier1_core(inr ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
@@ -328,12 +334,23 @@ __device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
 template <int V, bool CLAMP>
 __device__ __forceinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
   Vec<V> r;
+  if constexpr (CLAMP && V % 2 == 0) {   // two at a time (packed f32x2 arithmetic)
+#pragma unroll
+    for (int j = 0; j < V; j += 2) {
+      float a = A.v[j], b = A.v[j + 1];
+      a = clamp_pm4(a);
+      b = clamp_pm4(b);
+      const f2 e = exp2_faithful_mid(f2{a, b});
+      r.v[j] = e.x;
+      r.v[j + 1] = e.y;
+    }
+    return r;
+  }
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     float a = A.v[j];
     if (CLAMP) {
-      a = a > -4.0f ? a : -4.0f;
-      a = a < 4.0f ? a : 4.0f;
+      a = clamp_pm4(a);
       r.v[j] = exp_fast_mid(a);
     } else {
       r.v[j] = exp_fast(a);

@@ -67,4 +67,24 @@ PSK_HD f2 exp2_faithful_nonpos(f2 t) {
   return f2_mul(f2_mul(p, s), f2_splat(0x1p-64f));
 }
 
+// exp of a pair with |t| <= 88 and normal results (t >= -87.3), no special
+// cases: the same reduction and polynomial as above, 2^k added to the
+// exponent field of the polynomial's value (the sum's bit pattern shifted
+// left by 23 is k << 23).  The groups' fast EXP-clamp node (t in [-4, 4]).
+PSK_HD f2 exp2_faithful_mid(f2 t) {
+  const f2 z = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), f2_splat(PAIR_EXP_MAGIC));
+  const f2 kf = f2_add(z, f2_splat(-PAIR_EXP_MAGIC));
+  f2 r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_HI), t);
+  r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_LO), r);
+  f2 p = f2_splat(1.0f / 5040.0f);
+  p = f2_fma(p, r, f2_splat(1.0f / 720.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 120.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 24.0f));
+  p = f2_fma(p, r, f2_splat(1.0f / 6.0f));
+  p = f2_fma(p, r, f2_splat(0.5f));
+  p = f2_fma(p, r, f2_splat(1.0f));
+  p = f2_fma(p, r, f2_splat(1.0f));
+  return f2{u2f(f2u(p.x) + f2u(z.x) * (1u << 23)), u2f(f2u(p.y) + f2u(z.y) * (1u << 23))};
+}
+
 }  // namespace psk

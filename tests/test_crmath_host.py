@@ -293,3 +293,21 @@ def test_pair_exp_faithful_over_its_range(hm):
     span = int(np.float32(-105.0).view(np.uint32)) - 0x80000000
     worst = ctypes.c_float(0)
     assert L.psk_host_exp_pair_maxulp(span, 61, ctypes.byref(worst)) <= 1
+
+
+def test_group_pair_exp_faithful_on_the_clamped_range(hm):
+    """The groups' fast EXP-clamp node evaluates exp on [-4, 4] two at a time
+    (pair arithmetic, 2^k added to the exponent field): within one ulp of the
+    correctly rounded oracle on uniform samples and on the floats of [-4, 4]
+    taken with a stride of 53 bit patterns, both signs (measured over every
+    float of that range the bound is exactly one ulp)."""
+    unary, _ = hm
+    rng = np.random.default_rng(73)
+    x = np.concatenate([rng.uniform(-4, 4, 1_000_000).astype(np.float32),
+                        np.array([-4.0, 4.0, 0.0, -0.0, 1e-38, -1e-38, 0.34657359, -0.34657359], np.float32)])
+    assert _ulps(unary(9, x), exp_f32(x)).max() <= 1
+    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
+    L.psk_host_exp_mid_maxulp.restype = ctypes.c_long
+    L.psk_host_exp_mid_maxulp.argtypes = [ctypes.c_float, ctypes.c_uint32, ctypes.POINTER(ctypes.c_float)]
+    worst = ctypes.c_float(0)
+    assert L.psk_host_exp_mid_maxulp(4.0, 53, ctypes.byref(worst)) <= 1
