@@ -1,0 +1,448 @@
+// Lane-per-row softmax region: Reduce(Max) -> Sub -> Exp -> Reduce(Sum) ->
+// Div over bf16 rows (poot "Fusion and Planning", Reduction-rooted regions),
+// the sum in the declared order's bracketing tree (presk "Native execution",
+// the realization's order; metrale "The LKB in Mathematics", section 2):
+// sequential and blocked(w), one chain ((e0 + e1) + e2) + ... per row.
+//
+// Each lane of a warp owns one row of the warp's batch (nb <= 32 consecutive
+// rows) and runs the three passes over it itself:
+//   pass 0: m = max over the row (on the stored bf16 pairs, exact);
+//   pass 1: e_j = exp(x_j - m), added to the row's chain in index order;
+//   pass 2: e_j recomputed (the same operations on the same values: the same
+//           bits), y_j = bf16_rn(e_j / s).
+// The rows are never held whole on chip: every pass streams the batch
+// through a ring of tiles of 64 columns x nb rows in shared memory, each one
+// 2-D tensor copy (TMA), and the outputs leave through a ring of output tiles
+// with 2-D tensor stores.  The passes run over the tiles right to left, left
+// to right (the chains' index order), then right to left again, so that each
+// pass starts on the tiles the one before it read last, which L2 still holds
+// (evict-last hints until the last pass, evict-first after).  Tiles use the 128-byte swizzle, so a lane's
+// 16-byte reads and writes of its own row never share a bank group with the
+// seven lanes beside it.  Rows past the tensor's end read as zeros and are
+// never stored.
+//
+// Against the pipelined kernel (regions.cu), which computes each exp once
+// into a shared f32 row and leaves the sum to a few chain lanes, this costs a
+// second exp per element but keeps up to 32 rows in their chains per warp
+// (eight warps per SM, two per scheduler) instead of about eight per SM: the
+// sequential order's 4096 dependent adds per row are no longer the bound, and
+// a warp's lanes do the exp work of their rows in step.  The kernel serves
+// the fast realization (faithful exp on f32 pairs); with the correctly
+// rounded exp the doubled exp work costs more than the chains save.
+//
+// Every wait is bounded (pipe.cuh); a timeout is recorded in the status word
+// and the warp winds down after its copies in flight have landed.
+
+#include "common.cuh"
+#include "crmath.cuh"
+#include "pipe.cuh"
+#include "pair.cuh"
+#include "rowmath.cuh"
+
+#include <cuda.h>
+#include <stdlib.h>
+
+namespace psk {
+
+constexpr int LANE_WARPS = 8;                                  // warps per CTA (two per scheduler)
+constexpr int LANE_TC = 64;                                    // columns of a tile (128 bytes of bf16)
+constexpr int LANE_TILE = 32 * 128;                            // a tile's slot: up to 32 rows of 128 bytes
+constexpr int LANE_NI = 4;                                     // input tiles per warp
+constexpr int LANE_NO = 2;                                     // output tiles per warp
+constexpr int LANE_WARP_SMEM = (LANE_NI + LANE_NO) * LANE_TILE;
+constexpr int LANE_SMEM = LANE_WARPS * LANE_WARP_SMEM + 1024;  // + room to align the base to 1024 bytes
+constexpr int LANE_MAX_COLS = 4096;
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 2-D tensor copy of the tile at (column c0, row r0) into shared memory,
+// completing on `bar`, with an L2 cache policy.
+__device__ __forceinline__ void tile_load(uint32_t dst, const CUtensorMap* map, int c0, int r0, uint64_t* bar,
+                                          uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(r0), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// 2-D tensor store of a shared-memory tile to (column c0, row r0), in the
+// thread's current bulk async-group; elements outside the tensor are skipped.
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, int c0, int r0, uint32_t src, uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::
+                   "l"(map),
+               "r"(c0), "r"(r0), "r"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of the thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's shared-memory accesses before its later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The eight exp values of a 16-byte group of bf16 x (element 2k in the low
+// half of word k): x - m, then the region's exp -- the same operations as the
+// pipelined kernel's (fast: x + (-m) and the exp on f32 pairs; exact: the
+// correctly rounded exp of RN(x - m)).
+template <int EXPM>
+__device__ __forceinline__ void lane_exp8(const uint4 wv, float m, float* e) {
+  const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+  if constexpr (EXPM == PSK_EXP_FAST) {
+    const f2 nm = f2_splat(-m);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const f2 r = exp2_faithful_nonpos(f2_add(f2{__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xFFFF0000u)}, nm));
+      e[2 * k] = r.x;
+      e[2 * k + 1] = r.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      e[2 * k] = __fsub_rn(__uint_as_float(wd[k] << 16), m);
+      e[2 * k + 1] = __fsub_rn(__uint_as_float(wd[k] & 0xFFFF0000u), m);
+    }
+    region_exp8<EXPM>(e);
+  }
+}
+
+
+// A full tile (64 columns) of the lane's row: its eight groups loaded first,
+// then the 64 exp values, then the adds, one basic block, so that the
+// scheduler overlaps the exp chains of different groups and the dependent
+// adds with them.
+template <int EXPM>
+__device__ __forceinline__ void lane_load8(const unsigned char* tile, uint32_t lrow, uint32_t sw, uint4* v) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
+}
+
+template <int EXPM>
+__device__ __forceinline__ void lane_chain_tile(const unsigned char* tile, uint32_t lrow, uint32_t sw, float m,
+                                                float& acc) {
+  uint4 v[8];
+  lane_load8<EXPM>(tile, lrow, sw, v);
+  float e[64];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) lane_exp8<EXPM>(v[k], m, e + 8 * k);
+#pragma unroll
+  for (int j = 0; j < 64; ++j) acc = __fadd_rn(acc, e[j]);
+}
+
+// e / s for the eight values of a group, rounded to bf16 pairs.
+template <int EXPM>
+__device__ __forceinline__ uint4 lane_div8(float* e, float s, float rs, f2 rs2, f2 ns2, bool fast_ok) {
+  if (EXPM == PSK_EXP_FAST && fast_ok) {
+    // Markstein's correction two at a time, as the pipelined kernel's fast
+    // realization does (no per-element range test)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const f2 ea{e[2 * h], e[2 * h + 1]};
+      const f2 qa = f2_mul(ea, rs2);
+      const f2 ya = f2_fma(f2_fma(qa, ns2, ea), rs2, qa);
+      e[2 * h] = ya.x;
+      e[2 * h + 1] = ya.y;
+    }
+  } else {
+    row_div_n<8>(e, s, rs, fast_ok);
+  }
+  return make_uint4(f32x2_to_bf16x2(e[0], e[1]), f32x2_to_bf16x2(e[2], e[3]), f32x2_to_bf16x2(e[4], e[5]),
+                    f32x2_to_bf16x2(e[6], e[7]));
+}
+
+template <int EXPM>
+__global__ void __launch_bounds__(LANE_WARPS * 32, 1)
+    softmax_lane_kernel(const __grid_constant__ RegionParams P, const __grid_constant__ CUtensorMap tx,
+                        const __grid_constant__ CUtensorMap ty) {
+  extern __shared__ unsigned char lane_smem_raw[];
+  __shared__ __align__(8) uint64_t full[LANE_WARPS][LANE_NI];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cols = (int)P.cols;
+  const int nch = (cols + LANE_TC - 1) / LANE_TC;             // tiles per pass
+  const int nb = P.nb;                                         // rows per batch (a tile's height)
+  const int64_t nbatch_all = (P.rows + nb - 1) / nb;
+  const int64_t gw = (int64_t)blockIdx.x * LANE_WARPS + w;
+  const int64_t wtot = (int64_t)gridDim.x * LANE_WARPS;
+  const int my_batches = gw < nbatch_all ? (int)((nbatch_all - 1 - gw) / wtot + 1) : 0;
+  const int64_t total = (int64_t)my_batches * 3 * nch;       // tile requests of this warp
+  // tiles start on 1024-byte boundaries (the period of the 128-byte swizzle)
+  const uint32_t raw = smem_addr(lane_smem_raw);
+  unsigned char* wp = lane_smem_raw + (((raw + 1023u) & ~1023u) - raw) + (size_t)w * LANE_WARP_SMEM;
+  const uint32_t wa = smem_addr(wp);
+  unsigned char* op = wp + (size_t)LANE_NI * LANE_TILE;
+  // the lane's row in a tile; its k-th 16-byte group sits at group k ^ (lane % 8)
+  const uint32_t lrow = (uint32_t)lane * 128u, sw = (uint32_t)(lane & 7);
+  uint64_t* bars = full[w];
+  const uint64_t pol_keep = policy_evict_last(), pol_drop = policy_evict_first();
+  const long long drop = g_pipe_drop_row;
+
+  // zero the warp's tiles: rows beyond the batch are never copied in and read
+  // as zeros (benign values, no slow paths), like rows past the tensor's end
+  for (int o = lane * 16; o < LANE_WARP_SMEM; o += 32 * 16) *reinterpret_cast<uint4*>(wp + o) = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (lane == 0) {
+    for (int i = 0; i < LANE_NI; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // ---- requests (lane 0): q = ((batch * 3) + pass) * nch + tile, into slot q % NI;
+  // the request state is kept by every lane alike
+  int64_t rq = 0;
+  int rb = 0, rp = 0, rc = 0;
+  int64_t withheld = -1;                                     // test hook: the request never made
+  auto issue = [&]() {
+    const int slot = (int)(rq % LANE_NI);
+    const int64_t r0 = (gw + (int64_t)rb * wtot) * nb;
+    const int tc = rp == 1 ? rc : nch - 1 - rc;               // the pass's tile order
+    if (rp == 0 && rc == 0 && drop >= (long long)rb * nb && drop < (long long)rb * nb + nb) {
+      withheld = rq;                                         // as if this copy were lost
+    } else if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[slot], (uint32_t)nb * 128u);
+      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)r0, &bars[slot], rp < 2 ? pol_keep : pol_drop);
+    }
+    ++rq;
+    if (++rc == nch) {
+      rc = 0;
+      if (++rp == 3) { rp = 0; ++rb; }
+    }
+  };
+  for (int i = 0; i < LANE_NI && rq < total; ++i) issue();
+
+  // ---- consumption in request order
+  int64_t cq = 0;
+  bool dead = false;
+  auto take = [&]() -> bool {
+    const bool ok = mbar_wait(&bars[cq % LANE_NI], (uint32_t)(cq / LANE_NI) & 1u);
+    return !__any_sync(0xffffffffu, !ok);
+  };
+  auto release = [&]() {                                     // every lane has read the tile: refill its slot
+    __syncwarp();
+    ++cq;
+    if (lane == 0) fence_proxy_async_smem();
+    if (rq < total) issue();
+  };
+  auto group = [&](int k) -> uint4 {                         // the lane's k-th group of the tile being read
+    return *reinterpret_cast<const uint4*>(wp + (size_t)(cq % LANE_NI) * LANE_TILE + lrow + (((uint32_t)k ^ sw) << 4));
+  };
+  int64_t oq = 0;                                            // output tiles written
+
+  for (int b = 0; b < my_batches && !dead; ++b) {
+    const int64_t r0 = (gw + (int64_t)b * wtot) * nb;
+    // pass 0: the max, on the stored bf16 pairs
+    uint32_t mb = 0xFF80FF80u;                              // (-inf, -inf)
+    for (int t = 0; t < nch; ++t) {
+      const int c = nch - 1 - t;                             // right to left (the max is order-free)
+      if (!take()) { dead = true; break; }
+      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < ng) {
+          const uint4 v = group(k);
+          mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.x, v.y));
+          mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.z, v.w));
+        }
+      }
+      release();
+    }
+    if (dead) break;
+    const float m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
+
+    // pass 1: the chain, left to right
+    float acc = 0.0f;                                        // 0 + e_0 = e_0: the chain starts at e_0
+    for (int c = 0; c < nch; ++c) {
+      if (!take()) { dead = true; break; }
+      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
+      if (ng == 8) {
+        lane_chain_tile<EXPM>(wp + (size_t)(cq % LANE_NI) * LANE_TILE, lrow, sw, m, acc);
+      } else {
+        for (int k = 0; k < ng; ++k) {
+          float e[8];
+          lane_exp8<EXPM>(group(k), m, e);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc = __fadd_rn(acc, e[q]);
+        }
+      }
+      release();
+    }
+    if (dead) break;
+    const float s = acc;
+    const float rs = __frcp_rn(s);
+    const bool fast_ok = s >= 1.0f && s < 0x1p20f;
+
+    // pass 2: e recomputed, divided, rounded to bf16, staged and stored
+    const f2 rs2 = f2_splat(rs), ns2 = f2_splat(-s);
+    for (int t = 0; t < nch; ++t) {
+      const int c = nch - 1 - t;                             // right to left (elementwise)
+      if (!take()) { dead = true; break; }
+      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
+      if (lane == 0) bulk_wait_read<LANE_NO - 1>();         // the store that last used this slot has read it
+      __syncwarp();
+      unsigned char* ot = op + (size_t)(oq % LANE_NO) * LANE_TILE;
+      if (ng == 8) {
+        uint4 v[8], o8[8];
+        lane_load8<EXPM>(wp + (size_t)(cq % LANE_NI) * LANE_TILE, lrow, sw, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float e[8];
+          lane_exp8<EXPM>(v[k], m, e);
+          o8[k] = lane_div8<EXPM>(e, s, rs, rs2, ns2, fast_ok);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = o8[k];
+      } else {
+        for (int k = 0; k < ng; ++k) {
+          float e[8];
+          lane_exp8<EXPM>(group(k), m, e);
+          *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = lane_div8<EXPM>(e, s, rs, rs2, ns2, fast_ok);
+        }
+      }
+      fence_proxy_async_smem();                              // this lane's writes, before the async store
+      __syncwarp();
+      if (lane == 0) {
+        tile_store(&ty, c * LANE_TC, (int)r0, smem_addr(ot), pol_drop);
+        bulk_commit();
+      }
+      ++oq;
+      release();
+    }
+  }
+
+  if (dead) {
+    // a withheld copy (the test hook) is arrived for now, so that its phase
+    // completes; then every request made is waited for (bounded) before the
+    // warp leaves
+    if (lane == 0 && withheld >= cq) mbar_arrive(&bars[withheld % LANE_NI]);
+    __syncwarp();
+    for (int64_t q = cq; q < rq; ++q) mbar_wait(&bars[q % LANE_NI], (uint32_t)(q / LANE_NI) & 1u);
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+// ------------------------------------------------------------------ host
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link
+// against the driver library), resolved once.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return (EncodeTiledFn)p;
+  }();
+  return fn;
+}
+
+// The tensor map of bf16 rows [rows, cols] with row stride ld elements, in
+// tiles of 64 columns x nb rows, 128-byte swizzled, zeros outside.
+static int encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int nb) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return fail(PSK_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2u};
+  const cuuint32_t box[2] = {(cuuint32_t)LANE_TC, (cuuint32_t)nb};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PSK_E_CUDA, "tensor map encoding failed (CUresult %d)", (int)r);
+  return PSK_OK;
+}
+
+// Rows per batch: the fewest batches of at most 32 rows that cover a warp's
+// share, split evenly (32768 rows on 1216 warps: one batch of 27).
+static int lane_batch_rows(int64_t rows, int64_t wtot) {
+  const int64_t rpw = (rows + wtot - 1) / wtot;
+  const int64_t nbat = (rpw + 31) / 32;
+  return (int)((rpw + nbat - 1) / nbat);
+}
+
+static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUtensorMap& ty, int64_t sms,
+                        cudaStream_t stream) {
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)softmax_lane_kernel<PSK_EXP_FAST>, LANE_SMEM, attr);
+  const int64_t nbatch = (P.rows + P.nb - 1) / P.nb;
+  const int64_t need = (nbatch + LANE_WARPS - 1) / LANE_WARPS;
+  const unsigned grid = (unsigned)(need < sms ? need : sms);
+  softmax_lane_kernel<PSK_EXP_FAST><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
+  return check_launch("softmax region kernel (lane per row)");
+}
+
+// The kernel takes the fast realization of the one-chain orders (sequential,
+// blocked) over bf16 rows (x and y) of 64 <= cols <= 4096 columns, cols a
+// multiple of 8, whose rows start on 16-byte boundaries, and at least 8 rows
+// per warp of a full grid (fewer rows leave most lanes idle; the pipelined
+// kernel spreads each row over a team instead).  Interleaved orders stay with
+// the pipelined kernel: their chains are short there, and the second exp per
+// element would cost more than the lane kernel saves.  Tuning
+// aids, read once: PSK_LANES=0 turns the kernel off, PSK_LANE_MIN_ROWS sets
+// the row threshold, PSK_LANE_NB (1..32) the rows per batch.
+int softmax_lanes(const RegionParams& P0, int exp_mode, cudaStream_t stream, bool* taken) {
+  *taken = false;
+  if (exp_mode != PSK_EXP_FAST) return PSK_OK;
+  static const char* off = getenv("PSK_LANES");
+  if (off && off[0] == '0') return PSK_OK;
+  if (P0.partials != 1) return PSK_OK;
+  if (P0.cols < LANE_TC || P0.cols > LANE_MAX_COLS || P0.cols % 8 != 0 || P0.ldx % 8 != 0 || P0.ldy % 8 != 0 ||
+      (uintptr_t)P0.x % 16 != 0 || (uintptr_t)P0.y % 16 != 0 || P0.rows >= ((int64_t)1 << 31))
+    return PSK_OK;
+  const int64_t sms = device_sm_count();
+  const int64_t wtot = sms * LANE_WARPS;
+  static const char* min_env = getenv("PSK_LANE_MIN_ROWS");
+  const int64_t min_rows = min_env ? atoll(min_env) : 8 * wtot;
+  if (P0.rows < min_rows) return PSK_OK;
+  RegionParams P = P0;
+  P.nb = lane_batch_rows(P.rows, wtot);
+  static const char* nb_env = getenv("PSK_LANE_NB");
+  if (nb_env) {
+    const int v = atoi(nb_env);
+    if (v >= 1 && v <= 32) P.nb = v;
+  }
+  if (P.nb > P.rows) P.nb = (int)P.rows;
+  CUtensorMap tx, ty;
+  int rc = encode_rows(&tx, P.x, P.rows, P.cols, P.ldx, P.nb);
+  if (rc) return rc;
+  rc = encode_rows(&ty, P.y, P.rows, P.cols, P.ldy, P.nb);
+  if (rc) return rc;
+  *taken = true;
+  return launch_lanes(P, tx, ty, sms, stream);
+}
+
+// The status word and test hook of this translation unit's kernels (pipe.cuh
+// keeps one copy per unit): read / reset and set by the entry points in
+// regions.cu.
+int lanes_status(unsigned int* v, bool reset) {
+  if (cudaMemcpyFromSymbol(v, g_pipe_status, sizeof(*v)) != cudaSuccess) return check_launch("device status read");
+  if (reset) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_pipe_status, &z, sizeof(z)) != cudaSuccess) return check_launch("device status reset");
+  }
+  return PSK_OK;
+}
+
+int lanes_set_drop_row(long long row) {
+  if (cudaMemcpyToSymbol(g_pipe_drop_row, &row, sizeof(row)) != cudaSuccess) return check_launch("test hook write");
+  return PSK_OK;
+}
+
+}  // namespace psk

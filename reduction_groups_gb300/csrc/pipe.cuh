@@ -11,14 +11,16 @@
 
 namespace psk {
 
-// Status word of the pipelined kernels: 0 = no timeout seen.  Read by
-// psk_device_status() on the host.
-__device__ unsigned int g_pipe_status;
+// Status word of the pipelined kernels: 0 = no timeout seen.  One copy per
+// translation unit that includes this header (each is its own device module);
+// psk_device_status() reads and resets every copy.
+static __device__ unsigned int g_pipe_status;
 
 // Test hook (psk_test_drop_row): the local row at which every pipelined
 // region CTA's producer stops, as if that row's copy were lost, so that the
-// bounded waits run out; -1 (the default) never.
-__device__ long long g_pipe_drop_row = -1;
+// bounded waits run out; -1 (the default) never.  One copy per translation
+// unit, like the status word; psk_test_drop_row() sets every copy.
+static __device__ long long g_pipe_drop_row = -1;
 
 constexpr unsigned int PIPE_TIMEOUT = 1u;
 constexpr long long PIPE_WAIT_CYCLES = 4000000000LL;   // ~2 s at 2 GHz: far beyond any legitimate wait
