@@ -92,6 +92,63 @@ def _peaks():
 
 
 # ----------------------------------------------------------------- clocks
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the library
+    nvidia-smi reads), polled every 2 ms from a helper thread, so that a timed
+    region of a few tens of milliseconds holds a dozen samples.  Read-only
+    queries; nothing about the GPU is set."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid: str, period: float = 0.002):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.L, self.h = L, ctypes.c_void_p()
+        if L.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for " + gpu_uuid)
+        self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))      # 1: the SM clock
+        self.max_mhz = mx.value
+        self.period, self.samples = period, []
+        self.stop_ev, self.th = threading.Event(), threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        c, r = self.ct.c_uint(0), self.ct.c_ulonglong(0)
+        while not self.stop_ev.is_set():
+            t = time.perf_counter()
+            if self.L.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(c)) == 0:
+                ok = self.reasons_fn(self.h, self.ct.byref(r)) == 0
+                self.samples.append((t, c.value, r.value if ok else 0))
+            time.sleep(self.period)
+
+    def start(self):
+        self.th.start()
+
+    def stop(self, t0: float, t1: float):
+        """Stop polling; the summary of the samples taken between host times t0
+        and t1 (the timed region), or of all samples if none fell there."""
+        self.stop_ev.set()
+        self.th.join(timeout=5)
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        use = inside or self.samples
+        if not use:
+            return None
+        bits = 0
+        for s in use:
+            bits |= s[2]
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in self.REASONS.items() if bits & b), "samples": len(inside),
+                "source": "NVML, 2 ms polling" + ("" if inside else "; none inside the timed region, all shown")}
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -110,7 +167,7 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -158,8 +215,10 @@ def _gpu_uuid(torch, dev):
 _KERNEL_SOURCES = {
     "adamw": ["adamw.cu"],
     "group": ["group.cu", "group_dev.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
-    "softmax_sequential": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
-    "softmax_interleaved8": ["regions.cu", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc", "pair.cuh"],
+    "softmax_sequential": ["lanes.cu", "rowmath.cuh", "pipe.cuh", "devcommon.cuh", "crmath.cuh", "crmath_tables.inc",
+                           "pair.cuh"],
+    "softmax_interleaved8": ["regions.cu", "rowmath.cuh", "pipe.cuh", "devcommon.cuh", "crmath.cuh",
+                             "crmath_tables.inc", "pair.cuh"],
 }
 
 
@@ -335,6 +394,13 @@ def run_ours(a, ws, rank, local):
             if ev is not None:
                 ev[j][1].record()
 
+    # clocks sampled from before the warm-up (the sampler is running when the
+    # timed region starts) to after the timed region
+    try:
+        sampler = NvmlSampler(_gpu_uuid(torch, local))
+    except Exception:
+        sampler = ClockSampler(_gpu_uuid(torch, local))
+    sampler.start()
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
@@ -348,17 +414,17 @@ def run_ours(a, ws, rank, local):
     evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in kernels]
            for _ in range(a.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(_gpu_uuid(torch, local))
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
+    t_host0 = time.perf_counter()
     start.record()
     for i in range(a.steps):
         step(evs[i])
     end.record()
     torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_host0, t_host1)
     total_ms = start.elapsed_time(end)
     per_kernel_ms = {k: sum(evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(a.steps)) / a.steps
                      for j, k in enumerate(kernels)}
@@ -414,11 +480,29 @@ def run_ours(a, ws, rank, local):
         host_sx = sx.cpu().pin_memory()
         sy2 = torch.empty_like(sy)
         host_sy = [torch.empty(sy.shape, dtype=sy.dtype, pin_memory=True) for _ in range(2)]
-        host_leaves = [tuple(t.cpu().pin_memory() for t in leaf) for leaf in leaves]
+        # the AdamW leaves as views of four flat buffers (theta, m, v, grad) on
+        # the device and in pinned host memory, each leaf starting on a 256-byte
+        # boundary, so that a slice of consecutive leaves moves in one copy per
+        # buffer instead of one per leaf and tensor
+        numels = [leaf[0].numel() for leaf in leaves]
+        offs, o = [], 0
+        for n in numels:
+            offs.append(o)
+            o += (n + 63) // 64 * 64
+        flat_d = [torch.empty(o, dtype=leaves[0][q].dtype, device="cuda") for q in range(4)]
+        flat_h = [torch.empty(o, dtype=leaves[0][q].dtype, pin_memory=True) for q in range(4)]
+        e_leaves = []
+        for i, leaf in enumerate(leaves):
+            views = tuple(flat_d[q][offs[i]:offs[i] + numels[i]] for q in range(4))
+            for q in range(4):
+                views[q].copy_(leaf[q])
+                flat_h[q][offs[i]:offs[i] + numels[i]].copy_(leaf[q])
+            e_leaves.append(views)
+        torch.cuda.synchronize()
         h2d = sum(t.numel() * t.element_size() for t in host_g) + host_sx.numel() * 2 + \
-            sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf)
+            sum(t.numel() * t.element_size() for t in flat_h)
         d2h = host_gout.numel() * 2 + 2 * host_sy[0].numel() * 2 + \
-            sum(t.numel() * t.element_size() for leaf in host_leaves for t in leaf[:3])
+            sum(t.numel() * t.element_size() for t in flat_h[:3])
         # AdamW slices of about a tenth of the parameters each, in leaf order
         slices, cur, acc_n = [], [], 0
         per = max(1, tree.n_params // 10)
@@ -438,10 +522,12 @@ def run_ours(a, ws, rank, local):
                       [lambda st: R.psk_softmax_region(sx, sy, ("sequential",), em, st),
                        lambda st: R.psk_softmax_region(sx, sy2, ("interleaved", 8), em, st)],
                       [(sy, host_sy[0]), (sy2, host_sy[1])]))
-        for sl in slices:
-            units.append(([(d_, h_) for i in sl for d_, h_ in zip(leaves[i], host_leaves[i])],
-                          [lambda st, sl=sl: R.psk_adamw_tree([leaves[i] for i in sl], tree.hp, st)],
-                          [(d_, h_) for i in sl for d_, h_ in zip(leaves[i][:3], host_leaves[i][:3])]))
+        for k, sl in enumerate(slices):
+            lo = offs[sl[0]]
+            hi = offs[slices[k + 1][0]] if k + 1 < len(slices) else o   # the slice's span, padding included
+            units.append(([(flat_d[q][lo:hi], flat_h[q][lo:hi]) for q in range(4)],
+                          [lambda st, sl=sl: R.psk_adamw_tree([e_leaves[i] for i in sl], tree.hp, st)],
+                          [(flat_d[q][lo:hi], flat_h[q][lo:hi]) for q in range(3)]))
         n_cs = a.e2e_copy_streams
         s_ins = [torch.cuda.Stream() for _ in range(n_cs)]
         s_outs = [torch.cuda.Stream() for _ in range(n_cs)]
