@@ -373,6 +373,10 @@ def run_ours(a, ws, rank, local):
         extra_launches[f"group_{g_other}_math"] = lambda: R.psk_group_run(wl.tokens, wl.imm, g_args, g_out,
                                                                           math=g_other)
         b_all[f"group_{g_other}_math"] = b_group
+        # the same program, math mode and shape through the precompiled
+        # interpreter kernel: the baseline of the program-specialised kernel
+        extra_launches["group_interpreter"] = lambda: R.psk_group_run_interp(wl.tokens, wl.imm, g_args, g_out, math=gm)
+        b_all["group_interpreter"] = b_group
         # the extended op set (LOG, TANH, RECIP, SELECT on an int32 mask) on the
         # group's shape
         xw = W.select_group(rows=max(1, int(8192 * sc)))
@@ -601,7 +605,7 @@ def run_ours(a, ws, rank, local):
         if k == "group_select_log_tanh":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["elems_per_s"] = round(xw.out_shape[0] * xw.out_shape[1] / (ms / 1e3), 1)
-        if k.startswith("group_") and k.endswith("_math"):
+        if (k.startswith("group_") and k.endswith("_math")) or k == "group_interpreter":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["elems_per_s"] = round(wl.out_shape[0] * wl.out_shape[1] / (ms / 1e3), 1)
     for k in extra_launches:

@@ -186,6 +186,20 @@ int psk_group_run_ex(const psk_program* prog, const psk_input* inputs, int32_t n
 int psk_group_prepare_ex(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
                          const psk_output* out, int32_t math_mode);
 
+/* psk_group_run_ex through one kernel compiled with the library for every
+ * program, which walks the program's node list per element (the group as one
+ * loop nest whose body is the chain of members, PSK-Realize "What a group
+ * is"; each node evaluated as the unfused op would be, presk "Native
+ * execution": fusion reassociates nothing).  The same validation, refusals,
+ * aliasing rule and result bits as psk_group_run_ex with the same math mode;
+ * no run-time compilation, so no first-use compile and no run-time compiler
+ * needed; slower than the kernel specialised for the program (the dispatch
+ * per node and the values' trips through per-thread local memory), and the
+ * baseline that specialisation is measured against.  Asynchronous on the
+ * stream; PSK_E_CUDA if the launch fails. */
+int psk_group_run_interp(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
+                         const psk_output* out, int32_t math_mode, void* stream);
+
 /* ================================================== psk_softmax_region
  * y[r, :] = softmax(x[r, :]) over rows of `cols` elements: m = max_j x[r,j]
  * (NaN propagates), e_j = exp(x[r,j] - m), s = the sum of e_j in the declared

@@ -16,6 +16,7 @@ from .ops import (  # noqa: F401
     psk_group_check,
     psk_group_prepare,
     psk_group_run,
+    psk_group_run_interp,
     psk_norm_region,
     psk_softmax_backward,
     psk_softmax_masked,

@@ -25,7 +25,7 @@ ERRORS = {
     -5: "PSK_E_NULL", -6: "PSK_E_ORDER", -7: "PSK_E_CUDA", -8: "PSK_E_ALIAS", -9: "PSK_E_ARG",
 }
 
-EXPORTS = ("psk_group_run", "psk_group_run_ex", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex", "psk_softmax_region", "psk_softmax_masked",
+EXPORTS = ("psk_group_run", "psk_group_run_ex", "psk_group_run_interp", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex", "psk_softmax_region", "psk_softmax_masked",
            "psk_softmax_backward", "psk_norm_region",
            "psk_adamw_tree", "psk_adamw_tree_ex", "psk_adamw_tree_static", "psk_adamw_lr", "psk_adamw_workspace",
            "psk_adamw_scalars", "psk_device_status", "psk_test_drop_row", "psk_last_error")
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.psk_group_run_ex.argtypes = [P(psk_program), P(psk_input), ctypes.c_int32, P(psk_output), ctypes.c_int32,
                                        ctypes.c_void_p]
         L.psk_group_prepare_ex.argtypes = [P(psk_program), P(psk_input), ctypes.c_int32, P(psk_output), ctypes.c_int32]
+        L.psk_group_run_interp.argtypes = [P(psk_program), P(psk_input), ctypes.c_int32, P(psk_output),
+                                           ctypes.c_int32, ctypes.c_void_p]
         L.psk_softmax_region.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                          psk_order, ctypes.c_int32, ctypes.c_void_p]
@@ -112,7 +114,7 @@ def lib() -> ctypes.CDLL:
         L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_test_drop_row.argtypes = [ctypes.c_int64]
         L.psk_last_error.restype = ctypes.c_char_p
-        for f in ("psk_group_run", "psk_group_run_ex", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex",
+        for f in ("psk_group_run", "psk_group_run_ex", "psk_group_run_interp", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex",
                   "psk_softmax_region", "psk_norm_region",
                   "psk_softmax_masked", "psk_softmax_backward",
                   "psk_adamw_tree",

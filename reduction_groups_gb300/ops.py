@@ -96,6 +96,16 @@ def psk_group_run(tokens, imm, inputs, out, stream=None, math: str = "exact") ->
     N.check(N.lib().psk_group_run_ex(ctypes.byref(p), arr, n, ctypes.byref(o), _MATH[math], _stream_handle(stream)))
 
 
+def psk_group_run_interp(tokens, imm, inputs, out, stream=None, math: str = "exact") -> None:
+    """psk_group_run through the library's precompiled interpreter kernel (no
+    run-time compilation): the same arguments and the same result bits,
+    slower."""
+    p, keep = _program(tokens, imm)
+    arr, n, o = _group_args(inputs, out)
+    N.check(N.lib().psk_group_run_interp(ctypes.byref(p), arr, n, ctypes.byref(o), _MATH[math],
+                                         _stream_handle(stream)))
+
+
 _ORDER = {"sequential": N.PSK_ORDER_SEQUENTIAL, "blocked": N.PSK_ORDER_BLOCKED,
           "interleaved": N.PSK_ORDER_INTERLEAVED}
 
