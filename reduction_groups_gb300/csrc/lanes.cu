@@ -121,53 +121,136 @@ __device__ __forceinline__ void lane_exp8(const uint4 wv, float m, float* e) {
 }
 
 
-// A full tile (64 columns) of the lane's row: its eight groups loaded first,
-// then the 64 exp values, then the adds, one basic block, so that the
-// scheduler overlaps the exp chains of different groups and the dependent
-// adds with them.
-template <int EXPM>
+// ------------------------------------------------------------ tile pieces
+// A lane's eight 16-byte groups of one tile (its row's 64 columns), loaded
+// together so that the work on them overlaps.
 __device__ __forceinline__ void lane_load8(const unsigned char* tile, uint32_t lrow, uint32_t sw, uint4* v) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) v[k] = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
 }
 
-template <int EXPM>
-__device__ __forceinline__ void lane_chain_tile(const unsigned char* tile, uint32_t lrow, uint32_t sw, float m,
-                                                float& acc) {
-  uint4 v[8];
-  lane_load8<EXPM>(tile, lrow, sw, v);
-  float e[64];
+__device__ __forceinline__ void widen8(const uint4 w, float* v) {
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int k = 0; k < 8; ++k) lane_exp8<EXPM>(v[k], m, e + 8 * k);
-#pragma unroll
-  for (int j = 0; j < 64; ++j) acc = __fadd_rn(acc, e[j]);
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __uint_as_float(wd[k] << 16);
+    v[2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
+  }
 }
 
-// e / s for the eight values of a group, rounded to bf16 pairs.
-template <int EXPM>
-__device__ __forceinline__ uint4 lane_div8(float* e, float s, float rs, f2 rs2, f2 ns2, bool fast_ok) {
-  if (EXPM == PSK_EXP_FAST && fast_ok) {
-    // Markstein's correction two at a time, as the pipelined kernel's fast
-    // realization does (no per-element range test)
+__device__ __forceinline__ uint4 pack8(const float* o) {
+  return make_uint4(f32x2_to_bf16x2(o[0], o[1]), f32x2_to_bf16x2(o[2], o[3]), f32x2_to_bf16x2(o[4], o[5]),
+                    f32x2_to_bf16x2(o[6], o[7]));
+}
+
+// Eight consecutive norm parameters from global memory (the same address in
+// every lane: one broadcast load).
+template <int PT>
+__device__ __forceinline__ void load_param8(const void* base, int j, float* v) {
+  if (PT == PSK_BF16) {
+    widen8(__ldg(reinterpret_cast<const uint4*>((const uint16_t*)base + j)), v);
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>((const float*)base + j));
+    const float4 b = __ldg(reinterpret_cast<const float4*>((const float*)base + j) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+// What a row carries from pass to pass.
+struct LaneRow {
+  float m = 0.0f;                     // softmax: the max
+  float s = 1.0f, rs = 1.0f;          // softmax: the sum and RN(1 / s)
+  bool fast_ok = true;
+  f2 rs2 = {1.0f, 1.0f}, ns2 = {-1.0f, -1.0f};
+  float mu = 0.0f;                    // LayerNorm: the mean
+  RowDivisor D;                       // norms: the divisor sqrt(var + eps)
+};
+
+// Passes per region kind, and their direction: the chains run left to right
+// (their index order); the other passes right to left, so that each pass
+// starts on the tiles the one before it read last.
+template <int KIND>
+__host__ __device__ constexpr int lane_passes() { return KIND == REGION_RMS ? 2 : 3; }
+template <int KIND>
+__host__ __device__ constexpr bool lane_rev(int pass) {
+  return KIND == REGION_SOFTMAX ? pass != 1 : pass == lane_passes<KIND>() - 1;
+}
+
+// The values a chain pass adds for a group of eight stored elements:
+// softmax e = exp(x - m) (fast realization); RMSNorm RN(x^2); LayerNorm x,
+// then RN(RN(x - mu)^2).
+template <int KIND>
+__device__ __forceinline__ void chain_values8(const uint4 w, int pass, const LaneRow& R, float* f) {
+  if constexpr (KIND == REGION_SOFTMAX) {
+    lane_exp8<PSK_EXP_FAST>(w, R.m, f);
+  } else {
+    widen8(w, f);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const f2 ea{e[2 * h], e[2 * h + 1]};
-      const f2 qa = f2_mul(ea, rs2);
-      const f2 ya = f2_fma(f2_fma(qa, ns2, ea), rs2, qa);
-      e[2 * h] = ya.x;
-      e[2 * h + 1] = ya.y;
+    for (int q = 0; q < 8; ++q) {
+      if (KIND == REGION_RMS) {
+        f[q] = __fmul_rn(f[q], f[q]);
+      } else if (pass == 1) {
+        const float c = __fsub_rn(f[q], R.mu);
+        f[q] = __fmul_rn(c, c);
+      }
+    }
+  }
+}
+
+// The outputs of a group of eight stored elements at column j, rounded to
+// bf16 pairs: softmax e / s (the pipelined kernel's fast realization); norms
+// (x - mu) / d, * gamma, + beta.
+template <int KIND, int PT>
+__device__ __forceinline__ uint4 out_group8(const uint4 w, int j, const LaneRow& R, const RegionParams& P) {
+  float o[8];
+  if constexpr (KIND == REGION_SOFTMAX) {
+    lane_exp8<PSK_EXP_FAST>(w, R.m, o);
+    if (R.fast_ok) {
+      // Markstein's correction two at a time (no per-element range test)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const f2 ea{o[2 * h], o[2 * h + 1]};
+        const f2 qa = f2_mul(ea, R.rs2);
+        const f2 ya = f2_fma(f2_fma(qa, R.ns2, ea), R.rs2, qa);
+        o[2 * h] = ya.x;
+        o[2 * h + 1] = ya.y;
+      }
+    } else {
+      row_div_n<8>(o, R.s, R.rs, false);
     }
   } else {
-    row_div_n<8>(e, s, rs, fast_ok);
+    widen8(w, o);
+    if (KIND == REGION_LAYER) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = __fsub_rn(o[q], R.mu);
+    }
+    divide_n<8>(o, R.D);
+    if (P.gamma) {
+      float g[8];
+      load_param8<PT>(P.gamma, j, g);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(o[q], g[q]);
+    }
+    if (KIND == REGION_LAYER && P.beta) {
+      float bb[8];
+      load_param8<PT>(P.beta, j, bb);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) o[q] = __fadd_rn(o[q], bb[q]);
+    }
   }
-  return make_uint4(f32x2_to_bf16x2(e[0], e[1]), f32x2_to_bf16x2(e[2], e[3]), f32x2_to_bf16x2(e[4], e[5]),
-                    f32x2_to_bf16x2(e[6], e[7]));
+  return pack8(o);
 }
 
-template <int EXPM>
+// ------------------------------------------------------------ the kernel
+// KIND: the region; PP: the declared order's partial chains (element j feeds
+// chain j mod PP; the entry points launch the one-chain orders, PP = 1); PT:
+// the norms' parameter storage type.
+template <int KIND, int PP, int PT>
 __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
-    softmax_lane_kernel(const __grid_constant__ RegionParams P, const __grid_constant__ CUtensorMap tx,
-                        const __grid_constant__ CUtensorMap ty) {
+    region_lane_kernel(const __grid_constant__ RegionParams P, const __grid_constant__ CUtensorMap tx,
+                       const __grid_constant__ CUtensorMap ty) {
+  constexpr int NP = lane_passes<KIND>();
   extern __shared__ unsigned char lane_smem_raw[];
   __shared__ __align__(8) uint64_t full[LANE_WARPS][LANE_NI];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -178,7 +261,7 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   const int64_t gw = (int64_t)blockIdx.x * LANE_WARPS + w;
   const int64_t wtot = (int64_t)gridDim.x * LANE_WARPS;
   const int my_batches = gw < nbatch_all ? (int)((nbatch_all - 1 - gw) / wtot + 1) : 0;
-  const int64_t total = (int64_t)my_batches * 3 * nch;       // tile requests of this warp
+  const int64_t total = (int64_t)my_batches * NP * nch;      // tile requests of this warp
   // tiles start on 1024-byte boundaries (the period of the 128-byte swizzle)
   const uint32_t raw = smem_addr(lane_smem_raw);
   unsigned char* wp = lane_smem_raw + (((raw + 1023u) & ~1023u) - raw) + (size_t)w * LANE_WARP_SMEM;
@@ -189,10 +272,13 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   uint64_t* bars = full[w];
   const uint64_t pol_keep = policy_evict_last(), pol_drop = policy_evict_first();
   const long long drop = g_pipe_drop_row;
+  const float n_f = (float)cols;                               // exact: cols <= 4096
 
-  // zero the warp's tiles: rows beyond the batch are never copied in and read
-  // as zeros (benign values, no slow paths), like rows past the tensor's end
-  for (int o = lane * 16; o < LANE_WARP_SMEM; o += 32 * 16) *reinterpret_cast<uint4*>(wp + o) = make_uint4(0, 0, 0, 0);
+  // fill the warp's tiles with bf16 ones: rows beyond the batch are never
+  // copied in, and their lanes then compute on benign values that take no
+  // slow path in any region (rows past the tensor's end read as zeros)
+  for (int o = lane * 16; o < LANE_WARP_SMEM; o += 32 * 16)
+    *reinterpret_cast<uint4*>(wp + o) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   fence_proxy_async_smem();
   if (lane == 0) {
     for (int i = 0; i < LANE_NI; ++i) mbar_init(&bars[i], 1);
@@ -200,25 +286,26 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   }
   __syncwarp();
 
-  // ---- requests (lane 0): q = ((batch * 3) + pass) * nch + tile, into slot q % NI;
-  // the request state is kept by every lane alike
+  // ---- requests (lane 0): q = ((batch * NP) + pass) * nch + tile, into slot
+  // q % NI; the request state is kept by every lane alike
   int64_t rq = 0;
   int rb = 0, rp = 0, rc = 0;
   int64_t withheld = -1;                                     // test hook: the request never made
   auto issue = [&]() {
     const int slot = (int)(rq % LANE_NI);
     const int64_t r0 = (gw + (int64_t)rb * wtot) * nb;
-    const int tc = rp == 1 ? rc : nch - 1 - rc;               // the pass's tile order
+    const int tc = lane_rev<KIND>(rp) ? nch - 1 - rc : rc;   // the pass's tile order
     if (rp == 0 && rc == 0 && drop >= (long long)rb * nb && drop < (long long)rb * nb + nb) {
       withheld = rq;                                         // as if this copy were lost
     } else if (lane == 0) {
       mbar_arrive_expect_tx(&bars[slot], (uint32_t)nb * 128u);
-      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)r0, &bars[slot], rp < 2 ? pol_keep : pol_drop);
+      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)r0, &bars[slot],
+                rp < NP - 1 ? pol_keep : pol_drop);
     }
     ++rq;
     if (++rc == nch) {
       rc = 0;
-      if (++rp == 3) { rp = 0; ++rb; }
+      if (++rp == NP) { rp = 0; ++rb; }
     }
   };
   for (int i = 0; i < LANE_NI && rq < total; ++i) issue();
@@ -236,89 +323,97 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     if (lane == 0) fence_proxy_async_smem();
     if (rq < total) issue();
   };
-  auto group = [&](int k) -> uint4 {                         // the lane's k-th group of the tile being read
-    return *reinterpret_cast<const uint4*>(wp + (size_t)(cq % LANE_NI) * LANE_TILE + lrow + (((uint32_t)k ^ sw) << 4));
-  };
   int64_t oq = 0;                                            // output tiles written
 
   for (int b = 0; b < my_batches && !dead; ++b) {
     const int64_t r0 = (gw + (int64_t)b * wtot) * nb;
-    // pass 0: the max, on the stored bf16 pairs
-    uint32_t mb = 0xFF80FF80u;                              // (-inf, -inf)
-    for (int t = 0; t < nch; ++t) {
-      const int c = nch - 1 - t;                             // right to left (the max is order-free)
-      if (!take()) { dead = true; break; }
-      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
+    LaneRow R;
+    for (int pass = 0; pass < NP && !dead; ++pass) {
+      const bool rev = lane_rev<KIND>(pass);
+      const bool out_pass = pass == NP - 1;
+      const bool max_pass = KIND == REGION_SOFTMAX && pass == 0;
+      uint32_t mb = 0xFF80FF80u;                            // softmax max: (-inf, -inf)
+      float acc[PP];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (k < ng) {
-          const uint4 v = group(k);
-          mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.x, v.y));
-          mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.z, v.w));
-        }
-      }
-      release();
-    }
-    if (dead) break;
-    const float m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
-
-    // pass 1: the chain, left to right
-    float acc = 0.0f;                                        // 0 + e_0 = e_0: the chain starts at e_0
-    for (int c = 0; c < nch; ++c) {
-      if (!take()) { dead = true; break; }
-      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
-      if (ng == 8) {
-        lane_chain_tile<EXPM>(wp + (size_t)(cq % LANE_NI) * LANE_TILE, lrow, sw, m, acc);
-      } else {
-        for (int k = 0; k < ng; ++k) {
-          float e[8];
-          lane_exp8<EXPM>(group(k), m, e);
+      for (int p = 0; p < PP; ++p) acc[p] = -0.0f;          // -0 + f = f for every f: the chain starts at f(x_p)
+      for (int t = 0; t < nch; ++t) {
+        const int c = rev ? nch - 1 - t : t;
+        if (!take()) { dead = true; break; }
+        const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
+        const unsigned char* tile = wp + (size_t)(cq % LANE_NI) * LANE_TILE;
+        if (out_pass) {
+          if (lane == 0) bulk_wait_read<LANE_NO - 1>();     // the store that last used this slot has read it
+          __syncwarp();
+          unsigned char* ot = op + (size_t)(oq % LANE_NO) * LANE_TILE;
+          if (ng == 8) {
+            uint4 v[8], o8[8];
+            lane_load8(tile, lrow, sw, v);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc = __fadd_rn(acc, e[q]);
-        }
-      }
-      release();
-    }
-    if (dead) break;
-    const float s = acc;
-    const float rs = __frcp_rn(s);
-    const bool fast_ok = s >= 1.0f && s < 0x1p20f;
-
-    // pass 2: e recomputed, divided, rounded to bf16, staged and stored
-    const f2 rs2 = f2_splat(rs), ns2 = f2_splat(-s);
-    for (int t = 0; t < nch; ++t) {
-      const int c = nch - 1 - t;                             // right to left (elementwise)
-      if (!take()) { dead = true; break; }
-      const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
-      if (lane == 0) bulk_wait_read<LANE_NO - 1>();         // the store that last used this slot has read it
-      __syncwarp();
-      unsigned char* ot = op + (size_t)(oq % LANE_NO) * LANE_TILE;
-      if (ng == 8) {
-        uint4 v[8], o8[8];
-        lane_load8<EXPM>(wp + (size_t)(cq % LANE_NI) * LANE_TILE, lrow, sw, v);
+            for (int k = 0; k < 8; ++k) o8[k] = out_group8<KIND, PT>(v[k], c * LANE_TC + 8 * k, R, P);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          float e[8];
-          lane_exp8<EXPM>(v[k], m, e);
-          o8[k] = lane_div8<EXPM>(e, s, rs, rs2, ns2, fast_ok);
-        }
+            for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = o8[k];
+          } else {
+            for (int k = 0; k < ng; ++k) {
+              const uint4 v = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
+              *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) =
+                  out_group8<KIND, PT>(v, c * LANE_TC + 8 * k, R, P);
+            }
+          }
+          fence_proxy_async_smem();                          // this lane's writes, before the async store
+          __syncwarp();
+          if (lane == 0) {
+            tile_store(&ty, c * LANE_TC, (int)r0, smem_addr(ot), pol_drop);
+            bulk_commit();
+          }
+          ++oq;
+        } else if (max_pass) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = o8[k];
-      } else {
-        for (int k = 0; k < ng; ++k) {
-          float e[8];
-          lane_exp8<EXPM>(group(k), m, e);
-          *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = lane_div8<EXPM>(e, s, rs, rs2, ns2, fast_ok);
+          for (int k = 0; k < 8; ++k) {
+            if (k < ng) {
+              const uint4 v = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
+              mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.x, v.y));
+              mb = bf16x2_max_nan(mb, bf16x2_max_nan(v.z, v.w));
+            }
+          }
+        } else if (ng == 8) {
+          // a chain pass over a full tile: element 8 k + q feeds chain q mod P
+          uint4 v[8];
+          lane_load8(tile, lrow, sw, v);
+          float f[64];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) chain_values8<KIND>(v[k], pass, R, f + 8 * k);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) acc[j % PP] = __fadd_rn(acc[j % PP], f[j]);
+        } else {
+          for (int k = 0; k < ng; ++k) {
+            float f[8];
+            chain_values8<KIND>(*reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4)), pass, R, f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q % PP] = __fadd_rn(acc[q % PP], f[q]);
+          }
         }
+        release();
       }
-      fence_proxy_async_smem();                              // this lane's writes, before the async store
-      __syncwarp();
-      if (lane == 0) {
-        tile_store(&ty, c * LANE_TC, (int)r0, smem_addr(ot), pol_drop);
-        bulk_commit();
+      if (dead) break;
+      // what the pass leaves for the next ones
+      float sum = acc[0];
+#pragma unroll
+      for (int p = 1; p < PP; ++p) sum = __fadd_rn(sum, acc[p]);   // partials left to right
+      if (KIND == REGION_SOFTMAX) {
+        if (pass == 0) {
+          R.m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
+        } else if (pass == 1) {
+          R.s = sum;
+          R.rs = __frcp_rn(sum);
+          R.fast_ok = sum >= 1.0f && sum < 0x1p20f;
+          R.rs2 = f2_splat(R.rs);
+          R.ns2 = f2_splat(-sum);
+        }
+      } else if (KIND == REGION_LAYER && pass == 0) {
+        R.mu = __fdiv_rn(sum, n_f);
+      } else if (!out_pass) {                                // the sum of squares: the divisor
+        R.D = make_divisor(__fsqrt_rn(__fadd_rn(__fdiv_rn(sum, n_f), P.eps)));
       }
-      ++oq;
-      release();
     }
   }
 
@@ -377,41 +472,38 @@ static int lane_batch_rows(int64_t rows, int64_t wtot) {
   return (int)((rpw + nbat - 1) / nbat);
 }
 
+template <int KIND, int PP, int PT>
 static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUtensorMap& ty, int64_t sms,
                         cudaStream_t stream) {
   static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)softmax_lane_kernel<PSK_EXP_FAST>, LANE_SMEM, attr);
+  smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT>, LANE_SMEM, attr);
   const int64_t nbatch = (P.rows + P.nb - 1) / P.nb;
   const int64_t need = (nbatch + LANE_WARPS - 1) / LANE_WARPS;
   const unsigned grid = (unsigned)(need < sms ? need : sms);
-  softmax_lane_kernel<PSK_EXP_FAST><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
-  return check_launch("softmax region kernel (lane per row)");
+  region_lane_kernel<KIND, PP, PT><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
+  return check_launch("row region kernel (lane per row)");
 }
 
-// The kernel takes the fast realization of the one-chain orders (sequential,
-// blocked) over bf16 rows (x and y) of 64 <= cols <= 4096 columns, cols a
-// multiple of 8, whose rows start on 16-byte boundaries, and at least 8 rows
-// per warp of a full grid (fewer rows leave most lanes idle; the pipelined
-// kernel spreads each row over a team instead).  Interleaved orders stay with
-// the pipelined kernel: their chains are short there, and the second exp per
-// element would cost more than the lane kernel saves.  Tuning
-// aids, read once: PSK_LANES=0 turns the kernel off, PSK_LANE_MIN_ROWS sets
-// the row threshold, PSK_LANE_NB (1..32) the rows per batch.
-int softmax_lanes(const RegionParams& P0, int exp_mode, cudaStream_t stream, bool* taken) {
-  *taken = false;
-  if (exp_mode != PSK_EXP_FAST) return PSK_OK;
+// The rows every lane-kernel region takes: bf16 x and y (checked by the
+// callers) of 64 <= cols <= 4096 columns, cols a multiple of 8, rows on
+// 16-byte boundaries, at least 8 rows per warp of a full grid (fewer rows
+// leave most lanes idle; the pipelined kernel spreads each row over a team
+// instead).  On success P carries the batch height and tx / ty the maps.
+// Tuning aids, read once: PSK_LANES=0 turns the kernel off,
+// PSK_LANE_MIN_ROWS sets the row threshold, PSK_LANE_NB (1..32) the rows per
+// batch.
+static bool lanes_take(RegionParams& P, CUtensorMap& tx, CUtensorMap& ty, int64_t& sms, int& rc) {
+  rc = PSK_OK;
   static const char* off = getenv("PSK_LANES");
-  if (off && off[0] == '0') return PSK_OK;
-  if (P0.partials != 1) return PSK_OK;
-  if (P0.cols < LANE_TC || P0.cols > LANE_MAX_COLS || P0.cols % 8 != 0 || P0.ldx % 8 != 0 || P0.ldy % 8 != 0 ||
-      (uintptr_t)P0.x % 16 != 0 || (uintptr_t)P0.y % 16 != 0 || P0.rows >= ((int64_t)1 << 31))
-    return PSK_OK;
-  const int64_t sms = device_sm_count();
+  if (off && off[0] == '0') return false;
+  if (P.cols < LANE_TC || P.cols > LANE_MAX_COLS || P.cols % 8 != 0 || P.ldx % 8 != 0 || P.ldy % 8 != 0 ||
+      (uintptr_t)P.x % 16 != 0 || (uintptr_t)P.y % 16 != 0 || P.rows >= ((int64_t)1 << 31))
+    return false;
+  sms = device_sm_count();
   const int64_t wtot = sms * LANE_WARPS;
   static const char* min_env = getenv("PSK_LANE_MIN_ROWS");
   const int64_t min_rows = min_env ? atoll(min_env) : 8 * wtot;
-  if (P0.rows < min_rows) return PSK_OK;
-  RegionParams P = P0;
+  if (P.rows < min_rows) return false;
   P.nb = lane_batch_rows(P.rows, wtot);
   static const char* nb_env = getenv("PSK_LANE_NB");
   if (nb_env) {
@@ -419,13 +511,48 @@ int softmax_lanes(const RegionParams& P0, int exp_mode, cudaStream_t stream, boo
     if (v >= 1 && v <= 32) P.nb = v;
   }
   if (P.nb > P.rows) P.nb = (int)P.rows;
-  CUtensorMap tx, ty;
-  int rc = encode_rows(&tx, P.x, P.rows, P.cols, P.ldx, P.nb);
-  if (rc) return rc;
+  if ((rc = encode_rows(&tx, P.x, P.rows, P.cols, P.ldx, P.nb))) return true;
   rc = encode_rows(&ty, P.y, P.rows, P.cols, P.ldy, P.nb);
-  if (rc) return rc;
+  return true;
+}
+
+// The softmax region: the fast realization of the one-chain orders
+// (sequential, blocked).  Interleaved orders stay with the pipelined kernel:
+// their chains are short there, and the second exp per element would cost
+// more than the lane kernel saves; so does the correctly rounded exp.
+int softmax_lanes(const RegionParams& P0, int exp_mode, cudaStream_t stream, bool* taken) {
+  *taken = false;
+  if (exp_mode != PSK_EXP_FAST || P0.partials != 1) return PSK_OK;
+  RegionParams P = P0;
+  CUtensorMap tx, ty;
+  int64_t sms = 0;
+  int rc = PSK_OK;
+  if (!lanes_take(P, tx, ty, sms, rc)) return PSK_OK;
   *taken = true;
-  return launch_lanes(P, tx, ty, sms, stream);
+  if (rc) return rc;
+  return launch_lanes<REGION_SOFTMAX, 1, PSK_F32>(P, tx, ty, sms, stream);
+}
+
+// RMSNorm and LayerNorm: the one-chain orders too (interleaved orders run
+// faster on the pipelined kernel, whose chains are short there); scale and
+// bias (if any) on 16-byte boundaries.
+int norm_lanes(const RegionParams& P0, int kind, cudaStream_t stream, bool* taken) {
+  *taken = false;
+  if (P0.partials != 1) return PSK_OK;
+  if ((uintptr_t)P0.gamma % 16 != 0 || (uintptr_t)P0.beta % 16 != 0) return PSK_OK;
+  RegionParams P = P0;
+  CUtensorMap tx, ty;
+  int64_t sms = 0;
+  int rc = PSK_OK;
+  if (!lanes_take(P, tx, ty, sms, rc)) return PSK_OK;
+  *taken = true;
+  if (rc) return rc;
+  const bool bf = P.param_dtype == PSK_BF16;
+  if (kind == REGION_RMS)
+    return bf ? launch_lanes<REGION_RMS, 1, PSK_BF16>(P, tx, ty, sms, stream)
+              : launch_lanes<REGION_RMS, 1, PSK_F32>(P, tx, ty, sms, stream);
+  return bf ? launch_lanes<REGION_LAYER, 1, PSK_BF16>(P, tx, ty, sms, stream)
+            : launch_lanes<REGION_LAYER, 1, PSK_F32>(P, tx, ty, sms, stream);
 }
 
 // The status word and test hook of this translation unit's kernels (pipe.cuh

@@ -237,49 +237,6 @@ __device__ __forceinline__ float run_chain(const float* E, int n, int p, int P) 
   return run_chain(E, n, p, P, ChainIdentity());
 }
 
-// Division by a row's divisor d > 0 of any magnitude (the norms' sqrt):
-// d = dd 2^-k with dd in [1, 2); a / d = (a 2^k) / dd exactly, and for
-// 2^-100 <= |a 2^k| <= 2^100 Markstein's correction through RN(1/dd) gives the
-// IEEE quotient; other operands, and rows whose d is not a normal number
-// below 2^127, take IEEE division.
-struct RowDivisor {
-  float d, dd, rdd, scale;
-  bool ok;
-};
-
-__device__ __forceinline__ RowDivisor make_divisor(float d) {
-  RowDivisor r;
-  r.d = d;
-  const uint32_t b = __float_as_uint(d);
-  const int e = (int)((b >> 23) & 0xFFu) - 127;
-  r.ok = d > 0.0f && e >= -126 && e <= 126;
-  r.dd = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
-  r.scale = __uint_as_float((uint32_t)(r.ok ? 127 - e : 127) << 23);
-  r.rdd = __frcp_rn(r.dd);
-  return r;
-}
-
-template <int N>
-__device__ __forceinline__ void divide_n(float* o, const RowDivisor& D) {
-  float y[N];
-  bool bad = !D.ok;
-#pragma unroll
-  for (int q = 0; q < N; ++q) {
-    const float a = __fmul_rn(o[q], D.scale);
-    const float qq = a * D.rdd;
-    const float r = fmaf(-qq, D.dd, a);
-    y[q] = fmaf(r, D.rdd, qq);
-    const float aa = fabsf(a);
-    bad = bad || !(aa >= 0x1p-100f && aa <= 0x1p100f);
-  }
-  if (bad) {
-#pragma unroll
-    for (int q = 0; q < N; ++q) y[q] = __fdiv_rn(o[q], D.d);
-  }
-#pragma unroll
-  for (int q = 0; q < N; ++q) o[q] = y[q];
-}
-
 // --------------------------------------------------- resident rows (<= 4096)
 template <int XT, int YT, int EXPM, bool VEC>
 __global__ void __launch_bounds__(SM_THREADS, 3) softmax_batch_kernel(const __grid_constant__ RegionParams P) {
@@ -1396,6 +1353,11 @@ extern "C" int psk_norm_region(const void* x, int32_t xt, void* y, int32_t yt, i
                     partials <= 32 && (uintptr_t)x % 16 == 0 && (uintptr_t)y % 16 == 0 &&
                     (uintptr_t)gamma % 16 == 0 && (uintptr_t)beta % 16 == 0;
   cudaStream_t s = (cudaStream_t)stream;
+  if (xt == PSK_BF16 && yt == PSK_BF16) {   // many rows: a lane per row (lanes.cu)
+    bool taken = false;
+    const int rc = norm_lanes(P, kind == PSK_NORM_RMS ? REGION_RMS : REGION_LAYER, s, &taken);
+    if (taken) return rc;
+  }
   return kind == PSK_NORM_RMS ? dispatch_norm_types<REGION_RMS>(P, xt, yt, pipe, s)
                               : dispatch_norm_types<REGION_LAYER>(P, xt, yt, pipe, s);
 }

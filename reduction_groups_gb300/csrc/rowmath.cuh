@@ -130,11 +130,58 @@ __device__ __forceinline__ void row_div_n(float* o, float s, float rs, bool fast
   for (int q = 0; q < N; ++q) o[q] = y[q];
 }
 
-// Launches the lane-per-row softmax kernel (lanes.cu) for rows it takes
-// (the fast realization of the one-chain orders over bf16 x and y, 16-byte
-// aligned rows of 64 to 4096 columns, a multiple of 8, enough rows to fill
-// the GPU); *taken is false, and nothing is launched, for other rows.
+// Division by a row's divisor d > 0 of any magnitude (the norms' sqrt):
+// d = dd 2^-k with dd in [1, 2); a / d = (a 2^k) / dd exactly, and for
+// 2^-100 <= |a 2^k| <= 2^100 Markstein's correction through RN(1/dd) gives the
+// IEEE quotient; a zero dividend gives itself (+-0 / d = +-0 for d > 0; the
+// correction would turn -0 into +0); other operands, and rows whose d is not
+// a normal number below 2^127, take IEEE division.
+struct RowDivisor {
+  float d, dd, rdd, scale;
+  bool ok;
+};
+
+__device__ __forceinline__ RowDivisor make_divisor(float d) {
+  RowDivisor r;
+  r.d = d;
+  const uint32_t b = __float_as_uint(d);
+  const int e = (int)((b >> 23) & 0xFFu) - 127;
+  r.ok = d > 0.0f && e >= -126 && e <= 126;
+  r.dd = __uint_as_float((b & 0x007FFFFFu) | 0x3F800000u);
+  r.scale = __uint_as_float((uint32_t)(r.ok ? 127 - e : 127) << 23);
+  r.rdd = __frcp_rn(r.dd);
+  return r;
+}
+
+template <int N>
+__device__ __forceinline__ void divide_n(float* o, const RowDivisor& D) {
+  float y[N];
+  bool bad = !D.ok;
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const float a = __fmul_rn(o[q], D.scale);
+    const float qq = a * D.rdd;
+    const float r = fmaf(-qq, D.dd, a);
+    y[q] = fmaf(r, D.rdd, qq);
+    const float aa = fabsf(a);
+    if (aa == 0.0f) y[q] = a;
+    bad = bad || !((aa >= 0x1p-100f && aa <= 0x1p100f) || aa == 0.0f);
+  }
+  if (bad) {
+#pragma unroll
+    for (int q = 0; q < N; ++q) y[q] = __fdiv_rn(o[q], D.d);
+  }
+#pragma unroll
+  for (int q = 0; q < N; ++q) o[q] = y[q];
+}
+
+// Launch the lane-per-row kernel (lanes.cu) for rows it takes: bf16 x and y,
+// 16-byte aligned rows of 64 to 4096 columns (a multiple of 8), enough rows
+// to fill the GPU, the one-chain orders (sequential, blocked); for the softmax
+// its fast realization; for the norms kind REGION_RMS or REGION_LAYER.
+// *taken is false, and nothing is launched, for other rows.
 int softmax_lanes(const RegionParams& P, int exp_mode, cudaStream_t stream, bool* taken);
+int norm_lanes(const RegionParams& P, int kind, cudaStream_t stream, bool* taken);
 // The lane kernel's status word (read, then zeroed if `reset`) and its copy
 // of the lost-copy test hook (lanes.cu keeps its own, like every unit).
 int lanes_status(unsigned int* v, bool reset);
