@@ -96,30 +96,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // The eight exp values of a 16-byte group of bf16 x (element 2k in the low
-// half of word k): x - m, then the region's exp -- the same operations as the
-// pipelined kernel's (fast: x + (-m) and the exp on f32 pairs; exact: the
-// correctly rounded exp of RN(x - m)).
-template <int EXPM>
+// half of word k): x + (-m) and the faithful exp on f32 pairs -- the same
+// operations as the pipelined kernel's fast realization, so the same bits.
 __device__ __forceinline__ void lane_exp8(const uint4 wv, float m, float* e) {
   const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-  if constexpr (EXPM == PSK_EXP_FAST) {
-    const f2 nm = f2_splat(-m);
+  const f2 nm = f2_splat(-m);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const f2 r = exp2_faithful_nonpos(f2_add(f2{__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xFFFF0000u)}, nm));
-      e[2 * k] = r.x;
-      e[2 * k + 1] = r.y;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      e[2 * k] = __fsub_rn(__uint_as_float(wd[k] << 16), m);
-      e[2 * k + 1] = __fsub_rn(__uint_as_float(wd[k] & 0xFFFF0000u), m);
-    }
-    region_exp8<EXPM>(e);
+  for (int k = 0; k < 4; ++k) {
+    const f2 r = exp2_faithful_nonpos(f2_add(f2{__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xFFFF0000u)}, nm));
+    e[2 * k] = r.x;
+    e[2 * k + 1] = r.y;
   }
 }
-
 
 // ------------------------------------------------------------ tile pieces
 // A lane's eight 16-byte groups of one tile (its row's 64 columns), loaded
@@ -183,7 +171,7 @@ __host__ __device__ constexpr bool lane_rev(int pass) {
 template <int KIND>
 __device__ __forceinline__ void chain_values8(const uint4 w, int pass, const LaneRow& R, float* f) {
   if constexpr (KIND == REGION_SOFTMAX) {
-    lane_exp8<PSK_EXP_FAST>(w, R.m, f);
+    lane_exp8(w, R.m, f);
   } else {
     widen8(w, f);
 #pragma unroll
@@ -205,7 +193,7 @@ template <int KIND, int PT>
 __device__ __forceinline__ uint4 out_group8(const uint4 w, int j, const LaneRow& R, const RegionParams& P) {
   float o[8];
   if constexpr (KIND == REGION_SOFTMAX) {
-    lane_exp8<PSK_EXP_FAST>(w, R.m, o);
+    lane_exp8(w, R.m, o);
     if (R.fast_ok) {
       // Markstein's correction two at a time (no per-element range test)
 #pragma unroll
