@@ -300,6 +300,21 @@ def cpu_sample(scale: float = 1.0, min_seconds: float = 0.0):
     return nbytes, dt, desc
 
 
+def cpu_small_group_ms(reps: int = 20) -> float:
+    """The oracle on the five-op group over 64x64 f32 (the launch-latency
+    case), milliseconds per evaluation on one host core."""
+    import oracle.group as OG
+    from synth import workloads as W
+
+    wl = W.small_group()
+    args = [(a_, dt, s.strides) for (a_, dt), s in zip(wl.host_inputs(), wl.inputs)]
+    OG.evaluate(wl.tokens, wl.imm, args, wl.out_shape, wl.out_dtype)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        OG.evaluate(wl.tokens, wl.imm, args, wl.out_shape, wl.out_dtype)
+    return (time.perf_counter() - t0) * 1e3 / reps
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(a, ws, rank, local):
     import numpy as np
@@ -469,6 +484,42 @@ def run_ours(a, ws, rank, local):
             e1.record()
             torch.cuda.synchronize()
             extra_ms[name] = e0.elapsed_time(e1) / a.steps
+
+    # the launch-latency cases beside the step: the five-op group on 64x64 f32
+    # and the 28-leaf GPT tree (108,032 parameters) as one launch against one
+    # launch per leaf
+    latency = None
+    if a.only == "all":
+        def per_launch_us(fn, reps=200):
+            for _ in range(10):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / reps
+
+        sg = W.small_group()
+        sg_in = sg.device_inputs()
+        sg_args = [(t, s_.strides) for t, s_ in zip(sg_in, sg.inputs)]
+        sg_out = torch.empty(sg.out_shape, dtype=torch.float32, device="cuda")
+        us_g = per_launch_us(lambda: R.psk_group_run(sg.tokens, sg.imm, sg_args, sg_out))
+        gt = W.gpt_adamw_leaves()
+        g_leaves = [gt.device_leaf(i) for i in range(len(gt.leaves))]
+        us_tree = per_launch_us(lambda: R.psk_adamw_tree(g_leaves, gt.hp))
+        us_per_leaf = per_launch_us(lambda: [R.psk_adamw_tree([lf], gt.hp) for lf in g_leaves], reps=50)
+        latency = {
+            "small_group_64x64_f32": {"us_per_launch": round(us_g, 2), "bytes": sg.algorithmic_bytes(),
+                                      "gbs": round(sg.algorithmic_bytes() / (us_g * 1e3), 2)},
+            "gpt_tree_28_leaves": {"us_one_launch": round(us_tree, 2), "us_one_launch_per_leaf": round(us_per_leaf, 2),
+                                   "launches": [1, len(g_leaves)], "params": gt.n_params,
+                                   "params_per_s": round(gt.n_params / (us_tree * 1e-6), 1)},
+            "note": "back-to-back calls through the Python binding on one stream, CUDA events over the batch, "
+                    "outside the timed region: host-bound (argument marshalling, planning, the launch), not device "
+                    "time",
+        }
 
     # end to end through the public API with host buffers: per step, copy every
     # input from pinned host memory, run the step, read every result back.
@@ -645,7 +696,8 @@ def run_ours(a, ws, rank, local):
     if not a.no_cpu and ws == 1 and a.only == "all":
         nb, dt, desc = cpu_sample(15.0, min_seconds=10.0)
         cpu = {"value": round(nb / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": desc + f"; {dt:.1f} s of one host core (numpy ufuncs run single-threaded)"}
+               "sample": desc + f"; {dt:.1f} s of one host core (numpy ufuncs run single-threaded)",
+               "small_group_64x64_ms": round(cpu_small_group_ms(), 3)}
 
     value = job_value(bytes_step, a.steps, ws, total_ms)
     line = {
@@ -658,6 +710,7 @@ def run_ours(a, ws, rank, local):
                    "softmax_exp": em, "group_math": gm, "l2": "inputs larger than L2 (no flush needed)",
                    "bytes_per_step": int(bytes_step), "parallelism": f"replicas x{ws}"},
         "kernels": kinfo, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "latency_cases": latency,
         "gpu_launches": len(kernels) * a.steps,
     }
     if a.only != "all" or a.scale != 1.0:
