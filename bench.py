@@ -501,24 +501,43 @@ def run_ours(a, ws, rank, local):
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) * 1e3 / reps
 
+        import ctypes
+
+        from reduction_groups_gb300 import _native as N
+        from reduction_groups_gb300 import ops as O
+
         sg = W.small_group()
         sg_in = sg.device_inputs()
         sg_args = [(t, s_.strides) for t, s_ in zip(sg_in, sg.inputs)]
         sg_out = torch.empty(sg.out_shape, dtype=torch.float32, device="cuda")
         us_g = per_launch_us(lambda: R.psk_group_run(sg.tokens, sg.imm, sg_args, sg_out))
+        # the same calls with the C structs built once (what a C caller pays)
+        lib, st = N.lib(), O._stream_handle(None)
+        p_, keep_ = O._program(sg.tokens, sg.imm)
+        arr_, n_, o_ = O._group_args(sg_args, sg_out)
+        us_g_c = per_launch_us(lambda: lib.psk_group_run_ex(ctypes.byref(p_), arr_, n_, ctypes.byref(o_), 0, st))
         gt = W.gpt_adamw_leaves()
         g_leaves = [gt.device_leaf(i) for i in range(len(gt.leaves))]
         us_tree = per_launch_us(lambda: R.psk_adamw_tree(g_leaves, gt.hp))
         us_per_leaf = per_launch_us(lambda: [R.psk_adamw_tree([lf], gt.hp) for lf in g_leaves], reps=50)
+        tab_, nt_ = O._leaf_table(g_leaves)
+        h_ = O._hparams(gt.hp)
+        one_ = [O._leaf_table([lf]) for lf in g_leaves]
+        us_tree_c = per_launch_us(lambda: lib.psk_adamw_tree(tab_, nt_, ctypes.byref(h_), st))
+        us_per_leaf_c = per_launch_us(lambda: [lib.psk_adamw_tree(t_, k_, ctypes.byref(h_), st) for t_, k_ in one_],
+                                      reps=50)
         latency = {
-            "small_group_64x64_f32": {"us_per_launch": round(us_g, 2), "bytes": sg.algorithmic_bytes(),
-                                      "gbs": round(sg.algorithmic_bytes() / (us_g * 1e3), 2)},
+            "small_group_64x64_f32": {"us_per_call": round(us_g, 2), "us_per_call_c_abi": round(us_g_c, 2),
+                                      "bytes": sg.algorithmic_bytes(),
+                                      "gbs": round(sg.algorithmic_bytes() / (us_g_c * 1e3), 2)},
             "gpt_tree_28_leaves": {"us_one_launch": round(us_tree, 2), "us_one_launch_per_leaf": round(us_per_leaf, 2),
+                                   "us_one_launch_c_abi": round(us_tree_c, 2),
+                                   "us_one_launch_per_leaf_c_abi": round(us_per_leaf_c, 2),
                                    "launches": [1, len(g_leaves)], "params": gt.n_params,
-                                   "params_per_s": round(gt.n_params / (us_tree * 1e-6), 1)},
-            "note": "back-to-back calls through the Python binding on one stream, CUDA events over the batch, "
-                    "outside the timed region: host-bound (argument marshalling, planning, the launch), not device "
-                    "time",
+                                   "params_per_s": round(gt.n_params / (us_tree_c * 1e-6), 1)},
+            "note": "back-to-back calls on one stream, CUDA events over the batch, outside the timed region; "
+                    "through the Python binding, and through the C ABI with its argument structs built once; "
+                    "host-bound at these sizes (argument handling, planning, the launch), not device time",
         }
 
     # end to end through the public API with host buffers: per step, copy every
