@@ -126,6 +126,36 @@ def test_refusals_name_the_fault(native):
         ops.psk_group_check(W.encode([("IN", 0), ("NEG",)]), 17)
 
 
+def test_interpreter_refuses_before_any_device_work(native):
+    """psk_group_run_interp validates exactly as psk_group_run does and
+    refuses before touching a device (host tensors stand in for the
+    pointers, which a refusal never dereferences)."""
+    import torch
+
+    from reduction_groups_gb300 import ops
+
+    x = torch.zeros((4, 8))
+    y = torch.empty((4, 8))
+    L = native.lib()
+
+    def call(tokens, inputs, out, math=0):
+        p, keep = ops._program(tokens, [])
+        arr, n, o = ops._group_args(inputs, out)
+        rc = L.psk_group_run_interp(ctypes.byref(p), arr, n, ctypes.byref(o), math, None)
+        return rc, L.psk_last_error().decode()
+
+    rc, msg = call(W.encode([("IN", 0)] + [("NEG",)] * 65), [(x, (8, 1))], y)
+    assert rc == -2 and "cap" in msg                                 # PSK_E_TOO_MANY_NODES
+    rc, _ = call(W.encode([("IN", 1), ("NEG",)]), [(x, (8, 1))], y)
+    assert rc == -1                                                   # PSK_E_PROGRAM
+    rc, _ = call(W.encode([("IN", 0), ("NEG",)]), [(x, (8, 1))], y, math=3)
+    assert rc == -9                                                   # PSK_E_ARG
+    # an input overlapping the output with another layout
+    buf = torch.zeros(64)
+    rc, msg = call(W.encode([("IN", 0), ("NEG",)]), [(buf[1:33].view(4, 8), (8, 1))], buf[:32].view(4, 8))
+    assert rc == -8                                                   # PSK_E_ALIAS
+
+
 def test_adamw_scalars_equal_oracle_injection(native):
     from reduction_groups_gb300 import ops
 
