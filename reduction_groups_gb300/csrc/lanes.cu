@@ -1,34 +1,40 @@
-// Lane-per-row softmax region: Reduce(Max) -> Sub -> Exp -> Reduce(Sum) ->
-// Div over bf16 rows (poot "Fusion and Planning", Reduction-rooted regions),
-// the sum in the declared order's bracketing tree (presk "Native execution",
-// the realization's order; metrale "The LKB in Mathematics", section 2):
-// sequential and blocked(w), one chain ((e0 + e1) + e2) + ... per row.
+// Lane-per-row row regions over bf16 rows (poot "Fusion and Planning",
+// Reduction-rooted regions): the softmax, Reduce(Max) -> Sub -> Exp ->
+// Reduce(Sum) -> Div, and the norms, RMSNorm's Reduce(Sum of x^2) and
+// LayerNorm's Reduce(Sum) then Reduce(Sum of (x - mu)^2), each followed by its
+// divide (presk PSK-Realize, "What it removes"); every sum in the declared
+// order's bracketing tree (presk "Native execution", the realization's order;
+// metrale "The LKB in Mathematics", section 2): the sequential and blocked(w)
+// orders, one chain ((f0 + f1) + f2) + ... per row.
 //
 // Each lane of a warp owns one row of the warp's batch (nb <= 32 consecutive
-// rows) and runs the three passes over it itself:
-//   pass 0: m = max over the row (on the stored bf16 pairs, exact);
-//   pass 1: e_j = exp(x_j - m), added to the row's chain in index order;
-//   pass 2: e_j recomputed (the same operations on the same values: the same
-//           bits), y_j = bf16_rn(e_j / s).
+// rows) and runs every pass over it itself:
+//   softmax:   m = max over the row (on the stored bf16 pairs, exact); the
+//              chain of e_j = exp(x_j - m); the output pass, e_j recomputed
+//              (the same operations on the same values: the same bits) and
+//              y_j = bf16_rn(e_j / s);
+//   RMSNorm:   the chain of RN(x_j^2); the output pass x_j / d, * gamma;
+//   LayerNorm: the chain of x_j (the mean), the chain of RN(RN(x_j - mu)^2);
+//              the output pass (x_j - mu) / d, * gamma, + beta.
 // The rows are never held whole on chip: every pass streams the batch
 // through a ring of tiles of 64 columns x nb rows in shared memory, each one
 // 2-D tensor copy (TMA), and the outputs leave through a ring of output tiles
-// with 2-D tensor stores.  The passes run over the tiles right to left, left
-// to right (the chains' index order), then right to left again, so that each
-// pass starts on the tiles the one before it read last, which L2 still holds
-// (evict-last hints until the last pass, evict-first after).  Tiles use the 128-byte swizzle, so a lane's
-// 16-byte reads and writes of its own row never share a bank group with the
-// seven lanes beside it.  Rows past the tensor's end read as zeros and are
-// never stored.
+// with 2-D tensor stores.  The chains run over the tiles left to right (their
+// index order), the other passes right to left, so that a pass that can
+// starts on the tiles the one before it read last, which L2 still holds
+// (evict-last hints until the last pass, evict-first after).  Tiles use the
+// 128-byte swizzle, so a lane's 16-byte reads and writes of its own row never
+// share a bank group with the seven lanes beside it.  Rows past the tensor's
+// end read as zeros and are never stored.
 //
-// Against the pipelined kernel (regions.cu), which computes each exp once
-// into a shared f32 row and leaves the sum to a few chain lanes, this costs a
-// second exp per element but keeps up to 32 rows in their chains per warp
-// (eight warps per SM, two per scheduler) instead of about eight per SM: the
-// sequential order's 4096 dependent adds per row are no longer the bound, and
-// a warp's lanes do the exp work of their rows in step.  The kernel serves
-// the fast realization (faithful exp on f32 pairs); with the correctly
-// rounded exp the doubled exp work costs more than the chains save.
+// Against the pipelined kernel (regions.cu), which keeps each row's values
+// once in a shared f32 row and leaves the sums to a few chain lanes, this
+// reads every row once per pass (and, for the softmax, evaluates the exp
+// twice) but keeps up to 32 rows in their chains per warp (eight warps per
+// SM, two per scheduler) instead of about eight per SM: a one-chain order's
+// 4096 dependent adds per row are no longer the bound.  The softmax takes
+// only its fast realization (faithful exp on f32 pairs) here; with the
+// correctly rounded exp the doubled exp work costs more than the chains save.
 //
 // Every wait is bounded (pipe.cuh); a timeout is recorded in the status word
 // and the warp winds down after its copies in flight have landed.
