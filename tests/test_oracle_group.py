@@ -4,6 +4,8 @@
   programs with re-read (REF) nodes, against an element-by-element evaluator in
   exact rational arithmetic with one binary32 rounding per node;
 * the small 6-node workload against mpmath's erf and exact arithmetic;
+* the exp-clamp node, clamped by the builtins' rule and exponentiated by
+  mpmath, inside, at and beyond the bounds, at the infinities and at NaN;
 * broadcasting equals evaluating over the materialised expansion, bit for bit;
 * bf16 storage: interior values stay in f32 (rounding each node to bf16
   changes results);
@@ -155,6 +157,38 @@ def test_small_group_against_mpmath_per_node():
             g = f32_binop("MUL", t, f32_binop("MUL", np.float32(0.5), f32_binop("ADD", np.float32(1.0), e)))
             want = f32_binop("ADD", f32_binop("MUL", g, s), r[i, j])
             assert same_bits(y[i, j], want), (i, j)
+
+
+def _expc_reference(a):
+    """exp(clamp(a, -4, 4)) without the oracle: clamp(x, lo, hi) =
+    min(max(x, lo), hi) with the builtins' tie rule (max(a, b) = a if a > b
+    else b, min likewise), so a NaN gives the second operand at each step and
+    leaves the clamp as -4; then the exponential at 200 bits, rounded once."""
+    import mpmath
+
+    mpmath.mp.prec = 200
+    a = float(a)
+    c = a if a > -4.0 else -4.0
+    c = c if c < 4.0 else 4.0
+    return rn32(mpf_fraction(mpmath.exp(mpmath.mpf(c))))
+
+
+def test_expc_clamp_bounds_against_mpmath():
+    pytest.importorskip("mpmath")
+    f = np.float32
+    special = [0.0, -0.0, 1.0, -1.0, 3.999999, -3.999999, 4.0, -4.0,
+               float(np.nextafter(f(4), f(np.inf))), float(np.nextafter(f(-4), f(-np.inf))),
+               4.0000005, -4.0000005, 5.0, -5.0, 7.99, -7.99, 8.0, -8.0, 10.0, -10.0, 1e30, -1e30,
+               1e-40, -1e-40, np.inf, -np.inf, np.nan]
+    rng = np.random.default_rng(34)
+    x = np.concatenate([np.array(special, dtype=np.float32),
+                        (rng.random(400) * 24 - 12).astype(np.float32)])
+    y = OG.evaluate(W.encode([("IN", 0), ("EXPC",)]), [], [(x, "f32", (1,))], x.shape, "f32")
+    want = np.array([_expc_reference(v) for v in x], dtype=np.float32)
+    assert same_bits(y, want)
+    # the bounds are the only values it takes outside (-4, 4); NaN reads as -4
+    assert y[np.isnan(x)][0] == want[special.index(-4.0)]
+    assert y[x == np.float32(1e30)][0] == want[special.index(4.0)]
 
 
 def test_broadcast_equals_materialised_expansion():

@@ -38,6 +38,28 @@ def _gelu_half_off(monkeypatch):
     monkeypatch.setattr(OG, "INV_SQRT2", np.float32(0.7071068))
 
 
+def _expc_clamp_at_eight(monkeypatch):
+    real = OG.apply_op
+
+    def wrong(name, a, b=None):
+        if name == "EXPC":
+            return real("EXP", OG._min(OG._max(a, np.float32(-8.0)), np.float32(8.0)))
+        return real(name, a, b)
+
+    monkeypatch.setattr(OG, "apply_op", wrong)
+
+
+def _expc_min_max_swapped(monkeypatch):
+    real = OG.apply_op
+
+    def wrong(name, a, b=None):
+        if name == "EXPC":
+            return real("EXP", OG._max(OG._min(a, np.float32(4.0)), np.float32(-4.0)))
+        return real(name, a, b)
+
+    monkeypatch.setattr(OG, "apply_op", wrong)
+
+
 def _bf16_truncates(monkeypatch):
     monkeypatch.setattr(OF, "f32_to_bf16",
                         lambda x: (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16))
@@ -204,6 +226,8 @@ CASES = [
     (_sub_reversed, TG.test_all_programs_up_to_two_nodes_bitwise),
     (_max_tie_first, TG.test_max_min_tie_gives_second_operand),
     (_gelu_half_off, TG.test_small_group_against_mpmath_per_node),
+    (_expc_clamp_at_eight, TG.test_expc_clamp_bounds_against_mpmath),
+    (_expc_min_max_swapped, TG.test_expc_clamp_bounds_against_mpmath),
     (_bf16_truncates, TF.test_bf16_rounding_matches_torch),
     (_exp_in_binary32, TC.test_exp_correctly_rounded_across_binades),
     (_interleaved_combined_backwards, lambda: TS.test_tiny_rows_exact(("interleaved", 3))),
