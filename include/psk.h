@@ -173,13 +173,14 @@ int psk_group_prepare(const psk_program* prog, const psk_input* inputs, int32_t 
 
 /* psk_group_run / psk_group_prepare with a math mode (a psk_exp_mode, below):
  * PSK_EXP_EXACT is psk_group_run itself (every node correctly rounded);
- * PSK_EXP_FAST is a declared fast realization of the EXP, EXPC, ERF and GELU
+ * PSK_EXP_FAST is a declared fast realization of the EXP, EXPC and ERF
  * nodes: exp within one f32 ulp and erf within two of the correctly rounded
- * values (measured over every float of their ranges), gelu's f32 chain
- * unchanged around the faster erf (so its error is erf's, two ulp of 1,
- * scaled by |a| / 2, which near gelu's negative tail is large relative to a
- * tiny result).  LOG and TANH stay correctly rounded.  Not bit-identical to
- * the oracle; on the 64-node workload 4 outputs in 10^6 differ, by one bf16
+ * values (measured over every float of their ranges).  GELU, LOG and TANH
+ * stay correctly rounded in this mode: gelu's 1 + erf(t) is exact and
+ * cancels where erf(t) < -1/2, so any error in erf there is magnified in
+ * gelu's result, and only the correctly rounded erf keeps gelu within two
+ * ulp.  Not bit-identical to the oracle; on the 64-node workload a few
+ * outputs in 10^6 differ, by one bf16
  * ulp.  PSK_E_ARG for another mode; otherwise as psk_group_run. */
 int psk_group_run_ex(const psk_program* prog, const psk_input* inputs, int32_t n_inputs,
                      const psk_output* out, int32_t math_mode, void* stream);
@@ -344,9 +345,16 @@ int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_
 /* psk_adamw_tree_ex without a caller workspace: when clipping, its scratch
  * is a fixed buffer of PSK_ADAMW_STATIC_WORKSPACE bytes inside the library's
  * device module (one per device, reserved when the module loads), so the call
- * allocates nothing and needs no workspace argument.  The pages have no
- * counterpart: it exists for callers that cannot hand the library device
- * memory.  Limits: trees whose clipping scratch exceeds the buffer (about
+ * allocates nothing: no device memory (no cudaMalloc, no caller workspace)
+ * and no host heap (its kernel-parameter staging is per host thread, reused
+ * from call to call).  The pages have no counterpart: it exists for callers
+ * that cannot hand the library device memory -- code whose device memory
+ * belongs to another allocator (a framework's pool that holds it all), or
+ * that must not fail for lack of memory in the middle of a training step.
+ * The buffer's device
+ * address is looked up on the first call per device and CUDA context (the
+ * set-up runs with that device current; make the first call before any stream
+ * capture).  Limits: trees whose clipping scratch exceeds the buffer (about
  * 2 * 10^9 parameters) are refused with PSK_E_ARG; calls that overlap in time
  * on one device (other streams, other threads) share the buffer and race, so
  * they must be serialised (one stream, or events).  Without clipping it is

@@ -613,10 +613,10 @@ PSK_HD float exp_faithful(float x) {
 }
 
 // ====================================== faithful exp and erf for groups
-// A group's declared fast realization of its EXP, EXP-clamp, ERF and GELU
-// nodes (math mode FAST): each within two f32 ulp of the correctly rounded
-// value (measured over their ranges by the host tests), not correctly
-// rounded and not bit-identical to the oracle.
+// A group's declared fast realization of its EXP, EXP-clamp and ERF nodes
+// (math mode FAST): each within two f32 ulp of the correctly rounded value
+// (measured over their ranges by the host tests), not correctly rounded and
+// not bit-identical to the oracle.  (GELU keeps the correctly rounded erf.)
 
 // exp on |x| <= 88 without special cases: Cody-Waite reduction to |r| <=
 // ln2/2, degree-7 Taylor polynomial, 2^k applied to the exponent field (k in

@@ -1,9 +1,8 @@
 """The fast math mode of groups (psk_group_run_ex, PSK_EXP_FAST) against the
 correctly rounded oracle, within its declared tolerance: EXP and EXPC nodes
-within one f32 ulp, ERF within two, GELU within two ulp of its result plus
-erf's two ulp of 1 carried through its chain (|a| 2^-23), the same NaNs and
-infinities everywhere; on the 64-node workload every output within one bf16
-ulp of the oracle's and almost all identical.
+within one f32 ulp, ERF within two, GELU (correctly rounded in this mode too)
+identical, the same NaNs and infinities everywhere; on the 64-node workload
+every output within one bf16 ulp of the oracle's and almost all identical.
 """
 
 import numpy as np
@@ -64,7 +63,7 @@ def _inputs(op, n, rng):
     return x
 
 
-@pytest.mark.parametrize("op,ulps", [("EXP", 1), ("EXPC", 1), ("ERF", 2), ("GELU", 2)])
+@pytest.mark.parametrize("op,ulps", [("EXP", 1), ("EXPC", 1), ("ERF", 2), ("GELU", 0)])
 def test_fast_node_within_its_tolerance(dev, op, ulps):
     rng = np.random.default_rng(81)
     n = (1 << 22) + 5
@@ -80,13 +79,8 @@ def test_fast_node_within_its_tolerance(dev, op, ulps):
     fin = ~np.isnan(want)
     assert np.array_equal(np.isinf(got[fin]), np.isinf(want[fin]))
     u = _ulps32(got[fin], want[fin])
-    if op == "GELU":
-        # erf's two ulp of 1 pass through 0.5 (1 + e) and the product by a
-        slack = np.abs(x[fin].astype(np.float64)) * 2.0 ** -23
-        bad = (u > ulps) & (np.abs(got[fin].astype(np.float64) - want[fin]) > slack)
-        assert not bad.any(), f"{bad.sum()} beyond tolerance, e.g. x={x[fin][bad][:4]}"
-    else:
-        assert u.max() <= ulps, f"max {u.max()} ulp at x={x[fin][np.argmax(u)]}"
+    print(f"{op} fast: max gap {u.max()} f32 ulp over {fin.sum()} inputs")
+    assert u.max() <= ulps, f"max {u.max()} ulp at x={x[fin][np.argmax(u)]}"
 
 
 @pytest.mark.parametrize("shape", [(96, 200), (37, 53), (130, 1024)])
