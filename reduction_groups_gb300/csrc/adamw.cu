@@ -31,6 +31,8 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace psk {
@@ -606,8 +608,8 @@ static int check_schedule(const psk_adamw_schedule* sc) {
 
 // ||g||^2 tree and the clip scale into the workspace (launches only).
 static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace& W, char* ws, float clip,
-                       cudaStream_t stream) {
-  SqParams* P = new SqParams;
+                       cudaStream_t stream, SqParams* staging) {
+  SqParams* P = staging ? staging : new SqParams;
   float* blocks = (float*)(ws + W.blocks_off);
   float* groups = (float*)(ws + W.groups_off);
   float* leaf_sums = (float*)(ws + W.leaves_off);
@@ -647,19 +649,28 @@ static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace
     block0 += nb_batch;
     group0 += ng_batch;
   }
-  delete P;
+  if (!staging) delete P;
   if (rc) return rc;
   sq_scale_kernel<<<1, 1, 0, stream>>>(leaf_sums, (int32_t)W.n_leaves, clip, (float*)(ws + W.scale_off));
   return check_launch("clip scale kernel");
 }
 
+// Host staging of the kernel parameters (the leaf tables, about 28 KB and 20
+// KB): from the heap per call, or the caller's (the allocation-free entry
+// point passes thread-local ones).
+struct HostStaging {
+  AdamParams adam;
+  SqParams sq;
+};
+
 static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
-                     const psk_adamw_schedule* sc, void* workspace, uint64_t workspace_bytes, void* stream) {
+                     const psk_adamw_schedule* sc, void* workspace, uint64_t workspace_bytes, void* stream,
+                     HostStaging* staging = nullptr) {
   int rc = check_leaves(leaves, n_leaves);
   if (rc) return rc;
   rc = check_schedule(sc);
   if (rc) return rc;
-  AdamParams* P = new AdamParams;   // host staging of the kernel parameter
+  AdamParams* P = staging ? &staging->adam : new AdamParams;   // host staging of the kernel parameter
   rc = make_scalars(hp, P->s);
   if (rc == PSK_OK) rc = scheduled_lr(hp, sc, P->s.lr);
   const bool clip = sc && sc->grad_clip > 0.0;
@@ -681,7 +692,8 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
   cudaStream_t s = (cudaStream_t)stream;
   const float* scale = clip ? (const float*)((char*)workspace + W.scale_off) : nullptr;
   if (rc == PSK_OK && clip && W.n_leaves > 0) rc = launch_clip(leaves, n_leaves, W, (char*)workspace,
-                                                               (float)sc->grad_clip, s);
+                                                               (float)sc->grad_clip, s,
+                                                               staging ? &staging->sq : nullptr);
   // one launch per PSK_ADAMW_MAX_LEAVES non-empty leaves of each parameter
   // storage type (one launch for the trees here)
   for (int pdt = PSK_F32; pdt <= PSK_BF16 && rc == PSK_OK; ++pdt) {
@@ -718,28 +730,49 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
     rc = check_launch("adamw tree kernel");
   }
   }
-  delete P;
+  if (!staging) delete P;
   return rc;
 }
 
 // Scratch of psk_adamw_tree_static: one fixed buffer in the library's module
-// per device, reserved when the module loads; its address comes from
-// cudaGetSymbolAddress, once per device.  Every value in it is written before
-// it is read, so nothing is cleared.
+// per device, reserved when the module loads.  Host code must not hand the
+// symbol itself to a kernel (on the host it names a host-side stand-in); its
+// device address comes from cudaGetSymbolAddress, with the device current,
+// once per device and CUDA context (a context created anew, after a device
+// reset for instance, gets the address again).  Every value in it is written
+// before it is read, so nothing is cleared.
 static __device__ __align__(256) unsigned char g_adamw_static_ws[PSK_ADAMW_STATIC_WORKSPACE];
 
 static int static_workspace(void** ptr) {
-  static void* addr[PSK_MAX_DEVICES] = {};
+  struct Entry { CUcontext ctx; void* addr; };
+  static Entry cache[PSK_MAX_DEVICES] = {};
   static std::mutex mu;
+  static CUresult (*ctx_get_current)(CUcontext*) = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return (CUresult(*)(CUcontext*))fn;
+  }();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= PSK_MAX_DEVICES)
     return fail(PSK_E_CUDA, "no current CUDA device below %d", PSK_MAX_DEVICES);
+  if (!ctx_get_current) return fail(PSK_E_CUDA, "cuCtxGetCurrent is not available from the driver");
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_adamw_static_ws) != cudaSuccess) {
-    addr[dev] = nullptr;
-    return check_launch("static workspace address");
+  CUcontext ctx = nullptr;
+  if (ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  Entry& e = cache[dev];
+  if (!ctx || ctx != e.ctx || !e.addr) {
+    void* addr = nullptr;   // cudaGetSymbolAddress also makes the device's primary context current
+    if (cudaGetSymbolAddress(&addr, g_adamw_static_ws) != cudaSuccess || !addr) {
+      e = Entry{nullptr, nullptr};
+      return check_launch("static workspace address");
+    }
+    if (ctx_get_current(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    e = Entry{ctx, addr};
   }
-  *ptr = addr[dev];
+  *ptr = e.addr;
   return PSK_OK;
 }
 
@@ -750,8 +783,9 @@ using namespace psk;
 extern "C" int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
                                      const psk_adamw_schedule* sched, void* stream) {
   clear_error();
+  static thread_local HostStaging staging;   // no heap allocation per call
   const bool clip = sched && sched->grad_clip > 0.0;
-  if (!clip) return adamw_run(leaves, n_leaves, hp, sched, nullptr, 0, stream);
+  if (!clip) return adamw_run(leaves, n_leaves, hp, sched, nullptr, 0, stream, &staging);
   int rc = check_leaves(leaves, n_leaves);
   if (rc == PSK_OK) rc = check_schedule(sched);
   if (rc) return rc;
@@ -762,7 +796,7 @@ extern "C" int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, c
   void* ws = nullptr;
   rc = static_workspace(&ws);
   if (rc) return rc;
-  return adamw_run(leaves, n_leaves, hp, sched, ws, PSK_ADAMW_STATIC_WORKSPACE, stream);
+  return adamw_run(leaves, n_leaves, hp, sched, ws, PSK_ADAMW_STATIC_WORKSPACE, stream, &staging);
 }
 
 extern "C" int psk_adamw_scalars(const psk_adamw_hparams* hp, float out[9]) {

@@ -1,8 +1,10 @@
 """psk_adamw_tree_static (clipping scratch in the library's fixed device
-buffer) against psk_adamw_tree_ex (scratch in a caller workspace): two calls
-in a row on copies of one tree give the same bits after each call.  The file
-sorts last so it also runs after every other GPU test in one process; it
-passes alone as well."""
+buffer, for callers that cannot hand the library device memory) against
+psk_adamw_tree_ex (scratch in a caller workspace): two calls in a row on
+copies of one tree give the same bits after each call, and once the first
+call has set up the buffer's address, further calls leave the device's free
+memory unchanged.  The file sorts last so it also runs after every other GPU
+test in one process; it passes alone as well."""
 
 import numpy as np
 import pytest
@@ -61,3 +63,16 @@ def test_static_scratch_on_a_side_stream(dev):
     s.synchronize()
     torch.cuda.synchronize()
     assert _same(a, b)
+
+
+def test_static_calls_take_no_device_memory(dev):
+    tree = W.llama_adamw_leaves(layers=1)
+    b = [tree.device_leaf(i) for i in range(len(tree.leaves))]
+    dev.psk_adamw_tree_static(b, tree.hp, "cosine", 10, 500, 1.0)   # first call: the set-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        dev.psk_adamw_tree_static(b, tree.hp, "cosine", 10, 500, 1.0)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
