@@ -385,6 +385,61 @@ PSK_HD void taylor32_tier1_core(float a, const float* p2, const float* h, float&
   d = vl - (R - vh);
 }
 
+// The same tables as one record of 12 floats per interval (three 16-byte
+// groups: coefficients 7, 6, 5, 4; then 3 and 2 as (hi, lo) pairs; then 1
+// and 0), so that a lookup is three 16-byte loads instead of eight: record i
+// is rec[12 i .. 12 i + 11].
+PSK_HD void erf_record(const float* p2, const float* h, int i, float* rec) {
+  for (int k = 0; k < 4; ++k) rec[k] = h[(3 - k) * PSK_ERF_N32 + i];
+  for (int k = 0; k < 4; ++k) {
+    rec[4 + 2 * k] = p2[(3 - k) * 2 * PSK_ERF_N32 + 2 * i];
+    rec[5 + 2 * k] = p2[(3 - k) * 2 * PSK_ERF_N32 + 2 * i + 1];
+  }
+}
+
+PSK_HD void load_record12(const float* rec, int i, float* v) {
+#if defined(PSK_HOST_BUILD)
+  for (int k = 0; k < 12; ++k) v[k] = rec[12 * i + k];
+#else
+  const float4* r = reinterpret_cast<const float4*>(rec) + 3 * i;
+  const float4 a = r[0], b = r[1], c = r[2];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  v[8] = c.x; v[9] = c.y; v[10] = c.z; v[11] = c.w;
+#endif
+}
+
+// erf tier 1 from the record tables: the same operations on the same
+// coefficients as erf_tier1_core (degree 7, four float-float steps), so the
+// same R and d.
+PSK_HD void erf_tier1_core_rec(float a, const float* rec, float& R, float& d) {
+  static_assert(PSK_ERF_D32 == 7 && PSK_ERF_NPAIR == 4, "erf record layout");
+  const float fi = rintf(a * 32.0f);
+  const int i = (int)fi;
+  const float t = fmaf(fi, -0.03125f, a);   // exact
+  float c[12];
+  load_record12(rec, i, c);
+  float H = c[0];
+  H = fmaf(H, t, c[1]);
+  H = fmaf(H, t, c[2]);
+  H = fmaf(H, t, c[3]);
+  float p, pe, vh, vl;
+  two_prod(t, H, p, pe);
+  fast_two_sum(c[4], p, vh, vl);
+  vl = vl + (pe + c[5]);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) {
+    two_prod(t, vh, p, pe);
+    pe = fmaf(t, vl, pe);
+    float sh, sl;
+    fast_two_sum(c[4 + 2 * k], p, sh, sl);
+    vh = sh;
+    vl = sl + (pe + c[5 + 2 * k]);
+  }
+  R = vh + vl;
+  d = vl - (R - vh);
+}
+
 // erf tier 1, 2^-60 <= a < PSK_ERF_ONE_FROM (< 3.9375): p2 / h are
 // psk_erf_p2 / psk_erf_h or copies in shared memory.  Relative error below
 // 2^-42 (the coefficients' terms from 4 on stay below 2^-18 of erf(a)).
@@ -676,6 +731,24 @@ PSK_HD float erf_fast_abs(float a, const float* p2, const float* h) {
   for (int k = DF - 1; k >= PSK_ERF_NPAIR; --k) H = fmaf(H, t, h[(k - PSK_ERF_NPAIR) * PSK_ERF_N32 + i]);
 #pragma unroll
   for (int k = PSK_ERF_NPAIR - 1; k >= 0; --k) H = fmaf(H, t, p2[k * 2 * PSK_ERF_N32 + 2 * i]);
+  return a >= PSK_ERF_ONE_FROM ? 1.0f : H;
+}
+
+// erf_fast_abs from the record tables (the same operations on the same
+// coefficients: the same result): coefficient 4 and the high parts of 3..0.
+PSK_HD float erf_fast_abs_rec(float a, const float* rec) {
+  static_assert(ERF_FAST_DEGREE == 4, "erf record layout");
+  const float ac = fminf(a, 3.9f);
+  const float fi = rintf(ac * 32.0f);
+  const int i = (int)fi;
+  const float t = fmaf(fi, -0.03125f, ac);         // exact
+  float c[12];
+  load_record12(rec, i, c);
+  float H = c[3];
+  H = fmaf(H, t, c[4]);
+  H = fmaf(H, t, c[6]);
+  H = fmaf(H, t, c[8]);
+  H = fmaf(H, t, c[10]);
   return a >= PSK_ERF_ONE_FROM ? 1.0f : H;
 }
 

@@ -10,10 +10,36 @@ using namespace psk;
 
 extern "C" {
 
+// erf's Taylor tables as records (erf_record), built once
+static const float* erf_records() {
+  static float rec[12 * PSK_ERF_N32];
+  static bool built = false;
+  if (!built) {
+    for (int i = 0; i < PSK_ERF_N32; ++i) erf_record(&psk_erf_p2[0][0], &psk_erf_h[0][0], i, rec + 12 * i);
+    built = true;
+  }
+  return rec;
+}
+
 // which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
 // 6 erf_fast (signed), 7 exp_fast_mid, 8 the softmax region's pair exp
-// (x <= 0, taken two at a time), 9 the groups' pair exp (|x| <= 87)
+// (x <= 0, taken two at a time), 9 the groups' pair exp (|x| <= 87),
+// 10 erf tier 1 from the record tables (R; inputs in tier 1's range),
+// 11 erf_fast of |x| from the record tables
 void psk_host_unary(int which, const float* x, float* y, long n) {
+  if (which == 10 || which == 11) {
+    const float* rec = erf_records();
+    for (long i = 0; i < n; ++i) {
+      if (which == 11) {
+        y[i] = erf_fast_abs_rec(fabsf(x[i]), rec);
+      } else {
+        float R, d;
+        erf_tier1_core_rec(x[i], rec, R, d);
+        y[i] = R;
+      }
+    }
+    return;
+  }
   if (which == 8 || which == 9) {
     for (long i = 0; i < n; i += 2) {
       const f2 a{x[i], i + 1 < n ? x[i + 1] : 0.0f};

@@ -41,17 +41,14 @@ struct GroupParams {
 // exp and erf tables staged once per CTA in shared memory.
 struct MathTables {
   float2 exp_tab[PSK_EXP_TAB_N];   // 2^(j/1024) as (hi, lo)
-  float2 erf_p2[PSK_ERF_NPAIR * PSK_ERF_N32];                  // coefficients 0..3 as (hi, lo)
-  float erf_h[(PSK_ERF_D32 + 1 - PSK_ERF_NPAIR) * PSK_ERF_N32];  // coefficients 4..D
+  float4 erf_rec[3 * PSK_ERF_N32];  // erf's Taylor coefficients, one 48-byte record per interval (erf_record)
 };
 
 __device__ __forceinline__ void load_tables(MathTables& t) {
   const float2* src = reinterpret_cast<const float2*>(psk_exp_tab2);
   for (int i = threadIdx.x; i < PSK_EXP_TAB_N; i += blockDim.x) t.exp_tab[i] = src[i];
-  const float2* p2 = reinterpret_cast<const float2*>(&psk_erf_p2[0][0]);
-  for (int i = threadIdx.x; i < PSK_ERF_NPAIR * PSK_ERF_N32; i += blockDim.x) t.erf_p2[i] = p2[i];
-  for (int i = threadIdx.x; i < (PSK_ERF_D32 + 1 - PSK_ERF_NPAIR) * PSK_ERF_N32; i += blockDim.x)
-    t.erf_h[i] = (&psk_erf_h[0][0])[i];
+  for (int i = threadIdx.x; i < PSK_ERF_N32; i += blockDim.x)
+    erf_record(&psk_erf_p2[0][0], &psk_erf_h[0][0], i, reinterpret_cast<float*>(&t.erf_rec[3 * i]));
 }
 
 // log and tanh tables, staged per CTA only by kernels with such nodes.
@@ -255,7 +252,7 @@ __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
     tt[j] = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
     const float aa = fabsf(tt[j]);
     const bool inr = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
-    erf_tier1_core(inr ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h, R[j], d[j]);
+    erf_tier1_core_rec(inr ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_rec), R[j], d[j]);
     ok[j] = inr && tier1_decided(R[j], d[j]);
     all = all && ok[j];
   }
@@ -366,7 +363,7 @@ __device__ __forceinline__ Vec<V> node_erf_fast_any(Vec<V> A, const MathTables& 
   for (int j = 0; j < V; ++j) {
     const float t = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
     const float aa = fabsf(t);
-    float e = erf_fast_abs(aa, reinterpret_cast<const float*>(tab.erf_p2), tab.erf_h);
+    float e = erf_fast_abs_rec(aa, reinterpret_cast<const float*>(tab.erf_rec));
     e = t == t ? copysignf(e, t) : t;
     r.v[j] = GELU ? __fmul_rn(A.v[j], __fmul_rn(0.5f, __fadd_rn(1.0f, e))) : e;
   }

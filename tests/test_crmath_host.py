@@ -89,6 +89,23 @@ def test_tier1_keeps_only_correct_roundings(hm):
     assert 1 - ok.mean() < 2.0 ** -12
 
 
+def test_erf_record_tables_give_the_same_bits(hm):
+    """The group kernels read erf's Taylor coefficients as one record per
+    interval (three 16-byte loads); tier 1 and the fast erf from the records
+    equal tier 1 and the fast erf from the separate tables, bit for bit, over
+    every interval (4·10^6 arguments and every binade below 1)."""
+    unary, tier = hm
+    rng = np.random.default_rng(13)
+    a = np.concatenate([rng.uniform(2.0 ** -60, 3.919, 4_000_000).astype(np.float32),
+                        np.abs(_all_binades(-60, 1, 2000, 4)),
+                        (np.arange(126, dtype=np.float32) + np.float32(0.5)) / np.float32(32)])
+    a = a[(a >= 2.0 ** -60) & (a < 3.919)]
+    r_sep, _ = tier(1, 1, a)
+    assert same_bits(unary(10, a), r_sep)
+    x = np.concatenate([a, np.array([3.92, 4.0, 10.0, 0.0], dtype=np.float32)])
+    assert same_bits(unary(11, x), unary(6, x))
+
+
 @pytest.mark.parametrize("t", [2, 3])
 def test_tiers_2_and_3_correctly_rounded_alone(hm, t):
     _, tier = hm
