@@ -45,6 +45,8 @@ def _args():
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     p.add_argument("--e2e-copy-streams", type=int, default=1,
                    help="streams per copy direction in the end-to-end leg (units alternate between them)")
+    p.add_argument("--e2e-slices", type=int, default=10,
+                   help="AdamW leaf slices of the end-to-end leg (smaller slices: shorter pipeline fill and drain)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline sample")
     p.add_argument("--softmax-exp", choices=["exact", "fast"], default="fast",
                    help="exp of the softmax region inside the step (the other mode is timed beside it)")
@@ -756,9 +758,9 @@ def run_ours(a, ws, rank, local):
             sum(t.numel() * t.element_size() for t in flat_h)
         d2h = host_gout.numel() * 2 + 2 * host_sy[0].numel() * 2 + \
             sum(t.numel() * t.element_size() for t in flat_h[:3])
-        # AdamW slices of about a tenth of the parameters each, in leaf order
+        # AdamW slices of about 1/e2e_slices of the parameters each, in leaf order
         slices, cur, acc_n = [], [], 0
-        per = max(1, n_adam // 10)
+        per = max(1, n_adam // max(1, a.e2e_slices))
         for i, leaf in enumerate(leaves):
             cur.append(i)
             acc_n += leaf[0].numel()
