@@ -211,8 +211,9 @@ int psk_group_run_interp(const psk_program* prog, const psk_input* inputs, int32
  *                    partials are then added left to right; 1 <= P <= 64
  *                    (INTERLEAVED(1) is SEQUENTIAL).
  * exp_mode EXACT uses the correctly rounded exp (bit-identical to a group's EXP
- * node); FAST uses a faithful exp (at most one f32 ulp from it), a declared
- * realization that owes its measured gap.  x and y are row-major with leading
+ * node); FAST uses a fast exp (within two f32 ulp of it, the tolerance stated
+ * for exp nodes; measured over [-104.5, 0]), a declared realization that owes
+ * its measured gap.  x and y are row-major with leading
  * dimensions ldx, ldy >= cols (elements); y must not overlap x unless y == x
  * with the same dtype and leading dimension (in place).  rows or cols == 0 is
  * an empty region (nothing launched, returns 0). */
@@ -379,6 +380,17 @@ int psk_device_status(uint32_t* status, int32_t reset);
  * it off.  Host-only, synchronous; for tests, never for production use.
  * PSK_E_ARG for row < -1. */
 int psk_test_drop_row(int64_t row);
+
+/* Test hook for the softmax region's fast realization (presk "Native
+ * execution": a realization that approximates owes a measured gap; the exp
+ * nodes' tolerance is two f32 ulp): y[i] = the fast exp of x[i], the function
+ * the region's fast realization applies to every x - max (x[i] <= 0, NaN or
+ * -inf; larger x are outside its domain and give unspecified values), so
+ * that tests can measure its bound over whole binades.  x and y: n floats in
+ * DEVICE memory (y may be x); asynchronous on the stream.  PSK_E_NULL for a
+ * NULL pointer with n > 0, PSK_E_SHAPE for n < 0, PSK_E_CUDA if the launch
+ * fails; n = 0 launches nothing.  For tests, never for production use. */
+int psk_test_fast_exp(const float* x, float* y, int64_t n, void* stream);
 
 /* Thread-local description of the last refusal of this thread ("" if none). */
 const char* psk_last_error(void);

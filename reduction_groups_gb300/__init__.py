@@ -22,5 +22,6 @@ from .ops import (  # noqa: F401
     psk_softmax_masked,
     psk_softmax_region,
     psk_test_drop_row,
+    psk_test_fast_exp,
 )
 from ._native import PskError  # noqa: F401

@@ -752,26 +752,5 @@ PSK_HD float erf_fast_abs_rec(float a, const float* rec) {
   return a >= PSK_ERF_ONE_FROM ? 1.0f : H;
 }
 
-// The same faithful exp for x <= 0, NaN or -inf (the softmax region's
-// x - max), without branches: 2^k is applied as 2^(k+64) and then 2^-64 (one
-// rounding, in the second product, where the result is subnormal; exact
-// scalings otherwise), k held at -189, and x < -104 (below half the least
-// subnormal; -inf, whose reduction is NaN, included) gives 0.
-PSK_HD float exp_faithful_nonpos(float x) {
-  const float kf = rintf(x * PSK_FEXP_INV_LN2);
-  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);
-  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
-  float p = 1.0f / 5040.0f;
-  p = fmaf(p, r, 1.0f / 720.0f);
-  p = fmaf(p, r, 1.0f / 120.0f);
-  p = fmaf(p, r, 1.0f / 24.0f);
-  p = fmaf(p, r, 1.0f / 6.0f);
-  p = fmaf(p, r, 0.5f);
-  p = fmaf(p, r, 1.0f);
-  p = fmaf(p, r, 1.0f);
-  const int k = kf > -189.0f ? (int)kf : -189;
-  const float y = (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
-  return x < -104.0f ? 0.0f : y;
-}
 
 }  // namespace psk

@@ -22,8 +22,8 @@ static const float* erf_records() {
 }
 
 // which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
-// 6 erf_fast (signed), 7 exp_fast_mid, 8 the softmax region's pair exp
-// (x <= 0, taken two at a time), 9 the groups' pair exp (|x| <= 87),
+// 6 erf_fast (signed), 7 exp_fast_mid, 9 the groups' pair exp (|x| <= 87,
+// taken two at a time),
 // 10 erf tier 1 from the record tables (R; inputs in tier 1's range),
 // 11 erf_fast of |x| from the record tables
 void psk_host_unary(int which, const float* x, float* y, long n) {
@@ -40,10 +40,10 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
     }
     return;
   }
-  if (which == 8 || which == 9) {
+  if (which == 9) {
     for (long i = 0; i < n; i += 2) {
       const f2 a{x[i], i + 1 < n ? x[i + 1] : 0.0f};
-      const f2 r = which == 8 ? exp2_faithful_nonpos(a) : exp2_faithful_mid(a);
+      const f2 r = exp2_faithful_mid(a);
       y[i] = r.x;
       if (i + 1 < n) y[i + 1] = r.y;
     }
@@ -143,25 +143,6 @@ long psk_host_div_check(unsigned long seed, long n, float a_lo_exp, float a_hi_e
   return bad;
 }
 
-// The pair exp against the correctly rounded exp over the floats t <= 0
-// whose bit patterns are 0x80000000 + i * stride for i * stride <= span
-// (t = -0 down to -(span)); returns the largest distance in ulps and stores
-// the first input that reaches it.
-long psk_host_exp_pair_maxulp(uint32_t span, uint32_t stride, float* worst) {
-  long maxd = 0;
-  for (uint64_t i = 0; i <= span; i += 2 * (uint64_t)stride) {
-    const float a = u2f(0x80000000u + (uint32_t)i);
-    const float b = u2f(0x80000000u + (uint32_t)(i + stride <= span ? i + stride : i));
-    const f2 r = exp2_faithful_nonpos(f2{a, b});
-    const float ra[2] = {r.x, r.y}, ta[2] = {a, b};
-    for (int q = 0; q < 2; ++q) {
-      const float want = exp_cr(ta[q], psk_exp_tab2);
-      const long d = labs((long)f2u(ra[q]) - (long)f2u(want));
-      if (d > maxd) { maxd = d; if (worst) *worst = ta[q]; }
-    }
-  }
-  return maxd;
-}
 
 // The groups' pair exp (exp2_faithful_mid) against the correctly rounded
 // exp over the floats of [-a, a] whose bit patterns (of |x|) are multiples of

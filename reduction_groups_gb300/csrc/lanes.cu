@@ -33,7 +33,7 @@
 // twice) but keeps up to 32 rows in their chains per warp (eight warps per
 // SM, two per scheduler) instead of about eight per SM: a one-chain order's
 // 4096 dependent adds per row are no longer the bound.  The softmax takes
-// only its fast realization (faithful exp on f32 pairs) here; with the
+// only its fast realization (the fast exp on f32 pairs) here; with the
 // correctly rounded exp the doubled exp work costs more than the chains save.
 //
 // Every wait is bounded (pipe.cuh); a timeout is recorded in the status word
@@ -102,14 +102,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // The eight exp values of a 16-byte group of bf16 x (element 2k in the low
-// half of word k): x + (-m) and the faithful exp on f32 pairs -- the same
+// half of word k): x + (-m) and the fast exp on f32 pairs -- the same
 // operations as the pipelined kernel's fast realization, so the same bits.
 __device__ __forceinline__ void lane_exp8(const uint4 wv, float m, float* e) {
   const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
   const f2 nm = f2_splat(-m);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const f2 r = exp2_faithful_nonpos(f2_add(f2{__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xFFFF0000u)}, nm));
+    const f2 r = exp2_unit_nonpos(f2_add(f2{__uint_as_float(wd[k] << 16), __uint_as_float(wd[k] & 0xFFFF0000u)}, nm));
     e[2 * k] = r.x;
     e[2 * k + 1] = r.y;
   }

@@ -859,9 +859,9 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
           const int j = c4 * (PIPE_TT * 4) + 4 * tt;
           if (j < cols) {
-            const f2 a = exp2_faithful_nonpos(f2_add(
+            const f2 a = exp2_unit_nonpos(f2_add(
                 f2{__uint_as_float(xw[c4].x << 16), __uint_as_float(xw[c4].x & 0xFFFF0000u)}, nm));
-            const f2 b = exp2_faithful_nonpos(f2_add(
+            const f2 b = exp2_unit_nonpos(f2_add(
                 f2{__uint_as_float(xw[c4].y << 16), __uint_as_float(xw[c4].y & 0xFFFF0000u)}, nm));
             *reinterpret_cast<float4*>(Er + j) = make_float4(a.x, a.y, b.x, b.y);
           }
@@ -1368,6 +1368,25 @@ extern "C" int psk_test_drop_row(int64_t row) {
   const long long v = row;
   if (cudaMemcpyToSymbol(g_pipe_drop_row, &v, sizeof(v)) != cudaSuccess) return check_launch("test hook write");
   return lanes_set_drop_row(v);
+}
+
+namespace psk {
+// The softmax region's fast exp, elementwise (the test hook below).
+__global__ void fast_exp_kernel(const float* x, float* y, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    y[i] = exp_unit_nonpos(x[i]);
+}
+}  // namespace psk
+
+extern "C" int psk_test_fast_exp(const float* x, float* y, int64_t n, void* stream) {
+  clear_error();
+  if (n < 0) return fail(PSK_E_SHAPE, "n %lld", (long long)n);
+  if (n == 0) return PSK_OK;
+  if (!x || !y) return fail(PSK_E_NULL, "x or y is NULL");
+  const int64_t blocks = (n + 255) / 256;
+  const int64_t cap = device_sm_count() * 8;
+  fast_exp_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, (cudaStream_t)stream>>>(x, y, n);
+  return check_launch("fast exp test kernel");
 }
 
 extern "C" int psk_device_status(uint32_t* status, int32_t reset) {

@@ -1,12 +1,13 @@
 // Row-region arithmetic shared by the row kernels (regions.cu) and the
 // lane-per-row softmax kernel (lanes.cu): the launch parameters, the exact
-// NaN-propagating max, the region's exp (correctly rounded or faithful) and
+// NaN-propagating max, the region's exp (correctly rounded or fast) and
 // the row division e / s, so that every kernel computing a softmax row does
 // the same operations on the same values and gives the same bits.
 #pragma once
 
 #include "common.cuh"
 #include "crmath.cuh"
+#include "pair.cuh"
 
 namespace psk {
 
@@ -58,7 +59,7 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 
 template <int EXPM>
 __device__ __forceinline__ float region_exp(float d) {
-  if (EXPM == PSK_EXP_FAST) return exp_faithful_nonpos(d);
+  if (EXPM == PSK_EXP_FAST) return exp_unit_nonpos(d);
   return exp_cr(d, psk_exp_tab2);
 }
 
@@ -68,7 +69,7 @@ template <int EXPM>
 __device__ __forceinline__ void region_exp8(float* v) {
   if constexpr (EXPM == PSK_EXP_FAST) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = exp_faithful_nonpos(v[q]);
+    for (int q = 0; q < 8; ++q) v[q] = exp_unit_nonpos(v[q]);
   } else {
     float R[8], d[8];
     int n[8];

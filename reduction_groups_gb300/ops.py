@@ -208,6 +208,18 @@ def psk_test_drop_row(row: int) -> None:
     N.check(N.lib().psk_test_drop_row(int(row)))
 
 
+def psk_test_fast_exp(x, y, stream=None) -> None:
+    """Test hook: y = the softmax region's fast exp of x elementwise (f32
+    device tensors of equal size, x <= 0)."""
+    import torch
+
+    if x.dtype != torch.float32 or y.dtype != torch.float32 or x.numel() != y.numel():
+        raise TypeError("x and y must be f32 tensors of equal size")
+    if not (x.is_contiguous() and y.is_contiguous()):
+        raise ValueError("x and y must be contiguous")
+    N.check(N.lib().psk_test_fast_exp(x.data_ptr(), y.data_ptr(), x.numel(), _stream_handle(stream)))
+
+
 def _hparams(hp) -> N.psk_adamw_hparams:
     h = N.psk_adamw_hparams()
     h.lr, h.beta1, h.beta2 = float(hp.lr), float(hp.beta1), float(hp.beta2)

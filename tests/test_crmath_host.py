@@ -284,34 +284,6 @@ def test_fast_exp_and_erf_within_their_bounds(hm):
     assert _ulps(y[ok], ref[ok]).max() <= 2
 
 
-# ------------------------------- the softmax region's fast exp, on f32 pairs
-
-def test_pair_exp_faithful_over_its_range(hm):
-    """The pipelined softmax's fast exp (pair arithmetic, t <= 0) against the
-    correctly rounded oracle: within one ulp on every binade, on the floats of
-    [-105, 0] taken with a stride of 61 bit patterns (measured over every float
-    of that range the bound is exactly one ulp), zeros below -104.5, -inf to 0,
-    NaN kept."""
-    unary, _ = hm
-    rng = np.random.default_rng(71)
-    sp = np.array([0.0, -0.0, -np.inf, np.nan, -1e-45, -2.0 ** -126, -87.33654, -87.3365478515625,
-                   -103.97207, -103.97208, -103.9721, -104.0, -104.5, -104.50001, -200.0, -3e38,
-                   -0.34657359, -0.3465736, -0.6931472], dtype=np.float32)
-    x = np.concatenate([-np.abs(rng.uniform(0, 105, 1_000_000)).astype(np.float32),
-                        -np.abs(_all_binades(-149 + 23, 6, 2000, 72)), sp])
-    y, ref = unary(8, x), exp_f32(x)
-    assert np.array_equal(np.isnan(y), np.isnan(ref))
-    ok = ~np.isnan(ref)
-    assert _ulps(y[ok], ref[ok]).max() <= 1
-    assert np.all(y[x <= -104.5] == 0)
-    L = ctypes.CDLL(os.path.join(ROOT, "reduction_groups_gb300", "_build", "libpsk_hostmath.so"))
-    L.psk_host_exp_pair_maxulp.restype = ctypes.c_long
-    L.psk_host_exp_pair_maxulp.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(ctypes.c_float)]
-    span = int(np.float32(-105.0).view(np.uint32)) - 0x80000000
-    worst = ctypes.c_float(0)
-    assert L.psk_host_exp_pair_maxulp(span, 61, ctypes.byref(worst)) <= 1
-
-
 def test_group_pair_exp_faithful_on_the_clamped_range(hm):
     """The groups' fast EXP-clamp node evaluates exp on [-4, 4] two at a time
     (pair arithmetic, 2^k added to the exponent field): within one ulp of the
