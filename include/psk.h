@@ -174,8 +174,9 @@ int psk_group_prepare(const psk_program* prog, const psk_input* inputs, int32_t 
 /* psk_group_run / psk_group_prepare with a math mode (a psk_exp_mode, below):
  * PSK_EXP_EXACT is psk_group_run itself (every node correctly rounded);
  * PSK_EXP_FAST is a declared fast realization of the EXP, EXPC and ERF
- * nodes: exp within one f32 ulp and erf within two of the correctly rounded
- * values (measured over every float of their ranges).  GELU, LOG and TANH
+ * nodes: EXP within one f32 ulp, EXPC (the multifunction unit's 2^f after an
+ * exact reduction) and ERF within two of the correctly rounded values
+ * (measured over their ranges).  GELU, LOG and TANH
  * stay correctly rounded in this mode: gelu's 1 + erf(t) is exact and
  * cancels where erf(t) < -1/2, so any error in erf there is magnified in
  * gelu's result, and only the correctly rounded erf keeps gelu within two

@@ -644,53 +644,12 @@ PSK_HD float div_by_recip(float a, float b, float rb) {
   return fmaf(r, rb, q);
 }
 
-// ============================================ exp, fast faithful variant
-// Used only where a realization declares the fast exp (the softmax region's
-// fast mode): Cody-Waite reduction to |r| <= ln2/2 and a degree-7 Taylor
-// polynomial; error at most one ulp, not correctly rounded.
-PSK_HD float exp_faithful(float x) {
-  float kf = rintf(x * PSK_FEXP_INV_LN2);
-  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);         // exact: ln2 hi carries 16 bits
-  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
-  float p = 1.0f / 5040.0f;
-  p = fmaf(p, r, 1.0f / 720.0f);
-  p = fmaf(p, r, 1.0f / 120.0f);
-  p = fmaf(p, r, 1.0f / 24.0f);
-  p = fmaf(p, r, 1.0f / 6.0f);
-  p = fmaf(p, r, 0.5f);
-  p = fmaf(p, r, 1.0f);
-  p = fmaf(p, r, 1.0f);
-  int k = (int)kf;
-  if (k > 127) return (x == x) ? INFINITY : x;
-  if (k < -149 - 24) return 0.0f;
-  if (k >= -125) return p * u2f((uint32_t)(k + 127) << 23);
-  return (p * u2f((uint32_t)(k + 127 + 64) << 23)) * 0x1p-64f;
-}
-
 // ====================================== faithful exp and erf for groups
-// A group's declared fast realization of its EXP, EXP-clamp and ERF nodes
-// (math mode FAST): each within two f32 ulp of the correctly rounded value
-// (measured over their ranges by the host tests), not correctly rounded and
-// not bit-identical to the oracle.  (GELU keeps the correctly rounded erf.)
-
-// exp on |x| <= 88 without special cases: Cody-Waite reduction to |r| <=
-// ln2/2, degree-7 Taylor polynomial, 2^k applied to the exponent field (k in
-// [-127, 127]: normal results down to x = -87.3; below, the bit add would
-// leave the normal range, so callers clamp or use exp_fast).
-PSK_HD float exp_fast_mid(float x) {
-  const float kf = rintf(x * PSK_FEXP_INV_LN2);
-  float r = fmaf(-kf, PSK_FEXP_LN2_HI, x);         // exact: ln2 hi carries 16 bits
-  r = fmaf(-kf, PSK_FEXP_LN2_LO, r);
-  float p = 1.0f / 5040.0f;
-  p = fmaf(p, r, 1.0f / 720.0f);
-  p = fmaf(p, r, 1.0f / 120.0f);
-  p = fmaf(p, r, 1.0f / 24.0f);
-  p = fmaf(p, r, 1.0f / 6.0f);
-  p = fmaf(p, r, 0.5f);
-  p = fmaf(p, r, 1.0f);
-  p = fmaf(p, r, 1.0f);
-  return u2f((uint32_t)((int32_t)f2u(p) + ((int)kf << 23)));
-}
+// A group's declared fast realization of its EXP and ERF nodes (math mode
+// FAST): within one and two f32 ulp of the correctly rounded value (measured
+// over their ranges by the host tests), not correctly rounded and not
+// bit-identical to the oracle.  (The EXP-clamp node's fast exp is in
+// pair.cuh; GELU keeps the correctly rounded erf.)
 
 // exp over every f32: x clamped to [-104.5, 89] (beyond, the result is 0 or
 // infinity either way), 2^k applied in two exact halves and one rounding at

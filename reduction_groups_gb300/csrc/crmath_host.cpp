@@ -21,9 +21,8 @@ static const float* erf_records() {
   return rec;
 }
 
-// which: 0 exp_cr, 1 erf_cr, 2 exp_faithful, 3 log_cr, 4 tanh_cr, 5 exp_fast,
-// 6 erf_fast (signed), 7 exp_fast_mid, 9 the groups' pair exp (|x| <= 87,
-// taken two at a time),
+// which: 0 exp_cr, 1 erf_cr, 3 log_cr, 4 tanh_cr, 5 exp_fast,
+// 6 erf_fast (signed),
 // 10 erf tier 1 from the record tables (R; inputs in tier 1's range),
 // 11 erf_fast of |x| from the record tables
 void psk_host_unary(int which, const float* x, float* y, long n) {
@@ -40,15 +39,6 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
     }
     return;
   }
-  if (which == 9) {
-    for (long i = 0; i < n; i += 2) {
-      const f2 a{x[i], i + 1 < n ? x[i + 1] : 0.0f};
-      const f2 r = exp2_faithful_mid(a);
-      y[i] = r.x;
-      if (i + 1 < n) y[i + 1] = r.y;
-    }
-    return;
-  }
   for (long i = 0; i < n; ++i) {
     switch (which) {
       case 0: y[i] = exp_cr(x[i], psk_exp_tab2); break;
@@ -62,8 +52,7 @@ void psk_host_unary(int which, const float* x, float* y, long n) {
         y[i] = copysignf(r, x[i]);
         break;
       }
-      case 7: y[i] = exp_fast_mid(x[i]); break;
-      default: y[i] = exp_faithful(x[i]); break;
+      default: y[i] = NAN; break;
     }
   }
 }
@@ -143,27 +132,5 @@ long psk_host_div_check(unsigned long seed, long n, float a_lo_exp, float a_hi_e
   return bad;
 }
 
-
-// The groups' pair exp (exp2_faithful_mid) against the correctly rounded
-// exp over the floats of [-a, a] whose bit patterns (of |x|) are multiples of
-// stride, both signs; returns the largest distance in ulps.
-long psk_host_exp_mid_maxulp(float a, uint32_t stride, float* worst) {
-  long maxd = 0;
-  const uint32_t top = f2u(a);
-  for (uint64_t i = 0; i <= top; i += 2 * (uint64_t)stride) {
-    for (uint32_t sign = 0; sign <= 0x80000000u; sign += 0x80000000u) {
-      const float xa = u2f(sign | (uint32_t)i);
-      const float xb = u2f(sign | (uint32_t)(i + stride <= top ? i + stride : i));
-      const f2 r = exp2_faithful_mid(f2{xa, xb});
-      const float ra[2] = {r.x, r.y}, ta[2] = {xa, xb};
-      for (int q = 0; q < 2; ++q) {
-        const long d = labs((long)f2u(ra[q]) - (long)f2u(exp_cr(ta[q], psk_exp_tab2)));
-        if (d > maxd) { maxd = d; if (worst) *worst = ta[q]; }
-      }
-      if (sign) break;
-    }
-  }
-  return maxd;
-}
 
 }  // extern "C"

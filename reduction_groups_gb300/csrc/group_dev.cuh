@@ -324,8 +324,9 @@ __device__ __noinline__ Vec<V> node_tanh(Vec<V> A, const TanhTables& tab) {
 }
 
 // The fast realization (math mode FAST) of the exp, exp-clamp and erf nodes:
-// faithful exp (at most one ulp; the clamped argument needs no special cases)
-// and erf (at most two ulp) from the same tables.
+// a faithful exp (at most one ulp) for EXP, the multifunction unit's 2^f
+// after an exact split for EXP-clamp (at most two ulp; the clamped argument
+// needs no special cases) and a faithful erf (at most two ulp).
 // Short enough to inline at every node (1.22 -> 1.11 ms on the 64-node group
 // against one out-of-line copy each).
 template <int V, bool CLAMP>
@@ -337,7 +338,7 @@ __device__ __forceinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
       float a = A.v[j], b = A.v[j + 1];
       a = clamp_pm4(a);
       b = clamp_pm4(b);
-      const f2 e = exp2_faithful_mid(f2{a, b});
+      const f2 e = exp2_unit_mid(f2{a, b});
       r.v[j] = e.x;
       r.v[j + 1] = e.y;
     }
@@ -348,7 +349,7 @@ __device__ __forceinline__ Vec<V> node_exp_fast_any(Vec<V> A) {
     float a = A.v[j];
     if (CLAMP) {
       a = clamp_pm4(a);
-      r.v[j] = exp_fast_mid(a);
+      r.v[j] = exp_unit_mid(a);
     } else {
       r.v[j] = exp_fast(a);
     }

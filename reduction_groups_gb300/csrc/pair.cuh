@@ -86,26 +86,31 @@ __device__ __forceinline__ float exp_unit_nonpos(float t) {
   const float s = u2f(f2u(z) * (1u << 23) + (191u << 23));
   return __fmul_rn(__fmul_rn(p, s), 0x1p-64f);
 }
-#endif
 
-// exp of a pair with |t| <= 88 and normal results (t >= -87.3), no special
-// cases: the same reduction and polynomial as above, 2^k added to the
-// exponent field of the polynomial's value (the sum's bit pattern shifted
-// left by 23 is k << 23).  The groups' fast EXP-clamp node (t in [-4, 4]).
-PSK_HD f2 exp2_faithful_mid(f2 t) {
+// The groups' fast EXP-clamp node: exp of t in [-4, 4] (the clamped
+// argument) by the same split and ex2.approx as above; k is in [-6, 6] and
+// every result normal, so 2^k goes on in one step (exponent field: the sum's
+// bit pattern shifted left by 23, plus 127) and the product is the one
+// rounding after ex2.approx.  Within two f32 ulp over [-4, 4] (measured on
+// the GPU against the correctly rounded exp).  Pair and scalar forms: the
+// same bits.
+__device__ __forceinline__ f2 exp2_unit_mid(f2 t) {
   const f2 z = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), f2_splat(PAIR_EXP_MAGIC));
   const f2 kf = f2_add(z, f2_splat(-PAIR_EXP_MAGIC));
-  f2 r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_HI), t);
-  r = f2_fma(kf, f2_splat(-PSK_FEXP_LN2_LO), r);
-  f2 p = f2_splat(1.0f / 5040.0f);
-  p = f2_fma(p, r, f2_splat(1.0f / 720.0f));
-  p = f2_fma(p, r, f2_splat(1.0f / 120.0f));
-  p = f2_fma(p, r, f2_splat(1.0f / 24.0f));
-  p = f2_fma(p, r, f2_splat(1.0f / 6.0f));
-  p = f2_fma(p, r, f2_splat(0.5f));
-  p = f2_fma(p, r, f2_splat(1.0f));
-  p = f2_fma(p, r, f2_splat(1.0f));
-  return f2{u2f(f2u(p.x) + f2u(z.x) * (1u << 23)), u2f(f2u(p.y) + f2u(z.y) * (1u << 23))};
+  f2 f = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), f2{-kf.x, -kf.y});
+  f = f2_fma(t, f2_splat(PAIR_LOG2E_LO), f);
+  const f2 p{ex2_unit(f.x), ex2_unit(f.y)};
+  const f2 s{u2f(f2u(z.x) * (1u << 23) + (127u << 23)), u2f(f2u(z.y) * (1u << 23) + (127u << 23))};
+  return f2_mul(p, s);
 }
+
+__device__ __forceinline__ float exp_unit_mid(float t) {
+  const float z = fmaf(t, PSK_FEXP_INV_LN2, PAIR_EXP_MAGIC);
+  const float kf = __fadd_rn(z, -PAIR_EXP_MAGIC);
+  float f = fmaf(t, PSK_FEXP_INV_LN2, -kf);
+  f = fmaf(t, PAIR_LOG2E_LO, f);
+  return __fmul_rn(ex2_unit(f), u2f(f2u(z) * (1u << 23) + (127u << 23)));
+}
+#endif
 
 }  // namespace psk

@@ -444,6 +444,7 @@ constexpr int PIPE_SX_MAX = 16;                              // x ring slots (ba
 constexpr int PIPE_SX_DEEP = 8;                              // the deep x ring of the default depths
 constexpr int PIPE_SE_MAX = 16;                              // value ring slots (a multiple of the teams)
 constexpr size_t PIPE_SMEM_BUDGET = 225 * 1024;              // dynamic shared memory of one CTA
+constexpr int PIPE_EXP_TAB_BYTES = 2048 * 4;                 // the exact softmax's copy of psk_exp_tab2
 
 // Four consecutive stored elements at j, widened.
 template <int T>
@@ -662,6 +663,14 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   unsigned char* X = pipe_smem;
   float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xslot);
   const int estride = P.estride;
+  // the correctly rounded exp's pair table, copied after the value ring
+  constexpr bool STAGE_TAB = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT;
+  float* tab = E + (size_t)SE * estride;
+  static_assert(sizeof(psk_exp_tab2) == PIPE_EXP_TAB_BYTES, "exp table size");
+  if (STAGE_TAB) {
+    for (int q = tid; q < PIPE_EXP_TAB_BYTES / 16; q += PIPE_THREADS)
+      reinterpret_cast<float4*>(tab)[q] = reinterpret_cast<const float4*>(psk_exp_tab2)[q];
+  }
   const int parts = P.partials < cols ? P.partials : cols;  // a partial beyond the row is empty
   const int G = P.nb;                                        // rows per chain group
   const int n_local = blockIdx.x < P.rows ? (int)((P.rows - 1 - blockIdx.x) / gridDim.x + 1) : 0;
@@ -873,7 +882,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
           if (KIND == REGION_SOFTMAX) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
-            region_exp8<EXPM>(u);
+            region_exp8<EXPM>(u, STAGE_TAB ? tab : psk_exp_tab2);
           } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = v[8 * h + q];
@@ -1075,7 +1084,8 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const size_t xsz = XT == PSK_F32 ? 4 : 2;
   const size_t xrow = (size_t)((P.cols * xsz * (KIND == REGION_SOFTMAX_BWD ? 2 : 1) + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
-  const size_t budget = PIPE_SMEM_BUDGET;
+  const size_t tab = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT) ? PIPE_EXP_TAB_BYTES : 0;
+  const size_t budget = PIPE_SMEM_BUDGET - tab;
   // the correctly rounded exp makes a team's row work long enough that with
   // short chains the sums are ready in time, and the x ring's depth pays
   // instead (interleaved(8): 0.466 ms with SX = 8, SE = 8; 0.500 with 4, 12)
@@ -1107,9 +1117,9 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   // most (P partials, at most one per column)
   const int glanes = 32 / (P.partials < P.cols ? P.partials : (int)P.cols);
   P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
-  const size_t smem = sx * xrow + se * erow;
+  const size_t smem = sx * xrow + se * erow + tab;
   static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK>, (int)budget, attr);
+  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK>, (int)PIPE_SMEM_BUDGET, attr);
   const int64_t sms = device_sm_count();
   const unsigned grid = (unsigned)(P.rows < sms ? P.rows : sms);
   region_pipe_kernel<KIND, XT, YT, EXPM, MASK><<<grid, PIPE_THREADS, smem, stream>>>(P);

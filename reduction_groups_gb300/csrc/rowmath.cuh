@@ -65,8 +65,12 @@ __device__ __forceinline__ float region_exp(float d) {
 
 // exp of eight values: the correctly rounded tier-1 cores run side by side
 // (independent chains for the scheduler), the rare undecided lanes after.
+// tab2: the 2^(j/1024) pair table (psk_exp_tab2 or its copy in shared
+// memory: the lookups' indices differ per lane, and a shared-memory load of
+// 32 random pairs takes a few bank wavefronts where the global table's takes
+// one L1 wavefront per distinct 128-byte line, about 25).
 template <int EXPM>
-__device__ __forceinline__ void region_exp8(float* v) {
+__device__ __forceinline__ void region_exp8(float* v, const float* tab2 = psk_exp_tab2) {
   if constexpr (EXPM == PSK_EXP_FAST) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = exp_unit_nonpos(v[q]);
@@ -78,7 +82,7 @@ __device__ __forceinline__ void region_exp8(float* v) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const bool inr = fabsf(v[q]) <= 87.0f;
-      exp_tier1_core(inr ? v[q] : 0.0f, psk_exp_tab2, R[q], d[q], n[q]);
+      exp_tier1_core(inr ? v[q] : 0.0f, tab2, R[q], d[q], n[q]);
       ok[q] = inr && tier1_decided(R[q], d[q]);
       all = all && ok[q];
     }

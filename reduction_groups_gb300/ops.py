@@ -90,8 +90,8 @@ def psk_group_run(tokens, imm, inputs, out, stream=None, math: str = "exact") ->
     """inputs: list of (tensor, strides) with one element stride per output axis
     (0 = broadcast), f32 or bf16 values or int32 SELECT conditions; out: a
     contiguous row-major tensor (f32 or bf16).  math "exact" (every node
-    correctly rounded) or "fast" (faithful exp / erf in EXP, EXPC, ERF; GELU,
-    LOG and TANH stay correctly rounded)."""
+    correctly rounded) or "fast" (EXP within one f32 ulp, EXPC and ERF within
+    two; GELU, LOG and TANH stay correctly rounded)."""
     p, keep = _program(tokens, imm)
     arr, n, o = _group_args(inputs, out)
     N.check(N.lib().psk_group_run_ex(ctypes.byref(p), arr, n, ctypes.byref(o), _MATH[math], _stream_handle(stream)))
