@@ -239,8 +239,12 @@ __device__ __forceinline__ uint4 out_group8(const uint4 w, int j, const LaneRow&
 // ------------------------------------------------------------ the kernel
 // KIND: the region; PP: the declared order's partial chains (element j feeds
 // chain j mod PP; the entry points launch the one-chain orders, PP = 1); PT:
-// the norms' parameter storage type.
-template <int KIND, int PP, int PT>
+// the norms' parameter storage type; FULL: rows of exactly LANE_MAX_COLS
+// columns (a compile-time row length: every tile whole).
+// The request and consumption counters are 32-bit: a warp makes at most
+// (2^31 rows / the grid's warps) batches x 3 passes x 64 tiles requests,
+// far below 2^31.
+template <int KIND, int PP, int PT, bool FULL = false>
 __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     region_lane_kernel(const __grid_constant__ RegionParams P, const __grid_constant__ CUtensorMap tx,
                        const __grid_constant__ CUtensorMap ty) {
@@ -248,14 +252,14 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   extern __shared__ unsigned char lane_smem_raw[];
   __shared__ __align__(8) uint64_t full[LANE_WARPS][LANE_NI];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cols = (int)P.cols;
+  const int cols = FULL ? LANE_MAX_COLS : (int)P.cols;
   const int nch = (cols + LANE_TC - 1) / LANE_TC;             // tiles per pass
   const int nb = P.nb;                                         // rows per batch (a tile's height)
   const int64_t nbatch_all = (P.rows + nb - 1) / nb;
   const int64_t gw = (int64_t)blockIdx.x * LANE_WARPS + w;
   const int64_t wtot = (int64_t)gridDim.x * LANE_WARPS;
   const int my_batches = gw < nbatch_all ? (int)((nbatch_all - 1 - gw) / wtot + 1) : 0;
-  const int64_t total = (int64_t)my_batches * NP * nch;      // tile requests of this warp
+  const int total = my_batches * NP * nch;                   // tile requests of this warp
   // tiles start on 1024-byte boundaries (the period of the 128-byte swizzle)
   const uint32_t raw = smem_addr(lane_smem_raw);
   unsigned char* wp = lane_smem_raw + (((raw + 1023u) & ~1023u) - raw) + (size_t)w * LANE_WARP_SMEM;
@@ -282,30 +286,34 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
 
   // ---- requests (lane 0): q = ((batch * NP) + pass) * nch + tile, into slot
   // q % NI; the request state is kept by every lane alike
-  int64_t rq = 0;
+  int rq = 0;
   int rb = 0, rp = 0, rc = 0;
-  int64_t withheld = -1;                                     // test hook: the request never made
+  int64_t rrow = gw * nb;                                    // the first row of the request's batch
+  int withheld = -1;                                         // test hook: the request never made
   auto issue = [&]() {
-    const int slot = (int)(rq % LANE_NI);
-    const int64_t r0 = (gw + (int64_t)rb * wtot) * nb;
+    const int slot = rq % LANE_NI;
     const int tc = lane_rev<KIND>(rp) ? nch - 1 - rc : rc;   // the pass's tile order
     if (rp == 0 && rc == 0 && drop >= (long long)rb * nb && drop < (long long)rb * nb + nb) {
       withheld = rq;                                         // as if this copy were lost
     } else if (lane == 0) {
       mbar_arrive_expect_tx(&bars[slot], (uint32_t)nb * 128u);
-      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)r0, &bars[slot],
+      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)rrow, &bars[slot],
                 rp < NP - 1 ? pol_keep : pol_drop);
     }
     ++rq;
     if (++rc == nch) {
       rc = 0;
-      if (++rp == NP) { rp = 0; ++rb; }
+      if (++rp == NP) {
+        rp = 0;
+        ++rb;
+        rrow += wtot * nb;
+      }
     }
   };
   for (int i = 0; i < LANE_NI && rq < total; ++i) issue();
 
   // ---- consumption in request order
-  int64_t cq = 0;
+  int cq = 0;
   bool dead = false;
   auto take = [&]() -> bool {
     const bool ok = mbar_wait(&bars[cq % LANE_NI], (uint32_t)(cq / LANE_NI) & 1u);
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     if (lane == 0) fence_proxy_async_smem();
     if (rq < total) issue();
   };
-  int64_t oq = 0;                                            // output tiles written
+  int oq = 0;                                                // output tiles written
 
   for (int b = 0; b < my_batches && !dead; ++b) {
     const int64_t r0 = (gw + (int64_t)b * wtot) * nb;
@@ -417,7 +425,7 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     // warp leaves
     if (lane == 0 && withheld >= cq) mbar_arrive(&bars[withheld % LANE_NI]);
     __syncwarp();
-    for (int64_t q = cq; q < rq; ++q) mbar_wait(&bars[q % LANE_NI], (uint32_t)(q / LANE_NI) & 1u);
+    for (int q = cq; q < rq; ++q) mbar_wait(&bars[q % LANE_NI], (uint32_t)(q / LANE_NI) & 1u);
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -469,11 +477,19 @@ static int lane_batch_rows(int64_t rows, int64_t wtot) {
 template <int KIND, int PP, int PT>
 static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUtensorMap& ty, int64_t sms,
                         cudaStream_t stream) {
-  static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT>, LANE_SMEM, attr);
   const int64_t nbatch = (P.rows + P.nb - 1) / P.nb;
   const int64_t need = (nbatch + LANE_WARPS - 1) / LANE_WARPS;
   const unsigned grid = (unsigned)(need < sms ? need : sms);
+  if constexpr (KIND == REGION_SOFTMAX) {   // the softmax over full rows: the full-row variant
+    if (P.cols == LANE_MAX_COLS) {
+      static bool attr_full[PSK_MAX_DEVICES] = {};
+      smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT, true>, LANE_SMEM, attr_full);
+      region_lane_kernel<KIND, PP, PT, true><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
+      return check_launch("row region kernel (lane per row)");
+    }
+  }
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT>, LANE_SMEM, attr);
   region_lane_kernel<KIND, PP, PT><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
   return check_launch("row region kernel (lane per row)");
 }
