@@ -53,8 +53,8 @@ namespace psk {
 constexpr int LANE_WARPS = 8;                                  // warps per CTA (two per scheduler)
 constexpr int LANE_TC = 64;                                    // columns of a tile (128 bytes of bf16)
 constexpr int LANE_TILE = 32 * 128;                            // a tile's slot: up to 32 rows of 128 bytes
-constexpr int LANE_NI = 4;                                     // input tiles per warp
-constexpr int LANE_NO = 2;                                     // output tiles per warp
+constexpr int LANE_NI = 6;                                     // input tiles per warp
+constexpr int LANE_NO = 1;                                     // output tiles per warp
 constexpr int LANE_WARP_SMEM = (LANE_NI + LANE_NO) * LANE_TILE;
 constexpr int LANE_SMEM = LANE_WARPS * LANE_WARP_SMEM + 1024;  // + room to align the base to 1024 bytes
 constexpr int LANE_MAX_COLS = 4096;
