@@ -775,13 +775,30 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   const int team = w / PIPE_TW, tw = w % PIPE_TW, tt = tid % PIPE_TT;
   bool dead = false;
   const size_t ysz = YT == PSK_F32 ? 4 : 2;
-  for (int k = 0;; ++k) {
+  // ring positions of the rows i and o below, kept without a division per
+  // row: i advances by the team count, which divides SX and SE; o starts at
+  // team - PIPE_TEAMS * LAG >= -SE (SE = PIPE_TEAMS * (LAG + 1)), its
+  // position and phase taken with floor division
+  int xs = team, xpar = 0;                                    // i % SX, (i / SX) & 1
+  int ei = team;                                              // i % SE
+  const int o0 = team - PIPE_TEAMS * LAG;
+  int eo = o0 >= 0 ? o0 % SE : o0 + SE;                       // o % SE
+  int opar = o0 >= 0 ? (o0 / SE) & 1 : 1;                     // floor(o / SE) & 1
+  auto advance = [&]() {
+    xs += PIPE_TEAMS;
+    if (xs >= SX) { xs -= SX; xpar ^= 1; }
+    ei += PIPE_TEAMS;
+    if (ei >= SE) ei -= SE;
+    eo += PIPE_TEAMS;
+    if (eo >= SE) { eo -= SE; opar ^= 1; }
+  };
+  for (int k = 0;; ++k, advance()) {
     const int i = team + PIPE_TEAMS * k;                     // row produced in this team iteration
     const int o = i - PIPE_TEAMS * LAG;                      // row output in this team iteration
     if (o >= n_local) break;
     dead = dead || abort_flag;
     if (i < n_local) {
-      const int s = i % SX;
+      const int s = xs;
       // masked softmax: the row's mask words, loaded before the wait for x
       constexpr bool masked = KIND == REGION_SOFTMAX && MASK;
       uint32_t mk[PIPE_EPT / 4];
@@ -793,7 +810,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
           mk[c4] = j < cols ? __ldg(reinterpret_cast<const uint32_t*>(mrow + j)) : 0u;
         }
       }
-      if (!dead && !mbar_wait(&xfull[s], (uint32_t)(i / SX) & 1u)) { abort_flag = 1; dead = true; }
+      if (!dead && !mbar_wait(&xfull[s], (uint32_t)xpar)) { abort_flag = 1; dead = true; }
       const unsigned char* xs = X + (size_t)s * xslot;
       float v[FASTSM ? 1 : PIPE_EPT];
       uint2 xw[FASTSM ? PIPE_EPT / 4 : 1];                   // fast softmax: the row's bf16 pairs as stored
@@ -859,7 +876,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         }
       }
       if (tt == 0) mbar_arrive(&xempty[s]);
-      const int se = i % SE;
+      const int se = ei;
       float* Er = E + (size_t)se * estride;
       if (FASTSM && !dead) {
         // e = exp(x - m) two at a time: x - m as x + (-m) (the same rounding)
@@ -898,8 +915,8 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
       mbar_arrive(&efull[se]);
     }
     if (o >= 0 && !dead) {
-      const int se = o % SE;
-      const uint32_t par = (uint32_t)(o / SE) & 1u;
+      const int se = eo;
+      const uint32_t par = (uint32_t)opar;
       const float* Er = E + (size_t)se * estride;
       char* yr = (char*)P.y + ((int64_t)blockIdx.x + (int64_t)o * gridDim.x) * P.ldy * ysz;
       if (BWD) {
