@@ -4,7 +4,6 @@
 
 #define PSK_HOST_BUILD 1
 #include "crmath.cuh"
-#include "pair.cuh"
 
 using namespace psk;
 

@@ -2,11 +2,8 @@
 // (fma / add / mul .rn.f32x2: one issue slot, two IEEE operations, each
 // rounded to nearest even with gradual underflow, exactly as two scalar
 // operations), the softmax region's fast exp (on pairs and alone) and the
-// groups' fast exp-clamp on pairs.
-//
-// The same source compiles as plain C++ for the host (PSK_HOST_BUILD), where a
-// pair operation is the two scalar operations; the host tests measure the
-// pair exp's error over the floats of its range on that build.
+// groups' fast exp-clamp (device code only: the exps take the multifunction
+// unit's ex2.approx, so their bounds are measured on the GPU).
 
 #pragma once
 
@@ -14,31 +11,20 @@
 
 namespace psk {
 
-#if defined(PSK_HOST_BUILD)
-struct f2 {
-  float x, y;
-};
-PSK_HD f2 f2_fma(f2 a, f2 b, f2 c) { return f2{fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y)}; }
-PSK_HD f2 f2_add(f2 a, f2 b) { return f2{a.x + b.x, a.y + b.y}; }
-PSK_HD f2 f2_mul(f2 a, f2 b) { return f2{a.x * b.x, a.y * b.y}; }
-// max with NaN propagation (either operand NaN gives NaN)
-PSK_HD float fmax_nan(float a, float b) { return (a != a || b != b) ? (a + b) : (a > b ? a : b); }
-#else
 typedef float2 f2;
 PSK_HD f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 PSK_HD f2 f2_add(f2 a, f2 b) { return __fadd2_rn(a, b); }
 PSK_HD f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
+// max with NaN propagation (either operand NaN gives NaN)
 PSK_HD float fmax_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
-#endif
 PSK_HD f2 f2_splat(float v) { return f2{v, v}; }
 
 constexpr float PAIR_EXP_MAGIC = 12582912.0f;   // 1.5 * 2^23
 
-#if !defined(PSK_HOST_BUILD)
 // 2^f for |f| <= 1/2 by the multifunction unit's ex2.approx (device only).
 __device__ __forceinline__ float ex2_unit(float f) {
   float r;
@@ -111,6 +97,5 @@ __device__ __forceinline__ float exp_unit_mid(float t) {
   f = fmaf(t, PAIR_LOG2E_LO, f);
   return __fmul_rn(ex2_unit(f), u2f(f2u(z) * (1u << 23) + (127u << 23)));
 }
-#endif
 
 }  // namespace psk
