@@ -242,18 +242,34 @@ __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
 }
 
 // gelu(a) = a * (0.5 * (1 + erf(a * RN(1/sqrt 2)))), every step rounded.
+// Where |t| >= PSK_ERF_ONE_FROM (infinities included) erf(|t|) rounds to 1:
+// taken here, without the slow tiers; a warp none of whose elements is in
+// tier 1's range skips tier 1 altogether.
 template <int V, bool GELU>
 __device__ __noinline__ Vec<V> node_erf_any(Vec<V> A, const MathTables& tab) {
-  float tt[V], R[V], d[V];
-  bool ok[V];
-  bool all = true;
+  float tt[V], aa[V], R[V], d[V];
+  bool ok[V], inr[V];
+  bool any = false;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     tt[j] = GELU ? __fmul_rn(A.v[j], PSK_INV_SQRT2) : A.v[j];
-    const float aa = fabsf(tt[j]);
-    const bool inr = aa < PSK_ERF_ONE_FROM && aa >= 0x1p-60f;
-    erf_tier1_core_rec(inr ? aa : 0.5f, reinterpret_cast<const float*>(tab.erf_rec), R[j], d[j]);
-    ok[j] = inr && tier1_decided(R[j], d[j]);
+    aa[j] = fabsf(tt[j]);
+    inr[j] = aa[j] < PSK_ERF_ONE_FROM && aa[j] >= 0x1p-60f;
+    any = any || inr[j];
+    R[j] = 1.0f;
+    d[j] = 0.0f;
+  }
+  if (__any_sync(__activemask(), any)) {
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      erf_tier1_core_rec(inr[j] ? aa[j] : 0.5f, reinterpret_cast<const float*>(tab.erf_rec), R[j], d[j]);
+  }
+  bool all = true;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const bool sat = aa[j] >= PSK_ERF_ONE_FROM;               // false for NaN
+    ok[j] = (inr[j] && tier1_decided(R[j], d[j])) || sat;
+    if (sat) R[j] = 1.0f;
     all = all && ok[j];
   }
   if (!all) {
