@@ -213,26 +213,45 @@ __device__ __forceinline__ Vec<V> node_select(const Vec<V>& C, const Vec<V>& A, 
 // instruction cache).  The tier-1 cores of the V elements run side by side
 // (independent chains for the scheduler); one branch per call sends the
 // undecided elements on to the slower tiers.
+// The exp-clamp node at a clamp bound takes the correctly rounded constant
+// (RN(e^4) = 0x1.b4c902p+5, RN(e^-4) = 0x1.2c155cp-6), and a warp whose
+// every argument sits at a bound skips tier 1.
+constexpr float PSK_EXP_P4 = 0x1.b4c902p+5f;
+constexpr float PSK_EXP_M4 = 0x1.2c155cp-6f;
 template <int V, bool CLAMP>
 __device__ __noinline__ Vec<V> node_exp_any(Vec<V> A, const MathTables& tab) {
   float a[V], R[V], d[V];
   int n[V];
-  bool ok[V];
-  bool all = true;
+  bool ok[V], bnd[V];
+  bool any = !CLAMP;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
     a[j] = A.v[j];
     if (CLAMP) {
-      a[j] = clamp_pm4(a[j]);
+      a[j] = clamp_pm4(a[j]);                         // NaN clamps to -4
     }
-    const bool inr = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range (NaN clamps to -4)
-    exp_tier1_core(inr ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
-    ok[j] = inr && tier1_decided(R[j], d[j]);
-    all = all && ok[j];
+    bnd[j] = CLAMP && fabsf(a[j]) == 4.0f;
+    any = any || !bnd[j];
+    R[j] = 1.0f;
+    d[j] = 0.0f;
+    n[j] = 0;
+  }
+  bool all = true;
+  if (!CLAMP || __any_sync(__activemask(), any)) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const bool inr = CLAMP || fabsf(a[j]) <= 87.0f;   // a clamped argument is in range
+      exp_tier1_core(inr ? a[j] : 0.0f, reinterpret_cast<const float*>(tab.exp_tab), R[j], d[j], n[j]);
+      ok[j] = (inr && tier1_decided(R[j], d[j])) || bnd[j];
+      all = all && ok[j];
+    }
   }
   Vec<V> r;
 #pragma unroll
-  for (int j = 0; j < V; ++j) r.v[j] = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
+  for (int j = 0; j < V; ++j) {
+    r.v[j] = u2f((uint32_t)((int32_t)f2u(R[j]) + n[j] * (1 << 23)));
+    if (bnd[j]) r.v[j] = a[j] > 0.0f ? PSK_EXP_P4 : PSK_EXP_M4;
+  }
   if (!all) {   // one branch per call; the elements tier 1 left undecided
 #pragma unroll
     for (int j = 0; j < V; ++j)
