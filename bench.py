@@ -502,6 +502,7 @@ def run_ours(a, ws, rank, local):
     sy = torch.empty_like(sx)
     tree = W.llama_adamw_leaves(layers=max(1, int(round(22 * sc))))
     leaves = [tree.device_leaf(i) for i in range(len(tree.leaves))]
+    clip_leaves = leaves
     split = a.split and ws > 1
     if split:
         # this rank's share of one workload: output rows of the group (the
@@ -515,6 +516,9 @@ def run_ours(a, ws, rank, local):
         g_out = g_out[g0:g1]
         s0, s1 = SH.row_range(sw.rows, ws, rank)
         sx, sy = sx[s0:s1], sy[s0:s1]
+        # the clipped step's share is cut on its squared-norm tree's group
+        # boundaries (the group sums are gathered across the ranks)
+        clip_leaves = [tuple(t[p0:p1] for t in leaves[i]) for i, p0, p1 in SH.clip_pieces(tree.numels, ws, rank)]
         leaves = [tuple(t[p0:p1] for t in leaves[i]) for i, p0, p1 in SH.param_pieces(tree.numels, ws, rank)]
     torch.cuda.synchronize()
 
@@ -649,11 +653,20 @@ def run_ours(a, ws, rank, local):
     # every gradient once more before the update), beside the step
     clip_ws = None
     if a.only in ("all", "adamw"):
-        clip_ws = torch.empty(max(16, R.psk_adamw_workspace(leaves, "cosine", 100, 5000, 1.0)), dtype=torch.uint8,
-                              device="cuda")
-        extra_launches["adamw_clip_cosine"] = lambda: R.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000, 1.0,
-                                                                         clip_ws)
-        b_all["adamw_clip_cosine"] = b_adam + n_adam * (2 if tree.grad_dtype == "bf16" else 4)
+        clip_ws = torch.empty(max(16, R.psk_adamw_workspace(clip_leaves, "cosine", 100, 5000, 1.0)),
+                              dtype=torch.uint8, device="cuda")
+        if split:
+            # each rank's group sums of ||g||^2, all-gathered, then the scale
+            # and the rank's pieces: the one-process step's bits
+            from reduction_groups_gb300 import sharded as SHD
+
+            extra_launches["adamw_clip_cosine"] = lambda: SHD.adamw_tree_clipped(
+                clip_leaves, tree.numels, ws, rank, tree.hp, 1.0, clip_ws, "cosine", 100, 5000)
+        else:
+            extra_launches["adamw_clip_cosine"] = lambda: R.psk_adamw_tree_ex(leaves, tree.hp, "cosine", 100, 5000,
+                                                                             1.0, clip_ws)
+        n_clip = sum(leaf[0].numel() for leaf in clip_leaves)
+        b_all["adamw_clip_cosine"] = n_clip * (tree.bytes_per_param() + (2 if tree.grad_dtype == "bf16" else 4))
     if a.only in ("all", "adamw", "softmax", "group"):
         for name, fn in extra_launches.items():
             for _ in range(2):
@@ -853,7 +866,7 @@ def run_ours(a, ws, rank, local):
                                         1)}
         if k == "adamw_clip_cosine":
             del kinfo[k]["rows_per_s"]
-            kinfo[k]["params_per_s"] = round(n_adam / (ms / 1e3), 1)
+            kinfo[k]["params_per_s"] = round(n_clip / (ms / 1e3), 1)
         if k == "group_select_log_tanh":
             del kinfo[k]["rows_per_s"]
             kinfo[k]["elems_per_s"] = round(xw.out_shape[0] * xw.out_shape[1] / (ms / 1e3), 1)

@@ -365,6 +365,44 @@ int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_
 int psk_adamw_tree_static(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
                           const psk_adamw_schedule* sched, void* stream);
 
+/* ------------------------------------ the clipped step over several ranks
+ * presk PSK-Realize, "Memory placement and collectives": a tree split across
+ * processes (one per GPU) updates with no exchange, except that clipping
+ * needs the global ||g||^2.  Its declared tree (blocks of 1024 elements,
+ * groups of 64 blocks, a leaf's groups, the leaves, each in order; see
+ * "schedules and clipping") makes the group sums the unit to exchange: a
+ * rank whose pieces of leaves start on group boundaries (multiples of 65,536
+ * elements of their leaf) computes its pieces' group sums exactly as the
+ * one-process step does; gathered in leaf order they give the same ||g||^2,
+ * scale and update bits on every rank.  The three calls:
+ *
+ * psk_adamw_group_sqsums: the group sums of `leaves` (pieces of the tree's
+ * leaves, each starting on a group boundary of its leaf), leaf after leaf in
+ * order, into group_sums (DEVICE, ceil(ceil(numel / 1024) / 64) floats per
+ * non-empty leaf); workspace as for psk_adamw_tree_ex with clipping
+ * (psk_adamw_workspace with grad_clip > 0).
+ *
+ * psk_adamw_clip_scale: from the whole tree's group sums (DEVICE, the
+ * gathered lists in leaf order) and the number of groups of each of its
+ * n_leaves leaves (HOST array; 0 for an empty leaf; n_leaves <=
+ * PSK_ADAMW_MAX_LEAVES), the scale min(1, c / (sqrt(||g||^2) + 1e-6)) into
+ * *scale (DEVICE); c = grad_clip > 0, finite.
+ *
+ * psk_adamw_tree_scaled: psk_adamw_tree_ex on the rank's pieces with every
+ * gradient scaled by *scale (DEVICE) as clipping does, the schedule's lr
+ * (its grad_clip is not used; NULL: constant lr).
+ *
+ * Refusals as for psk_adamw_tree_ex (PSK_E_NULL for a NULL scale, group_sums
+ * or workspace where one is needed; PSK_E_ARG otherwise).  Asynchronous on
+ * the stream; the exchange between the first two calls is the caller's (an
+ * all-gather of the group sums). */
+int psk_adamw_group_sqsums(const psk_leaf* leaves, int32_t n_leaves, float* group_sums, void* workspace,
+                           uint64_t workspace_bytes, void* stream);
+int psk_adamw_clip_scale(const float* group_sums, const int64_t* groups_per_leaf, int32_t n_leaves, double grad_clip,
+                         float* scale, void* stream);
+int psk_adamw_tree_scaled(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                          const psk_adamw_schedule* sched, const float* scale, void* stream);
+
 /* Host-only, synchronous: the device status word of the pipelined kernels of
  * the current device (0 = no bounded wait ever timed out; bit 0 = a wait gave
  * up and the kernel wound down, its output then unspecified).  reset != 0

@@ -171,24 +171,43 @@ def _seq_sum_rows(a: np.ndarray) -> np.ndarray:
     return s
 
 
-def grad_sq_norm(grads, grad_dtype: str) -> np.float32:
-    """||g||^2 over the tree in the declared f32 tree (see the module text)."""
-    total = None
-    for g in grads:
-        gf = widen(np.asarray(g), grad_dtype).reshape(-1)
-        if gf.size == 0:
-            continue
-        with np.errstate(all="ignore"):
-            sq = (gf * gf).astype(np.float32)
-            nb = -(-sq.size // SQ_BLOCK)
-            blocks = _seq_sum_rows(np.pad(sq, (0, nb * SQ_BLOCK - sq.size)).reshape(nb, SQ_BLOCK))
-            ng = -(-nb // SQ_GROUP)
-            groups = _seq_sum_rows(np.pad(blocks, (0, ng * SQ_GROUP - nb)).reshape(ng, SQ_GROUP))
-            leaf = groups[0]
-            for v in groups[1:]:
+def leaf_group_sqsums(g, grad_dtype: str) -> np.ndarray:
+    """The group sums of one leaf's ||g||^2 tree (see the module text): the
+    RN(g^2) of each block of 1024 consecutive elements added in order, the
+    block sums of each group of 64 added in order; f32, one per group."""
+    gf = widen(np.asarray(g), grad_dtype).reshape(-1)
+    if gf.size == 0:
+        return np.zeros(0, dtype=np.float32)
+    with np.errstate(all="ignore"):
+        sq = (gf * gf).astype(np.float32)
+        nb = -(-sq.size // SQ_BLOCK)
+        blocks = _seq_sum_rows(np.pad(sq, (0, nb * SQ_BLOCK - sq.size)).reshape(nb, SQ_BLOCK))
+        ng = -(-nb // SQ_GROUP)
+        return _seq_sum_rows(np.pad(blocks, (0, ng * SQ_GROUP - nb)).reshape(ng, SQ_GROUP))
+
+
+def sq_norm_from_groups(group_sums, groups_per_leaf) -> np.float32:
+    """||g||^2 from the tree's group sums in leaf order: each leaf's groups
+    added in order, then the non-empty leaves' sums in order."""
+    group_sums = np.asarray(group_sums, dtype=np.float32).reshape(-1)
+    total, at = None, 0
+    with np.errstate(all="ignore"):
+        for n in groups_per_leaf:
+            if n == 0:
+                continue
+            leaf = group_sums[at]
+            for v in group_sums[at + 1:at + n]:
                 leaf = np.float32(leaf + v)
+            at += n
             total = leaf if total is None else np.float32(total + leaf)
     return np.float32(0.0) if total is None else np.float32(total)
+
+
+def grad_sq_norm(grads, grad_dtype: str) -> np.float32:
+    """||g||^2 over the tree in the declared f32 tree (see the module text)."""
+    groups = [leaf_group_sqsums(g, grad_dtype) for g in grads]
+    return sq_norm_from_groups(np.concatenate(groups) if groups else np.zeros(0, np.float32),
+                               [len(x) for x in groups])
 
 
 def clip_scale(sq_norm: np.float32, grad_clip: float) -> np.float32:
@@ -205,13 +224,22 @@ def step_tree_scheduled(leaves, grad_dtype: str, hp, kind: str = LR_CONSTANT, wa
     """step_tree with the lr schedule and (grad_clip > 0) global-norm clipping.
     Returns (list of (theta', m', v'), scale or None)."""
     leaves = list(leaves)
-    h = hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
-    h["lr"] = lr_scheduled(hp.lr, kind, warmup, total, hp.t)
     scale = None
     if grad_clip > 0:
         scale = clip_scale(grad_sq_norm([g for _, _, _, g in leaves], grad_dtype), grad_clip)
+    return step_tree_scaled(leaves, grad_dtype, hp, scale, kind, warmup, total), scale
+
+
+def step_tree_scaled(leaves, grad_dtype: str, hp, scale, kind: str = LR_CONSTANT, warmup: int = 0, total: int = 1):
+    """The scheduled step with every gradient first scaled by `scale` (f32,
+    RN(g * scale)) when scale is not None: a clipped step whose scale is
+    known (for a tree split across ranks, from the gathered group sums)."""
+    h = hyper_f32(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.t)
+    h["lr"] = lr_scheduled(hp.lr, kind, warmup, total, hp.t)
+    leaves = list(leaves)
+    if scale is not None:
         with np.errstate(all="ignore"):
-            leaves = [(th, m, v, (widen(np.asarray(g), grad_dtype) * scale).astype(np.float32))
+            leaves = [(th, m, v, (widen(np.asarray(g), grad_dtype) * np.float32(scale)).astype(np.float32))
                       for th, m, v, g in leaves]
         grad_dtype = "f32"
-    return [step_leaf(th, m, v, g, grad_dtype, h) for th, m, v, g in leaves], scale
+    return [step_leaf(th, m, v, g, grad_dtype, h) for th, m, v, g in leaves]

@@ -6,10 +6,13 @@ parameter tree, each one CUDA launch through a C ABI (include/psk.h).
 """
 
 from .ops import (  # noqa: F401
+    psk_adamw_clip_scale,
+    psk_adamw_group_sqsums,
     psk_adamw_lr,
     psk_adamw_scalars,
     psk_adamw_tree,
     psk_adamw_tree_ex,
+    psk_adamw_tree_scaled,
     psk_adamw_tree_static,
     psk_adamw_workspace,
     psk_device_status,

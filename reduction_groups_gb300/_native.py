@@ -28,7 +28,8 @@ ERRORS = {
 EXPORTS = ("psk_group_run", "psk_group_run_ex", "psk_group_run_interp", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex", "psk_softmax_region", "psk_softmax_masked",
            "psk_softmax_backward", "psk_norm_region",
            "psk_adamw_tree", "psk_adamw_tree_ex", "psk_adamw_tree_static", "psk_adamw_lr", "psk_adamw_workspace",
-           "psk_adamw_scalars", "psk_device_status", "psk_test_drop_row", "psk_test_fast_exp", "psk_last_error")
+           "psk_adamw_scalars", "psk_adamw_group_sqsums", "psk_adamw_clip_scale", "psk_adamw_tree_scaled",
+           "psk_device_status", "psk_test_drop_row", "psk_test_fast_exp", "psk_last_error")
 
 
 class psk_program(ctypes.Structure):
@@ -114,6 +115,12 @@ def lib() -> ctypes.CDLL:
         L.psk_device_status.argtypes = [P(ctypes.c_uint32), ctypes.c_int32]
         L.psk_test_drop_row.argtypes = [ctypes.c_int64]
         L.psk_test_fast_exp.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        L.psk_adamw_group_sqsums.argtypes = [P(psk_leaf), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_uint64, ctypes.c_void_p]
+        L.psk_adamw_clip_scale.argtypes = [ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_int32, ctypes.c_double,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+        L.psk_adamw_tree_scaled.argtypes = [P(psk_leaf), ctypes.c_int32, P(psk_adamw_hparams),
+                                            P(psk_adamw_schedule), ctypes.c_void_p, ctypes.c_void_p]
         L.psk_last_error.restype = ctypes.c_char_p
         for f in ("psk_group_run", "psk_group_run_ex", "psk_group_run_interp", "psk_group_check", "psk_group_prepare", "psk_group_prepare_ex",
                   "psk_softmax_region", "psk_norm_region",
@@ -121,6 +128,7 @@ def lib() -> ctypes.CDLL:
                   "psk_adamw_tree",
                   "psk_adamw_scalars", "psk_adamw_lr", "psk_adamw_workspace", "psk_adamw_tree_ex",
                   "psk_adamw_tree_static",
+                  "psk_adamw_group_sqsums", "psk_adamw_clip_scale", "psk_adamw_tree_scaled",
                   "psk_device_status", "psk_test_drop_row", "psk_test_fast_exp"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L

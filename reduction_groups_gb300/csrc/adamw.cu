@@ -606,12 +606,14 @@ static int check_schedule(const psk_adamw_schedule* sc) {
   return PSK_OK;
 }
 
-// ||g||^2 tree and the clip scale into the workspace (launches only).
-static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace& W, char* ws, float clip,
-                       cudaStream_t stream, SqParams* staging) {
+// The block and group stages of the ||g||^2 tree (launches only): the group
+// sums of the leaves in order into `groups_out` (NULL: the workspace's), the
+// leaf sums into the workspace.
+static int launch_sq_groups(const psk_leaf* leaves, int32_t n_leaves, const Workspace& W, char* ws,
+                            float* groups_out, cudaStream_t stream, SqParams* staging) {
   SqParams* P = staging ? staging : new SqParams;
   float* blocks = (float*)(ws + W.blocks_off);
-  float* groups = (float*)(ws + W.groups_off);
+  float* groups = groups_out ? groups_out : (float*)(ws + W.groups_off);
   float* leaf_sums = (float*)(ws + W.leaves_off);
   int rc = PSK_OK, i = 0, leaf_index = 0;
   int64_t block0 = 0, group0 = 0;
@@ -650,9 +652,54 @@ static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace
     group0 += ng_batch;
   }
   if (!staging) delete P;
+  return rc;
+}
+
+// ||g||^2 tree and the clip scale into the workspace (launches only).
+static int launch_clip(const psk_leaf* leaves, int32_t n_leaves, const Workspace& W, char* ws, float clip,
+                       cudaStream_t stream, SqParams* staging) {
+  const int rc = launch_sq_groups(leaves, n_leaves, W, ws, nullptr, stream, staging);
   if (rc) return rc;
-  sq_scale_kernel<<<1, 1, 0, stream>>>(leaf_sums, (int32_t)W.n_leaves, clip, (float*)(ws + W.scale_off));
+  sq_scale_kernel<<<1, 1, 0, stream>>>((const float*)(ws + W.leaves_off), (int32_t)W.n_leaves, clip,
+                                       (float*)(ws + W.scale_off));
   return check_launch("clip scale kernel");
+}
+
+// The clip scale from a whole tree's group sums (the groups of its leaves in
+// leaf order; leaf l owns groups [begin[l], begin[l + 1])): each leaf's sum
+// of its groups in order, by one thread each, then the sum of the non-empty
+// leaves' sums in order and the scale, by thread 0 -- the tree and the
+// operations of the one-call step.
+struct ClipFromGroups {
+  int32_t n_leaves;
+  float clip;
+  int64_t begin[PSK_ADAMW_MAX_LEAVES + 1];
+};
+
+__global__ void __launch_bounds__(SQ_THREADS) clip_from_groups_kernel(const float* group_sums,
+                                                                      const __grid_constant__ ClipFromGroups P,
+                                                                      float* scale) {
+  __shared__ float leaf_sum[PSK_ADAMW_MAX_LEAVES];
+  for (int l = threadIdx.x; l < P.n_leaves; l += SQ_THREADS) {
+    const int64_t g0 = P.begin[l], g1 = P.begin[l + 1];
+    float acc = g1 > g0 ? group_sums[g0] : 0.0f;
+    for (int64_t g = g0 + 1; g < g1; ++g) acc = __fadd_rn(acc, group_sums[g]);
+    leaf_sum[l] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float acc = 0.0f;
+    bool first = true;
+    for (int l = 0; l < P.n_leaves; ++l) {
+      if (P.begin[l + 1] == P.begin[l]) continue;            // an empty leaf has no groups
+      acc = first ? leaf_sum[l] : __fadd_rn(acc, leaf_sum[l]);
+      first = false;
+    }
+    const float norm = __fsqrt_rn(acc);
+    const float den = __fadd_rn(norm, 1e-6f);
+    const float q = __fdiv_rn(P.clip, den);
+    *scale = q < 1.0f ? q : 1.0f;
+  }
 }
 
 // Host staging of the kernel parameters (the leaf tables, about 28 KB and 20
@@ -663,9 +710,11 @@ struct HostStaging {
   SqParams sq;
 };
 
+// ext_scale: a clip scale already on the device (the sharded step's), used
+// in place of the tree's own clipping.
 static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
                      const psk_adamw_schedule* sc, void* workspace, uint64_t workspace_bytes, void* stream,
-                     HostStaging* staging = nullptr) {
+                     HostStaging* staging = nullptr, const float* ext_scale = nullptr) {
   int rc = check_leaves(leaves, n_leaves);
   if (rc) return rc;
   rc = check_schedule(sc);
@@ -673,9 +722,10 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
   AdamParams* P = staging ? &staging->adam : new AdamParams;   // host staging of the kernel parameter
   rc = make_scalars(hp, P->s);
   if (rc == PSK_OK) rc = scheduled_lr(hp, sc, P->s.lr);
-  const bool clip = sc && sc->grad_clip > 0.0;
-  const Workspace W = plan_workspace(leaves, n_leaves, clip);
-  if (rc == PSK_OK && clip) {
+  const bool own_clip = !ext_scale && sc && sc->grad_clip > 0.0;
+  const bool clip = own_clip || ext_scale;
+  const Workspace W = plan_workspace(leaves, n_leaves, own_clip);
+  if (rc == PSK_OK && own_clip) {
     if (!workspace) rc = fail(PSK_E_NULL, "clipping needs a workspace of %llu bytes", (unsigned long long)W.bytes);
     else if (workspace_bytes < W.bytes)
       rc = fail(PSK_E_ARG, "workspace of %llu bytes, clipping needs %llu", (unsigned long long)workspace_bytes,
@@ -690,8 +740,8 @@ static int adamw_run(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_h
     if (per_sm < 1) per_sm = 1;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  const float* scale = clip ? (const float*)((char*)workspace + W.scale_off) : nullptr;
-  if (rc == PSK_OK && clip && W.n_leaves > 0) rc = launch_clip(leaves, n_leaves, W, (char*)workspace,
+  const float* scale = ext_scale ? ext_scale : (own_clip ? (const float*)((char*)workspace + W.scale_off) : nullptr);
+  if (rc == PSK_OK && own_clip && W.n_leaves > 0) rc = launch_clip(leaves, n_leaves, W, (char*)workspace,
                                                                (float)sc->grad_clip, s,
                                                                staging ? &staging->sq : nullptr);
   // one launch per PSK_ADAMW_MAX_LEAVES non-empty leaves of each parameter
@@ -841,4 +891,48 @@ extern "C" int psk_adamw_tree_ex(const psk_leaf* leaves, int32_t n_leaves, const
                                  void* stream) {
   clear_error();
   return adamw_run(leaves, n_leaves, hp, sched, workspace, workspace_bytes, stream);
+}
+
+extern "C" int psk_adamw_group_sqsums(const psk_leaf* leaves, int32_t n_leaves, float* group_sums, void* workspace,
+                                      uint64_t workspace_bytes, void* stream) {
+  clear_error();
+  int rc = check_leaves(leaves, n_leaves);
+  if (rc) return rc;
+  const Workspace W = plan_workspace(leaves, n_leaves, true);
+  if (W.n_groups == 0) return PSK_OK;
+  if (!group_sums) return fail(PSK_E_NULL, "group_sums is NULL");
+  if (!workspace) return fail(PSK_E_NULL, "the group sums need a workspace of %llu bytes", (unsigned long long)W.bytes);
+  if (workspace_bytes < W.bytes)
+    return fail(PSK_E_ARG, "workspace of %llu bytes, the group sums need %llu", (unsigned long long)workspace_bytes,
+                (unsigned long long)W.bytes);
+  if ((uintptr_t)workspace % 16 != 0) return fail(PSK_E_ARG, "workspace must be 16-byte aligned");
+  return launch_sq_groups(leaves, n_leaves, W, (char*)workspace, group_sums, (cudaStream_t)stream, nullptr);
+}
+
+extern "C" int psk_adamw_clip_scale(const float* group_sums, const int64_t* groups_per_leaf, int32_t n_leaves,
+                                    double grad_clip, float* scale, void* stream) {
+  clear_error();
+  if (n_leaves < 0 || n_leaves > PSK_ADAMW_MAX_LEAVES)
+    return fail(PSK_E_ARG, "n_leaves %d (at most %d)", n_leaves, PSK_ADAMW_MAX_LEAVES);
+  if (!(grad_clip > 0.0) || !isfinite(grad_clip)) return fail(PSK_E_ARG, "grad_clip must be finite and > 0");
+  if (!scale) return fail(PSK_E_NULL, "scale is NULL");
+  if (n_leaves > 0 && !groups_per_leaf) return fail(PSK_E_NULL, "groups_per_leaf is NULL");
+  ClipFromGroups P;
+  P.n_leaves = n_leaves;
+  P.clip = (float)grad_clip;
+  P.begin[0] = 0;
+  for (int l = 0; l < n_leaves; ++l) {
+    if (groups_per_leaf[l] < 0) return fail(PSK_E_ARG, "groups_per_leaf[%d] = %lld", l, (long long)groups_per_leaf[l]);
+    P.begin[l + 1] = P.begin[l] + groups_per_leaf[l];
+  }
+  if (P.begin[n_leaves] > 0 && !group_sums) return fail(PSK_E_NULL, "group_sums is NULL");
+  clip_from_groups_kernel<<<1, SQ_THREADS, 0, (cudaStream_t)stream>>>(group_sums, P, scale);
+  return check_launch("clip scale from group sums");
+}
+
+extern "C" int psk_adamw_tree_scaled(const psk_leaf* leaves, int32_t n_leaves, const psk_adamw_hparams* hp,
+                                     const psk_adamw_schedule* sched, const float* scale, void* stream) {
+  clear_error();
+  if (!scale) return fail(PSK_E_NULL, "scale is NULL");
+  return adamw_run(leaves, n_leaves, hp, sched, nullptr, 0, stream, nullptr, scale);
 }

@@ -289,6 +289,35 @@ def psk_adamw_tree_ex(leaves, hp, kind="constant", warmup=0, total=1, grad_clip=
                                       _stream_handle(stream)))
 
 
+def psk_adamw_group_sqsums(leaves, group_sums, workspace, stream=None) -> None:
+    """The squared-norm tree's group sums of `leaves` (pieces of a tree's
+    leaves, each starting on a 65,536-element boundary of its leaf), leaf
+    after leaf, into the f32 device tensor group_sums; workspace as for
+    psk_adamw_tree_ex with clipping."""
+    arr, n = _leaf_table(leaves)
+    N.check(N.lib().psk_adamw_group_sqsums(arr, n, group_sums.data_ptr(), workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+def psk_adamw_clip_scale(group_sums, groups_per_leaf, grad_clip, scale, stream=None) -> None:
+    """The clip scale from a whole tree's group sums (f32 device tensor, leaf
+    order) and its leaves' group counts (ints), into the one-element f32
+    device tensor scale."""
+    counts = (ctypes.c_int64 * max(1, len(groups_per_leaf)))(*[int(c) for c in groups_per_leaf])
+    N.check(N.lib().psk_adamw_clip_scale(group_sums.data_ptr() if group_sums.numel() else None, counts,
+                                         len(groups_per_leaf), float(grad_clip), scale.data_ptr(),
+                                         _stream_handle(stream)))
+
+
+def psk_adamw_tree_scaled(leaves, hp, scale, kind="constant", warmup=0, total=1, stream=None) -> None:
+    """psk_adamw_tree_ex with every gradient scaled by the device scalar
+    `scale` (a sharded step's clip scale) and the schedule's lr."""
+    arr, n = _leaf_table(leaves)
+    h, sc = _hparams(hp), _schedule(kind, warmup, total, 0.0)
+    N.check(N.lib().psk_adamw_tree_scaled(arr, n, ctypes.byref(h), ctypes.byref(sc), scale.data_ptr(),
+                                          _stream_handle(stream)))
+
+
 def psk_adamw_tree_static(leaves, hp, kind="constant", warmup=0, total=1, grad_clip=0.0, stream=None) -> None:
     """psk_adamw_tree_ex whose clipping scratch is the library's fixed device
     buffer (no workspace argument; overlapping calls on one device race)."""

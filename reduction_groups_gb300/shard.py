@@ -15,6 +15,12 @@ takes a disjoint share and runs it alone:
 
 The shares of ranks 0..world-1 cover every row and parameter exactly once, in
 order.  Pure host arithmetic on sizes; no device work, no torch types.
+
+The clipped AdamW step is the one case with an exchange: the global
+||g||^2 (presk "The language", The optimizer) over a declared tree of
+blocks of 1024 elements and groups of 64 blocks.  For it the tree is cut on
+group boundaries (clip_pieces), so that each rank's group sums are the
+one-process step's, and the ranks gather them (reduction_groups_gb300.sharded).
 """
 
 from __future__ import annotations
@@ -68,3 +74,65 @@ def param_pieces(numels, world: int, rank: int, quantum: int = PARAM_CUT_QUANTUM
             out.append((i, lo - base, hi - base))
         base += n
     return out
+
+
+# The squared-norm tree of clipping: blocks of SQ_BLOCK elements, groups of
+# SQ_GROUP blocks, within each leaf.
+SQ_BLOCK = 1024
+SQ_GROUP = 64
+CLIP_QUANTUM = SQ_BLOCK * SQ_GROUP
+
+
+def leaf_groups(n: int) -> int:
+    """Groups of the squared-norm tree in a leaf (or piece) of n elements."""
+    nb = -(-int(n) // SQ_BLOCK)
+    return -(-nb // SQ_GROUP)
+
+
+def groups_per_leaf(numels):
+    """Groups of every leaf of the tree, in leaf order (0 for an empty leaf)."""
+    return [leaf_groups(n) for n in numels]
+
+
+def clip_cut(numels, world: int, k: int) -> int:
+    """The k-th cut point of the tree's flattened parameters for the sharded
+    clipped step: k * total / world moved down to the nearest group boundary
+    of the leaf it falls in (a multiple of CLIP_QUANTUM elements from the
+    leaf's start, or the leaf's start); cut 0 is 0, cut `world` is total."""
+    numels = [int(n) for n in numels]
+    total = sum(numels)
+    if k <= 0:
+        return 0
+    if k >= world:
+        return total
+    t = total * k // world
+    base = 0
+    for n in numels:
+        if t < base + n:
+            return base + (t - base) // CLIP_QUANTUM * CLIP_QUANTUM
+        base += n
+    return total
+
+
+def clip_pieces(numels, world: int, rank: int):
+    """The pieces of rank `rank` for the sharded clipped step: (leaf index,
+    lo, hi) element ranges within their leaves, in order, between clip cuts
+    rank and rank + 1 -- every piece starts on a group boundary of its leaf
+    (lo a multiple of CLIP_QUANTUM), so its group sums are the leaf's."""
+    _check(world, rank)
+    numels = [int(n) for n in numels]
+    if any(n < 0 for n in numels):
+        raise ValueError("negative leaf size")
+    a, b = clip_cut(numels, world, rank), clip_cut(numels, world, rank + 1)
+    out, base = [], 0
+    for i, n in enumerate(numels):
+        lo, hi = max(a, base), min(b, base + n)
+        if hi > lo:
+            out.append((i, lo - base, hi - base))
+        base += n
+    return out
+
+
+def clip_piece_groups(numels, world: int, rank: int) -> int:
+    """Group sums rank `rank` contributes: the groups of its clip pieces."""
+    return sum(leaf_groups(hi - lo) for _, lo, hi in clip_pieces(numels, world, rank))

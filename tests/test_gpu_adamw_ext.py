@@ -200,3 +200,102 @@ def test_clip_norm_over_mixed_gradient_types_in_one_warp(dev):
         assert np.array_equal(_to_host(th).view(np.uint32), wt.view(np.uint32))
         assert np.array_equal(_to_host(m).view(np.uint32), wm.view(np.uint32))
         assert np.array_equal(_to_host(v).view(np.uint32), wv.view(np.uint32))
+
+
+def _clip_tree(seed, numels, grad_dtype):
+    rng = np.random.default_rng(seed)
+    host = []
+    for n in numels:
+        th = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        m = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+        v = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+        host.append((th, m, v, f32_to_bf16(g) if grad_dtype == "bf16" else g))
+    return host
+
+
+@pytest.mark.parametrize("world", [2, 3, 5])
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+def test_sharded_clipped_step_equals_one_call(dev, world, grad_dtype):
+    """The clipped step of a tree split into `world` ranks' pieces (cut on
+    the squared-norm tree's group boundaries), run rank after rank on one
+    GPU: each rank's group sums (psk_adamw_group_sqsums), the sums gathered
+    in rank order, the scale from them (psk_adamw_clip_scale), each rank's
+    pieces updated with it (psk_adamw_tree_scaled) -- the scale and every
+    parameter bit for bit those of one psk_adamw_tree_ex call and of the
+    oracle."""
+    from reduction_groups_gb300 import shard as S
+
+    numels = [200_000, 5, 70_000, 131_072, 0, 65_536 * 3 + 7, 1000]
+    host = _clip_tree(17, numels, grad_dtype)
+    hp, clip = W.AdamWHyper(lr=1e-3, t=7), 1e-2
+    want, wscale = OA.step_tree_scheduled(host, grad_dtype, hp, "cosine", 2, 30, grad_clip=clip)
+    # one call
+    one = [tuple(_to_dev(a, grad_dtype if k == 3 else "f32") for k, a in enumerate(h)) for h in host]
+    ws = _workspace(dev, one, kind="cosine", warmup=2, total=30, grad_clip=clip)
+    dev.psk_adamw_tree_ex(one, hp, "cosine", 2, 30, clip, ws)
+    # the ranks
+    full = [tuple(_to_dev(a, grad_dtype if k == 3 else "f32") for k, a in enumerate(h)) for h in host]
+    shares = [[tuple(t[lo:hi] for t in full[i]) for i, lo, hi in S.clip_pieces(numels, world, r)]
+              for r in range(world)]
+    sums = []
+    for r in range(world):
+        n_r = S.clip_piece_groups(numels, world, r)
+        gs = torch.empty(max(n_r, 1), dtype=torch.float32, device="cuda")
+        if n_r:
+            dev.psk_adamw_group_sqsums(shares[r], gs[:n_r], _workspace(dev, shares[r], grad_clip=clip))
+        sums.append(gs[:n_r])
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    dev.psk_adamw_clip_scale(torch.cat(sums), S.groups_per_leaf(numels), clip, scale)
+    for r in range(world):
+        dev.psk_adamw_tree_scaled(shares[r], hp, scale, "cosine", 2, 30)
+    torch.cuda.synchronize()
+    assert scale.cpu().numpy().view(np.uint32)[0] == np.float32(wscale).view(np.uint32)
+    assert ws[:4].cpu().numpy().view(np.uint32)[0] == np.float32(wscale).view(np.uint32)
+    _check(full, want)
+    _check(one, want)
+
+
+def test_sharded_clip_through_a_one_rank_process_group(dev):
+    """reduction_groups_gb300.sharded.adamw_tree_clipped on a one-rank NCCL
+    group (the path's collective with nothing to gather) equals the oracle."""
+    import datetime
+    import os
+
+    import torch.distributed as dist
+
+    from reduction_groups_gb300 import shard as S
+    from reduction_groups_gb300 import sharded as SH
+
+    if not dist.is_nccl_available():
+        pytest.skip("no NCCL")
+    numels = [70_000, 3, 131_072]
+    host = _clip_tree(23, numels, "bf16")
+    hp, clip = W.AdamWHyper(lr=1e-3, t=3), 1e-2
+    want, wscale = OA.step_tree_scheduled(host, "bf16", hp, grad_clip=clip)
+    full = [tuple(_to_dev(a, "bf16" if k == 3 else "f32") for k, a in enumerate(h)) for h in host]
+    pieces = [tuple(t[lo:hi] for t in full[i]) for i, lo, hi in S.clip_pieces(numels, 1, 0)]
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29677")
+    dist.init_process_group("nccl", rank=0, world_size=1, timeout=datetime.timedelta(seconds=120))
+    try:
+        scale = SH.adamw_tree_clipped(pieces, numels, 1, 0, hp, clip, _workspace(dev, pieces, grad_clip=clip))
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert scale.cpu().numpy().view(np.uint32)[0] == np.float32(wscale).view(np.uint32)
+    _check(full, want)
+
+
+def test_sharded_clip_refusals(dev):
+    import ctypes
+
+    from reduction_groups_gb300 import _native as N
+
+    L = N.lib()
+    scale = torch.empty(1, dtype=torch.float32, device="cuda")
+    counts = (ctypes.c_int64 * 1)(1)
+    assert L.psk_adamw_clip_scale(None, counts, 1, 1.0, scale.data_ptr(), None) == -5         # no group sums
+    assert L.psk_adamw_clip_scale(None, counts, 1, 0.0, scale.data_ptr(), None) == -9         # clip must be > 0
+    assert L.psk_adamw_clip_scale(None, counts, 600, 1.0, scale.data_ptr(), None) == -9       # too many leaves
+    assert L.psk_adamw_tree_scaled(None, 0, None, None, None, None) == -5                    # no scale

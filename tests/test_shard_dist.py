@@ -2,7 +2,9 @@
 shares cover every row and parameter exactly once, and, over two gloo ranks
 on CPU, the oracle run on each rank's share, gathered in rank order, gives
 the one-rank result bit for bit (the cases are independent per row and per
-parameter: nothing is exchanged)."""
+parameter: nothing is exchanged).  The clipped AdamW step exchanges the
+group sums of its squared-norm tree: the tree cut on group boundaries, the
+sums gathered, the norm, scale and updates are the one-rank step's."""
 
 import os
 import sys
@@ -72,6 +74,32 @@ def test_param_pieces_cover_every_parameter_once(tree, world):
         assert max(shares) - min(shares) <= 2 * S.PARAM_CUT_QUANTUM
 
 
+@pytest.mark.parametrize("tree", ["llama", "ragged", "long"])
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_clip_pieces_start_on_group_boundaries_and_cover_once(tree, world):
+    if tree == "llama":
+        numels = W.llama_adamw_leaves().numels
+    elif tree == "ragged":
+        numels = [5, 0, 130, 1, 64, 0, 1000, 3]
+    else:
+        numels = [200_000, 5, 70_000, 131_072, 0, 65_536 * 3 + 7]
+    hits = [np.zeros(n, dtype=np.int64) for n in numels]
+    groups = 0
+    prev_end = 0
+    starts = np.concatenate([[0], np.cumsum(numels)])
+    for r in range(world):
+        pieces = S.clip_pieces(numels, world, r)
+        for i, lo, hi in pieces:
+            assert lo % S.CLIP_QUANTUM == 0 and 0 <= lo < hi <= numels[i]
+            hits[i][lo:hi] += 1
+            assert starts[i] + lo == prev_end          # contiguous, in rank order
+            prev_end = starts[i] + hi
+        groups += S.clip_piece_groups(numels, world, r)
+    assert prev_end == sum(numels)
+    assert all((h == 1).all() for h in hits)
+    assert groups == sum(S.groups_per_leaf(numels))
+
+
 def test_shares_refuse_a_bad_rank():
     with pytest.raises(ValueError):
         S.row_range(10, 2, 2)
@@ -105,7 +133,22 @@ def _worker(rank, world, port, q):
         hl = [tree.host_leaf(i) for i in range(len(tree.leaves))]
         pieces = S.param_pieces(tree.numels, world, rank)
         ay = OA.step_tree([tuple(t[p0:p1] for t in hl[i]) for i, p0, p1 in pieces], tree.grad_dtype, tree.hp)
-        mine = {"gy": gy, "sy": sy, "pieces": pieces, "ay": ay}
+        # the clipped step on a tree of leaves several groups long: the tree
+        # cut on group boundaries, each rank's group sums of ||g||^2 gathered
+        # (the one exchange), the scale formed from them, the pieces updated
+        rng = np.random.default_rng(5)
+        cn = [200_000, 5, 70_000, 131_072, 0, 65_536 * 3 + 7]
+        ct = [tuple(rng.standard_normal(n).astype(np.float32) * s_ for s_ in (0.02, 1e-3, 1e-4, 1e-2)) for n in cn]
+        ct = [(a, b, np.abs(c), d) for a, b, c, d in ct]
+        cp = S.clip_pieces(cn, world, rank)
+        cg = np.concatenate([OA.leaf_group_sqsums(ct[i][3][p0:p1], "f32") for i, p0, p1 in cp] or
+                            [np.zeros(0, np.float32)])
+        parts = [None] * world
+        dist.all_gather_object(parts, cg)
+        norm = OA.sq_norm_from_groups(np.concatenate(parts), S.groups_per_leaf(cn))
+        cscale = OA.clip_scale(norm, 0.5)
+        cy = OA.step_tree_scaled([tuple(t[p0:p1] for t in ct[i]) for i, p0, p1 in cp], "f32", tree.hp, cscale)
+        mine = {"gy": gy, "sy": sy, "pieces": pieces, "ay": ay, "norm": norm, "cp": cp, "cy": cy}
         every = [None] * world
         dist.all_gather_object(every, mine)
         if rank == 0:
@@ -128,6 +171,18 @@ def _worker(rank, world, port, q):
             ok.append(all((h == 1).all() for h in hits))
             ok.append(all(np.array_equal(g.view(np.uint32), w_.view(np.uint32))
                           for gl, wl_ in zip(got, whole) for g, w_ in zip(gl, wl_)))
+            # the sharded clipped step: the same norm on every rank, equal to
+            # the one-rank norm, and the pieces' updates the one-rank step's
+            want_norm = OA.grad_sq_norm([t[3] for t in ct], "f32")
+            ok.append(all(e["norm"].view(np.uint32) == want_norm.view(np.uint32) for e in every))
+            cwhole, _ = OA.step_tree_scheduled(ct, "f32", tree.hp, grad_clip=0.5)
+            cgot = [[np.zeros_like(t) for t in w] for w in cwhole]
+            for e in every:
+                for (i, p0, p1), res in zip(e["cp"], e["cy"]):
+                    for j in range(3):
+                        cgot[i][j][p0:p1] = res[j]
+            ok.append(all(np.array_equal(g.view(np.uint32), w_.view(np.uint32))
+                          for gl, wl_ in zip(cgot, cwhole) for g, w_ in zip(gl, wl_)))
             q.put(ok)
         dist.barrier()
     finally:
@@ -144,4 +199,4 @@ def test_sharded_oracle_equals_one_rank_gloo():
     for p in ps:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert ok == [True] * 5, ok
+    assert ok == [True] * 7, ok
