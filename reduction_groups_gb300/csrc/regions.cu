@@ -654,6 +654,10 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   // fast softmax over bf16 rows: the max on the stored pairs, exp and the
   // division on f32 pairs
   constexpr bool FASTSM = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_FAST && XT == PSK_BF16 && !MASK;
+  // the softmax with the correctly rounded exp: one copy of the eight-wide
+  // exp in a rolled loop over x re-read from its slot (four unrolled copies
+  // overflowed the instruction cache), the slot freed by each warp after it
+  constexpr bool REXP = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && !MASK;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cols = (int)P.cols;
   const uint32_t rbytes = (uint32_t)cols * XSZ;               // one stored row
@@ -676,7 +680,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   const int n_local = blockIdx.x < P.rows ? (int)((P.rows - 1 - blockIdx.x) / gridDim.x + 1) : 0;
 
   if (tid == 0) {
-    for (int i = 0; i < SX; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], 1); }
+    for (int i = 0; i < SX; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], REXP ? PIPE_TW : 1); }
     for (int i = 0; i < SE; ++i) { mbar_init(&efull[i], PIPE_TT); mbar_init(&sready[i], 1); }
     abort_flag = 0;
     fence_barrier_init();
@@ -875,7 +879,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
           if (!team_any) m = 0.0f;                           // a row the mask empties: every exp is 0
         }
       }
-      if (tt == 0) mbar_arrive(&xempty[s]);
+      if (!REXP && tt == 0) mbar_arrive(&xempty[s]);
       const int se = ei;
       float* Er = E + (size_t)se * estride;
       if (FASTSM && !dead) {
@@ -890,6 +894,29 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
             const f2 b = exp2_unit_nonpos(f2_add(
                 f2{__uint_as_float(xw[c4].y << 16), __uint_as_float(xw[c4].y & 0xFFFF0000u)}, nm));
             *reinterpret_cast<float4*>(Er + j) = make_float4(a.x, a.y, b.x, b.y);
+          }
+        }
+      } else if (REXP && !dead) {
+#pragma unroll 1
+        for (int h = 0; h < PIPE_EPT / 8; ++h) {
+          float u[8];
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int j = (2 * h + kk) * (PIPE_TT * 4) + 4 * tt;
+            if (j < cols) {
+              load4<XT>(xs, j, u + 4 * kk);
+            } else {
+              u[4 * kk] = u[4 * kk + 1] = u[4 * kk + 2] = u[4 * kk + 3] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(u[q], m);
+          region_exp8<EXPM>(u, tab);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int j = (2 * h + kk) * (PIPE_TT * 4) + 4 * tt;
+            if (j < cols)
+              *reinterpret_cast<float4*>(Er + j) = make_float4(u[4 * kk], u[4 * kk + 1], u[4 * kk + 2], u[4 * kk + 3]);
           }
         }
       } else if (!dead) {
@@ -911,6 +938,10 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
               *reinterpret_cast<float4*>(Er + j) = make_float4(u[4 * kk], u[4 * kk + 1], u[4 * kk + 2], u[4 * kk + 3]);
           }
         }
+      }
+      if (REXP) {                                            // this warp has read its x
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xempty[s]);
       }
       mbar_arrive(&efull[se]);
     }
