@@ -640,7 +640,9 @@ __device__ __forceinline__ bool bwd_epilogue(const RegionParams& P, char* yr, in
   return true;
 }
 
-template <int KIND, int XT, int YT, int EXPM, bool MASK>
+// TAB: the correctly rounded exp's table copied into shared memory (the
+// launch's choice: short chains), read from there with shared loads.
+template <int KIND, int XT, int YT, int EXPM, bool MASK, bool TAB = false>
 __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __grid_constant__ RegionParams P) {
   extern __shared__ __align__(128) unsigned char pipe_smem[];
   __shared__ __align__(8) uint64_t xfull[PIPE_SX_MAX], xempty[PIPE_SX_MAX], efull[PIPE_SE_MAX], sready[PIPE_SE_MAX];
@@ -668,13 +670,14 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   float* E = reinterpret_cast<float*>(pipe_smem + (size_t)SX * xslot);
   const int estride = P.estride;
   // the correctly rounded exp's pair table, copied after the value ring
-  constexpr bool STAGE_TAB = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT;
-  float* tab = E + (size_t)SE * estride;
+  constexpr bool STAGE_TAB = TAB && KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT;
   static_assert(sizeof(psk_exp_tab2) == PIPE_EXP_TAB_BYTES, "exp table size");
+  float* tab_smem = E + (size_t)SE * estride;
   if (STAGE_TAB) {
     for (int q = tid; q < PIPE_EXP_TAB_BYTES / 16; q += PIPE_THREADS)
-      reinterpret_cast<float4*>(tab)[q] = reinterpret_cast<const float4*>(psk_exp_tab2)[q];
+      reinterpret_cast<float4*>(tab_smem)[q] = reinterpret_cast<const float4*>(psk_exp_tab2)[q];
   }
+  const float* tab = STAGE_TAB ? tab_smem : psk_exp_tab2;
   const int parts = P.partials < cols ? P.partials : cols;  // a partial beyond the row is empty
   const int G = P.nb;                                        // rows per chain group
   const int n_local = blockIdx.x < P.rows ? (int)((P.rows - 1 - blockIdx.x) / gridDim.x + 1) : 0;
@@ -926,7 +929,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
           if (KIND == REGION_SOFTMAX) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = __fsub_rn(v[8 * h + q], m);
-            region_exp8<EXPM>(u, STAGE_TAB ? tab : psk_exp_tab2);
+            region_exp8<EXPM>(u, tab);
           } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = v[8 * h + q];
@@ -1132,12 +1135,17 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const size_t xsz = XT == PSK_F32 ? 4 : 2;
   const size_t xrow = (size_t)((P.cols * xsz * (KIND == REGION_SOFTMAX_BWD ? 2 : 1) + 127) / 128) * 128;
   const size_t erow = (size_t)P.estride * sizeof(float);
-  const size_t tab = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT) ? PIPE_EXP_TAB_BYTES : 0;
-  const size_t budget = PIPE_SMEM_BUDGET - tab;
   // the correctly rounded exp makes a team's row work long enough that with
   // short chains the sums are ready in time, and the x ring's depth pays
-  // instead (interleaved(8): 0.466 ms with SX = 8, SE = 8; 0.500 with 4, 12)
+  // instead (interleaved(8): 0.466 ms with SX = 8, SE = 8; 0.500 with 4, 12),
+  // as does the exp table in shared memory (0.337 ms against 0.362 without);
+  // long chains want the value ring deep instead (sequential: 0.423 ms with
+  // SE = 12 and the table in global memory, 0.502 with SE = 8 and the table
+  // in shared memory)
   const int64_t chain = (P.cols + P.partials - 1) / P.partials;
+  const bool stage_tab = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && chain < 1024;
+  const size_t tab = stage_tab ? PIPE_EXP_TAB_BYTES : 0;
+  const size_t budget = PIPE_SMEM_BUDGET - tab;
   int sx = (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT && chain < 1024) ? PIPE_SX_DEEP : 4;
   int se = (int)((budget - sx * xrow) / (PIPE_TEAMS * erow)) * PIPE_TEAMS;
   if (se > PIPE_SE_MAX) se = PIPE_SE_MAX;
@@ -1166,10 +1174,19 @@ static int launch_pipe(RegionParams P, cudaStream_t stream) {
   const int glanes = 32 / (P.partials < P.cols ? P.partials : (int)P.cols);
   P.nb = glanes >= 4 ? 4 : (glanes >= 2 ? 2 : 1);
   const size_t smem = sx * xrow + se * erow + tab;
-  static bool attr[PSK_MAX_DEVICES] = {};
-  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK>, (int)PIPE_SMEM_BUDGET, attr);
   const int64_t sms = device_sm_count();
   const unsigned grid = (unsigned)(P.rows < sms ? P.rows : sms);
+  if constexpr (KIND == REGION_SOFTMAX && EXPM == PSK_EXP_EXACT) {
+    if (stage_tab) {
+      static bool attr_tab[PSK_MAX_DEVICES] = {};
+      smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK, true>, (int)PIPE_SMEM_BUDGET,
+                      attr_tab);
+      region_pipe_kernel<KIND, XT, YT, EXPM, MASK, true><<<grid, PIPE_THREADS, smem, stream>>>(P);
+      return check_launch("row region kernel (pipelined)");
+    }
+  }
+  static bool attr[PSK_MAX_DEVICES] = {};
+  smem_limit_once((const void*)region_pipe_kernel<KIND, XT, YT, EXPM, MASK>, (int)PIPE_SMEM_BUDGET, attr);
   region_pipe_kernel<KIND, XT, YT, EXPM, MASK><<<grid, PIPE_THREADS, smem, stream>>>(P);
   return check_launch("row region kernel (pipelined)");
 }
