@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
   constexpr bool BWD = KIND == REGION_SOFTMAX_BWD;
   // fast softmax over bf16 rows: the max on the stored pairs, exp and the
   // division on f32 pairs
-  constexpr bool FASTSM = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_FAST && XT == PSK_BF16 && !MASK;
+  constexpr bool FASTSM = KIND == REGION_SOFTMAX && EXPM == PSK_EXP_FAST && XT == PSK_BF16;
   // the softmax with the correctly rounded exp: one copy of the eight-wide
   // exp in a rolled loop over x re-read from its slot (four unrolled copies
   // overflowed the instruction cache), the slot freed by each warp after it
@@ -829,6 +829,16 @@ __global__ void __launch_bounds__(PIPE_THREADS, 1) region_pipe_kernel(const __gr
         for (int c4 = 0; c4 < PIPE_EPT / 4; ++c4) {
           const int j = c4 * (PIPE_TT * 4) + 4 * tt;
           xw[c4] = (j < cols && !dead) ? *reinterpret_cast<const uint2*>(xs + 2 * j) : make_uint2(0xFF80FF80u, 0xFF80FF80u);
+          if (masked) {
+            // a refused position (mask byte 0; byte q is element j + q) reads
+            // as bf16 -inf, as the f32 path's -INFINITY
+            const uint32_t w = mk[c4];
+            const uint32_t ka = ((w & 0xFFu) ? 0x0000FFFFu : 0u) | ((w & 0xFF00u) ? 0xFFFF0000u : 0u);
+            const uint32_t kb = ((w & 0xFF0000u) ? 0x0000FFFFu : 0u) | ((w & 0xFF000000u) ? 0xFFFF0000u : 0u);
+            xw[c4].x = (xw[c4].x & ka) | (0xFF80FF80u & ~ka);
+            xw[c4].y = (xw[c4].y & kb) | (0xFF80FF80u & ~kb);
+            any |= (w != 0u);
+          }
           mb = bf16x2_max_nan(mb, bf16x2_max_nan(xw[c4].x, xw[c4].y));
         }
         m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
