@@ -107,6 +107,28 @@ def test_masked_softmax_fast_exp_and_bool_mask(dev):
         assert rel.max() <= 1e-6
 
 
+def test_masked_softmax_fast_bf16_out_one_mask_row(dev):
+    """The fast masked softmax with bf16 outputs and one mask row for every
+    row (a mask stride of 0, the benchmark's form): refused positions 0, the
+    rest within one bf16 ulp of the oracle; a mask refusing everything gives
+    zero rows."""
+    wl = W.softmax_rows(300, 4096)
+    x = wl.host_x()
+    rng = np.random.default_rng(12)
+    for keep in (0.7, 0.0):
+        mrow = rng.random(4096) < keep
+        mask = np.broadcast_to(mrow, (300, 4096))
+        for order in (("sequential",), ("interleaved", 8)):
+            want = OS.softmax_region(x, "bf16", "bf16", order, mask=np.ascontiguousarray(mask))
+            y = _empty((300, 4096), "bf16")
+            dev.psk_softmax_masked(_to_dev(x, "bf16"), y, torch.from_numpy(mrow).cuda(), order, "fast")
+            torch.cuda.synchronize()
+            got = _to_host(y)
+            assert np.all(got[:, ~mrow] == 0)
+            d = np.abs(got.astype(np.int32) - want.astype(np.int32))
+            assert d.max() <= 1, f"keep {keep}, order {order}: {d.max()} bf16 ulp"
+
+
 @pytest.mark.parametrize("order", ORDERS, ids=lambda o: "-".join(map(str, o)))
 @pytest.mark.parametrize("shape,yt,ct_t,dxt", [((300, 512), "bf16", "bf16", "bf16"), ((2000, 4096), "bf16", "bf16", "f32"),
                                                ((64, 640), "f32", "f32", "f32"), ((37, 999), "bf16", "f32", "bf16"),
