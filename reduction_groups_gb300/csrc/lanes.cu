@@ -165,7 +165,7 @@ struct LaneRow {
 // (their index order); the other passes right to left, so that each pass
 // starts on the tiles the one before it read last.
 template <int KIND>
-__host__ __device__ constexpr int lane_passes() { return KIND == REGION_RMS ? 2 : 3; }
+__host__ __device__ constexpr int lane_passes() { return KIND == REGION_RMS || KIND == REGION_SOFTMAX_BWD ? 2 : 3; }
 template <int KIND>
 __host__ __device__ constexpr bool lane_rev(int pass) {
   return KIND == REGION_SOFTMAX ? pass != 1 : pass == lane_passes<KIND>() - 1;
@@ -173,11 +173,17 @@ __host__ __device__ constexpr bool lane_rev(int pass) {
 
 // The values a chain pass adds for a group of eight stored elements:
 // softmax e = exp(x - m) (fast realization); RMSNorm RN(x^2); LayerNorm x,
-// then RN(RN(x - mu)^2).
+// then RN(RN(x - mu)^2); softmax backward RN(ct y) (w the stored y, cw ct).
 template <int KIND>
-__device__ __forceinline__ void chain_values8(const uint4 w, int pass, const LaneRow& R, float* f) {
+__device__ __forceinline__ void chain_values8(const uint4 w, const uint4 cw, int pass, const LaneRow& R, float* f) {
   if constexpr (KIND == REGION_SOFTMAX) {
     lane_exp8(w, R.m, f);
+  } else if constexpr (KIND == REGION_SOFTMAX_BWD) {
+    float c[8];
+    widen8(w, f);
+    widen8(cw, c);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) f[q] = __fmul_rn(c[q], f[q]);
   } else {
     widen8(w, f);
 #pragma unroll
@@ -194,11 +200,19 @@ __device__ __forceinline__ void chain_values8(const uint4 w, int pass, const Lan
 
 // The outputs of a group of eight stored elements at column j, rounded to
 // bf16 pairs: softmax e / s (the pipelined kernel's fast realization); norms
-// (x - mu) / d, * gamma, + beta.
+// (x - mu) / d, * gamma, + beta; softmax backward RN(y RN(ct - s)) (w the
+// stored y, cw ct).
 template <int KIND, int PT>
-__device__ __forceinline__ uint4 out_group8(const uint4 w, int j, const LaneRow& R, const RegionParams& P) {
+__device__ __forceinline__ uint4 out_group8(const uint4 w, const uint4 cw, int j, const LaneRow& R,
+                                            const RegionParams& P) {
   float o[8];
-  if constexpr (KIND == REGION_SOFTMAX) {
+  if constexpr (KIND == REGION_SOFTMAX_BWD) {
+    float c[8];
+    widen8(w, o);
+    widen8(cw, c);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(o[q], __fsub_rn(c[q], R.s));
+  } else if constexpr (KIND == REGION_SOFTMAX) {
     lane_exp8(w, R.m, o);
     if (R.fast_ok) {
       // Markstein's correction two at a time (no per-element range test)
@@ -244,11 +258,17 @@ __device__ __forceinline__ uint4 out_group8(const uint4 w, int j, const LaneRow&
 // The request and consumption counters are 32-bit: a warp makes at most
 // (2^31 rows / the grid's warps) batches x 3 passes x 64 tiles requests,
 // far below 2^31.
+// The softmax backward (KIND REGION_SOFTMAX_BWD; x is y, tct the cotangent's
+// map, y is dx) loads a y tile and a ct tile per request: its ring slots are
+// pairs of tiles, half as many.
 template <int KIND, int PP, int PT, bool FULL = false>
 __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     region_lane_kernel(const __grid_constant__ RegionParams P, const __grid_constant__ CUtensorMap tx,
-                       const __grid_constant__ CUtensorMap ty) {
+                       const __grid_constant__ CUtensorMap ty, const __grid_constant__ CUtensorMap tct) {
   constexpr int NP = lane_passes<KIND>();
+  constexpr bool BWD = KIND == REGION_SOFTMAX_BWD;
+  constexpr int TPR = BWD ? 2 : 1;                             // tiles per request
+  constexpr int NI = LANE_NI / TPR;                            // request slots
   extern __shared__ unsigned char lane_smem_raw[];
   __shared__ __align__(8) uint64_t full[LANE_WARPS][LANE_NI];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -291,14 +311,17 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   int64_t rrow = gw * nb;                                    // the first row of the request's batch
   int withheld = -1;                                         // test hook: the request never made
   auto issue = [&]() {
-    const int slot = rq % LANE_NI;
+    const int slot = rq % NI;
     const int tc = lane_rev<KIND>(rp) ? nch - 1 - rc : rc;   // the pass's tile order
     if (rp == 0 && rc == 0 && drop >= (long long)rb * nb && drop < (long long)rb * nb + nb) {
       withheld = rq;                                         // as if this copy were lost
     } else if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[slot], (uint32_t)nb * 128u);
-      tile_load(wa + (uint32_t)slot * LANE_TILE, &tx, tc * LANE_TC, (int)rrow, &bars[slot],
+      mbar_arrive_expect_tx(&bars[slot], (uint32_t)(nb * 128 * TPR));
+      tile_load(wa + (uint32_t)(slot * TPR) * LANE_TILE, &tx, tc * LANE_TC, (int)rrow, &bars[slot],
                 rp < NP - 1 ? pol_keep : pol_drop);
+      if (BWD)
+        tile_load(wa + (uint32_t)(slot * TPR + 1) * LANE_TILE, &tct, tc * LANE_TC, (int)rrow, &bars[slot],
+                  rp < NP - 1 ? pol_keep : pol_drop);
     }
     ++rq;
     if (++rc == nch) {
@@ -310,13 +333,13 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
       }
     }
   };
-  for (int i = 0; i < LANE_NI && rq < total; ++i) issue();
+  for (int i = 0; i < NI && rq < total; ++i) issue();
 
   // ---- consumption in request order
   int cq = 0;
   bool dead = false;
   auto take = [&]() -> bool {
-    const bool ok = mbar_wait(&bars[cq % LANE_NI], (uint32_t)(cq / LANE_NI) & 1u);
+    const bool ok = mbar_wait(&bars[cq % NI], (uint32_t)(cq / NI) & 1u);
     return !__any_sync(0xffffffffu, !ok);
   };
   auto release = [&]() {                                     // every lane has read the tile: refill its slot
@@ -342,23 +365,26 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
         const int c = rev ? nch - 1 - t : t;
         if (!take()) { dead = true; break; }
         const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
-        const unsigned char* tile = wp + (size_t)(cq % LANE_NI) * LANE_TILE;
+        const unsigned char* tile = wp + (size_t)((cq % NI) * TPR) * LANE_TILE;
+        const unsigned char* ctile = tile + LANE_TILE;            // the backward's ct tile
         if (out_pass) {
           if (lane == 0) bulk_wait_read<LANE_NO - 1>();     // the store that last used this slot has read it
           __syncwarp();
           unsigned char* ot = op + (size_t)(oq % LANE_NO) * LANE_TILE;
           if (ng == 8) {
-            uint4 v[8], o8[8];
+            uint4 v[8], cv[8], o8[8];
             lane_load8(tile, lrow, sw, v);
+            if (BWD) lane_load8(ctile, lrow, sw, cv);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) o8[k] = out_group8<KIND, PT>(v[k], c * LANE_TC + 8 * k, R, P);
+            for (int k = 0; k < 8; ++k) o8[k] = out_group8<KIND, PT>(v[k], BWD ? cv[k] : v[k], c * LANE_TC + 8 * k, R, P);
 #pragma unroll
             for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = o8[k];
           } else {
             for (int k = 0; k < ng; ++k) {
               const uint4 v = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
+              const uint4 cv = BWD ? *reinterpret_cast<const uint4*>(ctile + lrow + (((uint32_t)k ^ sw) << 4)) : v;
               *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) =
-                  out_group8<KIND, PT>(v, c * LANE_TC + 8 * k, R, P);
+                  out_group8<KIND, PT>(v, cv, c * LANE_TC + 8 * k, R, P);
             }
           }
           fence_proxy_async_smem();                          // this lane's writes, before the async store
@@ -379,17 +405,20 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
           }
         } else if (ng == 8) {
           // a chain pass over a full tile: element 8 k + q feeds chain q mod P
-          uint4 v[8];
+          uint4 v[8], cv[8];
           lane_load8(tile, lrow, sw, v);
+          if (BWD) lane_load8(ctile, lrow, sw, cv);
           float f[64];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) chain_values8<KIND>(v[k], pass, R, f + 8 * k);
+          for (int k = 0; k < 8; ++k) chain_values8<KIND>(v[k], BWD ? cv[k] : v[k], pass, R, f + 8 * k);
 #pragma unroll
           for (int j = 0; j < 64; ++j) acc[j % PP] = __fadd_rn(acc[j % PP], f[j]);
         } else {
           for (int k = 0; k < ng; ++k) {
             float f[8];
-            chain_values8<KIND>(*reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4)), pass, R, f);
+            const uint4 v = *reinterpret_cast<const uint4*>(tile + lrow + (((uint32_t)k ^ sw) << 4));
+            const uint4 cv = BWD ? *reinterpret_cast<const uint4*>(ctile + lrow + (((uint32_t)k ^ sw) << 4)) : v;
+            chain_values8<KIND>(v, cv, pass, R, f);
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q % PP] = __fadd_rn(acc[q % PP], f[q]);
           }
@@ -401,7 +430,9 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
       float sum = acc[0];
 #pragma unroll
       for (int p = 1; p < PP; ++p) sum = __fadd_rn(sum, acc[p]);   // partials left to right
-      if (KIND == REGION_SOFTMAX) {
+      if (BWD) {
+        R.s = sum;                                           // s = the sum of RN(ct y)
+      } else if (KIND == REGION_SOFTMAX) {
         if (pass == 0) {
           R.m = max_nan(__uint_as_float(mb << 16), __uint_as_float(mb & 0xFFFF0000u));
         } else if (pass == 1) {
@@ -423,9 +454,9 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
     // a withheld copy (the test hook) is arrived for now, so that its phase
     // completes; then every request made is waited for (bounded) before the
     // warp leaves
-    if (lane == 0 && withheld >= cq) mbar_arrive(&bars[withheld % LANE_NI]);
+    if (lane == 0 && withheld >= cq) mbar_arrive(&bars[withheld % NI]);
     __syncwarp();
-    for (int q = cq; q < rq; ++q) mbar_wait(&bars[q % LANE_NI], (uint32_t)(q / LANE_NI) & 1u);
+    for (int q = cq; q < rq; ++q) mbar_wait(&bars[q % NI], (uint32_t)(q / NI) & 1u);
   }
   if (lane == 0) bulk_wait_all();
 }
@@ -475,8 +506,8 @@ static int lane_batch_rows(int64_t rows, int64_t wtot) {
 }
 
 template <int KIND, int PP, int PT>
-static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUtensorMap& ty, int64_t sms,
-                        cudaStream_t stream) {
+static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUtensorMap& ty, const CUtensorMap& tct,
+                        int64_t sms, cudaStream_t stream) {
   const int64_t nbatch = (P.rows + P.nb - 1) / P.nb;
   const int64_t need = (nbatch + LANE_WARPS - 1) / LANE_WARPS;
   const unsigned grid = (unsigned)(need < sms ? need : sms);
@@ -484,13 +515,13 @@ static int launch_lanes(const RegionParams& P, const CUtensorMap& tx, const CUte
     if (P.cols == LANE_MAX_COLS) {
       static bool attr_full[PSK_MAX_DEVICES] = {};
       smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT, true>, LANE_SMEM, attr_full);
-      region_lane_kernel<KIND, PP, PT, true><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
+      region_lane_kernel<KIND, PP, PT, true><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty, tct);
       return check_launch("row region kernel (lane per row)");
     }
   }
   static bool attr[PSK_MAX_DEVICES] = {};
   smem_limit_once((const void*)region_lane_kernel<KIND, PP, PT>, LANE_SMEM, attr);
-  region_lane_kernel<KIND, PP, PT><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty);
+  region_lane_kernel<KIND, PP, PT><<<grid, LANE_WARPS * 32, LANE_SMEM, stream>>>(P, tx, ty, tct);
   return check_launch("row region kernel (lane per row)");
 }
 
@@ -540,7 +571,7 @@ int softmax_lanes(const RegionParams& P0, int exp_mode, cudaStream_t stream, boo
   if (!lanes_take(P, tx, ty, sms, rc)) return PSK_OK;
   *taken = true;
   if (rc) return rc;
-  return launch_lanes<REGION_SOFTMAX, 1, PSK_F32>(P, tx, ty, sms, stream);
+  return launch_lanes<REGION_SOFTMAX, 1, PSK_F32>(P, tx, ty, tx, sms, stream);
 }
 
 // RMSNorm and LayerNorm: the one-chain orders too (interleaved orders run
@@ -559,10 +590,26 @@ int norm_lanes(const RegionParams& P0, int kind, cudaStream_t stream, bool* take
   if (rc) return rc;
   const bool bf = P.param_dtype == PSK_BF16;
   if (kind == REGION_RMS)
-    return bf ? launch_lanes<REGION_RMS, 1, PSK_BF16>(P, tx, ty, sms, stream)
-              : launch_lanes<REGION_RMS, 1, PSK_F32>(P, tx, ty, sms, stream);
-  return bf ? launch_lanes<REGION_LAYER, 1, PSK_BF16>(P, tx, ty, sms, stream)
-            : launch_lanes<REGION_LAYER, 1, PSK_F32>(P, tx, ty, sms, stream);
+    return bf ? launch_lanes<REGION_RMS, 1, PSK_BF16>(P, tx, ty, tx, sms, stream)
+              : launch_lanes<REGION_RMS, 1, PSK_F32>(P, tx, ty, tx, sms, stream);
+  return bf ? launch_lanes<REGION_LAYER, 1, PSK_BF16>(P, tx, ty, tx, sms, stream)
+            : launch_lanes<REGION_LAYER, 1, PSK_F32>(P, tx, ty, tx, sms, stream);
+}
+
+// The softmax backward: the one-chain orders over bf16 y, ct and dx (the
+// chain of RN(ct y), then dx = RN(y RN(ct - s))), ct on 16-byte boundaries.
+int softmax_bwd_lanes(const RegionParams& P0, cudaStream_t stream, bool* taken) {
+  *taken = false;
+  if (P0.partials != 1 || P0.ct_dtype != PSK_BF16 || (uintptr_t)P0.ct % 16 != 0 || P0.ldc % 8 != 0) return PSK_OK;
+  RegionParams P = P0;
+  CUtensorMap tx, ty, tct;
+  int64_t sms = 0;
+  int rc = PSK_OK;
+  if (!lanes_take(P, tx, ty, sms, rc)) return PSK_OK;
+  *taken = true;
+  if (rc) return rc;
+  if ((rc = encode_rows(&tct, P.ct, P.rows, P.cols, P.ldc, P.nb))) return rc;
+  return launch_lanes<REGION_SOFTMAX_BWD, 1, PSK_F32>(P, tx, ty, tct, sms, stream);
 }
 
 // The status word and test hook of this translation unit's kernels (pipe.cuh

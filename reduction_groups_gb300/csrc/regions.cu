@@ -1375,6 +1375,11 @@ static int dispatch_masked(const RegionParams& P, int exp_mode, bool pipe, cudaS
 
 template <int XT, int YT>
 static int dispatch_bwd(const RegionParams& P, bool pipe, cudaStream_t s) {
+  if (XT == PSK_BF16 && YT == PSK_BF16 && pipe) {   // many rows, one chain: a lane per row (lanes.cu)
+    bool taken = false;
+    const int rc = softmax_bwd_lanes(P, s, &taken);
+    if (taken) return rc;
+  }
   if (pipe) return launch_pipe<REGION_SOFTMAX_BWD, XT, YT, PSK_EXP_EXACT>(P, s);
   return launch_region_rows<REGION_SOFTMAX_BWD, XT, YT, PSK_EXP_EXACT>(P, s);
 }

@@ -183,10 +183,12 @@ __device__ __forceinline__ void divide_n(float* o, const RowDivisor& D) {
 // Launch the lane-per-row kernel (lanes.cu) for rows it takes: bf16 x and y,
 // 16-byte aligned rows of 64 to 4096 columns (a multiple of 8), enough rows
 // to fill the GPU, the one-chain orders (sequential, blocked); for the softmax
-// its fast realization; for the norms kind REGION_RMS or REGION_LAYER.
+// its fast realization; for the norms kind REGION_RMS or REGION_LAYER; the
+// softmax backward with bf16 y, ct and dx.
 // *taken is false, and nothing is launched, for other rows.
 int softmax_lanes(const RegionParams& P, int exp_mode, cudaStream_t stream, bool* taken);
 int norm_lanes(const RegionParams& P, int kind, cudaStream_t stream, bool* taken);
+int softmax_bwd_lanes(const RegionParams& P, cudaStream_t stream, bool* taken);
 // The lane kernel's status word (read, then zeroed if `reset`) and its copy
 // of the lost-copy test hook (lanes.cu keeps its own, like every unit).
 int lanes_status(unsigned int* v, bool reset);

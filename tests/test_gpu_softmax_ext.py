@@ -149,6 +149,28 @@ def test_softmax_backward_bitwise(dev, order, shape, yt, ct_t, dxt):
     assert dev.psk_device_status() == 0
 
 
+@pytest.mark.parametrize("cols", [1000, 4096])
+def test_softmax_backward_lane_kernel_bitwise(dev, cols):
+    """Enough bf16 rows for the lane-per-row kernel (one lane per row, the
+    y and ct tiles of each step loaded together): the one-chain orders bit
+    for bit against the oracle, a ragged last tile included (1000 columns);
+    the interleaved order, on the pipelined kernel, equal to it where its
+    sum's order allows (checked against the oracle too)."""
+    rows = 10_000
+    rng = np.random.default_rng(cols + 1)
+    y32 = OS.softmax_region((rng.standard_normal((rows, cols)) * 2).astype(np.float32), "f32", "f32")
+    y = f32_to_bf16(y32)
+    ct = f32_to_bf16(rng.standard_normal((rows, cols)).astype(np.float32))
+    for order in (("sequential",), ("blocked", 64), ("interleaved", 8)):
+        want = OS.softmax_backward(y, ct, "bf16", "bf16", "bf16", order)
+        dx = _empty((rows, cols), "bf16")
+        dev.psk_softmax_backward(_to_dev(y, "bf16"), _to_dev(ct, "bf16"), dx, order)
+        torch.cuda.synchronize()
+        ok = _same(_to_host(dx), want, "bf16")
+        assert ok.all(), f"order {order}: {(~ok).sum()} of {ok.size} differ"
+    assert dev.psk_device_status() == 0
+
+
 def test_softmax_backward_in_place_and_refusals(dev):
     rng = np.random.default_rng(3)
     y = OS.softmax_region((rng.standard_normal((40, 256)) * 2).astype(np.float32), "f32", "f32")
