@@ -12,6 +12,11 @@
 namespace psk {
 
 typedef float2 f2;
+// A pair product must never feed a pair sum whose rounding matters: the
+// assembler has been seen to fuse such a product and sum into one fma (both
+// through these intrinsics and through PTX that states the rounding), where
+// scalar products (mul.rn) are never fused.  Here no pair product feeds a
+// sum except exact ones (the exps' power-of-two scalings).
 PSK_HD f2 f2_fma(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 PSK_HD f2 f2_add(f2 a, f2 b) { return __fadd2_rn(a, b); }
 PSK_HD f2 f2_mul(f2 a, f2 b) { return __fmul2_rn(a, b); }
