@@ -59,8 +59,8 @@ constexpr float PAIR_LOG2E_LO = 1.9259629911783687e-08f;   // RN(log2 e - RN(log
 __device__ __forceinline__ f2 exp2_unit_nonpos(f2 t) {
   const f2 tc{fmax_nan(t.x, -104.5f), fmax_nan(t.y, -104.5f)};
   const f2 z = f2_fma(tc, f2_splat(PSK_FEXP_INV_LN2), f2_splat(PAIR_EXP_MAGIC));
-  const f2 kf = f2_add(z, f2_splat(-PAIR_EXP_MAGIC));
-  f2 f = f2_fma(tc, f2_splat(PSK_FEXP_INV_LN2), f2{-kf.x, -kf.y});
+  const f2 nk = f2_fma(z, f2_splat(-1.0f), f2_splat(PAIR_EXP_MAGIC));   // -k (exact)
+  f2 f = f2_fma(tc, f2_splat(PSK_FEXP_INV_LN2), nk);
   f = f2_fma(tc, f2_splat(PAIR_LOG2E_LO), f);
   const f2 p{ex2_unit(f.x), ex2_unit(f.y)};
   const f2 s{u2f(f2u(z.x) * (1u << 23) + (191u << 23)), u2f(f2u(z.y) * (1u << 23) + (191u << 23))};
@@ -87,8 +87,8 @@ __device__ __forceinline__ float exp_unit_nonpos(float t) {
 // same bits.
 __device__ __forceinline__ f2 exp2_unit_mid(f2 t) {
   const f2 z = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), f2_splat(PAIR_EXP_MAGIC));
-  const f2 kf = f2_add(z, f2_splat(-PAIR_EXP_MAGIC));
-  f2 f = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), f2{-kf.x, -kf.y});
+  const f2 nk = f2_fma(z, f2_splat(-1.0f), f2_splat(PAIR_EXP_MAGIC));   // -k (exact)
+  f2 f = f2_fma(t, f2_splat(PSK_FEXP_INV_LN2), nk);
   f = f2_fma(t, f2_splat(PAIR_LOG2E_LO), f);
   const f2 p{ex2_unit(f.x), ex2_unit(f.y)};
   const f2 s{u2f(f2u(z.x) * (1u << 23) + (127u << 23)), u2f(f2u(z.y) * (1u << 23) + (127u << 23))};
