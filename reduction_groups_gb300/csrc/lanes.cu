@@ -201,10 +201,11 @@ __device__ __forceinline__ void chain_values8(const uint4 w, const uint4 cw, int
 // The outputs of a group of eight stored elements at column j, rounded to
 // bf16 pairs: softmax e / s (the pipelined kernel's fast realization); norms
 // (x - mu) / d, * gamma, + beta; softmax backward RN(y RN(ct - s)) (w the
-// stored y, cw ct).
-template <int KIND, int PT>
+// stored y, cw ct).  PRE: the norms' bf16 gamma and beta of the group come
+// in pg / pb (loaded before the tile's wait) instead of from global memory.
+template <int KIND, int PT, bool PRE = false>
 __device__ __forceinline__ uint4 out_group8(const uint4 w, const uint4 cw, int j, const LaneRow& R,
-                                            const RegionParams& P) {
+                                            const RegionParams& P, const uint4 pg = uint4{}, const uint4 pb = uint4{}) {
   float o[8];
   if constexpr (KIND == REGION_SOFTMAX_BWD) {
     float c[8];
@@ -236,13 +237,15 @@ __device__ __forceinline__ uint4 out_group8(const uint4 w, const uint4 cw, int j
     divide_n<8>(o, R.D);
     if (P.gamma) {
       float g[8];
-      load_param8<PT>(P.gamma, j, g);
+      if (PRE) widen8(pg, g);
+      else load_param8<PT>(P.gamma, j, g);
 #pragma unroll
       for (int q = 0; q < 8; ++q) o[q] = __fmul_rn(o[q], g[q]);
     }
     if (KIND == REGION_LAYER && P.beta) {
       float bb[8];
-      load_param8<PT>(P.beta, j, bb);
+      if (PRE) widen8(pb, bb);
+      else load_param8<PT>(P.beta, j, bb);
 #pragma unroll
       for (int q = 0; q < 8; ++q) o[q] = __fadd_rn(o[q], bb[q]);
     }
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
   constexpr bool BWD = KIND == REGION_SOFTMAX_BWD;
   constexpr int TPR = BWD ? 2 : 1;                             // tiles per request
   constexpr int NI = LANE_NI / TPR;                            // request slots
+  constexpr bool PRE = (KIND == REGION_RMS || KIND == REGION_LAYER) && PT == PSK_BF16;
   extern __shared__ unsigned char lane_smem_raw[];
   __shared__ __align__(8) uint64_t full[LANE_WARPS][LANE_NI];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -363,6 +367,18 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
       for (int p = 0; p < PP; ++p) acc[p] = -0.0f;          // -0 + f = f for every f: the chain starts at f(x_p)
       for (int t = 0; t < nch; ++t) {
         const int c = rev ? nch - 1 - t : t;
+        // the norms' output pass over a whole tile: its bf16 gamma and beta
+        // (the same in every lane) are loaded before the wait for the tile
+        uint4 gq[PRE ? 8 : 1], bq[PRE ? 8 : 1];
+        if (PRE && out_pass && cols - c * LANE_TC >= LANE_TC) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int j = c * LANE_TC + 8 * k;
+            gq[PRE ? k : 0] = P.gamma ? __ldg(reinterpret_cast<const uint4*>((const uint16_t*)P.gamma + j)) : uint4{};
+            bq[PRE ? k : 0] = KIND == REGION_LAYER && P.beta ? __ldg(reinterpret_cast<const uint4*>((const uint16_t*)P.beta + j))
+                                                              : uint4{};
+          }
+        }
         if (!take()) { dead = true; break; }
         const int ng = (cols - c * LANE_TC) / 8 < 8 ? (cols - c * LANE_TC) / 8 : 8;
         const unsigned char* tile = wp + (size_t)((cq % NI) * TPR) * LANE_TILE;
@@ -376,7 +392,9 @@ __global__ void __launch_bounds__(LANE_WARPS * 32, 1)
             lane_load8(tile, lrow, sw, v);
             if (BWD) lane_load8(ctile, lrow, sw, cv);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) o8[k] = out_group8<KIND, PT>(v[k], BWD ? cv[k] : v[k], c * LANE_TC + 8 * k, R, P);
+            for (int k = 0; k < 8; ++k)
+              o8[k] = out_group8<KIND, PT, PRE>(v[k], BWD ? cv[k] : v[k], c * LANE_TC + 8 * k, R, P, gq[PRE ? k : 0],
+                                                bq[PRE ? k : 0]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(ot + lrow + (((uint32_t)k ^ sw) << 4)) = o8[k];
           } else {
